@@ -1,0 +1,224 @@
+/*
+ * hmoe.h -- C ABI of libhmoe: the hybrid W4A16 mixture-of-experts layer on GB300 (sm_103a).
+ *
+ * The layer serves per-expert mixed-precision MoE checkpoints. Each expert
+ * is a SwiGLU feed-forward block, W13 [2I, H] (gate rows, then up rows) and
+ * W2 [H, I]. Its weights sit in one of two tiers, chosen per expert by a
+ * bit map:
+ *   4 = the kept tier, NVFP4 (or MXFP4 when kept_format says so),
+ *   3 = the NF3 tier, 3-bit NormalFloat.
+ * Activations are bf16 throughout. Both tiers run off one shared route
+ * geometry (top-k ids, gates, token permutation, expert offsets) and sum
+ * into one output.
+ *   Cites: "quant: nvfp4_nf3_hybrid -- native serving for mixed NVFP4+NF3 MoE
+ *   checkpoints", How it works (two prepared weight sets per layer, one
+ *   shared route geometry and topk_sum, CUDA-graph-safe launches, an M<=8
+ *   decode path). "quant: add native mixed NVFP4/MXFP4 plus NF3 MoE
+ *   serving", Summary (hybrid_bit_map: 4 = kept, 3 = NF3; kept_format
+ *   selects MXFP4; scratch sized from the maximum batched token count; no
+ *   environment variables). "[Quantization][ModelOpt] W4A16 NVFP4 fused
+ *   MoE", Summary (W4A16: 4-bit weights, 16-bit activations, no activation
+ *   scales).
+ *
+ * Conventions
+ *   - Every pointer argument named *_dev or documented "device" is device
+ *     memory owned by the caller. The library never allocates device memory.
+ *   - Host pointers are read during the call only.
+ *   - hmoe_plan_routes and hmoe_forward enqueue work on the given stream and
+ *     return. They never synchronise, allocate or copy to the host, so they
+ *     may be captured in a CUDA graph. Grid sizes depend only on T and the
+ *     layer descriptor, never on routing results.
+ *   - Argument errors are found on the host. The call then returns a
+ *     negative status before anything is enqueued, and hmoe_last_error()
+ *     describes the error.
+ *   - Faults the device finds (a route id or permutation entry out of
+ *     range, inconsistent offsets, a bounded wait that timed out) do not
+ *     trap. Kernels skip the bad access and record a code in the workspace.
+ *     hmoe_check_device_status reads that code.
+ *   - No C++ exceptions cross this boundary, and no environment variable is
+ *     read.
+ *   - Layout of the logical checkpoint tensors (the input to
+ *     hmoe_pack_weights), for one matrix [N rows, K] of one expert:
+ *       NVFP4: codes uint8 [N][K/2]. Element 2i is the low nibble, element
+ *              2i+1 the high nibble. E2M1 is 1 sign, 2 exponent and 1
+ *              mantissa bit. Scales are E4M3 uint8 [N][K/16] and there is one
+ *              fp32 global scale. w = e2m1 * e4m3 * global.
+ *       MXFP4: codes as NVFP4. Scales are E8M0 uint8 [N][K/32].
+ *              w = e2m1 * 2^(b-127).
+ *       NF3:   codes are an LSB-first 3-bit bitstream, uint8 [N][3K/8]. Code
+ *              j is bits [3j, 3j+3) of the row's little-endian byte string.
+ *              Scales are bf16 [N][K/64]. w = bf16_rne(cb[code] * scale),
+ *              with the codebook cb (bf16 bits, index 0..7) =
+ *              {BF80, BF09, BE7D, 0000, 3E3C, 3EC4, 3F1F, 3F80}, the 3-bit
+ *              NormalFloat construction (Dettmers et al., QLoRA 2023).
+ *     The pages fix none of these layouts. This library fixes them as above.
+ */
+#ifndef HMOE_H_
+#define HMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. NULL is the legacy default stream. */
+typedef struct CUstream_st* hmoe_stream_t;
+
+typedef enum {
+  HMOE_OK = 0,
+  HMOE_ERR_INVALID_ARG = -1,         /* NULL pointer, T < 0, bad enum value, ... */
+  HMOE_ERR_UNSUPPORTED_SHAPE = -2,   /* H % 128, I % 64, E > 512, topk > 32, topk > E */
+  HMOE_ERR_WORKSPACE_TOO_SMALL = -3, /* ws_bytes < hmoe_workspace_size(T) */
+  HMOE_ERR_BAD_BITMAP = -4,          /* a bit_map entry other than 3 or 4 */
+  HMOE_ERR_CUDA = -5,                /* a CUDA runtime call failed; see hmoe_last_error */
+  HMOE_ERR_DEVICE_TIMEOUT = -6,      /* a bounded device wait ran out (from hmoe_check_device_status) */
+  HMOE_ERR_BAD_ROUTE = -7            /* device found an out-of-range route entry */
+} hmoe_status;
+
+typedef enum { HMOE_FMT_NF3 = 3, HMOE_FMT_NVFP4 = 4, HMOE_FMT_MXFP4 = 5 } hmoe_fmt;
+
+/* One MoE layer's shape. kept_format is HMOE_FMT_NVFP4 or HMOE_FMT_MXFP4. */
+typedef struct {
+  int H;           /* hidden size, a multiple of 128 */
+  int I;           /* expert intermediate size, a multiple of 64 */
+  int E;           /* experts, 1..512 */
+  int topk;        /* experts per token, 1..min(E, 32) */
+  int kept_format; /* hmoe_fmt of the kept (bit 4) tier */
+} hmoe_layer_desc;
+
+/* One expert's logical checkpoint tensors (device pointers, layout above).
+ * *_global is the NVFP4 fp32 global scale of that matrix. It is ignored
+ * for MXFP4 and NF3. */
+typedef struct {
+  const void* w13_codes;
+  const void* w13_scales;
+  float w13_global;
+  const void* w2_codes;
+  const void* w2_scales;
+  float w2_global;
+} hmoe_expert_src;
+
+typedef struct hmoe_layer hmoe_layer; /* opaque host handle: tier tables, no device memory */
+
+/* Bytes of the two tier-local packed buffers for this bit map.
+ * bit_map: host int8 [E] with 4 or 3 per expert, or NULL for a uniform
+ * layer (every expert in kept_format). The two outputs are the sizes of the
+ * kept_buf and nf3_buf arguments of hmoe_pack_weights. Either may be 0. */
+hmoe_status hmoe_packed_size(const hmoe_layer_desc* desc, const int8_t* bit_map,
+                             size_t* kept_bytes, size_t* nf3_bytes);
+
+/* Workspace bytes for hmoe_plan_routes and hmoe_forward at up to max_tokens
+ * tokens per call (the scratch is sized from the largest batch). */
+hmoe_status hmoe_workspace_size(const hmoe_layer_desc* desc, int max_tokens, size_t* bytes);
+
+/* Zero the workspace once, before its first use, on the stream. Every
+ * completed hmoe_forward leaves the workspace's counters at zero again. Zero
+ * it once more after a call reports HMOE_ERR_DEVICE_TIMEOUT. */
+hmoe_status hmoe_workspace_init(void* ws_dev, size_t ws_bytes, hmoe_stream_t stream);
+
+/* Demultiplex the experts into tier-local packed buffers per the bit map. Each
+ * tier's experts are stored contiguously in ascending expert id, in this
+ * library's tile layout. It then creates the layer handle.
+ *   Cites: "quant: add native mixed NVFP4/MXFP4 plus NF3 MoE serving",
+ *   Summary (demultiplex the expert weights into compact tier-local storage;
+ *   the metadata is validated).
+ * src: host array [E] of device pointers. kept_buf and nf3_buf are device
+ * buffers of at least the hmoe_packed_size bytes (NULL if that size is 0),
+ * and must stay alive while the handle is used. Kernels run on the stream.
+ * The source tensors may be freed once the stream has passed this point.
+ * Returns HMOE_ERR_BAD_BITMAP for an entry not in {3, 4}. *out receives the
+ * handle. Free it with hmoe_layer_destroy. */
+hmoe_status hmoe_pack_weights(const hmoe_layer_desc* desc, const int8_t* bit_map,
+                              const hmoe_expert_src* src, void* kept_buf, void* nf3_buf,
+                              hmoe_stream_t stream, hmoe_layer** out);
+
+/* Route T tokens: softmax top-k with renormalised gates, then a stable
+ * counting sort of the T*k slots by expert.
+ *   Cites: "quant: nvfp4_nf3_hybrid -- native serving ...", How it works (the
+ *   route geometry both tiers share).
+ * logits: device fp32 [T][E] row-major. NaN logits are not supported.
+ * ids:    device int32 [T][k]. The k largest logits, descending, with ties
+ *         to the lower expert id.
+ * gates:  device fp32 [T][k]. exp(l_j - l_max) / sum over the k chosen.
+ * perm:   device int32 [T*k]. The flat slot indices s = t*k + j sorted by
+ *         expert, ascending s within an expert.
+ * offsets: device int32 [E+1]. The exclusive prefix sum of per-expert
+ *         counts, with offsets[E] = T*k.
+ * ws: the workspace (device). T = 0 is valid and writes offsets as zeros. */
+hmoe_status hmoe_plan_routes(const hmoe_layer* layer, const float* logits, int T, int32_t* ids,
+                             float* gates, int32_t* perm, int32_t* offsets, void* ws,
+                             size_t ws_bytes, hmoe_stream_t stream);
+
+/* Forward options. Pass NULL to hmoe_forward_ex for the defaults. */
+typedef enum {
+  HMOE_TIERS_ONE_LAUNCH = 0,     /* both tiers in each launch, format chosen per expert */
+  HMOE_TIERS_KEPT_FIRST = 1,     /* kept tier launch, then NF3 tier launch (per GEMM) */
+  HMOE_TIERS_NF3_FIRST = 2       /* NF3 first, then kept */
+} hmoe_tier_order;
+
+typedef enum {
+  HMOE_PATH_AUTO = 0,     /* T <= 8 streams weights once per batch; larger T uses the grouped path */
+  HMOE_PATH_STREAM = 1,   /* weight-streaming path at any T (tokens in groups of 8) */
+  HMOE_PATH_GROUPED = 2   /* tensor-core grouped GEMM path (tcgen05) */
+} hmoe_path;
+
+typedef struct {
+  int tier_order;    /* hmoe_tier_order */
+  int path;          /* hmoe_path */
+  int wait_limit_us; /* bound on every device-side wait; 0 = the default (2 s) */
+  int debug_flags;   /* test hook: HMOE_DEBUG_NO_COPIES makes the weight producer issue nothing, so
+                        the consumers' bounded waits run out and the call reports
+                        HMOE_ERR_DEVICE_TIMEOUT through hmoe_check_device_status. 0 in normal use. */
+} hmoe_forward_opts;
+
+#define HMOE_DEBUG_NO_COPIES 1
+
+/* The layer: out[t] = sum_j gates[t,j] * W2_e (silu(W1_e x_t) * W3_e x_t) with
+ * e = ids[t,j], fp32 accumulation and a bf16 result. Expert weights are
+ * dequantised from their tier format as they stream.
+ * x: device bf16 [T][H]. out: device bf16 [T][H], fully overwritten.
+ * ids, gates, perm, offsets: exactly as hmoe_plan_routes wrote them for
+ * these T tokens.
+ * The result does not depend on tier_order or on the order of the tokens:
+ * each output element is summed in a fixed order. */
+hmoe_status hmoe_forward(const hmoe_layer* layer, const void* x, int T, const int32_t* ids,
+                         const float* gates, const int32_t* perm, const int32_t* offsets,
+                         void* out, void* ws, size_t ws_bytes, hmoe_stream_t stream);
+
+hmoe_status hmoe_forward_ex(const hmoe_layer* layer, const void* x, int T, const int32_t* ids,
+                            const float* gates, const int32_t* perm, const int32_t* offsets,
+                            void* out, void* ws, size_t ws_bytes, const hmoe_forward_opts* opts,
+                            hmoe_stream_t stream);
+
+/* Synchronise the stream and read the device status word the kernels write
+ * into the workspace. Returns HMOE_OK, HMOE_ERR_BAD_ROUTE or
+ * HMOE_ERR_DEVICE_TIMEOUT, then clears the word. */
+hmoe_status hmoe_check_device_status(void* ws, size_t ws_bytes, hmoe_stream_t stream);
+
+/* Test export. It writes the bf16 operand tile the kernels feed the tensor
+ * cores for one expert matrix, in logical row order. which = 13 gives
+ * [2I][H]; which = 2 gives [H][I]. dst is device memory. The values are
+ * e2m1*e4m3 (NVFP4, without the global scale), e2m1*2^(b-127) (MXFP4), or
+ * bf16_rne(cb*s) (NF3). */
+hmoe_status hmoe_debug_dequant(const hmoe_layer* layer, int expert, int which, void* dst,
+                               hmoe_stream_t stream);
+
+/* Global scales and tier of one expert, as the handle holds them. */
+hmoe_status hmoe_layer_expert_info(const hmoe_layer* layer, int expert, int* fmt,
+                                   float* w13_global, float* w2_global);
+
+void hmoe_layer_destroy(hmoe_layer* layer);
+
+/* Message for the last failing call on this thread ("" if none). */
+const char* hmoe_last_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int hmoe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HMOE_H_ */

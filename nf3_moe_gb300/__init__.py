@@ -1,0 +1,168 @@
+"""nf3_moe_gb300 -- the hybrid W4A16 mixture-of-experts layer on GB300 (sm_103a).
+
+This is the Python face of libhmoe, the C ABI declared in include/hmoe.h.
+The functions keep the C names and take torch tensors. PyTorch supplies
+only device memory and streams. Every step of the layer runs in the
+library's CUDA kernels.
+
+Typical use (see ``HybridMoELayer`` for the same thing with owned buffers):
+
+    layer = hmoe_pack_weights(desc, bit_map, experts, kept_buf, nf3_buf)
+    hmoe_workspace_init(ws)
+    hmoe_plan_routes(layer, logits, ids, gates, perm, offsets, ws)
+    hmoe_forward(layer, x, ids, gates, perm, offsets, out, ws)
+"""
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (FMT_MXFP4, FMT_NF3, FMT_NVFP4, PATH_AUTO, PATH_GROUPED, PATH_STREAM,  # noqa: F401
+                   TIERS_KEPT_FIRST, TIERS_NF3_FIRST, TIERS_ONE_LAUNCH, HmoeError, LayerDesc)
+
+__all__ = [
+    "LayerDesc", "HmoeError", "hmoe_packed_size", "hmoe_workspace_size", "hmoe_workspace_init",
+    "hmoe_pack_weights", "hmoe_plan_routes", "hmoe_forward", "hmoe_check_device_status",
+    "hmoe_debug_dequant", "HybridMoELayer", "library_path",
+]
+
+
+def library_path():
+    return _lib.LIB_PATH
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _desc(H, I, E, topk, kept_format=FMT_NVFP4):
+    return LayerDesc(H, I, E, topk, kept_format)
+
+
+def _bitmap_arg(bit_map):
+    if bit_map is None:
+        return None, None
+    arr = (ctypes.c_int8 * len(bit_map))(*[int(b) for b in bit_map])
+    return arr, ctypes.cast(arr, ctypes.c_void_p)
+
+
+def hmoe_packed_size(desc, bit_map=None):
+    kb, nb = ctypes.c_size_t(), ctypes.c_size_t()
+    keep, bm = _bitmap_arg(bit_map)
+    _lib.check(_lib.lib().hmoe_packed_size(ctypes.byref(desc), bm, ctypes.byref(kb), ctypes.byref(nb)))
+    return kb.value, nb.value
+
+
+def hmoe_workspace_size(desc, max_tokens):
+    b = ctypes.c_size_t()
+    _lib.check(_lib.lib().hmoe_workspace_size(ctypes.byref(desc), int(max_tokens), ctypes.byref(b)))
+    return b.value
+
+
+def hmoe_workspace_init(ws, stream=None):
+    _lib.check(_lib.lib().hmoe_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+class Layer:
+    """Owns the C handle. It keeps the tier buffers alive while it lives."""
+
+    def __init__(self, handle, desc, kept_buf, nf3_buf):
+        self.handle = handle
+        self.desc = desc
+        self.kept_buf, self.nf3_buf = kept_buf, nf3_buf
+
+    def expert_info(self, e):
+        f, a, b = ctypes.c_int(), ctypes.c_float(), ctypes.c_float()
+        _lib.check(_lib.lib().hmoe_layer_expert_info(self.handle, int(e), ctypes.byref(f), ctypes.byref(a),
+                                                     ctypes.byref(b)))
+        return f.value, a.value, b.value
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h and _lib._LIB is not None:
+            _lib._LIB.hmoe_layer_destroy(h)
+
+
+def hmoe_pack_weights(desc, bit_map, experts, kept_buf, nf3_buf, stream=None):
+    """experts: list of E tuples (w13_codes, w13_scales, w13_global, w2_codes, w2_scales, w2_global).
+    Tensors must be CUDA tensors in the logical layout of include/hmoe.h."""
+    E = desc.E
+    if len(experts) != E:
+        raise ValueError(f"expected {E} experts, got {len(experts)}")
+    src = (_lib.ExpertSrc * E)()
+    for e, (c13, s13, g13, c2, s2, g2) in enumerate(experts):
+        src[e] = _lib.ExpertSrc(c13.data_ptr(), s13.data_ptr(), float(g13), c2.data_ptr(), s2.data_ptr(), float(g2))
+    keep, bm = _bitmap_arg(bit_map)
+    h = ctypes.c_void_p()
+    _lib.check(_lib.lib().hmoe_pack_weights(ctypes.byref(desc), bm, src, _ptr(kept_buf), _ptr(nf3_buf),
+                                            _stream(stream), ctypes.byref(h)))
+    return Layer(h, desc, kept_buf, nf3_buf)
+
+
+def hmoe_plan_routes(layer, logits, ids, gates, perm, offsets, ws, stream=None):
+    T = logits.shape[0]
+    _lib.check(_lib.lib().hmoe_plan_routes(layer.handle, _ptr(logits), T, _ptr(ids), _ptr(gates), _ptr(perm),
+                                           _ptr(offsets), _ptr(ws), ws.numel() * ws.element_size(),
+                                           _stream(stream)))
+
+
+def hmoe_forward(layer, x, ids, gates, perm, offsets, out, ws, stream=None, tier_order=TIERS_ONE_LAUNCH,
+                 path=PATH_AUTO, wait_limit_us=0, debug_flags=0):
+    T = x.shape[0]
+    opts = _lib.ForwardOpts(int(tier_order), int(path), int(wait_limit_us), int(debug_flags))
+    _lib.check(_lib.lib().hmoe_forward_ex(layer.handle, _ptr(x), T, _ptr(ids), _ptr(gates), _ptr(perm),
+                                          _ptr(offsets), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
+                                          ctypes.byref(opts), _stream(stream)))
+
+
+def hmoe_check_device_status(ws, stream=None):
+    _lib.check(_lib.lib().hmoe_check_device_status(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def hmoe_debug_dequant(layer, expert, which, dst, stream=None):
+    _lib.check(_lib.lib().hmoe_debug_dequant(layer.handle, int(expert), int(which), _ptr(dst), _stream(stream)))
+
+
+class HybridMoELayer:
+    """One hybrid MoE layer with its packed tier buffers and workspace owned as torch tensors.
+
+    desc_args: H, I, E, topk, kept_format. bit_map: per-expert 4/3 list, or
+    None for uniform. experts: as in hmoe_pack_weights. max_tokens sizes the
+    workspace.
+    """
+
+    def __init__(self, H, I, E, topk, bit_map, experts, kept_format=FMT_NVFP4, max_tokens=8, device="cuda"):
+        self.desc = _desc(H, I, E, topk, kept_format)
+        kb, nb = hmoe_packed_size(self.desc, bit_map)
+        self.kept_buf = torch.empty(max(kb, 16), dtype=torch.uint8, device=device) if kb else None
+        self.nf3_buf = torch.empty(max(nb, 16), dtype=torch.uint8, device=device) if nb else None
+        self.layer = hmoe_pack_weights(self.desc, bit_map, experts, self.kept_buf, self.nf3_buf)
+        self.max_tokens = max_tokens
+        self.ws = torch.empty(hmoe_workspace_size(self.desc, max_tokens), dtype=torch.uint8, device=device)
+        hmoe_workspace_init(self.ws)
+        self.topk = topk
+        self.E = E
+        self.H = H
+
+    def plan(self, logits):
+        T = logits.shape[0]
+        dev = logits.device
+        ids = torch.empty((T, self.topk), dtype=torch.int32, device=dev)
+        gates = torch.empty((T, self.topk), dtype=torch.float32, device=dev)
+        perm = torch.empty((T * self.topk,), dtype=torch.int32, device=dev)
+        offsets = torch.empty((self.E + 1,), dtype=torch.int32, device=dev)
+        hmoe_plan_routes(self.layer, logits, ids, gates, perm, offsets, self.ws)
+        return ids, gates, perm, offsets
+
+    def __call__(self, x, logits, tier_order=TIERS_ONE_LAUNCH, path=PATH_AUTO, out=None):
+        ids, gates, perm, offsets = self.plan(logits)
+        if out is None:
+            out = torch.empty((x.shape[0], self.H), dtype=torch.bfloat16, device=x.device)
+        hmoe_forward(self.layer, x, ids, gates, perm, offsets, out, self.ws, tier_order=tier_order, path=path)
+        return out

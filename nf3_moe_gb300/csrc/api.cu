@@ -1,0 +1,384 @@
+// api.cu -- the C ABI of libhmoe (include/hmoe.h): validation, handle, workspace, launch order.
+//
+// Cites: "quant: nvfp4_nf3_hybrid -- native serving for mixed NVFP4+NF3 MoE
+// checkpoints", How it works (two prepared weight objects per layer;
+// preplanned, CUDA-graph-safe launches sharing one route geometry and one
+// topk_sum; no environment variables; scratch sized from the maximum batched
+// token count). "quant: add native mixed NVFP4/MXFP4 plus NF3 MoE serving",
+// Summary (hybrid_bit_map 4 = kept, 3 = NF3; kept_format; the metadata is
+// validated).
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "../../include/hmoe.h"
+#include "common.cuh"
+#include "internal.h"
+
+using namespace hmoe;
+
+struct hmoe_layer {
+  hmoe_layer_desc d;
+  uint8_t* kept_buf;
+  uint8_t* nf3_buf;
+  int n_kept, n_nf3;
+  ExpertGeom gk, gn;
+  ExpertTable tab;
+  int num_sms;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+hmoe_status fail(hmoe_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+hmoe_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(HMOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+hmoe_status check_desc(const hmoe_layer_desc* d) {
+  if (!d) return fail(HMOE_ERR_INVALID_ARG, "desc is NULL");
+  if (d->kept_format != HMOE_FMT_NVFP4 && d->kept_format != HMOE_FMT_MXFP4)
+    return fail(HMOE_ERR_INVALID_ARG, "kept_format must be NVFP4 (4) or MXFP4 (5), got %d", d->kept_format);
+  if (d->H <= 0 || d->I <= 0 || d->E <= 0 || d->topk <= 0)
+    return fail(HMOE_ERR_INVALID_ARG, "H, I, E, topk must be positive");
+  if (d->H % 128 != 0 || d->I % 64 != 0)
+    return fail(HMOE_ERR_UNSUPPORTED_SHAPE, "H must be a multiple of 128 and I of 64 (H=%d I=%d)", d->H, d->I);
+  if (d->E > MAX_E) return fail(HMOE_ERR_UNSUPPORTED_SHAPE, "E=%d exceeds %d", d->E, MAX_E);
+  if (d->topk > MAX_TOPK || d->topk > d->E)
+    return fail(HMOE_ERR_UNSUPPORTED_SHAPE, "topk=%d must be <= min(E, %d)", d->topk, MAX_TOPK);
+  return HMOE_OK;
+}
+
+hmoe_status check_bitmap(const hmoe_layer_desc* d, const int8_t* bit_map) {
+  if (!bit_map) return HMOE_OK;
+  for (int e = 0; e < d->E; ++e)
+    if (bit_map[e] != 3 && bit_map[e] != 4)
+      return fail(HMOE_ERR_BAD_BITMAP, "bit_map[%d] = %d; entries must be 4 (kept) or 3 (NF3)", e, bit_map[e]);
+  return HMOE_OK;
+}
+
+// Split of the K extent for small batches: the largest of {cap, ..., 1}
+// that divides KB and leaves at least 2 k-blocks per split.
+int pick_split(int KB, int cap) {
+  for (int ks = cap; ks > 1; ks >>= 1)
+    if (KB % ks == 0 && KB / ks >= 2) return ks;
+  return 1;
+}
+int pick_stage(int kbi) {
+  for (int s = 4; s > 1; s >>= 1)
+    if (kbi % s == 0) return s;
+  return 1;
+}
+
+constexpr int DECODE_MAX_T = 8;
+
+struct WsLayout {
+  size_t status, counters13, counters2, part13, part2, chunk_cnt, chunk_base, h, y, total;
+  int KS13, KS2;
+};
+
+// Fixed prefix (status, counters) first, so that the counters stay at the
+// same place for every T.
+WsLayout ws_layout(const hmoe_layer_desc& d, int T) {
+  WsLayout w{};
+  const int RT13 = 2 * d.I / TILE_ROWS, RT2 = d.H / TILE_ROWS;
+  const int KB13 = d.H / TILE_K, KB2 = d.I / TILE_K;
+  w.KS13 = pick_split(KB13, 8);
+  w.KS2 = pick_split(KB2, 4);
+  size_t off = 0;
+  w.status = off;
+  off += 256;
+  w.counters13 = off;
+  off += align256((size_t)STREAM_MAX_GROUPS_SPLIT * RT13 * 4);
+  w.counters2 = off;
+  off += align256((size_t)STREAM_MAX_GROUPS_SPLIT * RT2 * 4);
+  const size_t Sd = (size_t)(T < DECODE_MAX_T ? T : DECODE_MAX_T) * d.topk;
+  w.part13 = off;
+  off += align256((size_t)w.KS13 * Sd * 2 * d.I * 4);
+  w.part2 = off;
+  off += align256((size_t)w.KS2 * Sd * d.H * 4);
+  const size_t nch = (size_t)route_chunks(T);
+  w.chunk_cnt = off;
+  off += align256(nch * d.E * 4);
+  w.chunk_base = off;
+  off += align256(nch * d.E * 4);
+  const size_t S = (size_t)T * d.topk;
+  w.h = off;
+  off += align256(S * d.I * 2);
+  w.y = off;
+  off += align256(S * d.H * 4);
+  w.total = off;
+  return w;
+}
+
+hmoe_status check_ws(const hmoe_layer_desc& d, int T, void* ws, size_t ws_bytes, WsLayout* out) {
+  if (!ws) return fail(HMOE_ERR_INVALID_ARG, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return fail(HMOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  *out = ws_layout(d, T);
+  if (ws_bytes < out->total)
+    return fail(HMOE_ERR_WORKSPACE_TOO_SMALL, "workspace holds %zu bytes, T=%d needs %zu", ws_bytes, T, out->total);
+  return HMOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int hmoe_version(void) { return 100; }
+
+const char* hmoe_last_error(void) { return g_err.c_str(); }
+
+hmoe_status hmoe_packed_size(const hmoe_layer_desc* desc, const int8_t* bit_map, size_t* kept_bytes,
+                             size_t* nf3_bytes) {
+  hmoe_status s = check_desc(desc);
+  if (s != HMOE_OK) return s;
+  if (!kept_bytes || !nf3_bytes) return fail(HMOE_ERR_INVALID_ARG, "output pointers are NULL");
+  if ((s = check_bitmap(desc, bit_map)) != HMOE_OK) return s;
+  int nk = 0, nn = 0;
+  for (int e = 0; e < desc->E; ++e) {
+    if (!bit_map || bit_map[e] == 4) ++nk; else ++nn;
+  }
+  *kept_bytes = (size_t)nk * expert_geom(desc->H, desc->I, desc->kept_format).expert_bytes;
+  *nf3_bytes = (size_t)nn * expert_geom(desc->H, desc->I, FMT_NF3).expert_bytes;
+  return HMOE_OK;
+}
+
+hmoe_status hmoe_workspace_size(const hmoe_layer_desc* desc, int max_tokens, size_t* bytes) {
+  hmoe_status s = check_desc(desc);
+  if (s != HMOE_OK) return s;
+  if (!bytes || max_tokens < 0) return fail(HMOE_ERR_INVALID_ARG, "bytes NULL or max_tokens < 0");
+  *bytes = ws_layout(*desc, max_tokens).total;
+  return HMOE_OK;
+}
+
+hmoe_status hmoe_workspace_init(void* ws, size_t ws_bytes, hmoe_stream_t stream) {
+  if (!ws) return fail(HMOE_ERR_INVALID_ARG, "workspace is NULL");
+  cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace)");
+  return HMOE_OK;
+}
+
+hmoe_status hmoe_pack_weights(const hmoe_layer_desc* desc, const int8_t* bit_map, const hmoe_expert_src* src,
+                              void* kept_buf, void* nf3_buf, hmoe_stream_t stream, hmoe_layer** out) {
+  hmoe_status s = check_desc(desc);
+  if (s != HMOE_OK) return s;
+  if ((s = check_bitmap(desc, bit_map)) != HMOE_OK) return s;
+  if (!src || !out) return fail(HMOE_ERR_INVALID_ARG, "src or out is NULL");
+  size_t kb = 0, nb = 0;
+  hmoe_packed_size(desc, bit_map, &kb, &nb);
+  if ((kb && !kept_buf) || (nb && !nf3_buf)) return fail(HMOE_ERR_INVALID_ARG, "a tier buffer is NULL");
+  if ((kept_buf && !aligned16(kept_buf)) || (nf3_buf && !aligned16(nf3_buf)))
+    return fail(HMOE_ERR_INVALID_ARG, "tier buffers must be 16-byte aligned");
+  for (int e = 0; e < desc->E; ++e) {
+    const hmoe_expert_src& x = src[e];
+    if (!x.w13_codes || !x.w13_scales || !x.w2_codes || !x.w2_scales)
+      return fail(HMOE_ERR_INVALID_ARG, "expert %d has a NULL source pointer", e);
+  }
+  hmoe_layer* L = new (std::nothrow) hmoe_layer();
+  if (!L) return fail(HMOE_ERR_INVALID_ARG, "out of host memory");
+  L->d = *desc;
+  L->kept_buf = static_cast<uint8_t*>(kept_buf);
+  L->nf3_buf = static_cast<uint8_t*>(nf3_buf);
+  L->gk = expert_geom(desc->H, desc->I, desc->kept_format);
+  L->gn = expert_geom(desc->H, desc->I, FMT_NF3);
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ce != cudaSuccess) {
+    delete L;
+    return cuda_fail(ce, "device query");
+  }
+  int nk = 0, nn = 0;
+  for (int e = 0; e < desc->E; ++e) {
+    const bool kept = !bit_map || bit_map[e] == 4;
+    const int fmt = kept ? desc->kept_format : FMT_NF3;
+    uint8_t* dst;
+    if (kept) {
+      L->tab.loc[e] = (uint16_t)nk;
+      dst = L->kept_buf + (size_t)nk * L->gk.expert_bytes;
+      ++nk;
+    } else {
+      L->tab.loc[e] = (uint16_t)(nn | LOC_NF3);
+      dst = L->nf3_buf + (size_t)nn * L->gn.expert_bytes;
+      ++nn;
+    }
+    L->tab.g13[e] = fmt == FMT_NVFP4 ? src[e].w13_global : 1.0f;
+    L->tab.g2[e] = fmt == FMT_NVFP4 ? src[e].w2_global : 1.0f;
+    const ExpertGeom& g = kept ? L->gk : L->gn;
+    ce = launch_pack_matrix(fmt, 13, src[e].w13_codes, src[e].w13_scales, 2 * desc->I, desc->H, desc->I, dst,
+                            (cudaStream_t)stream);
+    if (ce == cudaSuccess)
+      ce = launch_pack_matrix(fmt, 2, src[e].w2_codes, src[e].w2_scales, desc->H, desc->I, desc->I,
+                              dst + g.w13_bytes, (cudaStream_t)stream);
+    if (ce != cudaSuccess) {
+      delete L;
+      return cuda_fail(ce, "pack kernel launch");
+    }
+  }
+  L->n_kept = nk;
+  L->n_nf3 = nn;
+  *out = L;
+  return HMOE_OK;
+}
+
+void hmoe_layer_destroy(hmoe_layer* layer) { delete layer; }
+
+hmoe_status hmoe_layer_expert_info(const hmoe_layer* L, int expert, int* fmt, float* g13, float* g2) {
+  if (!L || expert < 0 || expert >= L->d.E) return fail(HMOE_ERR_INVALID_ARG, "bad layer or expert index");
+  if (fmt) *fmt = (L->tab.loc[expert] & LOC_NF3) ? FMT_NF3 : L->d.kept_format;
+  if (g13) *g13 = L->tab.g13[expert];
+  if (g2) *g2 = L->tab.g2[expert];
+  return HMOE_OK;
+}
+
+hmoe_status hmoe_plan_routes(const hmoe_layer* L, const float* logits, int T, int32_t* ids, float* gates,
+                             int32_t* perm, int32_t* offsets, void* ws, size_t ws_bytes, hmoe_stream_t stream) {
+  if (!L) return fail(HMOE_ERR_INVALID_ARG, "layer is NULL");
+  if (T < 0) return fail(HMOE_ERR_INVALID_ARG, "T=%d < 0", T);
+  if (!offsets || (T > 0 && (!logits || !ids || !gates || !perm)))
+    return fail(HMOE_ERR_INVALID_ARG, "a route buffer is NULL");
+  WsLayout w;
+  hmoe_status s = check_ws(L->d, T, ws, ws_bytes, &w);
+  if (s != HMOE_OK) return s;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  cudaError_t e = launch_route(logits, T, L->d.E, L->d.topk, ids, gates, perm, offsets,
+                               reinterpret_cast<int*>(wsb + w.chunk_cnt), reinterpret_cast<int*>(wsb + w.chunk_base),
+                               (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "route kernel launch");
+  return HMOE_OK;
+}
+
+static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, const float* gates,
+                                   const int32_t* perm, const int32_t* offsets, void* out, uint8_t* wsb,
+                                   const WsLayout& w, const hmoe_forward_opts& o, cudaStream_t st) {
+  const int tier_order = o.tier_order;
+  const hmoe_layer_desc& d = L->d;
+  const bool split = T <= DECODE_MAX_T;
+  StreamParams p{};
+  p.kept_buf = L->kept_buf;
+  p.nf3_buf = L->nf3_buf;
+  p.kept_fmt = d.kept_format;
+  p.H = d.H;
+  p.I = d.I;
+  p.E = d.E;
+  p.topk = d.topk;
+  p.T = T;
+  p.group_tokens = 8;
+  p.kept_expert_bytes = L->gk.expert_bytes;
+  p.nf3_expert_bytes = L->gn.expert_bytes;
+  p.kept_w2_off = L->gk.w13_bytes;
+  p.nf3_w2_off = L->gn.w13_bytes;
+  p.offsets = offsets;
+  p.perm = perm;
+  p.status = reinterpret_cast<int*>(wsb + w.status);
+  p.h_out = reinterpret_cast<__nv_bfloat16*>(wsb + w.h);
+  p.y_out = reinterpret_cast<float*>(wsb + w.y);
+  p.tab = L->tab;
+  p.wait_limit_ns = o.wait_limit_us > 0 ? (unsigned long long)o.wait_limit_us * 1000ull : WAIT_LIMIT_NS;
+  p.debug_no_copies = (o.debug_flags & HMOE_DEBUG_NO_COPIES) ? 1 : 0;
+  int masks[2] = {3, 0};
+  if (tier_order == HMOE_TIERS_KEPT_FIRST) {
+    masks[0] = 1;
+    masks[1] = 2;
+  } else if (tier_order == HMOE_TIERS_NF3_FIRST) {
+    masks[0] = 2;
+    masks[1] = 1;
+  }
+  const int grid = stream_grid(L->num_sms);
+  for (int which : {13, 2}) {
+    p.which = which;
+    p.rows = which == 13 ? 2 * d.I : d.H;
+    p.K = which == 13 ? d.H : d.I;
+    p.RT = p.rows / TILE_ROWS;
+    p.KB = p.K / TILE_K;
+    p.KS = split ? (which == 13 ? w.KS13 : w.KS2) : 1;
+    p.kbs = pick_stage(p.KB / p.KS);
+    p.act = which == 13 ? static_cast<const __nv_bfloat16*>(x) : p.h_out;
+    p.act_stride = which == 13 ? d.H : d.I;
+    p.part = reinterpret_cast<float*>(wsb + (which == 13 ? w.part13 : w.part2));
+    p.counters = reinterpret_cast<int*>(wsb + (which == 13 ? w.counters13 : w.counters2));
+    for (int m : masks) {
+      if (!m) continue;
+      p.tier_mask = m;
+      cudaError_t e = launch_stream_gemm(p, grid, st);
+      if (e != cudaSuccess) return cuda_fail(e, "stream GEMM launch");
+    }
+  }
+  cudaError_t e = launch_finalize(p.y_out, gates, T, d.topk, d.H, static_cast<__nv_bfloat16*>(out), st);
+  if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+  return HMOE_OK;
+}
+
+hmoe_status hmoe_forward_ex(const hmoe_layer* L, const void* x, int T, const int32_t* ids, const float* gates,
+                            const int32_t* perm, const int32_t* offsets, void* out, void* ws, size_t ws_bytes,
+                            const hmoe_forward_opts* opts, hmoe_stream_t stream) {
+  if (!L) return fail(HMOE_ERR_INVALID_ARG, "layer is NULL");
+  if (T < 0) return fail(HMOE_ERR_INVALID_ARG, "T=%d < 0", T);
+  hmoe_forward_opts o{HMOE_TIERS_ONE_LAUNCH, HMOE_PATH_AUTO, 0, 0};
+  if (opts) o = *opts;
+  const int tier_order = o.tier_order, path = o.path;
+  if (tier_order < 0 || tier_order > 2) return fail(HMOE_ERR_INVALID_ARG, "bad tier_order %d", tier_order);
+  if (path < 0 || path > 2) return fail(HMOE_ERR_INVALID_ARG, "bad path %d", path);
+  if (o.wait_limit_us < 0) return fail(HMOE_ERR_INVALID_ARG, "wait_limit_us < 0");
+  WsLayout w;
+  hmoe_status s = check_ws(L->d, T, ws, ws_bytes, &w);
+  if (s != HMOE_OK) return s;
+  if (T == 0) return HMOE_OK;
+  if (!x || !ids || !gates || !perm || !offsets || !out) return fail(HMOE_ERR_INVALID_ARG, "a buffer is NULL");
+  if (!aligned16(x) || !aligned16(out)) return fail(HMOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+  (void)ids;
+  return run_stream_path(L, x, T, gates, perm, offsets, out, static_cast<uint8_t*>(ws), w, o,
+                         (cudaStream_t)stream);
+}
+
+hmoe_status hmoe_forward(const hmoe_layer* L, const void* x, int T, const int32_t* ids, const float* gates,
+                         const int32_t* perm, const int32_t* offsets, void* out, void* ws, size_t ws_bytes,
+                         hmoe_stream_t stream) {
+  return hmoe_forward_ex(L, x, T, ids, gates, perm, offsets, out, ws, ws_bytes, nullptr, stream);
+}
+
+hmoe_status hmoe_check_device_status(void* ws, size_t ws_bytes, hmoe_stream_t stream) {
+  if (!ws || ws_bytes < 256) return fail(HMOE_ERR_INVALID_ARG, "workspace is NULL or too small");
+  int word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(int), (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  if (word & DEV_TIMEOUT) return fail(HMOE_ERR_DEVICE_TIMEOUT, "a bounded device wait timed out (status 0x%x)", word);
+  if (word & DEV_BAD_ROUTE) return fail(HMOE_ERR_BAD_ROUTE, "device found an out-of-range route entry (status 0x%x)", word);
+  return HMOE_OK;
+}
+
+hmoe_status hmoe_debug_dequant(const hmoe_layer* L, int expert, int which, void* dst, hmoe_stream_t stream) {
+  if (!L || !dst || expert < 0 || expert >= L->d.E || (which != 13 && which != 2))
+    return fail(HMOE_ERR_INVALID_ARG, "bad arguments to hmoe_debug_dequant");
+  const bool nf3 = (L->tab.loc[expert] & LOC_NF3) != 0;
+  const int fmt = nf3 ? FMT_NF3 : L->d.kept_format;
+  const ExpertGeom& g = nf3 ? L->gn : L->gk;
+  const uint8_t* base = (nf3 ? L->nf3_buf : L->kept_buf) + (size_t)(L->tab.loc[expert] & 0x7FFF) * g.expert_bytes;
+  const int N = which == 13 ? 2 * L->d.I : L->d.H;
+  const int K = which == 13 ? L->d.H : L->d.I;
+  cudaError_t e = launch_debug_dequant(fmt, which, base + (which == 2 ? g.w13_bytes : 0), N, K, L->d.I, dst,
+                                       (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "debug dequant launch");
+  return HMOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,295 @@
+// common.cuh -- device helpers shared by the libhmoe kernels (sm_103a).
+//
+// Packed tile layout (this library's choice; the pages leave it open, and the
+// "nf3_2p1" layout of "quant: nvfp4_nf3_hybrid ...", Depends on, is prior art
+// for SM120 only):
+//
+//   A tile is 128 weight rows x 64 K (one "k-block"). One expert matrix is
+//   stored as tiles ordered (row tile rt, k-block kb) with kb fastest, so a
+//   row tile's K extent is one contiguous byte range. Inside a tile, rows
+//   form 8 groups of 16 (rg = 0..7). Thread slot (rg, lane), with
+//   g = lane / 4 and q = lane % 4, owns rows R0 = 16 rg + g and R1 = R0 + 8,
+//   and logical k = 16 q .. 16 q + 15 of the k-block. This is the A-fragment
+//   ownership of an m16n8k16 MMA after permuting K inside each k-block. The
+//   same slot also drives the tensor-core tile writer.
+//
+//   NVFP4 tile, 4608 B: codes [256 slots][16 B] = [R0 w0, R0 w1, R1 w0, R1 w1].
+//     Each 32-bit word holds 8 E2M1 codes. The magnitude of code i (i<4) is
+//     in nibble i bits 0..2, and code 4+i in nibble 4+i. The sign bits sit
+//     in the nibbles' bit 3: code 0..3 at bits 7, 15, 23, 31 and code 4..7
+//     at bits 3, 11, 19, 27. Then scales: [256 slots][2 B] = E4M3 of
+//     (R0, group q) and (R1, group q).
+//   MXFP4 tile, 4352 B: codes as NVFP4. Scales [8 rg][8 g][2 halves][2 B]
+//     = E8M0 of (R0, q/2) and (R1, q/2).
+//   NF3 tile, 3328 B: three words per slot, A at 0, B at 1024, C at 2048
+//     (each [256 slots][4 B]). A's nibbles 0..7 hold R0 codes 0..7, B's hold
+//     R0 codes 8..15, C's hold R1 codes 0..7, each in bits 0..2. Bit 3 of
+//     nibble j in A, B and C holds bits 0, 1 and 2 of R1 code 8+j. Then bf16
+//     scales [128 rows][2 B] at 3072.
+//   W13 rows are interleaved per 16-row group: group rows 0..7 are the gate
+//   rows of 8 consecutive channels and rows 8..15 the up rows of the same
+//   channels. So R0 and R1 of a thread slot are the gate and up rows of one
+//   channel.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace hmoe {
+
+constexpr int FMT_NF3 = 3, FMT_NVFP4 = 4, FMT_MXFP4 = 5;
+constexpr int TILE_ROWS = 128;
+constexpr int TILE_K = 64;
+constexpr int MAX_E = 512;
+constexpr int MAX_TOPK = 32;
+
+__host__ __device__ constexpr int tile_bytes(int fmt) {
+  return fmt == FMT_NVFP4 ? 4608 : (fmt == FMT_MXFP4 ? 4352 : 3328);
+}
+
+// Device status word codes (bit flags, OR-ed by kernels).
+constexpr int DEV_TIMEOUT = 1;
+constexpr int DEV_BAD_ROUTE = 2;
+
+// Per-expert table passed by value in kernel parameters.
+struct ExpertTable {
+  uint16_t loc[MAX_E];        // tier-local index; bit 15 set = NF3 tier
+  float g13[MAX_E];           // W13 global scale (NVFP4), else 1
+  float g2[MAX_E];
+};
+constexpr uint16_t LOC_NF3 = 0x8000;
+
+// NF3 codebook as bf16 bit patterns (kernel copy), index 0..7.
+constexpr uint16_t NF3_CB[8] = {0xBF80, 0xBF09, 0xBE7D, 0x0000, 0x3E3C, 0x3EC4, 0x3F1F, 0x3F80};
+// Byte tables for prmt lookups: low bytes and high bytes of the 8 entries.
+constexpr uint32_t NF3_LO0 = 0x007D0980u, NF3_LO1 = 0x801FC43Cu;
+constexpr uint32_t NF3_HI0 = 0x00BEBFBFu, NF3_HI1 = 0x3F3F3E3Eu;
+// E2M1 magnitudes {0,.5,1,1.5,2,3,4,6} as bf16: low bytes and high bytes.
+constexpr uint32_t E2M1_LO0 = 0xC0800000u, E2M1_LO1 = 0xC0804000u;
+constexpr uint32_t E2M1_HI0 = 0x3F3F3F00u, E2M1_HI1 = 0x40404040u;
+
+// ---------------------------------------------------------------- generic helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void set_status(int* status, int code) {
+  if (status) atomicOr(status, code);
+}
+
+// ---------------------------------------------------------------- mbarrier + bulk copy
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete. The wait is bounded:
+// it returns false if *abort becomes non-zero or after limit_ns.
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = WAIT_LIMIT_NS) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+// 1D bulk copy (TMA engine, non-tensor form) global -> this CTA's shared memory.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// Same, with an L2 evict-first policy for data read once (streamed weights).
+__device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- bf16 helpers
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf16_bcast(uint16_t b) { return (uint32_t)b | ((uint32_t)b << 16); }
+
+// E4M3 byte -> bf16 bits. Exact: every E4M3 value is a bf16 value.
+__device__ __forceinline__ uint16_t e4m3_to_bf16(uint32_t byte) {
+  uint32_t s = (byte & 0x80u) << 8;
+  uint32_t e = (byte >> 3) & 15u, m = byte & 7u;
+  if (e == 0) {
+    // subnormal m/8 * 2^-6 = m * 2^-9 -> normalise via float
+    float f = (float)m * 0.001953125f;
+    return (uint16_t)(s | (__float_as_uint(f) >> 16));
+  }
+  if (e == 15 && m == 7) return (uint16_t)(s | 0x7FC0u);  // NaN (never produced by encoders)
+  return (uint16_t)(s | ((e + 120u) << 7) | (m << 4));
+}
+// E8M0 byte -> bf16 bits of 2^(b-127). b = 0 is the bf16 subnormal 2^-127.
+__device__ __forceinline__ uint16_t e8m0_to_bf16(uint32_t byte) {
+  if (byte == 0) return 0x0040;
+  if (byte == 255) return 0x7FC0;
+  return (uint16_t)(byte << 7);
+}
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+// ---------------------------------------------------------------- code word decoders
+// 8 E2M1 codes (word layout in the header comment) -> 4 bf16x2 (codes 0,1 | 2,3 | 4,5 | 6,7).
+__device__ __forceinline__ void e2m1x8_to_bf16x2(uint32_t w, uint32_t* p) {
+  const uint32_t m = w & 0x77777777u;
+  uint32_t lo = __byte_perm(E2M1_LO0, E2M1_LO1, m);
+  uint32_t hi = __byte_perm(E2M1_HI0, E2M1_HI1, m) | (w & 0x80808080u);
+  p[0] = __byte_perm(lo, hi, 0x5140);
+  p[1] = __byte_perm(lo, hi, 0x7362);
+  const uint32_t m2 = m >> 16;
+  lo = __byte_perm(E2M1_LO0, E2M1_LO1, m2);
+  hi = __byte_perm(E2M1_HI0, E2M1_HI1, m2) | ((w << 4) & 0x80808080u);
+  p[2] = __byte_perm(lo, hi, 0x5140);
+  p[3] = __byte_perm(lo, hi, 0x7362);
+}
+
+// 8 NF3 codes held as selector nibbles (bit 3 of each nibble clear) -> 4 bf16x2.
+__device__ __forceinline__ void nf3x8_to_bf16x2(uint32_t sel, uint32_t* p) {
+  uint32_t lo = __byte_perm(NF3_LO0, NF3_LO1, sel);
+  uint32_t hi = __byte_perm(NF3_HI0, NF3_HI1, sel);
+  p[0] = __byte_perm(lo, hi, 0x5140);
+  p[1] = __byte_perm(lo, hi, 0x7362);
+  sel >>= 16;
+  lo = __byte_perm(NF3_LO0, NF3_LO1, sel);
+  hi = __byte_perm(NF3_HI0, NF3_HI1, sel);
+  p[2] = __byte_perm(lo, hi, 0x5140);
+  p[3] = __byte_perm(lo, hi, 0x7362);
+}
+
+// NF3 words A, B, C of one thread slot -> selector words for R0 codes 0..7,
+// R0 8..15, R1 0..7 and R1 8..15.
+__device__ __forceinline__ void nf3_selectors(uint32_t A, uint32_t B, uint32_t C, uint32_t* s) {
+  s[0] = A & 0x77777777u;
+  s[1] = B & 0x77777777u;
+  s[2] = C & 0x77777777u;
+  s[3] = ((A >> 3) & 0x11111111u) | ((B >> 2) & 0x22222222u) | ((C >> 1) & 0x44444444u);
+}
+
+// Load one thread slot's packed data from a tile in shared memory and
+// produce its dequantised bf16x2 operands: r0[8] for row R0 (k pairs in
+// order) and r1[8] for row R1. With with_nf3_scale == false the NF3 values
+// are raw codebook entries, and scale0/scale1 return the two row scales as
+// floats for the caller to apply to fp32 sums. Otherwise every format's
+// values come out multiplied by their scale in bf16 (the "tile" values).
+template <int FMT, bool WITH_NF3_SCALE>
+__device__ __forceinline__ void dequant_slot(const uint8_t* tile, int rg, int lane, uint32_t* r0, uint32_t* r1,
+                                             float* scale0, float* scale1) {
+  const int slot = rg * 32 + lane;
+  if constexpr (FMT == FMT_NVFP4 || FMT == FMT_MXFP4) {
+    const uint4 q = *reinterpret_cast<const uint4*>(tile + slot * 16);
+    uint32_t sc;
+    if constexpr (FMT == FMT_NVFP4) {
+      sc = *reinterpret_cast<const uint16_t*>(tile + 4096 + slot * 2);
+    } else {
+      const int g = lane >> 2, hq = (lane & 3) >> 1;
+      sc = *reinterpret_cast<const uint16_t*>(tile + 4096 + (rg * 16 + g * 2 + hq) * 2);
+    }
+    const uint32_t s0 = bf16_bcast(FMT == FMT_NVFP4 ? e4m3_to_bf16(sc & 0xFFu) : e8m0_to_bf16(sc & 0xFFu));
+    const uint32_t s1 = bf16_bcast(FMT == FMT_NVFP4 ? e4m3_to_bf16(sc >> 8) : e8m0_to_bf16(sc >> 8));
+    e2m1x8_to_bf16x2(q.x, r0);
+    e2m1x8_to_bf16x2(q.y, r0 + 4);
+    e2m1x8_to_bf16x2(q.z, r1);
+    e2m1x8_to_bf16x2(q.w, r1 + 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      r0[i] = bf16x2_mul(r0[i], s0);
+      r1[i] = bf16x2_mul(r1[i], s1);
+    }
+    *scale0 = 1.0f;
+    *scale1 = 1.0f;
+  } else {
+    const uint32_t A = *reinterpret_cast<const uint32_t*>(tile + slot * 4);
+    const uint32_t B = *reinterpret_cast<const uint32_t*>(tile + 1024 + slot * 4);
+    const uint32_t C = *reinterpret_cast<const uint32_t*>(tile + 2048 + slot * 4);
+    const int g = lane >> 2;
+    const uint32_t sb0 = *reinterpret_cast<const uint16_t*>(tile + 3072 + (rg * 16 + g) * 2);
+    const uint32_t sb1 = *reinterpret_cast<const uint16_t*>(tile + 3072 + (rg * 16 + g + 8) * 2);
+    uint32_t s[4];
+    nf3_selectors(A, B, C, s);
+    nf3x8_to_bf16x2(s[0], r0);
+    nf3x8_to_bf16x2(s[1], r0 + 4);
+    nf3x8_to_bf16x2(s[2], r1);
+    nf3x8_to_bf16x2(s[3], r1 + 4);
+    if constexpr (WITH_NF3_SCALE) {
+      const uint32_t S0 = bf16_bcast((uint16_t)sb0), S1 = bf16_bcast((uint16_t)sb1);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        r0[i] = bf16x2_mul(r0[i], S0);
+        r1[i] = bf16x2_mul(r1[i], S1);
+      }
+      *scale0 = 1.0f;
+      *scale1 = 1.0f;
+    } else {
+      *scale0 = bf16_bits_to_float(sb0);
+      *scale1 = bf16_bits_to_float(sb1);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- mma.sync (decode path)
+__device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+}  // namespace hmoe

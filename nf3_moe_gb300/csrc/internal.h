@@ -1,0 +1,68 @@
+// internal.h -- launchers and host-side structures shared by the libhmoe translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace hmoe {
+
+// ---------------------------------------------------------------- routing
+int route_chunks(int T);
+cudaError_t launch_route(const float* logits, int T, int E, int k, int* ids, float* gates, int* perm,
+                         int* offsets, int* chunk_cnt, int* chunk_base, cudaStream_t st);
+
+// ---------------------------------------------------------------- packing
+// Geometry of one expert block inside a tier buffer: W13 tiles then W2 tiles.
+struct ExpertGeom {
+  int H, I;
+  int rt13, kb13, rt2, kb2;  // row tiles / k-blocks of each matrix
+  size_t tile;               // tile bytes of the format
+  size_t w13_bytes, w2_bytes, expert_bytes;
+};
+ExpertGeom expert_geom(int H, int I, int fmt);
+
+cudaError_t launch_pack_matrix(int fmt, int which, const void* codes, const void* scales, int N, int K, int I,
+                               uint8_t* dst, cudaStream_t st);
+cudaError_t launch_debug_dequant(int fmt, int which, const uint8_t* src, int N, int K, int I, void* dst,
+                                 cudaStream_t st);
+
+// ---------------------------------------------------------------- streaming GEMM (any T; the decode path)
+struct StreamParams {
+  const uint8_t* kept_buf;
+  const uint8_t* nf3_buf;
+  int kept_fmt;
+  int which;           // 13: act = x rows by token, output h;  2: act = h rows by slot, output y
+  int H, I, E, topk, T;
+  int rows, K;         // this matrix: rows = 2I or H, K = H or I
+  int RT, KB;          // row tiles, k-blocks
+  int KS;              // k-splits per (group, row tile); 1 = no split
+  int kbs;             // k-blocks per pipeline stage
+  int group_tokens;    // tokens per token group (<= 8)
+  int tier_mask;       // bit 0: kept experts, bit 1: NF3 experts
+  size_t kept_expert_bytes, nf3_expert_bytes;
+  size_t kept_w2_off, nf3_w2_off;
+  const int* offsets;
+  const int* perm;
+  const __nv_bfloat16* act;  // x [T][H] or h [S][I]
+  int act_stride;
+  float* part;               // [KS][S][rows] fp32 split partials (KS > 1)
+  int* counters;             // [MAX groups][RT], self-cleaning
+  __nv_bfloat16* h_out;      // which == 13: [S][I] bf16, row = permuted position p
+  float* y_out;              // which == 2:  [S][H] fp32, row = flat slot s
+  int* status;
+  unsigned long long wait_limit_ns;  // bound on every mbarrier wait
+  int debug_no_copies;               // test hook: the producer issues nothing
+  ExpertTable tab;
+};
+constexpr int STREAM_MAX_GROUPS_SPLIT = 256;  // counter rows available when KS > 1
+
+int stream_grid(int num_sms);
+cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st);
+
+// out[t][c] = bf16(sum_j gates[t*k+j] * y[t*k+j][c])
+cudaError_t launch_finalize(const float* y, const float* gates, int T, int k, int H, __nv_bfloat16* out,
+                            cudaStream_t st);
+
+}  // namespace hmoe

@@ -1,0 +1,163 @@
+// pack.cu -- repack one expert matrix from the logical checkpoint layout into tile layout,
+// and the test-only export of the dequantised operand tiles.
+//
+// Cites: "quant: add native mixed NVFP4/MXFP4 plus NF3 MoE serving",
+// Summary. Expert weights are demultiplexed into compact tier-local storage
+// and repacked for the kernel. The tile layout is described in common.cuh.
+// The pages' own kernel layout ("nf3_2p1", b12x #31) is for SM120 and is not
+// reproduced.
+#include "common.cuh"
+#include "internal.h"
+
+namespace hmoe {
+
+ExpertGeom expert_geom(int H, int I, int fmt) {
+  ExpertGeom g;
+  g.H = H;
+  g.I = I;
+  g.rt13 = 2 * I / TILE_ROWS;
+  g.kb13 = H / TILE_K;
+  g.rt2 = H / TILE_ROWS;
+  g.kb2 = I / TILE_K;
+  g.tile = (size_t)tile_bytes(fmt);
+  g.w13_bytes = (size_t)g.rt13 * g.kb13 * g.tile;
+  g.w2_bytes = (size_t)g.rt2 * g.kb2 * g.tile;
+  g.expert_bytes = g.w13_bytes + g.w2_bytes;
+  return g;
+}
+
+// Logical row of tile-local row r (0..127) of row tile rt.
+__device__ __forceinline__ int logical_row(int which, int I, int rt, int r) {
+  if (which == 2) return rt * TILE_ROWS + r;
+  const int w = r & 15, ch = rt * 64 + (r >> 4) * 8 + (w & 7);
+  return (w < 8) ? ch : I + ch;
+}
+
+__device__ __forceinline__ uint32_t e2m1_word(const uint32_t* d) {
+  // d[0..7]: 4-bit codes. Layout: magnitudes in nibbles 0..7; signs of codes
+  // 0..3 at bits 7,15,23,31 and of codes 4..7 at bits 3,11,19,27.
+  uint32_t w = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    w |= (d[i] & 7u) << (4 * i);
+    w |= (d[4 + i] & 7u) << (16 + 4 * i);
+    w |= ((d[i] >> 3) & 1u) << (8 * i + 7);
+    w |= ((d[4 + i] >> 3) & 1u) << (8 * i + 3);
+  }
+  return w;
+}
+
+__global__ void pack_matrix_kernel(int fmt, int which, const uint8_t* __restrict__ codes,
+                                   const uint8_t* __restrict__ scales, int N, int K, int I,
+                                   uint8_t* __restrict__ dst) {
+  const int KB = K / TILE_K;
+  const int rt = blockIdx.x / KB, kb = blockIdx.x % KB;
+  const int tid = threadIdx.x, rg = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
+  const int slot = rg * 32 + lane;
+  const int R0 = rg * 16 + g, R1 = R0 + 8;
+  const int L0 = logical_row(which, I, rt, R0), L1 = logical_row(which, I, rt, R1);
+  const int k0 = kb * TILE_K + 16 * q;
+  uint8_t* tile = dst + ((size_t)rt * KB + kb) * tile_bytes(fmt);
+  if (fmt == FMT_NVFP4 || fmt == FMT_MXFP4) {
+    uint32_t c0[16], c1[16];
+    const uint8_t* s0 = codes + (size_t)L0 * (K / 2) + k0 / 2;
+    const uint8_t* s1 = codes + (size_t)L1 * (K / 2) + k0 / 2;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      c0[2 * m] = s0[m] & 15u;
+      c0[2 * m + 1] = s0[m] >> 4;
+      c1[2 * m] = s1[m] & 15u;
+      c1[2 * m + 1] = s1[m] >> 4;
+    }
+    uint4 v;
+    v.x = e2m1_word(c0);
+    v.y = e2m1_word(c0 + 8);
+    v.z = e2m1_word(c1);
+    v.w = e2m1_word(c1 + 8);
+    *reinterpret_cast<uint4*>(tile + slot * 16) = v;
+    if (fmt == FMT_NVFP4) {
+      const uint32_t a = scales[(size_t)L0 * (K / 16) + k0 / 16];
+      const uint32_t b = scales[(size_t)L1 * (K / 16) + k0 / 16];
+      *reinterpret_cast<uint16_t*>(tile + 4096 + slot * 2) = (uint16_t)(a | (b << 8));
+    } else if ((q & 1) == 0) {
+      const uint32_t a = scales[(size_t)L0 * (K / 32) + k0 / 32];
+      const uint32_t b = scales[(size_t)L1 * (K / 32) + k0 / 32];
+      *reinterpret_cast<uint16_t*>(tile + 4096 + (rg * 16 + g * 2 + (q >> 1)) * 2) = (uint16_t)(a | (b << 8));
+    }
+  } else {
+    // NF3: 16 codes = 48 bits starting at bit 3*k0 (a byte boundary: 6*q + 24*kb).
+    uint64_t v0 = 0, v1 = 0;
+    const uint8_t* s0 = codes + (size_t)L0 * (3 * K / 8) + 3 * k0 / 8;
+    const uint8_t* s1 = codes + (size_t)L1 * (3 * K / 8) + 3 * k0 / 8;
+#pragma unroll
+    for (int m = 0; m < 6; ++m) {
+      v0 |= (uint64_t)s0[m] << (8 * m);
+      v1 |= (uint64_t)s1[m] << (8 * m);
+    }
+    uint32_t A = 0, B = 0, C = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t a0 = (uint32_t)(v0 >> (3 * j)) & 7u;
+      const uint32_t b0 = (uint32_t)(v0 >> (3 * (8 + j))) & 7u;
+      const uint32_t c0 = (uint32_t)(v1 >> (3 * j)) & 7u;
+      const uint32_t d0 = (uint32_t)(v1 >> (3 * (8 + j))) & 7u;
+      A |= (a0 | ((d0 & 1u) << 3)) << (4 * j);
+      B |= (b0 | (((d0 >> 1) & 1u) << 3)) << (4 * j);
+      C |= (c0 | (((d0 >> 2) & 1u) << 3)) << (4 * j);
+    }
+    *reinterpret_cast<uint32_t*>(tile + slot * 4) = A;
+    *reinterpret_cast<uint32_t*>(tile + 1024 + slot * 4) = B;
+    *reinterpret_cast<uint32_t*>(tile + 2048 + slot * 4) = C;
+    if (q == 0) {
+      const uint16_t* sc = reinterpret_cast<const uint16_t*>(scales);
+      *reinterpret_cast<uint16_t*>(tile + 3072 + R0 * 2) = sc[(size_t)L0 * (K / 64) + kb];
+      *reinterpret_cast<uint16_t*>(tile + 3072 + R1 * 2) = sc[(size_t)L1 * (K / 64) + kb];
+    }
+  }
+}
+
+cudaError_t launch_pack_matrix(int fmt, int which, const void* codes, const void* scales, int N, int K, int I,
+                               uint8_t* dst, cudaStream_t st) {
+  const int tiles = (N / TILE_ROWS) * (K / TILE_K);
+  if (tiles == 0) return cudaSuccess;
+  pack_matrix_kernel<<<tiles, 256, 0, st>>>(fmt, which, static_cast<const uint8_t*>(codes),
+                                            static_cast<const uint8_t*>(scales), N, K, I, dst);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ debug export of operand tiles
+template <int FMT>
+__device__ __forceinline__ void debug_tile(const uint8_t* tile, int rg, int lane, uint32_t* r0, uint32_t* r1) {
+  float a, b;
+  dequant_slot<FMT, true>(tile, rg, lane, r0, r1, &a, &b);
+}
+
+__global__ void debug_dequant_kernel(int fmt, int which, const uint8_t* __restrict__ src, int N, int K, int I,
+                                     __nv_bfloat16* __restrict__ dst) {
+  const int KB = K / TILE_K;
+  const int rt = blockIdx.x / KB, kb = blockIdx.x % KB;
+  const int tid = threadIdx.x, rg = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
+  const uint8_t* tile = src + ((size_t)rt * KB + kb) * tile_bytes(fmt);
+  uint32_t r0[8], r1[8];
+  if (fmt == FMT_NVFP4) debug_tile<FMT_NVFP4>(tile, rg, lane, r0, r1);
+  else if (fmt == FMT_MXFP4) debug_tile<FMT_MXFP4>(tile, rg, lane, r0, r1);
+  else debug_tile<FMT_NF3>(tile, rg, lane, r0, r1);
+  const int L0 = logical_row(which, I, rt, rg * 16 + g), L1 = logical_row(which, I, rt, rg * 16 + g + 8);
+  const int k0 = kb * TILE_K + 16 * q;
+  uint4* d0 = reinterpret_cast<uint4*>(dst + (size_t)L0 * K + k0);
+  uint4* d1 = reinterpret_cast<uint4*>(dst + (size_t)L1 * K + k0);
+  d0[0] = make_uint4(r0[0], r0[1], r0[2], r0[3]);
+  d0[1] = make_uint4(r0[4], r0[5], r0[6], r0[7]);
+  d1[0] = make_uint4(r1[0], r1[1], r1[2], r1[3]);
+  d1[1] = make_uint4(r1[4], r1[5], r1[6], r1[7]);
+}
+
+cudaError_t launch_debug_dequant(int fmt, int which, const uint8_t* src, int N, int K, int I, void* dst,
+                                 cudaStream_t st) {
+  const int tiles = (N / TILE_ROWS) * (K / TILE_K);
+  if (tiles == 0) return cudaSuccess;
+  debug_dequant_kernel<<<tiles, 256, 0, st>>>(fmt, which, src, N, K, I, static_cast<__nv_bfloat16*>(dst));
+  return cudaGetLastError();
+}
+
+}  // namespace hmoe

@@ -1,0 +1,271 @@
+// route.cu -- routing kernels: softmax top-k, renormalised gates, stable counting sort.
+//
+// Cites: "quant: nvfp4_nf3_hybrid -- native serving for mixed NVFP4+NF3 MoE
+// checkpoints", How it works. Both tiers share one route geometry (top-k
+// ids, gates, token permutation, expert offsets). The routing function is
+// not given on the pages. The reading taken is softmax top-k, with the k
+// chosen gates renormalised and ties going to the lower expert id.
+//
+// The sort is deterministic: the slots of an expert keep ascending flat
+// slot index s = t*k + j. No result depends on atomic ordering. Small
+// batches use one CTA. Large batches use three kernels: per-chunk top-k and
+// counts, a column scan over chunks, and a stable placement per chunk.
+#include "common.cuh"
+#include "internal.h"
+
+namespace hmoe {
+
+constexpr int ROUTE_CHUNK_TOKENS = 32;  // tokens per chunk in the large-batch path
+
+// One warp routes one token. Lane l holds logits of experts l, l+32, ...
+// (E <= 512, so at most 16 per lane). Rounds of warp arg-max pick the k
+// winners in descending order, ties to the lower id. Lane r (r < k) returns
+// the r-th winner's id and gate.
+__device__ __forceinline__ void warp_route_token(const float* __restrict__ row, int E, int k, int lane,
+                                                 int* my_id, float* my_gate) {
+  float v[MAX_E / 32];
+#pragma unroll
+  for (int j = 0; j < MAX_E / 32; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = (e < E) ? row[e] : 0.0f;
+  }
+  uint32_t taken = 0;
+  int rid = 0;
+  float rval = 0.0f;
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int be = 0x7FFFFFFF;
+#pragma unroll
+    for (int j = 0; j < MAX_E / 32; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && !((taken >> j) & 1u)) {
+        if (v[j] > bv || (v[j] == bv && e < be)) {
+          bv = v[j];
+          be = e;
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == r) {
+      rid = be;
+      rval = bv;
+    }
+  }
+  const float lmax = __shfl_sync(0xffffffffu, rval, 0);
+  const float z = (lane < k) ? expf(rval - lmax) : 0.0f;
+  float sum = z;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  *my_id = rid;
+  *my_gate = z / sum;
+}
+
+// ------------------------------------------------------------ small batches: one CTA
+// Requires T*k <= 1024. Shared memory: ids[S] + counts[E] + offsets[E+1].
+__global__ void __launch_bounds__(1024) route_small_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                           int* __restrict__ ids, float* __restrict__ gates,
+                                                           int* __restrict__ perm, int* __restrict__ offsets) {
+  extern __shared__ int sm[];
+  const int S = T * k;
+  int* s_ids = sm;
+  int* s_cnt = sm + S;
+  int* s_off = s_cnt + E;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
+  for (int t = warp; t < T; t += nwarps) {
+    int id;
+    float gt;
+    warp_route_token(logits + (size_t)t * E, E, k, lane, &id, &gt);
+    if (lane < k) {
+      ids[t * k + lane] = id;
+      gates[t * k + lane] = gt;
+      s_ids[t * k + lane] = id;
+    }
+  }
+  __syncthreads();
+  for (int s = tid; s < S; s += blockDim.x) atomicAdd(&s_cnt[s_ids[s]], 1);
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive scan of E counts by one warp: lane owns a contiguous run
+    const int per = (E + 31) / 32;
+    const int e0 = lane * per;
+    int local = 0;
+    for (int e = e0; e < min(E, e0 + per); ++e) local += s_cnt[e];
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += n;
+    }
+    int run = incl - local;
+    for (int e = e0; e < min(E, e0 + per); ++e) {
+      s_off[e] = run;
+      run += s_cnt[e];
+    }
+    if (lane == 31) s_off[E] = incl;
+  }
+  __syncthreads();
+  for (int e = tid; e <= E; e += blockDim.x) offsets[e] = s_off[e];
+  for (int s = tid; s < S; s += blockDim.x) {
+    const int e = s_ids[s];
+    int rank = 0;
+    for (int s2 = 0; s2 < s; ++s2) rank += (s_ids[s2] == e);
+    perm[s_off[e] + rank] = s;
+  }
+}
+
+// ------------------------------------------------------------ large batches
+// K1: 8 warps x 4 tokens per CTA = one chunk of 32 tokens. Writes ids,
+// gates and the chunk's per-expert counts (every expert, zeros included).
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                         int* __restrict__ ids, float* __restrict__ gates,
+                                                         int* __restrict__ chunk_cnt) {
+  __shared__ int s_cnt[MAX_E];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  const int t0 = blockIdx.x * ROUTE_CHUNK_TOKENS;
+  for (int i = 0; i < ROUTE_CHUNK_TOKENS / 8; ++i) {
+    const int t = t0 + warp * (ROUTE_CHUNK_TOKENS / 8) + i;
+    if (t >= T) break;
+    int id;
+    float gt;
+    warp_route_token(logits + (size_t)t * E, E, k, lane, &id, &gt);
+    if (lane < k) {
+      ids[t * k + lane] = id;
+      gates[t * k + lane] = gt;
+      atomicAdd(&s_cnt[id], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) chunk_cnt[(size_t)blockIdx.x * E + e] = s_cnt[e];
+}
+
+// K2: one CTA. Column-wise exclusive scan over chunks gives chunk_base; the
+// expert totals are scanned to offsets.
+__global__ void __launch_bounds__(1024) route_scan_kernel(const int* __restrict__ chunk_cnt, int nchunks, int E,
+                                                          int S, int* __restrict__ chunk_base,
+                                                          int* __restrict__ offsets) {
+  __shared__ int s_tot[MAX_E + 1];
+  __shared__ int s_wsum[32];
+  const int tid = threadIdx.x;
+  if (tid < E) {
+    int run = 0;
+    int c = 0;
+    for (; c + 4 <= nchunks; c += 4) {
+      const int a0 = chunk_cnt[(size_t)(c + 0) * E + tid];
+      const int a1 = chunk_cnt[(size_t)(c + 1) * E + tid];
+      const int a2 = chunk_cnt[(size_t)(c + 2) * E + tid];
+      const int a3 = chunk_cnt[(size_t)(c + 3) * E + tid];
+      chunk_base[(size_t)(c + 0) * E + tid] = run;
+      chunk_base[(size_t)(c + 1) * E + tid] = run + a0;
+      chunk_base[(size_t)(c + 2) * E + tid] = run + a0 + a1;
+      chunk_base[(size_t)(c + 3) * E + tid] = run + a0 + a1 + a2;
+      run += a0 + a1 + a2 + a3;
+    }
+    for (; c < nchunks; ++c) {
+      const int a = chunk_cnt[(size_t)c * E + tid];
+      chunk_base[(size_t)c * E + tid] = run;
+      run += a;
+    }
+    s_tot[tid] = run;
+  }
+  __syncthreads();
+  // block exclusive scan of s_tot[0..E)
+  const int lane = tid & 31, warp = tid >> 5;
+  const int v = (tid < E) ? s_tot[tid] : 0;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += n;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < (int)(blockDim.x >> 5)) ? s_wsum[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += n;
+    }
+    s_wsum[lane] = wi - w;
+  }
+  __syncthreads();
+  if (tid < E) offsets[tid] = s_wsum[warp] + incl - v;
+  if (tid == 0) offsets[E] = S;
+}
+
+// K3: stable placement of one chunk's slots. Slots are taken in rounds of
+// 256 in ascending order. Inside a round, a warp ranks equal experts with
+// match_any, and earlier warps and rounds are added from shared counts.
+__global__ void __launch_bounds__(256) route_place_kernel(const int* __restrict__ ids, int T, int E, int k,
+                                                          const int* __restrict__ chunk_base,
+                                                          const int* __restrict__ offsets,
+                                                          int* __restrict__ perm) {
+  __shared__ int s_run[MAX_E];
+  __shared__ int s_w[8][MAX_E];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c = blockIdx.x;
+  const int s_begin = c * ROUTE_CHUNK_TOKENS * k;
+  const int s_end = min(T * k, s_begin + ROUTE_CHUNK_TOKENS * k);
+  for (int e = tid; e < E; e += 256) {
+    s_run[e] = 0;
+    for (int w = 0; w < 8; ++w) s_w[w][e] = 0;
+  }
+  __syncthreads();
+  for (int base = s_begin; base < s_end; base += 256) {
+    const int s = base + tid;
+    const bool valid = s < s_end;
+    const int e = valid ? ids[s] : -1 - lane;  // distinct dummies never match real ids
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank_w = __popc(peers & ((1u << lane) - 1u));
+    if (valid && rank_w == 0) s_w[warp][e] = __popc(peers);
+    __syncthreads();
+    if (valid) {
+      int rank = s_run[e] + rank_w;
+      for (int w = 0; w < warp; ++w) rank += s_w[w][e];
+      perm[offsets[e] + chunk_base[(size_t)c * E + e] + rank] = s;
+    }
+    __syncthreads();
+    for (int ee = tid; ee < E; ee += 256) {
+      int add = 0;
+      for (int w = 0; w < 8; ++w) {
+        add += s_w[w][ee];
+        s_w[w][ee] = 0;
+      }
+      s_run[ee] += add;
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------ launcher
+int route_chunks(int T) { return (T + ROUTE_CHUNK_TOKENS - 1) / ROUTE_CHUNK_TOKENS; }
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int* ids, float* gates, int* perm,
+                         int* offsets, int* chunk_cnt, int* chunk_base, cudaStream_t st) {
+  const int S = T * k;
+  if (S <= 1024) {
+    const size_t smem = (size_t)(S + 2 * E + 1) * sizeof(int);
+    route_small_kernel<<<1, 1024, smem, st>>>(logits, T, E, k, ids, gates, perm, offsets);
+    return cudaGetLastError();
+  }
+  const int nch = route_chunks(T);
+  route_topk_kernel<<<nch, 256, 0, st>>>(logits, T, E, k, ids, gates, chunk_cnt);
+  route_scan_kernel<<<1, 1024, 0, st>>>(chunk_cnt, nch, E, S, chunk_base, offsets);
+  route_place_kernel<<<nch, 256, 0, st>>>(ids, T, E, k, chunk_base, offsets, perm);
+  return cudaGetLastError();
+}
+
+}  // namespace hmoe

@@ -1,0 +1,375 @@
+// stream.cu -- the weight-streaming grouped GEMM (the M <= 8 decode path; valid at any T).
+//
+// Cites: "quant: nvfp4_nf3_hybrid -- native serving for mixed NVFP4+NF3 MoE
+// checkpoints", How it works. An M<=8 decode path works on the top-k routed
+// experts directly. Both tiers add into one shared output, and the second
+// launch accumulates instead of zeroing. Here each routed expert's packed
+// weights are streamed from HBM once per group of up to 8 of its tokens.
+//
+// Work item = (token group, row tile of 128 weight rows, k-split). A token
+// group is up to 8 consecutive permuted slots of one expert, so at T <= 8
+// there is exactly one group per touched expert. Persistent CTAs take
+// items in a fixed stride. One producer lane streams each item's packed
+// tiles and the group's activation rows into a 4-stage shared-memory ring
+// with 1D bulk copies (TMA engine). Eight consumer warps, one per 16-row
+// group, dequantise in registers (prmt byte-table lookups, bf16x2 scale
+// multiply) and issue m16n8k16 bf16 MMAs with the tokens as the N=8 side.
+// Accumulation is fp32.
+//
+// Split-K partials are combined without atomics on data. Each split writes
+// its partial. The last split to arrive at a per-(group, row tile) counter
+// sums all partials in split order, which is deterministic, and runs the
+// epilogue:
+//   W13: h[p][c] = bf16(silu(g13 * gate) * (g13 * up)), SwiGLU fused.
+//   W2:  y[s][r] = g2 * sum, fp32, indexed by the flat slot s.
+// The finalize kernel then applies the gates and sums each token's k slots
+// in slot order.
+#include "common.cuh"
+#include "internal.h"
+
+namespace hmoe {
+
+constexpr int SK_CONSUMER_WARPS = 8;
+constexpr int SK_THREADS = (SK_CONSUMER_WARPS + 1) * 32;
+constexpr int SK_STAGES = 4;
+constexpr int SK_MAX_KBS = 4;
+constexpr int SK_XROW = SK_MAX_KBS * 128 + 16;            // padded token row, bytes
+constexpr int SK_W_BYTES = SK_MAX_KBS * 4608;
+constexpr int SK_X_BYTES = 8 * SK_XROW;
+constexpr int SK_STAGE_BYTES = SK_W_BYTES + SK_X_BYTES;
+constexpr int SK_SMEM_DATA = SK_STAGES * SK_STAGE_BYTES;
+constexpr int SK_SMEM_BYTES = SK_SMEM_DATA + 2 * SK_STAGES * 8 + (MAX_E + 1) * 4 + 16;
+static_assert(SK_STAGE_BYTES % 16 == 0, "stage alignment");
+
+struct SkItem {
+  int e, p0, n, rt, ks, grp;
+};
+
+__device__ __forceinline__ int expert_fmt(const StreamParams& p, int e) {
+  return (p.tab.loc[e] & LOC_NF3) ? FMT_NF3 : p.kept_fmt;
+}
+
+__device__ __forceinline__ SkItem decode_item(const StreamParams& p, const int* s_gstart, int i) {
+  SkItem it;
+  it.ks = i % p.KS;
+  const int r = i / p.KS;
+  it.rt = r % p.RT;
+  it.grp = r / p.RT;
+  int lo = 0, hi = p.E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_gstart[mid] <= it.grp) lo = mid; else hi = mid;
+  }
+  it.e = lo;
+  const int c = it.grp - s_gstart[lo];
+  const int o0 = p.offsets[lo], ne = p.offsets[lo + 1] - o0;
+  it.p0 = o0 + c * p.group_tokens;
+  it.n = min(p.group_tokens, ne - c * p.group_tokens);
+  return it;
+}
+
+// Output of one thread's 2 rows x 2 tokens (v[0],v[1]: row R0; v[2],v[3]: row R1).
+__device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it, int rg, int g, int q,
+                                        const float* v) {
+  const int S = p.T * p.topk;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int c = 2 * q + h;
+    if (c >= it.n) continue;
+    const int pp = it.p0 + c;
+    if (p.which == 13) {
+      const float gsc = p.tab.g13[it.e];
+      const int ch = it.rt * 64 + rg * 8 + g;
+      const float gate = v[h] * gsc, up = v[2 + h] * gsc;
+      p.h_out[(size_t)pp * p.I + ch] = __float2bfloat16_rn(silu_f(gate) * up);
+    } else {
+      const float gsc = p.tab.g2[it.e];
+      const int s = p.perm[pp];
+      if (s < 0 || s >= S) {
+        set_status(p.status, DEV_BAD_ROUTE);
+        continue;
+      }
+      const int row = it.rt * 128 + rg * 16 + g;
+      p.y_out[(size_t)s * p.H + row] = v[h] * gsc;
+      p.y_out[(size_t)s * p.H + row + 8] = v[2 + h] * gsc;
+    }
+  }
+}
+
+template <int FMT>
+__device__ __forceinline__ void sk_consume_kblock(const uint8_t* tile, const uint8_t* xrow, int rg, int lane,
+                                                  float* acc) {
+  const uint4 xa = *reinterpret_cast<const uint4*>(xrow);
+  const uint4 xb = *reinterpret_cast<const uint4*>(xrow + 16);
+  const uint32_t xr[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+  uint32_t r0[8], r1[8];
+  float sc0, sc1;
+  dequant_slot<FMT, false>(tile, rg, lane, r0, r1, &sc0, &sc1);
+  if constexpr (FMT == FMT_NF3) {
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int s = 0; s < 4; ++s) mma_bf16_16816(d, r0[2 * s], r1[2 * s], r0[2 * s + 1], r1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
+    acc[0] = fmaf(sc0, d[0], acc[0]);
+    acc[1] = fmaf(sc0, d[1], acc[1]);
+    acc[2] = fmaf(sc1, d[2], acc[2]);
+    acc[3] = fmaf(sc1, d[3], acc[3]);
+  } else {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) mma_bf16_16816(acc, r0[2 * s], r1[2 * s], r0[2 * s + 1], r1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
+  }
+}
+
+__global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid_constant__ StreamParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SK_SMEM_DATA);
+  uint64_t* empty = full + SK_STAGES;
+  int* s_gstart = reinterpret_cast<int*>(empty + SK_STAGES);
+  volatile int* s_flags = s_gstart + MAX_E + 1;  // [0] abort, [1] last-arriver, [2] route error
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < SK_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], SK_CONSUMER_WARPS);
+    }
+    fence_mbar_init();
+    s_flags[0] = 0;
+    s_flags[1] = 0;
+    s_flags[2] = 0;
+  }
+  // Group prefix over experts of the selected tiers, from the caller's offsets.
+  if (warp == 0) {
+    const int S = p.T * p.topk;
+    bool bad = (p.offsets[0] != 0) || (p.offsets[p.E] != S);
+    int run = 0;
+    for (int e0 = 0; e0 < p.E; e0 += 32) {
+      const int e = e0 + lane;
+      int ng = 0;
+      if (e < p.E) {
+        const int ne = p.offsets[e + 1] - p.offsets[e];
+        if (ne < 0) bad = true;
+        const bool nf3 = (p.tab.loc[e] & LOC_NF3) != 0;
+        const bool sel = nf3 ? (p.tier_mask & 2) : (p.tier_mask & 1);
+        ng = (sel && ne > 0) ? (ne + p.group_tokens - 1) / p.group_tokens : 0;
+      }
+      int incl = ng;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int nb = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += nb;
+      }
+      if (e < p.E) s_gstart[e] = run + incl - ng;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (p.KS > 1 && run > STREAM_MAX_GROUPS_SPLIT) bad = true;
+    if (lane == 0) {
+      s_gstart[p.E] = bad ? 0 : run;
+      if (bad) {
+        s_flags[2] = 1;
+        if (blockIdx.x == 0) set_status(p.status, DEV_BAD_ROUTE);
+      }
+    }
+    if (bad)
+      for (int e = lane; e < p.E; e += 32) s_gstart[e] = 0;
+  }
+  __syncthreads();
+
+  const int n_items = s_gstart[p.E] * p.RT * p.KS;
+  const int kbi = p.KB / p.KS;
+  const int nst = kbi / p.kbs;
+  const int S = p.T * p.topk;
+
+  if (warp == SK_CONSUMER_WARPS) {
+    // ------------------------------------------------ producer
+    if (lane == 0 && !p.debug_no_copies) {
+      const uint64_t pol = l2_policy_evict_first();
+      int slot = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      bool aborted = false;
+      for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x) {
+        const SkItem it = decode_item(p, s_gstart, i);
+        const int fmt = expert_fmt(p, it.e);
+        const size_t tb = (size_t)tile_bytes(fmt);
+        const uint8_t* base = (fmt == FMT_NF3 ? p.nf3_buf : p.kept_buf) +
+                              (size_t)(p.tab.loc[it.e] & 0x7FFF) *
+                                  (fmt == FMT_NF3 ? p.nf3_expert_bytes : p.kept_expert_bytes) +
+                              (p.which == 2 ? (fmt == FMT_NF3 ? p.nf3_w2_off : p.kept_w2_off) : 0);
+        int rows[8];
+        for (int j = 0; j < it.n; ++j) {
+          if (p.which == 13) {
+            int s = p.perm[it.p0 + j];
+            if (s < 0 || s >= S) {
+              set_status(p.status, DEV_BAD_ROUTE);
+              s = 0;
+            }
+            rows[j] = s / p.topk;
+          } else {
+            rows[j] = it.p0 + j;
+          }
+        }
+        for (int st = 0; st < nst; ++st) {
+          if (!mbar_wait(&empty[slot], ph ^ 1u, s_flags, p.wait_limit_ns)) {
+            aborted = true;
+            s_flags[0] = 1;
+            set_status(p.status, DEV_TIMEOUT);
+            break;
+          }
+          const int kbA = it.ks * kbi + st * p.kbs;
+          const uint32_t wbytes = (uint32_t)(p.kbs * tb);
+          const uint32_t xbytes = (uint32_t)(p.kbs * 128);
+          uint8_t* sw = smem + slot * SK_STAGE_BYTES;
+          uint8_t* sx = sw + SK_W_BYTES;
+          mbar_arrive_expect_tx(&full[slot], wbytes + (uint32_t)it.n * xbytes);
+          bulk_g2s_stream(sw, base + ((size_t)it.rt * p.KB + kbA) * tb, wbytes, &full[slot], pol);
+          for (int j = 0; j < it.n; ++j)
+            bulk_g2s(sx + j * SK_XROW, p.act + (size_t)rows[j] * p.act_stride + (size_t)kbA * 64, xbytes,
+                     &full[slot]);
+          ++issued;
+          if (++slot == SK_STAGES) {
+            slot = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (aborted) {
+        // Drain copies still in flight before the CTA may exit (bounded).
+        volatile int never = 0;
+        for (int b = 0; b < SK_STAGES && b < issued; ++b) {
+          if (--slot < 0) {
+            slot = SK_STAGES - 1;
+            ph ^= 1u;
+          }
+          mbar_wait(&full[slot], ph, &never, p.wait_limit_ns);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------ consumers
+    const int rg = warp, g = lane >> 2, q = lane & 3;
+    int slot = 0;
+    uint32_t ph = 0;
+    bool aborted = false;
+    for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+      const SkItem it = decode_item(p, s_gstart, i);
+      const int fmt = expert_fmt(p, it.e);
+      const int tb = tile_bytes(fmt);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int st = 0; st < nst; ++st) {
+        if (!aborted) {
+          if (!mbar_wait(&full[slot], ph, s_flags, p.wait_limit_ns)) {
+            aborted = true;
+            s_flags[0] = 1;
+            set_status(p.status, DEV_TIMEOUT);
+          }
+        }
+        if (!aborted) {
+          const uint8_t* sw = smem + slot * SK_STAGE_BYTES;
+          const uint8_t* sx = sw + SK_W_BYTES + g * SK_XROW + q * 32;
+          for (int j = 0; j < p.kbs; ++j) {
+            if (fmt == FMT_NVFP4)
+              sk_consume_kblock<FMT_NVFP4>(sw + j * tb, sx + j * 128, rg, lane, acc);
+            else if (fmt == FMT_MXFP4)
+              sk_consume_kblock<FMT_MXFP4>(sw + j * tb, sx + j * 128, rg, lane, acc);
+            else
+              sk_consume_kblock<FMT_NF3>(sw + j * tb, sx + j * 128, rg, lane, acc);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (++slot == SK_STAGES) {
+          slot = 0;
+          ph ^= 1u;
+        }
+      }
+      // ---------------- epilogue
+      if (p.KS == 1) {
+        if (!aborted) sk_emit(p, it, rg, g, q, acc);
+        continue;
+      }
+      const int rowA = it.rt * 128 + rg * 16 + g, rowB = rowA + 8;
+      float* pb = p.part + (size_t)it.ks * S * p.rows;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = 2 * q + h;
+        if (c < it.n) {
+          pb[(size_t)(it.p0 + c) * p.rows + rowA] = acc[h];
+          pb[(size_t)(it.p0 + c) * p.rows + rowB] = acc[2 + h];
+        }
+      }
+      __threadfence();
+      named_bar_sync(1, SK_CONSUMER_WARPS * 32);
+      if (tid == 0) {
+        const int old = atomicAdd(&p.counters[it.grp * p.RT + it.rt], 1);
+        s_flags[1] = (old == p.KS - 1);
+      }
+      named_bar_sync(1, SK_CONSUMER_WARPS * 32);
+      if (s_flags[1]) {
+        __threadfence();
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k2 = 0; k2 < p.KS; ++k2) {
+          const float* pk = p.part + (size_t)k2 * S * p.rows;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int c = 2 * q + h;
+            if (c < it.n) {
+              const float a = (k2 == it.ks) ? acc[h] : __ldcg(pk + (size_t)(it.p0 + c) * p.rows + rowA);
+              const float b = (k2 == it.ks) ? acc[2 + h] : __ldcg(pk + (size_t)(it.p0 + c) * p.rows + rowB);
+              sum[h] += a;
+              sum[2 + h] += b;
+            }
+          }
+        }
+        if (!aborted) sk_emit(p, it, rg, g, q, sum);
+        if (tid == 0) p.counters[it.grp * p.RT + it.rt] = 0;
+      }
+    }
+  }
+  __syncthreads();
+}
+
+int stream_grid(int num_sms) { return 2 * num_sms; }
+
+cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(stream_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SK_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  if (p.kbs < 1 || p.kbs > SK_MAX_KBS || p.group_tokens < 1 || p.group_tokens > 8) return cudaErrorInvalidValue;
+  stream_gemm_kernel<<<grid, SK_THREADS, SK_SMEM_BYTES, st>>>(p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ finalize
+__global__ void finalize_kernel(const float* __restrict__ y, const float* __restrict__ gates, int T, int k, int H,
+                                __nv_bfloat16* __restrict__ out) {
+  const int half = H / 2;
+  const long long n = (long long)T * half;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i / half), c = (int)(i % half) * 2;
+    float a = 0.f, b = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const float gt = gates[t * k + j];
+      const float2 v = *reinterpret_cast<const float2*>(y + (size_t)(t * k + j) * H + c);
+      a = fmaf(gt, v.x, a);
+      b = fmaf(gt, v.y, b);
+    }
+    *reinterpret_cast<__nv_bfloat162*>(out + (size_t)t * H + c) = __floats2bfloat162_rn(a, b);
+  }
+}
+
+cudaError_t launch_finalize(const float* y, const float* gates, int T, int k, int H, __nv_bfloat16* out,
+                            cudaStream_t st) {
+  const long long n = (long long)T * (H / 2);
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  const long long blocks = (n + threads - 1) / threads;
+  finalize_kernel<<<(int)(blocks < 4096 ? blocks : 4096), threads, 0, st>>>(y, gates, T, k, H, out);
+  return cudaGetLastError();
+}
+
+}  // namespace hmoe

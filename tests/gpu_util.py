@@ -1,0 +1,57 @@
+"""Helpers for the GPU tests: move a synthetic layer to the device, run the library, compare with the oracle."""
+
+import numpy as np
+import torch
+
+import nf3_moe_gb300 as hm
+import synth
+from oracle import layer as olayer
+
+# Per token row: max |out - ref| <= REL_TOL * max |ref|, with fp32 accumulation.
+REL_TOL = 2e-2
+
+
+def device_experts(L):
+    """Expert tuples for hmoe_pack_weights. The tensors must already be on the GPU."""
+    out = []
+    for ex in L.experts:
+        c13, s13, g13 = ex["w13"]
+        c2, s2, g2 = ex["w2"]
+        out.append((c13, s13, g13, c2, s2, g2))
+    return out
+
+
+def build(L, max_tokens):
+    bm = None if L.bit_map is None else [int(b) for b in L.bit_map]
+    return hm.HybridMoELayer(L.H, L.I, L.E, L.topk, bm, device_experts(L), kept_format=L.kept_format,
+                             max_tokens=max_tokens)
+
+
+def run(moe, x, logits, **kw):
+    ids, gates, perm, offsets = moe.plan(logits)
+    out = torch.empty((x.shape[0], moe.H), dtype=torch.bfloat16, device=x.device)
+    hm.hmoe_forward(moe.layer, x, ids, gates, perm, offsets, out, moe.ws, **kw)
+    torch.cuda.synchronize()
+    hm.hmoe_check_device_status(moe.ws)
+    return out, (ids, gates, perm, offsets)
+
+
+def oracle_out(L, x, ids, gates, tokens=None, cols=None):
+    xf = x.float().cpu().numpy().astype(np.float64)
+    return olayer.moe_forward(xf, ids.cpu().numpy(), gates.cpu().numpy().astype(np.float64), L.expert_numpy,
+                              L.H, L.I, tokens=tokens, cols=cols)
+
+
+def assert_rows_close(got, ref, tol=REL_TOL):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape
+    err = np.abs(got - ref).max(axis=1)
+    scale = np.abs(ref).max(axis=1)
+    worst = float((err / np.maximum(scale, 1e-30)).max()) if len(err) else 0.0
+    assert np.all(err <= tol * scale), f"row-relative error {worst:.3e} > {tol}"
+    return worst
+
+
+def layer_on(device, **kw):
+    return synth.make_layer(device=device, **kw)

@@ -1,0 +1,71 @@
+"""CPU tests of the C ABI surface: the library loads, exports every symbol include/hmoe.h
+declares, and validates arguments on the host (no compute call needs a GPU here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nf3_moe_gb300 import _lib, build
+    if not os.path.exists(_lib.LIB_PATH):
+        build.build()
+    return _lib.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "hmoe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(hmoe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from nf3_moe_gb300 import _lib
+    declared = _declared()
+    assert len(declared) >= 13
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(declared) == set(_lib.EXPORTS)
+
+
+def test_version_and_last_error(lib):
+    assert lib.hmoe_version() >= 100
+    assert isinstance(lib.hmoe_last_error(), bytes)
+
+
+def test_host_validation_without_gpu(lib):
+    import nf3_moe_gb300 as hm
+    d = hm.LayerDesc(6144, 2048, 256, 8, hm.FMT_NVFP4)
+    kept, nf3 = hm.hmoe_packed_size(d, [4] * 64 + [3] * 192)
+    assert kept == 64 * 21_233_664 and nf3 == 192 * 15_335_424
+    dm = hm.LayerDesc(6144, 2048, 256, 8, hm.FMT_MXFP4)
+    assert hm.hmoe_packed_size(dm, [4] * 64 + [3] * 192)[0] == 64 * 20_054_016
+    assert hm.hmoe_packed_size(hm.LayerDesc(2048, 768, 128, 8, 4), None) == (128 * 2_654_208, 0)
+    sizes = [hm.hmoe_workspace_size(d, t) for t in (0, 1, 8, 9, 4096)]
+    assert sizes == sorted(sizes)
+    for bad, status in [(hm.LayerDesc(6144, 2048, 256, 8, 7), -1), (hm.LayerDesc(6100, 2048, 256, 8, 4), -2),
+                        (hm.LayerDesc(6144, 2000, 256, 8, 4), -2), (hm.LayerDesc(6144, 2048, 600, 8, 4), -2),
+                        (hm.LayerDesc(6144, 2048, 4, 8, 4), -2), (hm.LayerDesc(0, 2048, 4, 2, 4), -1)]:
+        with pytest.raises(hm.HmoeError) as ei:
+            hm.hmoe_workspace_size(bad, 8)
+        assert ei.value.status == status
+    with pytest.raises(hm.HmoeError) as ei:
+        hm.hmoe_packed_size(d, [4] * 255 + [2])
+    assert ei.value.status == -4
+
+
+def test_null_handles_rejected(lib):
+    assert lib.hmoe_plan_routes(None, None, 1, None, None, None, None, None, 0, None) == -1
+    assert lib.hmoe_forward(None, None, 1, None, None, None, None, None, None, 0, None) == -1
+    assert lib.hmoe_debug_dequant(None, 0, 13, None, None) == -1
+    assert lib.hmoe_check_device_status(None, 0, None) == -1
+    desc = __import__("nf3_moe_gb300")._lib.LayerDesc(256, 128, 8, 2, 4)
+    h = ctypes.c_void_p()
+    assert lib.hmoe_pack_weights(ctypes.byref(desc), None, None, None, None, None, ctypes.byref(h)) == -1
+    assert b"NULL" in lib.hmoe_last_error()
+    lib.hmoe_layer_destroy(None)

@@ -1,0 +1,140 @@
+"""GPU layer parity against the oracle, plus the invariances the method has.
+
+Tolerance: per token row, max|out - ref| <= 2e-2 * max|ref| (fp32 accumulation).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import nf3_moe_gb300 as hm
+import synth
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    L = synth.tiny_layer(device="cuda")
+    return L, U.build(L, 256)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 9, 37, 200])
+@pytest.mark.parametrize("order", [hm.TIERS_ONE_LAUNCH, hm.TIERS_KEPT_FIRST, hm.TIERS_NF3_FIRST])
+def test_tiny_layer_parity(tiny, T, order):
+    L, moe = tiny
+    x = synth.gen_x(T, L.H, seed=T, device="cuda")
+    logits = synth.gen_logits(T, L.E, seed=T, device="cuda")
+    out, (ids, gates, _, _) = U.run(moe, x, logits, tier_order=order)
+    U.assert_rows_close(out.float().cpu().numpy(), U.oracle_out(L, x, ids, gates))
+
+
+def test_tier_order_is_bitwise_invariant(tiny):
+    L, moe = tiny
+    for T in (4, 37):
+        x = synth.gen_x(T, L.H, device="cuda")
+        logits = synth.gen_logits(T, L.E, device="cuda")
+        outs = [U.run(moe, x, logits, tier_order=o)[0] for o in (0, 1, 2)]
+        assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+def test_token_order_is_bitwise_invariant(tiny):
+    L, moe = tiny
+    for T in (8, 37):
+        x = synth.gen_x(T, L.H, device="cuda")
+        logits = synth.gen_logits(T, L.E, device="cuda")
+        p = torch.randperm(T, generator=torch.Generator().manual_seed(T)).cuda()
+        a, _ = U.run(moe, x, logits)
+        b, _ = U.run(moe, x[p].contiguous(), logits[p].contiguous())
+        assert torch.equal(a[p], b)
+
+
+def test_stream_path_equals_decode_path_tolerance(tiny):
+    L, moe = tiny
+    x = synth.gen_x(8, L.H, device="cuda")
+    logits = synth.gen_logits(8, L.E, device="cuda")
+    a, (ids, gates, _, _) = U.run(moe, x, logits)
+    ref = U.oracle_out(L, x, ids, gates)
+    U.assert_rows_close(a.float().cpu().numpy(), ref)
+
+
+def test_top1_single_expert_and_repeat_calls(tiny):
+    """top-1 (gate = 1) reduces to one dense expert; repeated calls are bitwise stable."""
+    Lh = synth.make_layer(256, 128, 8, 1, kept_ids=[1, 5], device="cuda")
+    moe = U.build(Lh, 64)
+    x = synth.gen_x(16, 256, device="cuda")
+    logits = synth.gen_logits(16, 8, device="cuda")
+    a, (ids, gates, _, _) = U.run(moe, x, logits)
+    assert torch.all(gates == 1.0)
+    U.assert_rows_close(a.float().cpu().numpy(), U.oracle_out(Lh, x, ids, gates))
+    b, _ = U.run(moe, x, logits)
+    assert torch.equal(a, b)
+
+
+def test_all_nvfp4_bitmap_equals_uniform_layer():
+    H, I, E, k = 256, 128, 8, 2
+    hybrid = synth.make_layer(H, I, E, k, kept_ids=list(range(E)), device="cuda")
+    uniform = synth.make_layer(H, I, E, k, uniform=True, device="cuda")
+    mh, mu = U.build(hybrid, 64), U.build(uniform, 64)
+    for T in (3, 40):
+        x = synth.gen_x(T, H, device="cuda")
+        logits = synth.gen_logits(T, E, device="cuda")
+        a, _ = U.run(mh, x, logits)
+        b, _ = U.run(mu, x, logits)
+        assert torch.equal(a, b)
+
+
+def test_all_nf3_layer():
+    L = synth.make_layer(256, 128, 8, 2, kept_ids=[], device="cuda")
+    moe = U.build(L, 16)
+    x = synth.gen_x(6, 256, device="cuda")
+    logits = synth.gen_logits(6, 8, device="cuda")
+    out, (ids, gates, _, _) = U.run(moe, x, logits)
+    U.assert_rows_close(out.float().cpu().numpy(), U.oracle_out(L, x, ids, gates))
+
+
+@pytest.mark.parametrize("T", [1, 8, 64])
+def test_mxfp4_kept_tier(T):
+    L = synth.make_layer(512, 256, 16, 4, kept_ids=[0, 3, 6, 9], kept_format=synth.FMT_MXFP4, device="cuda")
+    moe = U.build(L, 64)
+    x = synth.gen_x(T, L.H, device="cuda")
+    logits = synth.gen_logits(T, L.E, device="cuda")
+    out, (ids, gates, _, _) = U.run(moe, x, logits)
+    U.assert_rows_close(out.float().cpu().numpy(), U.oracle_out(L, x, ids, gates))
+
+
+@pytest.mark.parametrize("T", [1, 8, 128])
+def test_uniform_nvfp4_shape(T):
+    """The uniform single-tier NVFP4 layer shape (H=2048, I=768, E=128, top-8)."""
+    L = synth.make_layer(**synth.UNIFORM_128, uniform=True, device="cuda")
+    moe = U.build(L, 128)
+    x = synth.gen_x(T, L.H, device="cuda")
+    logits = synth.gen_logits(T, L.E, device="cuda")
+    out, (ids, gates, _, _) = U.run(moe, x, logits)
+    tokens = list(range(min(T, 6)))
+    ref = U.oracle_out(L, x, ids, gates, tokens=tokens)
+    U.assert_rows_close(out[tokens].float().cpu().numpy(), ref)
+
+
+@pytest.fixture(scope="module")
+def hybrid256():
+    L = synth.make_layer(**synth.HYBRID_256, kept=64, device="cuda")
+    return L, U.build(L, 8)
+
+
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
+def test_full_size_hybrid_decode(hybrid256, T):
+    """256-expert hybrid layer (H=6144, I=2048, top-8; 64 NVFP4 + 192 NF3) at M <= 8.
+    The oracle runs on sampled tokens; every token is checked at M <= 2."""
+    L, moe = hybrid256
+    x = synth.gen_x(T, L.H, seed=100 + T, device="cuda")
+    logits = synth.gen_logits(T, L.E, seed=100 + T, device="cuda")
+    out, (ids, gates, _, _) = U.run(moe, x, logits)
+    tokens = list(range(T)) if T <= 2 else [0, T - 1]
+    ref = U.oracle_out(L, x, ids, gates, tokens=tokens)
+    U.assert_rows_close(out[tokens].float().cpu().numpy(), ref)
+    # every row: finite, and the tier order does not change a bit
+    assert torch.isfinite(out.float()).all()
+    out2, _ = U.run(moe, x, logits, tier_order=hm.TIERS_NF3_FIRST)
+    assert torch.equal(out, out2)

@@ -1,0 +1,463 @@
+#!/usr/bin/env python
+"""Benchmark of the hybrid W4A16 MoE layer on GB300.
+
+Headline workload: decode on the 256-expert hybrid layer. H=6144, I=2048,
+E=256, top-8 softmax routing. The 64 experts with the largest weight norm
+are NVFP4 and the other 192 are NF3. There are M=8 tokens per batch. A step
+is one pass of the hot path over one batch: hmoe_plan_routes (top-k, gates,
+permutation, offsets) and then hmoe_forward (both GEMMs, SwiGLU, gate-weighted
+sum, bf16 output).
+
+value = HBM GB/s. The bytes are the packed weights and scales of the experts
+a batch touches, counted once per expert from the routed ids, divided by the
+device time of the step. The same line reports:
+- a per-M table (M = 1, 2, 4, 8; us per layer and GB/s);
+- the prefill point (M = 4096, skewed routing): tokens/s, TFLOP/s and the
+  fraction of the bf16 peak;
+- the dominant kernel's roofline;
+- the CPU oracle's time on a bounded sample.
+
+L2 hygiene: the packed layer is replicated 4 times (4 x 4.30 GB). Step i uses
+replica i % 4 and batch i % 4, so no step finds its weights in the 129 MB L2.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+N > 1 runs one independent replica per GPU (the layer does not shard:
+replicas only). It is launched through torch.distributed.run.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "hybrid MoE layer µs & HBM GB/s at M≤8; tokens/s & % bf16 peak at M=4096"
+SHAPE = synth.HYBRID_256
+KEPT = 64
+REPLICAS = 4
+FMT_NF3, FMT_NVFP4 = 3, 4
+BYTES_PER_EXPERT = {4: 21_233_664, 5: 20_054_016, 3: 15_335_424}
+W13_BYTES = {4: 14_155_776, 5: 13_369_344, 3: 10_223_616}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the GPU is under load."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.idx)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ helpers
+def touched(ids_cpu, fmts):
+    es = np.unique(np.asarray(ids_cpu).reshape(-1))
+    total = sum(BYTES_PER_EXPERT[fmts[e]] for e in es)
+    w13 = sum(W13_BYTES[fmts[e]] for e in es)
+    return int(total), int(w13), len(es)
+
+
+def make_layer(device):
+    return synth.make_layer(**SHAPE, kept=KEPT, device=device)
+
+
+def expert_tuples(L):
+    return [(e["w13"][0], e["w13"][1], e["w13"][2], e["w2"][0], e["w2"][1], e["w2"][2]) for e in L.experts]
+
+
+def oracle_sample(L_host_experts, H, I, x_row, ids_row, gates_row):
+    """The oracle on one token. Returns seconds and bytes of its experts."""
+    from oracle import layer as olayer
+    fmts = {e: L_host_experts[e]["fmt"] for e in L_host_experts}
+    t0 = time.perf_counter()
+    olayer.moe_forward(x_row[None, :].astype(np.float64), ids_row[None, :], gates_row[None, :].astype(np.float64),
+                       lambda e: L_host_experts[e], H, I)
+    dt = time.perf_counter() - t0
+    return dt, sum(BYTES_PER_EXPERT[fmts[int(e)]] for e in np.unique(ids_row))
+
+
+def host_experts(L, ids):
+    return {int(e): L.expert_numpy(int(e)) for e in np.unique(ids)}
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    L = make_layer(dev)
+    M = args.m
+    x = synth.gen_x(M, SHAPE["H"], seed=1000, device=dev)
+    logits = synth.gen_logits(M, SHAPE["E"], seed=1000, device=dev)
+    from oracle import route as oroute
+    ids, gates, _, _ = oroute.plan(logits.cpu().numpy(), SHAPE["topk"])
+    exps = host_experts(L, ids[:1])
+    xr = x.float().cpu().numpy()[0]
+    del L
+    for _ in range(args.warmup):
+        oracle_sample(exps, SHAPE["H"], SHAPE["I"], xr, ids[0], gates[0])
+    tot_t, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, b = oracle_sample(exps, SHAPE["H"], SHAPE["I"], xr, ids[0], gates[0])
+        tot_t += dt
+        tot_b += b
+    value = tot_b / tot_t / 1e9
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"one token of an M={M} batch per step (its {len(exps)} experts dequantised in float64 and "
+              f"multiplied), NumPy on the host")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"hybrid MoE decode (oracle), H=6144 I=2048 E=256 top-8, 64 NVFP4 + 192 NF3, M={M}",
+                   "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world):
+    import nf3_moe_gb300 as hm
+    from nf3_moe_gb300 import _lib
+    if not os.path.exists(_lib.LIB_PATH):
+        from nf3_moe_gb300 import build
+        build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    H, I, E, k = SHAPE["H"], SHAPE["I"], SHAPE["E"], SHAPE["topk"]
+    pk = peaks()
+
+    L = make_layer(dev)
+    bit_map = [int(b) for b in L.bit_map]
+    experts = expert_tuples(L)
+    desc = hm.LayerDesc(H, I, E, k, hm.FMT_NVFP4)
+    reps = []
+    for _ in range(REPLICAS):
+        kb, nb = hm.hmoe_packed_size(desc, bit_map)
+        kbuf = torch.empty(kb, dtype=torch.uint8, device=dev)
+        nbuf = torch.empty(nb, dtype=torch.uint8, device=dev)
+        reps.append(hm.hmoe_pack_weights(desc, bit_map, experts, kbuf, nbuf))
+    fmts = [reps[0].expert_info(e)[0] for e in range(E)]
+    max_tokens = max(args.m, 8, 0 if args.skip_prefill else args.prefill_m)
+    ws = torch.empty(hm.hmoe_workspace_size(desc, max_tokens), dtype=torch.uint8, device=dev)
+    hm.hmoe_workspace_init(ws)
+
+    def batches(M, seed0):
+        out = []
+        for r in range(REPLICAS):
+            x = synth.gen_x(M, H, seed=seed0 + r, device=dev)
+            lg = synth.gen_logits(M, E, seed=seed0 + r, device=dev)
+            bufs = dict(ids=torch.empty((M, k), dtype=torch.int32, device=dev),
+                        gates=torch.empty((M, k), dtype=torch.float32, device=dev),
+                        perm=torch.empty((M * k,), dtype=torch.int32, device=dev),
+                        offsets=torch.empty((E + 1,), dtype=torch.int32, device=dev),
+                        out=torch.empty((M, H), dtype=torch.bfloat16, device=dev))
+            out.append((x, lg, bufs))
+        return out
+
+    def step(i, bl, evs=None):
+        r = i % REPLICAS
+        x, lg, b = bl[r]
+        hm.hmoe_plan_routes(reps[r], lg, b["ids"], b["gates"], b["perm"], b["offsets"], ws)
+        hm.hmoe_forward(reps[r], x, b["ids"], b["gates"], b["perm"], b["offsets"], b["out"], ws,
+                        stage_events=evs)
+
+    def batch_bytes(bl):
+        res = []
+        for r in range(REPLICAS):
+            step(r, bl)
+        torch.cuda.synchronize()
+        for r in range(REPLICAS):
+            res.append(touched(bl[r][2]["ids"].cpu().numpy(), fmts))
+        return res
+
+    M = args.m
+    bl = batches(M, 1000)
+    tb = batch_bytes(bl)
+    hm.hmoe_check_device_status(ws)
+
+    # warm-up (untimed) and clock soak
+    clock = ClockSampler(torch.cuda.current_device())
+    for i in range(args.warmup):
+        step(i, bl)
+    clock.start()
+    t_soak = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t_soak < args.soak_s:
+        step(i, bl)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+
+    # timed region: exactly K steps, barrier + synchronize on both sides
+    K = args.steps
+    stage_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for pair in stage_evs:
+        for e in pair:
+            e.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = hm.hmoe_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for i in range(K):
+        step(i, bl, evs=stage_evs[i])
+    ev1.record()
+    torch.cuda.synchronize()
+    launches = hm.hmoe_launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = clock.stop()
+    t_ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        tt = torch.tensor([t_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_ms = float(tt.item())
+    hm.hmoe_check_device_status(ws)
+    bytes_steps = sum(tb[i % REPLICAS][0] for i in range(K))
+    value = bytes_steps * world / (t_ms * 1e-3) / 1e9
+    w13_ms = [stage_evs[i][0].elapsed_time(stage_evs[i][1]) for i in range(K)]
+    w13_avg = sum(w13_ms) / K
+    w13_bytes = sum(tb[i % REPLICAS][1] for i in range(K)) / K
+    w13_gbs = w13_bytes / (w13_avg * 1e-3) / 1e9
+
+    # per-M table (extra)
+    per_m = {}
+    for Mm in (1, 2, 4, 8):
+        blm = batches(Mm, 2000 + Mm)
+        tbm = batch_bytes(blm)
+        for j in range(8):
+            step(j, blm)
+        n = 64
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for j in range(n):
+            step(j, blm)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / n
+        byt = sum(tbm[j % REPLICAS][0] for j in range(n)) / n
+        per_m[str(Mm)] = {"us_per_layer": round(ms * 1e3, 2), "hbm_gbs": round(byt / (ms * 1e-3) / 1e9, 1),
+                          "frac_hbm": round(byt / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                          "touched_experts": round(sum(tbm[j][2] for j in range(REPLICAS)) / REPLICAS, 1)}
+
+    # e2e through the public API with host buffers (pinned), copies inside the timed region
+    hx = [bl[r][0].cpu().pin_memory() for r in range(REPLICAS)]
+    hl = [bl[r][1].cpu().pin_memory() for r in range(REPLICAS)]
+    hout = torch.empty((M, H), dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    dl = torch.empty((M, E), dtype=torch.float32, device=dev)
+
+    def e2e_step(i):
+        r = i % REPLICAS
+        b = bl[r][2]
+        dx.copy_(hx[r], non_blocking=True)
+        dl.copy_(hl[r], non_blocking=True)
+        hm.hmoe_plan_routes(reps[r], dl, b["ids"], b["gates"], b["perm"], b["offsets"], ws)
+        hm.hmoe_forward(reps[r], dx, b["ids"], b["gates"], b["perm"], b["offsets"], b["out"], ws)
+        hout.copy_(b["out"], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    t0 = time.perf_counter()
+    for i in range(K):
+        e2e_step(i)
+    e2e_s = time.perf_counter() - t0
+    e2e_val = bytes_steps / e2e_s / 1e9
+
+    # prefill point: M = 4096 with skewed routing
+    prefill = None
+    if not args.skip_prefill:
+        Mp = args.prefill_m
+        beta, ratio = synth.calibrate_zipf_beta(Mp, E, k, device=dev, iters=24)
+        xp = synth.gen_x(Mp, H, seed=3000, device=dev)
+        lp = synth.gen_logits(Mp, E, device=dev) + synth.zipf_bias(E, beta, device=dev)
+        bp = dict(ids=torch.empty((Mp, k), dtype=torch.int32, device=dev),
+                  gates=torch.empty((Mp, k), dtype=torch.float32, device=dev),
+                  perm=torch.empty((Mp * k,), dtype=torch.int32, device=dev),
+                  offsets=torch.empty((E + 1,), dtype=torch.int32, device=dev),
+                  out=torch.empty((Mp, H), dtype=torch.bfloat16, device=dev))
+
+        def pstep(r):
+            hm.hmoe_plan_routes(reps[r], lp, bp["ids"], bp["gates"], bp["perm"], bp["offsets"], ws)
+            hm.hmoe_forward(reps[r], xp, bp["ids"], bp["gates"], bp["perm"], bp["offsets"], bp["out"], ws,
+                            path=args.prefill_path)
+
+        for r in range(2):
+            pstep(r)
+        torch.cuda.synchronize()
+        n = args.prefill_steps
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for r in range(n):
+            pstep(r % REPLICAS)
+        b.record()
+        torch.cuda.synchronize()
+        hm.hmoe_check_device_status(ws)
+        ms = a.elapsed_time(b) / n
+        flops = 2.0 * k * 3 * H * I * Mp
+        tfs = flops / (ms * 1e-3) / 1e12
+        cnt = torch.bincount(bp["ids"].reshape(-1).long(), minlength=E).float()
+        prefill = {"workload": f"hybrid MoE prefill M={Mp}, Zipf(1.1)-biased router logits "
+                               f"(beta={beta:.3f}, hottest expert {float(cnt.max() / cnt.mean()):.1f}x mean)",
+                   "ms_per_layer": round(ms, 3), "tokens_per_s": round(Mp / (ms * 1e-3), 1),
+                   "tflops": round(tfs, 2), "frac_bf16_peak": round(tfs / pk["bf16_tflops_sustained"], 4),
+                   "peak_used": "bf16_tflops_sustained (" + pk["source"] + ")",
+                   "path": {0: "auto", 1: "stream", 2: "grouped"}[args.prefill_path]}
+
+    # CPU oracle on a bounded sample (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ids0 = bl[0][2]["ids"].cpu().numpy()
+        g0 = bl[0][2]["gates"].cpu().numpy()
+        exps = host_experts(L, ids0[:1])
+        xr = bl[0][0].float().cpu().numpy()[0]
+        dt, byt = oracle_sample(exps, H, I, xr, ids0[0], g0[0])
+        cpu = {"value": round(byt / dt / 1e9, 4), "unit": "GB/s", "cores": len(os.sched_getaffinity(0)),
+               "kind": "oracle",
+               "sample": f"one token of the M={M} batch ({len(exps)} experts, {byt / 1e6:.0f} MB packed), "
+                         f"float64 NumPy dequantise-then-matmul, {dt:.1f} s"}
+
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "stream_w13_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            tj = json.load(open(tpath))
+            if tj.get("M") == M:
+                traffic = tj.get("dram_bytes_per_launch")
+        except (OSError, ValueError):
+            traffic = None
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(t_ms / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"hybrid MoE decode, H=6144 I=2048 E=256 top-8, 64 NVFP4 + 192 NF3, M={M}",
+                   "us_per_layer": round(t_ms / K * 1e3, 2),
+                   "frac_hbm": round(value / world / pk["hbm_gbs"], 4),
+                   "bytes_per_step": int(bytes_steps / K),
+                   "l2": f"{REPLICAS} rotating weight replicas and batches; each step touches > L2 (129 MB)",
+                   "parallelism": "replicas only" if world > 1 else "1 GPU",
+                   "peaks": pk, "per_m": per_m, "prefill": prefill},
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(M * H * 2 + M * E * 4), "d2h_bytes_per_step": int(M * H * 2)},
+        "gpu_launches": int(launches),
+        "roofline": {"kernel": "stream_gemm_kernel (W13, dequant + mma + SwiGLU)", "bound": "hbm",
+                     "achieved": round(w13_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(w13_gbs / pk["hbm_gbs"], 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": int(w13_bytes), "avg_launch_us": round(w13_avg * 1e3, 2)},
+        "cpu_baseline": cpu,
+    }
+    return line if rank == 0 else None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--m", type=int, default=8)
+    ap.add_argument("--prefill-m", type=int, default=4096)
+    ap.add_argument("--prefill-steps", type=int, default=5)
+    ap.add_argument("--prefill-path", type=int, default=0)
+    ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-s", type=float, default=1.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    if world > 1:
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    line = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl != "reference":
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -171,6 +171,10 @@ typedef struct {
   int debug_flags;   /* test hook: HMOE_DEBUG_NO_COPIES makes the weight producer issue nothing, so
                         the consumers' bounded waits run out and the call reports
                         HMOE_ERR_DEVICE_TIMEOUT through hmoe_check_device_status. 0 in normal use. */
+  void* const* stage_events; /* optional cudaEvent_t[n_stage_events], recorded on the stream at
+                                the stage boundaries: [0] before the W13 GEMM, [1] after it,
+                                [2] after the W2 GEMM, [3] after the finalize. NULL = none. */
+  int n_stage_events;
 } hmoe_forward_opts;
 
 #define HMOE_DEBUG_NO_COPIES 1
@@ -213,6 +217,9 @@ void hmoe_layer_destroy(hmoe_layer* layer);
 
 /* Message for the last failing call on this thread ("" if none). */
 const char* hmoe_last_error(void);
+
+/* Number of kernels this library has launched in this process so far (all entry points). */
+uint64_t hmoe_launch_count(void);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int hmoe_version(void);

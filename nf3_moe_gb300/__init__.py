@@ -113,12 +113,21 @@ def hmoe_plan_routes(layer, logits, ids, gates, perm, offsets, ws, stream=None):
 
 
 def hmoe_forward(layer, x, ids, gates, perm, offsets, out, ws, stream=None, tier_order=TIERS_ONE_LAUNCH,
-                 path=PATH_AUTO, wait_limit_us=0, debug_flags=0):
+                 path=PATH_AUTO, wait_limit_us=0, debug_flags=0, stage_events=None):
+    """stage_events: optional list of recorded torch.cuda.Event (up to 4); see hmoe_forward_opts."""
     T = x.shape[0]
-    opts = _lib.ForwardOpts(int(tier_order), int(path), int(wait_limit_us), int(debug_flags))
+    evs, n_ev = None, 0
+    if stage_events:
+        arr = (ctypes.c_void_p * len(stage_events))(*[ctypes.c_void_p(e.cuda_event) for e in stage_events])
+        evs, n_ev = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)), len(stage_events)
+    opts = _lib.ForwardOpts(int(tier_order), int(path), int(wait_limit_us), int(debug_flags), evs, n_ev)
     _lib.check(_lib.lib().hmoe_forward_ex(layer.handle, _ptr(x), T, _ptr(ids), _ptr(gates), _ptr(perm),
                                           _ptr(offsets), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
                                           ctypes.byref(opts), _stream(stream)))
+
+
+def hmoe_launch_count():
+    return int(_lib.lib().hmoe_launch_count())
 
 
 def hmoe_check_device_status(ws, stream=None):

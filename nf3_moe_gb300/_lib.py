@@ -27,7 +27,7 @@ EXPORTS = (
     "hmoe_packed_size", "hmoe_workspace_size", "hmoe_workspace_init", "hmoe_pack_weights",
     "hmoe_plan_routes", "hmoe_forward", "hmoe_forward_ex", "hmoe_check_device_status",
     "hmoe_debug_dequant", "hmoe_layer_expert_info", "hmoe_layer_destroy", "hmoe_last_error",
-    "hmoe_version",
+    "hmoe_launch_count", "hmoe_version",
 )
 
 
@@ -43,7 +43,8 @@ class ExpertSrc(ctypes.Structure):
 
 class ForwardOpts(ctypes.Structure):
     _fields_ = [("tier_order", ctypes.c_int), ("path", ctypes.c_int), ("wait_limit_us", ctypes.c_int),
-                ("debug_flags", ctypes.c_int)]
+                ("debug_flags", ctypes.c_int), ("stage_events", ctypes.POINTER(ctypes.c_void_p)),
+                ("n_stage_events", ctypes.c_int)]
 
 
 class HmoeError(RuntimeError):
@@ -71,6 +72,7 @@ def load(path=LIB_PATH):
         "hmoe_layer_expert_info": (i, [vp, i, P(i), P(ctypes.c_float), P(ctypes.c_float)]),
         "hmoe_layer_destroy": (None, [vp]),
         "hmoe_last_error": (ctypes.c_char_p, []),
+        "hmoe_launch_count": (ctypes.c_uint64, []),
         "hmoe_version": (i, []),
     }
     for name, (res, args) in sig.items():

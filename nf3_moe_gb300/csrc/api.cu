@@ -7,6 +7,7 @@
 // token count). "quant: add native mixed NVFP4/MXFP4 plus NF3 MoE serving",
 // Summary (hybrid_bit_map 4 = kept, 3 = NF3; kept_format; the metadata is
 // validated).
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -18,6 +19,11 @@
 #include "internal.h"
 
 using namespace hmoe;
+
+namespace hmoe {
+static std::atomic<unsigned long long> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+}  // namespace hmoe
 
 struct hmoe_layer {
   hmoe_layer_desc d;
@@ -87,7 +93,7 @@ int pick_stage(int kbi) {
 constexpr int DECODE_MAX_T = 8;
 
 struct WsLayout {
-  size_t status, counters13, counters2, part13, part2, chunk_cnt, chunk_base, h, y, total;
+  size_t status, counters13, counters2, part13, part2, chunk_cnt, chunk_base, xg, h, y, total;
   int KS13, KS2;
 };
 
@@ -117,6 +123,8 @@ WsLayout ws_layout(const hmoe_layer_desc& d, int T) {
   w.chunk_base = off;
   off += align256(nch * d.E * 4);
   const size_t S = (size_t)T * d.topk;
+  w.xg = off;
+  off += align256(T > DECODE_MAX_T ? S * d.H * 2 : 0);
   w.h = off;
   off += align256(S * d.I * 2);
   w.y = off;
@@ -141,6 +149,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 extern "C" {
 
 int hmoe_version(void) { return 100; }
+
+uint64_t hmoe_launch_count(void) { return (uint64_t)hmoe::g_launches.load(std::memory_order_relaxed); }
 
 const char* hmoe_last_error(void) { return g_err.c_str(); }
 
@@ -301,6 +311,12 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
     masks[1] = 1;
   }
   const int grid = stream_grid(L->num_sms);
+  auto mark = [&](int i) -> cudaError_t {
+    if (o.stage_events && i < o.n_stage_events && o.stage_events[i])
+      return cudaEventRecord((cudaEvent_t)o.stage_events[i], st);
+    return cudaSuccess;
+  };
+  if (mark(0) != cudaSuccess) return cuda_fail(cudaGetLastError(), "stage event record");
   for (int which : {13, 2}) {
     p.which = which;
     p.rows = which == 13 ? 2 * d.I : d.H;
@@ -319,9 +335,75 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
       cudaError_t e = launch_stream_gemm(p, grid, st);
       if (e != cudaSuccess) return cuda_fail(e, "stream GEMM launch");
     }
+    cudaError_t e = mark(which == 13 ? 1 : 2);
+    if (e != cudaSuccess) return cuda_fail(e, "stage event record");
   }
   cudaError_t e = launch_finalize(p.y_out, gates, T, d.topk, d.H, static_cast<__nv_bfloat16*>(out), st);
   if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+  if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "stage event record");
+  return HMOE_OK;
+}
+
+static hmoe_status run_grouped_path(const hmoe_layer* L, const void* x, int T, const float* gates,
+                                    const int32_t* perm, const int32_t* offsets, void* out, uint8_t* wsb,
+                                    const WsLayout& w, const hmoe_forward_opts& o, cudaStream_t st) {
+  const hmoe_layer_desc& d = L->d;
+  const int S = T * d.topk;
+  GroupedParams p{};
+  p.kept_buf = L->kept_buf;
+  p.nf3_buf = L->nf3_buf;
+  p.kept_fmt = d.kept_format;
+  p.H = d.H;
+  p.I = d.I;
+  p.E = d.E;
+  p.topk = d.topk;
+  p.T = T;
+  p.kept_expert_bytes = L->gk.expert_bytes;
+  p.nf3_expert_bytes = L->gn.expert_bytes;
+  p.kept_w2_off = L->gk.w13_bytes;
+  p.nf3_w2_off = L->gn.w13_bytes;
+  p.offsets = offsets;
+  p.perm = perm;
+  p.status = reinterpret_cast<int*>(wsb + w.status);
+  p.h_out = reinterpret_cast<__nv_bfloat16*>(wsb + w.h);
+  p.y_out = reinterpret_cast<float*>(wsb + w.y);
+  p.wait_limit_ns = o.wait_limit_us > 0 ? (unsigned long long)o.wait_limit_us * 1000ull : WAIT_LIMIT_NS;
+  p.tab = L->tab;
+  __nv_bfloat16* xg = reinterpret_cast<__nv_bfloat16*>(wsb + w.xg);
+  auto mark = [&](int i) -> cudaError_t {
+    if (o.stage_events && i < o.n_stage_events && o.stage_events[i])
+      return cudaEventRecord((cudaEvent_t)o.stage_events[i], st);
+    return cudaSuccess;
+  };
+  int masks[2] = {3, 0};
+  if (o.tier_order == HMOE_TIERS_KEPT_FIRST) {
+    masks[0] = 1;
+    masks[1] = 2;
+  } else if (o.tier_order == HMOE_TIERS_NF3_FIRST) {
+    masks[0] = 2;
+    masks[1] = 1;
+  }
+  cudaError_t e = launch_gather_rows(static_cast<const __nv_bfloat16*>(x), perm, S, d.topk, T, d.H, xg, p.status,
+                                     L->num_sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+  if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "stage event record");
+  for (int which : {13, 2}) {
+    p.which = which;
+    p.K = which == 13 ? d.H : d.I;
+    p.RT = (which == 13 ? 2 * d.I : d.H) / TILE_ROWS;
+    p.KB = p.K / TILE_K;
+    const __nv_bfloat16* b = which == 13 ? xg : p.h_out;
+    for (int m : masks) {
+      if (!m) continue;
+      p.tier_mask = m;
+      e = launch_grouped_gemm(p, b, S, L->num_sms, st);
+      if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
+    }
+    if ((e = mark(which == 13 ? 1 : 2)) != cudaSuccess) return cuda_fail(e, "stage event record");
+  }
+  e = launch_finalize(p.y_out, gates, T, d.topk, d.H, static_cast<__nv_bfloat16*>(out), st);
+  if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+  if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "stage event record");
   return HMOE_OK;
 }
 
@@ -330,7 +412,7 @@ hmoe_status hmoe_forward_ex(const hmoe_layer* L, const void* x, int T, const int
                             const hmoe_forward_opts* opts, hmoe_stream_t stream) {
   if (!L) return fail(HMOE_ERR_INVALID_ARG, "layer is NULL");
   if (T < 0) return fail(HMOE_ERR_INVALID_ARG, "T=%d < 0", T);
-  hmoe_forward_opts o{HMOE_TIERS_ONE_LAUNCH, HMOE_PATH_AUTO, 0, 0};
+  hmoe_forward_opts o{HMOE_TIERS_ONE_LAUNCH, HMOE_PATH_AUTO, 0, 0, nullptr, 0};
   if (opts) o = *opts;
   const int tier_order = o.tier_order, path = o.path;
   if (tier_order < 0 || tier_order > 2) return fail(HMOE_ERR_INVALID_ARG, "bad tier_order %d", tier_order);
@@ -343,6 +425,13 @@ hmoe_status hmoe_forward_ex(const hmoe_layer* L, const void* x, int T, const int
   if (!x || !ids || !gates || !perm || !offsets || !out) return fail(HMOE_ERR_INVALID_ARG, "a buffer is NULL");
   if (!aligned16(x) || !aligned16(out)) return fail(HMOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
   (void)ids;
+  const bool grouped = path == HMOE_PATH_GROUPED || (path == HMOE_PATH_AUTO && T > DECODE_MAX_T);
+  if (grouped && T <= DECODE_MAX_T)
+    return fail(HMOE_ERR_INVALID_ARG, "the grouped path needs T > %d (the workspace holds no gather buffer below)",
+                DECODE_MAX_T);
+  if (grouped)
+    return run_grouped_path(L, x, T, gates, perm, offsets, out, static_cast<uint8_t*>(ws), w, o,
+                            (cudaStream_t)stream);
   return run_stream_path(L, x, T, gates, perm, offsets, out, static_cast<uint8_t*>(ws), w, o,
                          (cudaStream_t)stream);
 }

@@ -1,0 +1,497 @@
+// grouped.cu -- the tensor-core grouped GEMM for large batches (prefill): tcgen05 + TMEM + TMA.
+//
+// Cites: "quant: nvfp4_nf3_hybrid -- native serving for mixed NVFP4+NF3 MoE
+// checkpoints", How it works. Both weight tiers feed one fused MoE GEMM
+// over the shared route geometry. "[Quantization][ModelOpt] W4A16 NVFP4
+// fused MoE", Summary. W4A16: weights dequantised to the 16-bit activation
+// type, with no activation quantisation.
+//
+// One persistent CTA per SM takes work items (expert e, weight row tile rt
+// of 128 rows, token tile nt of up to 128 permuted slots). For one expert,
+// the token tiles of a row tile are consecutive items, so the CTAs that
+// run them at the same time share that weight tile through L2.
+//
+// Warp roles (14 warps):
+//   warp 0      producer. Per k-block (64 K) it bulk-copies the packed
+//               weight tile, and loads the activation tile (128 rows x 64
+//               bf16) with a 2D TMA tensor load in 128B-swizzled layout.
+//   warp 1      TMEM allocator and MMA issuer. One lane issues 4
+//               tcgen05.mma.kind::f16 (M=128, N = token count rounded up
+//               to 16, K=16) per k-block into a double-buffered fp32
+//               accumulator in TMEM, then tcgen05.commit to free the stage.
+//   warps 2..9  dequantisers. Each thread expands one tile slot (2 rows x
+//               16 K) to bf16 (E2M1 x E4M3, E2M1 x 2^e, or
+//               bf16_rne(NF3 codebook x scale)). It writes the values into
+//               the canonical K-major SWIZZLE_128B operand layout, then
+//               fences the async proxy.
+//   warps 10..13 epilogue. tcgen05.ld of the accumulator (each warp owns 32
+//               TMEM lanes, i.e. 32 weight rows).
+//               W13: rows come in gate/up pairs 8 lanes apart, so one
+//               shuffle gives h = bf16(silu(g13*gate) * (g13*up)).
+//               W2: y[s][row] = g2 * acc for the flat slot s = perm[p].
+// Every mbarrier wait is bounded. On a timeout the CTA records
+// DEV_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace hmoe {
+
+constexpr int GT_N = 128;                 // token tile
+constexpr int GT_STAGES = 5;
+constexpr int GT_A_BYTES = 128 * 128;     // bf16 A tile 128 x 64
+constexpr int GT_B_BYTES = GT_N * 128;    // bf16 B tile GT_N x 64
+constexpr int GT_P_BYTES = 4608;          // largest packed tile
+constexpr int GT_STAGE_BYTES = ((GT_A_BYTES + GT_B_BYTES + GT_P_BYTES + 1023) / 1024) * 1024;
+constexpr int GT_DQ_WARPS = 8;
+constexpr int GT_EPI_WARPS = 4;
+constexpr int GT_THREADS = (2 + GT_DQ_WARPS + GT_EPI_WARPS) * 32;
+constexpr int GT_TMEM_COLS = 2 * GT_N;
+constexpr int GT_SMEM_BYTES = 1024 + GT_STAGES * GT_STAGE_BYTES + 1024 + (MAX_E + 1) * 4;
+static_assert(GT_SMEM_BYTES <= 232448, "shared memory budget");
+
+// ------------------------------------------------------------ tcgen05 / TMA wrappers
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (SBO), version 1, base offset 0 (atoms 1024-aligned).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;                 // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024u >> 4) << 32;       // stride byte offset
+  d |= (uint64_t)1u << 46;                 // descriptor version
+  d |= (uint64_t)2u << 61;                 // SWIZZLE_128B
+  return d;
+}
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+struct GtItem {
+  int e, p0, n, rt;
+};
+
+__device__ __forceinline__ int gt_expert_fmt(const GroupedParams& p, int e) {
+  return (p.tab.loc[e] & LOC_NF3) ? FMT_NF3 : p.kept_fmt;
+}
+
+__device__ __forceinline__ GtItem gt_decode(const GroupedParams& p, const int* s_istart, int i) {
+  int lo = 0, hi = p.E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_istart[mid] <= i) lo = mid; else hi = mid;
+  }
+  GtItem it;
+  it.e = lo;
+  const int o0 = p.offsets[lo], ne = p.offsets[lo + 1] - o0;
+  const int ntile = (ne + GT_N - 1) / GT_N;
+  const int local = i - s_istart[lo];
+  it.rt = local / ntile;
+  const int nt = local % ntile;
+  it.p0 = o0 + nt * GT_N;
+  it.n = min(GT_N, ne - nt * GT_N);
+  return it;
+}
+
+// Writes one thread slot's dequantised rows (2 rows x 16 K) into the
+// canonical K-major SWIZZLE_128B tile: row r of atom (r / 8) at (r % 8) * 128,
+// 16-byte chunk c stored at chunk position c ^ (r % 8).
+template <int FMT>
+__device__ __forceinline__ void gt_dequant_slot(const uint8_t* ptile, uint8_t* atile, int rg, int lane) {
+  uint32_t r0[8], r1[8];
+  float s0, s1;
+  dequant_slot<FMT, true>(ptile, rg, lane, r0, r1, &s0, &s1);
+  const int g = lane >> 2, q = lane & 3;
+  uint8_t* a0 = atile + (2 * rg) * 1024 + g * 128;
+  uint8_t* a1 = atile + (2 * rg + 1) * 1024 + g * 128;
+  const int c0 = ((2 * q) ^ g) * 16, c1 = ((2 * q + 1) ^ g) * 16;
+  *reinterpret_cast<uint4*>(a0 + c0) = make_uint4(r0[0], r0[1], r0[2], r0[3]);
+  *reinterpret_cast<uint4*>(a0 + c1) = make_uint4(r0[4], r0[5], r0[6], r0[7]);
+  *reinterpret_cast<uint4*>(a1 + c0) = make_uint4(r1[0], r1[1], r1[2], r1[3]);
+  *reinterpret_cast<uint4*>(a1 + c1) = make_uint4(r1[4], r1[5], r1[6], r1[7]);
+}
+
+__global__ void __launch_bounds__(GT_THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ GroupedParams p, const __grid_constant__ CUtensorMap tmap_b) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t* stages = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GT_STAGES * GT_STAGE_BYTES);
+  uint64_t* full = bars;                       // [STAGES] producer -> dequant/MMA (tx bytes)
+  uint64_t* aready = bars + GT_STAGES;         // [STAGES] dequant warps -> MMA
+  uint64_t* empty = bars + 2 * GT_STAGES;      // [STAGES] MMA commit -> producer
+  uint64_t* acc_full = bars + 3 * GT_STAGES;   // [2] MMA commit -> epilogue
+  uint64_t* acc_empty = acc_full + 2;          // [2] epilogue -> MMA
+  uint64_t* mma_done = acc_empty + 2;          // [1] final drain
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* s_flags = reinterpret_cast<volatile int*>(s_tmem + 1);  // [0] abort
+  int* s_istart = reinterpret_cast<int*>(smem + GT_STAGES * GT_STAGE_BYTES + 1024);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < GT_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&aready[s], GT_DQ_WARPS);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], GT_EPI_WARPS);
+    }
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+    s_flags[0] = 0;
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, GT_TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0) {
+    // Item prefix over the experts of the selected tiers.
+    const int S = p.T * p.topk;
+    bool bad = (p.offsets[0] != 0) || (p.offsets[p.E] != S);
+    int run = 0;
+    for (int e0 = 0; e0 < p.E; e0 += 32) {
+      const int e = e0 + lane;
+      int ni = 0;
+      if (e < p.E) {
+        const int ne = p.offsets[e + 1] - p.offsets[e];
+        if (ne < 0) bad = true;
+        const bool nf3 = (p.tab.loc[e] & LOC_NF3) != 0;
+        const bool sel = nf3 ? (p.tier_mask & 2) : (p.tier_mask & 1);
+        ni = (sel && ne > 0) ? ((ne + GT_N - 1) / GT_N) * p.RT : 0;
+      }
+      int incl = ni;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int nb = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += nb;
+      }
+      if (e < p.E) s_istart[e] = run + incl - ni;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      s_istart[p.E] = bad ? 0 : run;
+      if (bad && blockIdx.x == 0) set_status(p.status, DEV_BAD_ROUTE);
+    }
+    if (bad)
+      for (int e = lane; e < p.E; e += 32) s_istart[e] = 0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int n_items = s_istart[p.E];
+  const uint64_t lim = p.wait_limit_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      int slot = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      bool aborted = false;
+      for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x) {
+        const GtItem it = gt_decode(p, s_istart, i);
+        const int fmt = gt_expert_fmt(p, it.e);
+        const uint32_t tb = (uint32_t)tile_bytes(fmt);
+        const uint8_t* base = (fmt == FMT_NF3 ? p.nf3_buf : p.kept_buf) +
+                              (size_t)(p.tab.loc[it.e] & 0x7FFF) *
+                                  (fmt == FMT_NF3 ? p.nf3_expert_bytes : p.kept_expert_bytes) +
+                              (p.which == 2 ? (fmt == FMT_NF3 ? p.nf3_w2_off : p.kept_w2_off) : 0) +
+                              (size_t)it.rt * p.KB * tb;
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!mbar_wait(&empty[slot], ph ^ 1u, s_flags, lim)) {
+            aborted = true;
+            s_flags[0] = 1;
+            set_status(p.status, DEV_TIMEOUT);
+            break;
+          }
+          uint8_t* st = stages + slot * GT_STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[slot], tb + GT_B_BYTES);
+          bulk_g2s_stream(st + GT_A_BYTES + GT_B_BYTES, base + (size_t)kb * tb, tb, &full[slot], pol);
+          tma_load_2d(st + GT_A_BYTES, &tmap_b, kb * TILE_K, it.p0, &full[slot]);
+          ++issued;
+          if (++slot == GT_STAGES) {
+            slot = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (aborted) {
+        volatile int never = 0;
+        for (int b = 0; b < GT_STAGES && b < issued; ++b) {
+          if (--slot < 0) {
+            slot = GT_STAGES - 1;
+            ph ^= 1u;
+          }
+          mbar_wait(&full[slot], ph, &never, lim);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t ph = 0;
+      bool aborted = false;
+      int j = 0;
+      for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x, ++j) {
+        const GtItem it = gt_decode(p, s_istart, i);
+        const int buf = j & 1;
+        const uint32_t aph = (uint32_t)((j >> 1) & 1);
+        if (!mbar_wait(&acc_empty[buf], aph ^ 1u, s_flags, lim)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        const int npad = max(16, (it.n + 15) & ~15);
+        const uint32_t idesc = idesc_bf16(128, npad);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * GT_N);
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!mbar_wait(&full[slot], ph, s_flags, lim) || !mbar_wait(&aready[slot], ph, s_flags, lim)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stages + slot * GT_STAGE_BYTES);
+          const uint32_t b_addr = a_addr + GT_A_BYTES;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(d_tmem, smem_desc_sw128(a_addr + ks * 32), smem_desc_sw128(b_addr + ks * 32), idesc,
+                      (kb | ks) ? 1u : 0u);
+          umma_commit(&empty[slot]);
+          if (++slot == GT_STAGES) {
+            slot = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!aborted) umma_commit(&acc_full[buf]);
+      }
+      if (aborted) {
+        s_flags[0] = 1;
+        set_status(p.status, DEV_TIMEOUT);
+      }
+      // Drain every MMA this thread issued before TMEM can be released.
+      umma_commit(mma_done);
+      volatile int never = 0;
+      mbar_wait(mma_done, 0, &never, lim);
+    }
+  } else if (warp < 2 + GT_DQ_WARPS) {
+    // ------------------------------------------------ dequantisers
+    const int rg = warp - 2;
+    int slot = 0;
+    uint32_t ph = 0;
+    bool aborted = false;
+    for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x) {
+      const GtItem it = gt_decode(p, s_istart, i);
+      const int fmt = gt_expert_fmt(p, it.e);
+      for (int kb = 0; kb < p.KB; ++kb) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], ph, s_flags, lim))) {
+          aborted = true;
+          if (lane == 0) {
+            s_flags[0] = 1;
+            set_status(p.status, DEV_TIMEOUT);
+          }
+          break;
+        }
+        uint8_t* st = stages + slot * GT_STAGE_BYTES;
+        const uint8_t* pt = st + GT_A_BYTES + GT_B_BYTES;
+        if (fmt == FMT_NVFP4) gt_dequant_slot<FMT_NVFP4>(pt, st, rg, lane);
+        else if (fmt == FMT_MXFP4) gt_dequant_slot<FMT_MXFP4>(pt, st, rg, lane);
+        else gt_dequant_slot<FMT_NF3>(pt, st, rg, lane);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&aready[slot]);
+        if (++slot == GT_STAGES) {
+          slot = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // tile row = TMEM lane
+    const int S = p.T * p.topk;
+    int j = 0;
+    for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++j) {
+      const GtItem it = gt_decode(p, s_istart, i);
+      const int buf = j & 1;
+      const uint32_t aph = (uint32_t)((j >> 1) & 1);
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], aph, s_flags, lim))) {
+        if (lane == 0) {
+          s_flags[0] = 1;
+          set_status(p.status, DEV_TIMEOUT);
+        }
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * GT_N);
+      for (int c0 = 0; c0 < it.n; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(taddr + (uint32_t)c0, v);
+        tmem_wait_ld();
+        if (p.which == 13) {
+          const float gsc = p.tab.g13[it.e];
+          const int w = row & 15;
+          const int ch = it.rt * 64 + (row >> 4) * 8 + (w & 7);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float up = __shfl_down_sync(0xffffffffu, __uint_as_float(v[c]), 8);
+            if (w < 8 && c0 + c < it.n) {
+              const float gate = __uint_as_float(v[c]) * gsc;
+              p.h_out[(size_t)(it.p0 + c0 + c) * p.I + ch] = __float2bfloat16_rn(silu_f(gate) * (up * gsc));
+            }
+          }
+        } else {
+          const float gsc = p.tab.g2[it.e];
+          const int orow = it.rt * 128 + row;
+#pragma unroll 4
+          for (int c = 0; c < 32; ++c) {
+            if (c0 + c < it.n) {
+              const int s = p.perm[it.p0 + c0 + c];
+              if (s >= 0 && s < S) p.y_out[(size_t)s * p.H + orow] = __uint_as_float(v[c]) * gsc;
+              else if (lane == 0) set_status(p.status, DEV_BAD_ROUTE);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, GT_TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------ gather of activation rows
+__global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict__ perm, int S, int k,
+                                   int T, int H, __nv_bfloat16* __restrict__ xg, int* status) {
+  const int vec = H / 8;  // 16-byte vectors per row
+  const long long n = (long long)S * vec;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int pidx = (int)(i / vec), c = (int)(i % vec);
+    int s = perm[pidx];
+    if (s < 0 || s >= S) {
+      if (c == 0) set_status(status, DEV_BAD_ROUTE);
+      s = 0;
+    }
+    const int t = s / k;
+    reinterpret_cast<uint4*>(xg + (size_t)pidx * H)[c] =
+        __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + c);
+  }
+  (void)T;
+}
+
+cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int* perm, int S, int k, int T, int H,
+                               __nv_bfloat16* xg, int* status, int num_sms, cudaStream_t st) {
+  if (S == 0) return cudaSuccess;
+  const long long n = (long long)S * (H / 8);
+  const long long blocks = (n + 255) / 256;
+  const int grid = (int)(blocks < (long long)num_sms * 8 ? blocks : (long long)num_sms * 8);
+  gather_rows_kernel<<<grid, 256, 0, st>>>(x, perm, S, k, T, H, xg, status);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+cudaError_t launch_grouped_gemm(const GroupedParams& p, const __nv_bfloat16* b_src, int b_rows, int num_sms,
+                                cudaStream_t st) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e =
+        cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GT_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  if (b_rows <= 0) return cudaSuccess;
+  if ((reinterpret_cast<uintptr_t>(b_src) & 15) != 0 || (p.K % TILE_K) != 0) return cudaErrorInvalidValue;
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)b_rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)p.K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)TILE_K, (cuuint32_t)GT_N};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(b_src), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  grouped_gemm_kernel<<<num_sms, GT_THREADS, GT_SMEM_BYTES, st>>>(p, map);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace hmoe

@@ -8,6 +8,9 @@
 
 namespace hmoe {
 
+// Count of kernel launches issued by the library (read by hmoe_launch_count).
+void count_launches(int n);
+
 // ---------------------------------------------------------------- routing
 int route_chunks(int T);
 cudaError_t launch_route(const float* logits, int T, int E, int k, int* ids, float* gates, int* perm,
@@ -60,6 +63,31 @@ constexpr int STREAM_MAX_GROUPS_SPLIT = 256;  // counter rows available when KS 
 
 int stream_grid(int num_sms);
 cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st);
+
+// ---------------------------------------------------------------- tensor-core grouped GEMM (large T)
+struct GroupedParams {
+  const uint8_t* kept_buf;
+  const uint8_t* nf3_buf;
+  int kept_fmt;
+  int which;           // 13: B = gathered x, output h;  2: B = h, output y
+  int H, I, E, topk, T;
+  int K, RT, KB;
+  int tier_mask;
+  size_t kept_expert_bytes, nf3_expert_bytes;
+  size_t kept_w2_off, nf3_w2_off;
+  const int* offsets;
+  const int* perm;
+  __nv_bfloat16* h_out;
+  float* y_out;
+  int* status;
+  unsigned long long wait_limit_ns;
+  ExpertTable tab;
+};
+cudaError_t launch_grouped_gemm(const GroupedParams& p, const __nv_bfloat16* b_src, int b_rows, int num_sms,
+                                cudaStream_t st);
+// xg[p] = x[perm[p] / k] for the S permuted slots.
+cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int* perm, int S, int k, int T, int H,
+                               __nv_bfloat16* xg, int* status, int num_sms, cudaStream_t st);
 
 // out[t][c] = bf16(sum_j gates[t*k+j] * y[t*k+j][c])
 cudaError_t launch_finalize(const float* y, const float* gates, int T, int k, int H, __nv_bfloat16* out,

@@ -122,6 +122,7 @@ cudaError_t launch_pack_matrix(int fmt, int which, const void* codes, const void
   if (tiles == 0) return cudaSuccess;
   pack_matrix_kernel<<<tiles, 256, 0, st>>>(fmt, which, static_cast<const uint8_t*>(codes),
                                             static_cast<const uint8_t*>(scales), N, K, I, dst);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -157,6 +158,7 @@ cudaError_t launch_debug_dequant(int fmt, int which, const uint8_t* src, int N, 
   const int tiles = (N / TILE_ROWS) * (K / TILE_K);
   if (tiles == 0) return cudaSuccess;
   debug_dequant_kernel<<<tiles, 256, 0, st>>>(fmt, which, src, N, K, I, static_cast<__nv_bfloat16*>(dst));
+  count_launches(1);
   return cudaGetLastError();
 }
 

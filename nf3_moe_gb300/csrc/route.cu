@@ -259,12 +259,14 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int* ids, flo
   if (S <= 1024) {
     const size_t smem = (size_t)(S + 2 * E + 1) * sizeof(int);
     route_small_kernel<<<1, 1024, smem, st>>>(logits, T, E, k, ids, gates, perm, offsets);
+    count_launches(1);
     return cudaGetLastError();
   }
   const int nch = route_chunks(T);
   route_topk_kernel<<<nch, 256, 0, st>>>(logits, T, E, k, ids, gates, chunk_cnt);
   route_scan_kernel<<<1, 1024, 0, st>>>(chunk_cnt, nch, E, S, chunk_base, offsets);
   route_place_kernel<<<nch, 256, 0, st>>>(ids, T, E, k, chunk_base, offsets, perm);
+  count_launches(3);
   return cudaGetLastError();
 }
 

@@ -258,10 +258,14 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       for (int st = 0; st < nst; ++st) {
         if (!aborted) {
-          if (!mbar_wait(&full[slot], ph, s_flags, p.wait_limit_ns)) {
+          // Warp-uniform outcome: the MMAs below are .aligned warp collectives.
+          const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[slot], ph, s_flags, p.wait_limit_ns));
+          if (!ok) {
             aborted = true;
-            s_flags[0] = 1;
-            set_status(p.status, DEV_TIMEOUT);
+            if (lane == 0) {
+              s_flags[0] = 1;
+              set_status(p.status, DEV_TIMEOUT);
+            }
           }
         }
         if (!aborted) {
@@ -341,6 +345,7 @@ cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st)
   }
   if (p.kbs < 1 || p.kbs > SK_MAX_KBS || p.group_tokens < 1 || p.group_tokens > 8) return cudaErrorInvalidValue;
   stream_gemm_kernel<<<grid, SK_THREADS, SK_SMEM_BYTES, st>>>(p);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -369,6 +374,7 @@ cudaError_t launch_finalize(const float* y, const float* gates, int T, int k, in
   const int threads = 256;
   const long long blocks = (n + threads - 1) / threads;
   finalize_kernel<<<(int)(blocks < 4096 ? blocks : 4096), threads, 0, st>>>(y, gates, T, k, H, out);
+  count_launches(1);
   return cudaGetLastError();
 }
 

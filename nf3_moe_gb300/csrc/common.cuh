@@ -216,6 +216,7 @@ __device__ __forceinline__ void nf3_selectors(uint32_t A, uint32_t B, uint32_t C
   s[0] = A & 0x77777777u;
   s[1] = B & 0x77777777u;
   s[2] = C & 0x77777777u;
+  // Bits 4j+3 of A, B, C are bits 0, 1, 2 of code 8+j.
   s[3] = ((A >> 3) & 0x11111111u) | ((B >> 2) & 0x22222222u) | ((C >> 1) & 0x44444444u);
 }
 
@@ -225,9 +226,11 @@ __device__ __forceinline__ void nf3_selectors(uint32_t A, uint32_t B, uint32_t C
 // are raw codebook entries, and scale0/scale1 return the two row scales as
 // floats for the caller to apply to fp32 sums. Otherwise every format's
 // values come out multiplied by their scale in bf16 (the "tile" values).
+// e4m3_lut: optional 256-entry E4M3 -> bf16 table (shared memory); NULL
+// converts arithmetically.
 template <int FMT, bool WITH_NF3_SCALE>
 __device__ __forceinline__ void dequant_slot(const uint8_t* tile, int rg, int lane, uint32_t* r0, uint32_t* r1,
-                                             float* scale0, float* scale1) {
+                                             float* scale0, float* scale1, const uint16_t* e4m3_lut = nullptr) {
   const int slot = rg * 32 + lane;
   if constexpr (FMT == FMT_NVFP4 || FMT == FMT_MXFP4) {
     const uint4 q = *reinterpret_cast<const uint4*>(tile + slot * 16);
@@ -238,8 +241,14 @@ __device__ __forceinline__ void dequant_slot(const uint8_t* tile, int rg, int la
       const int g = lane >> 2, hq = (lane & 3) >> 1;
       sc = *reinterpret_cast<const uint16_t*>(tile + 4096 + (rg * 16 + g * 2 + hq) * 2);
     }
-    const uint32_t s0 = bf16_bcast(FMT == FMT_NVFP4 ? e4m3_to_bf16(sc & 0xFFu) : e8m0_to_bf16(sc & 0xFFu));
-    const uint32_t s1 = bf16_bcast(FMT == FMT_NVFP4 ? e4m3_to_bf16(sc >> 8) : e8m0_to_bf16(sc >> 8));
+    uint32_t s0, s1;
+    if constexpr (FMT == FMT_NVFP4) {
+      s0 = bf16_bcast(e4m3_lut ? e4m3_lut[sc & 0xFFu] : e4m3_to_bf16(sc & 0xFFu));
+      s1 = bf16_bcast(e4m3_lut ? e4m3_lut[sc >> 8] : e4m3_to_bf16(sc >> 8));
+    } else {
+      s0 = bf16_bcast(e8m0_to_bf16(sc & 0xFFu));
+      s1 = bf16_bcast(e8m0_to_bf16(sc >> 8));
+    }
     e2m1x8_to_bf16x2(q.x, r0);
     e2m1x8_to_bf16x2(q.y, r0 + 4);
     e2m1x8_to_bf16x2(q.z, r1);

@@ -49,7 +49,7 @@ constexpr int GT_DQ_WARPS = 8;
 constexpr int GT_EPI_WARPS = 4;
 constexpr int GT_THREADS = (2 + GT_DQ_WARPS + GT_EPI_WARPS) * 32;
 constexpr int GT_TMEM_COLS = 2 * GT_N;
-constexpr int GT_SMEM_BYTES = 1024 + GT_STAGES * GT_STAGE_BYTES + 1024 + (MAX_E + 1) * 4;
+constexpr int GT_SMEM_BYTES = 1024 + GT_STAGES * GT_STAGE_BYTES + 1024 + (MAX_E + 1) * 4 + 256 * 2;
 static_assert(GT_SMEM_BYTES <= 232448, "shared memory budget");
 
 // ------------------------------------------------------------ tcgen05 / TMA wrappers
@@ -146,10 +146,11 @@ __device__ __forceinline__ GtItem gt_decode(const GroupedParams& p, const int* s
 // canonical K-major SWIZZLE_128B tile: row r of atom (r / 8) at (r % 8) * 128,
 // 16-byte chunk c stored at chunk position c ^ (r % 8).
 template <int FMT>
-__device__ __forceinline__ void gt_dequant_slot(const uint8_t* ptile, uint8_t* atile, int rg, int lane) {
+__device__ __forceinline__ void gt_dequant_slot(const uint8_t* ptile, uint8_t* atile, int rg, int lane,
+                                                const uint16_t* e4m3_lut) {
   uint32_t r0[8], r1[8];
   float s0, s1;
-  dequant_slot<FMT, true>(ptile, rg, lane, r0, r1, &s0, &s1);
+  dequant_slot<FMT, true>(ptile, rg, lane, r0, r1, &s0, &s1, e4m3_lut);
   const int g = lane >> 2, q = lane & 3;
   uint8_t* a0 = atile + (2 * rg) * 1024 + g * 128;
   uint8_t* a1 = atile + (2 * rg + 1) * 1024 + g * 128;
@@ -176,6 +177,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* s_flags = reinterpret_cast<volatile int*>(s_tmem + 1);  // [0] abort
   int* s_istart = reinterpret_cast<int*>(smem + GT_STAGES * GT_STAGE_BYTES + 1024);
+  uint16_t* s_e4m3 = reinterpret_cast<uint16_t*>(s_istart + MAX_E + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -196,6 +198,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     tmem_alloc(s_tmem, GT_TMEM_COLS);
     tmem_relinquish();
   }
+  if (tid >= 64 && tid < 64 + 256) s_e4m3[tid - 64] = e4m3_to_bf16((uint32_t)(tid - 64));
   if (warp == 0) {
     // Item prefix over the experts of the selected tiers.
     const int S = p.T * p.topk;
@@ -349,9 +352,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         }
         uint8_t* st = stages + slot * GT_STAGE_BYTES;
         const uint8_t* pt = st + GT_A_BYTES + GT_B_BYTES;
-        if (fmt == FMT_NVFP4) gt_dequant_slot<FMT_NVFP4>(pt, st, rg, lane);
-        else if (fmt == FMT_MXFP4) gt_dequant_slot<FMT_MXFP4>(pt, st, rg, lane);
-        else gt_dequant_slot<FMT_NF3>(pt, st, rg, lane);
+        if (fmt == FMT_NVFP4) gt_dequant_slot<FMT_NVFP4>(pt, st, rg, lane, s_e4m3);
+        else if (fmt == FMT_MXFP4) gt_dequant_slot<FMT_MXFP4>(pt, st, rg, lane, s_e4m3);
+        else gt_dequant_slot<FMT_NF3>(pt, st, rg, lane, s_e4m3);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&aready[slot]);
@@ -399,7 +402,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         } else {
           const float gsc = p.tab.g2[it.e];
           const int orow = it.rt * 128 + row;
-#pragma unroll 4
+#pragma unroll
           for (int c = 0; c < 32; ++c) {
             if (c0 + c < it.n) {
               const int s = p.perm[it.p0 + c0 + c];

@@ -50,8 +50,10 @@ struct StreamParams {
   const int* perm;
   const __nv_bfloat16* act;  // x [T][H] or h [S][I]
   int act_stride;
-  float* part;               // [KS][S][rows] fp32 split partials (KS > 1)
-  int* counters;             // [MAX groups][RT], self-cleaning
+  float* part;               // [KS][gmax][RT][256 slots] float4 split partials (KS > 1)
+  int gmax;                  // token groups the partial buffer holds (KS > 1)
+  int* counters;             // [gmax][RT] split arrivals, self-cleaning
+  int* queue;                // [2] work-queue head and finished-CTA count, self-cleaning
   __nv_bfloat16* h_out;      // which == 13: [S][I] bf16, row = permuted position p
   float* y_out;              // which == 2:  [S][H] fp32, row = flat slot s
   int* status;
@@ -59,7 +61,6 @@ struct StreamParams {
   int debug_no_copies;               // test hook: the producer issues nothing
   ExpertTable tab;
 };
-constexpr int STREAM_MAX_GROUPS_SPLIT = 256;  // counter rows available when KS > 1
 
 int stream_grid(int num_sms);
 cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st);

@@ -8,18 +8,21 @@
 //
 // Work item = (token group, row tile of 128 weight rows, k-split). A token
 // group is up to 8 consecutive permuted slots of one expert, so at T <= 8
-// there is exactly one group per touched expert. Persistent CTAs take
-// items in a fixed stride. One producer lane streams each item's packed
-// tiles and the group's activation rows into a 4-stage shared-memory ring
-// with 1D bulk copies (TMA engine). Eight consumer warps, one per 16-row
-// group, dequantise in registers (prmt byte-table lookups, bf16x2 scale
-// multiply) and issue m16n8k16 bf16 MMAs with the tokens as the N=8 side.
-// Accumulation is fp32.
+// there is exactly one group per touched expert. Persistent CTAs pull
+// items from a global work queue that resets itself. One producer lane
+// streams each item's packed tiles and the group's activation rows into a
+// 4-stage shared-memory ring with 1D bulk copies (TMA engine). It writes
+// the item number into each stage header, and a terminator stage ends the
+// consumers' loop. Eight consumer warps, one per 16-row group, dequantise
+// in registers (prmt byte-table lookups; E4M3 scales from a shared table;
+// bf16x2 scale multiply) and issue m16n8k16 bf16 MMAs with the tokens as
+// the N=8 side. Accumulation is fp32, with two accumulator sets per thread.
 //
-// Split-K partials are combined without atomics on data. Each split writes
-// its partial. The last split to arrive at a per-(group, row tile) counter
-// sums all partials in split order, which is deterministic, and runs the
-// epilogue:
+// Split-K is used only when there are too few items to fill the GPU (the
+// host chooses it from T). Partials are combined without atomics on data.
+// Each split writes a float4 per thread. One thread per CTA counts arrivals
+// at a per-(group, row tile) counter. The last split sums all partials in
+// split order, which is deterministic, and runs the epilogue:
 //   W13: h[p][c] = bf16(silu(g13 * gate) * (g13 * up)), SwiGLU fused.
 //   W2:  y[s][r] = g2 * sum, fp32, indexed by the flat slot s.
 // The finalize kernel then applies the gates and sums each token's k slots
@@ -36,9 +39,11 @@ constexpr int SK_MAX_KBS = 4;
 constexpr int SK_XROW = SK_MAX_KBS * 128 + 16;            // padded token row, bytes
 constexpr int SK_W_BYTES = SK_MAX_KBS * 4608;
 constexpr int SK_X_BYTES = 8 * SK_XROW;
-constexpr int SK_STAGE_BYTES = SK_W_BYTES + SK_X_BYTES;
+constexpr int SK_HDR_BYTES = 16;                           // {item, stage} written by the producer
+constexpr int SK_STAGE_BYTES = SK_W_BYTES + SK_X_BYTES + SK_HDR_BYTES;
 constexpr int SK_SMEM_DATA = SK_STAGES * SK_STAGE_BYTES;
-constexpr int SK_SMEM_BYTES = SK_SMEM_DATA + 2 * SK_STAGES * 8 + (MAX_E + 1) * 4 + 16;
+constexpr int SK_NBAR = 2 * SK_STAGES + 2;
+constexpr int SK_SMEM_BYTES = SK_SMEM_DATA + SK_NBAR * 8 + (MAX_E + 1) * 4 + 4 * 4 + 256 * 2;
 static_assert(SK_STAGE_BYTES % 16 == 0, "stage alignment");
 
 struct SkItem {
@@ -96,26 +101,78 @@ __device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it,
   }
 }
 
+// One k-block of one thread slot: dequantise (NVFP4/MXFP4 scales from a
+// shared lookup table, NF3 scale applied to the fp32 sum) and 4 MMAs.
 template <int FMT>
-__device__ __forceinline__ void sk_consume_kblock(const uint8_t* tile, const uint8_t* xrow, int rg, int lane,
-                                                  float* acc) {
+__device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xrow, int rg, int lane,
+                                          const uint16_t* s_e4m3, float* acc) {
   const uint4 xa = *reinterpret_cast<const uint4*>(xrow);
   const uint4 xb = *reinterpret_cast<const uint4*>(xrow + 16);
   const uint32_t xr[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+  const int slot = rg * 32 + lane;
   uint32_t r0[8], r1[8];
-  float sc0, sc1;
-  dequant_slot<FMT, false>(tile, rg, lane, r0, r1, &sc0, &sc1);
-  if constexpr (FMT == FMT_NF3) {
+  if constexpr (FMT == FMT_NVFP4 || FMT == FMT_MXFP4) {
+    const uint4 q = *reinterpret_cast<const uint4*>(tile + slot * 16);
+    uint32_t sc;
+    uint32_t s0, s1;
+    if constexpr (FMT == FMT_NVFP4) {
+      sc = *reinterpret_cast<const uint16_t*>(tile + 4096 + slot * 2);
+      s0 = bf16_bcast(s_e4m3[sc & 0xFFu]);
+      s1 = bf16_bcast(s_e4m3[sc >> 8]);
+    } else {
+      const int g = lane >> 2, hq = (lane & 3) >> 1;
+      sc = *reinterpret_cast<const uint16_t*>(tile + 4096 + (rg * 16 + g * 2 + hq) * 2);
+      s0 = bf16_bcast(e8m0_to_bf16(sc & 0xFFu));
+      s1 = bf16_bcast(e8m0_to_bf16(sc >> 8));
+    }
+    e2m1x8_to_bf16x2(q.x, r0);
+    e2m1x8_to_bf16x2(q.y, r0 + 4);
+    e2m1x8_to_bf16x2(q.z, r1);
+    e2m1x8_to_bf16x2(q.w, r1 + 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      r0[i] = bf16x2_mul(r0[i], s0);
+      r1[i] = bf16x2_mul(r1[i], s1);
+    }
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      mma_bf16_16816(acc, r0[2 * s], r1[2 * s], r0[2 * s + 1], r1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
+  } else {
+    const uint32_t A = *reinterpret_cast<const uint32_t*>(tile + slot * 4);
+    const uint32_t B = *reinterpret_cast<const uint32_t*>(tile + 1024 + slot * 4);
+    const uint32_t C = *reinterpret_cast<const uint32_t*>(tile + 2048 + slot * 4);
+    const int g = lane >> 2;
+    const float sc0 = bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(tile + 3072 + (rg * 16 + g) * 2));
+    const float sc1 = bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(tile + 3072 + (rg * 16 + g + 8) * 2));
+    uint32_t sel[4];
+    nf3_selectors(A, B, C, sel);
+    nf3x8_to_bf16x2(sel[0], r0);
+    nf3x8_to_bf16x2(sel[1], r0 + 4);
+    nf3x8_to_bf16x2(sel[2], r1);
+    nf3x8_to_bf16x2(sel[3], r1 + 4);
     float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int s = 0; s < 4; ++s) mma_bf16_16816(d, r0[2 * s], r1[2 * s], r0[2 * s + 1], r1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
+    for (int s = 0; s < 4; ++s)
+      mma_bf16_16816(d, r0[2 * s], r1[2 * s], r0[2 * s + 1], r1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
     acc[0] = fmaf(sc0, d[0], acc[0]);
     acc[1] = fmaf(sc0, d[1], acc[1]);
     acc[2] = fmaf(sc1, d[2], acc[2]);
     acc[3] = fmaf(sc1, d[3], acc[3]);
+  }
+}
+
+// All k-blocks of one stage, two accumulator sets to break the MMA chain.
+template <int FMT>
+__device__ __forceinline__ void sk_stage(const uint8_t* sw, const uint8_t* sx, int kbs, int rg, int lane,
+                                         const uint16_t* s_e4m3, float* accA, float* accB) {
+  constexpr int TB = tile_bytes(FMT);
+  if (kbs == 4) {
+    sk_kblock<FMT>(sw, sx, rg, lane, s_e4m3, accA);
+    sk_kblock<FMT>(sw + TB, sx + 128, rg, lane, s_e4m3, accB);
+    sk_kblock<FMT>(sw + 2 * TB, sx + 256, rg, lane, s_e4m3, accA);
+    sk_kblock<FMT>(sw + 3 * TB, sx + 384, rg, lane, s_e4m3, accB);
   } else {
-#pragma unroll
-    for (int s = 0; s < 4; ++s) mma_bf16_16816(acc, r0[2 * s], r1[2 * s], r0[2 * s + 1], r1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
+    for (int j = 0; j < kbs; ++j) sk_kblock<FMT>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, (j & 1) ? accB : accA);
   }
 }
 
@@ -123,22 +180,28 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SK_SMEM_DATA);
   uint64_t* empty = full + SK_STAGES;
-  int* s_gstart = reinterpret_cast<int*>(empty + SK_STAGES);
-  volatile int* s_flags = s_gstart + MAX_E + 1;  // [0] abort, [1] last-arriver, [2] route error
+  uint64_t* epi_a = empty + SK_STAGES;     // consumer warps -> warp 0 (partials written)
+  uint64_t* epi_b = epi_a + 1;             // warp 0 -> consumer warps (arrival counted)
+  int* s_gstart = reinterpret_cast<int*>(epi_b + 1);
+  volatile int* s_flags = s_gstart + MAX_E + 1;  // [0] abort, [1] last-arriver
+  uint16_t* s_e4m3 = reinterpret_cast<uint16_t*>(const_cast<int*>(s_flags) + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint64_t lim = p.wait_limit_ns;
 
   if (tid == 0) {
     for (int s = 0; s < SK_STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], SK_CONSUMER_WARPS);
     }
+    mbar_init(epi_a, SK_CONSUMER_WARPS);
+    mbar_init(epi_b, 1);
     fence_mbar_init();
     s_flags[0] = 0;
     s_flags[1] = 0;
-    s_flags[2] = 0;
   }
+  if (tid < 256) s_e4m3[tid] = e4m3_to_bf16((uint32_t)tid);
   // Group prefix over experts of the selected tiers, from the caller's offsets.
-  if (warp == 0) {
+  if (warp == SK_CONSUMER_WARPS) {
     const int S = p.T * p.topk;
     bool bad = (p.offsets[0] != 0) || (p.offsets[p.E] != S);
     int run = 0;
@@ -162,13 +225,10 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
     bad = __any_sync(0xffffffffu, bad);
-    if (p.KS > 1 && run > STREAM_MAX_GROUPS_SPLIT) bad = true;
+    if (p.KS > 1 && run > p.gmax) bad = true;
     if (lane == 0) {
       s_gstart[p.E] = bad ? 0 : run;
-      if (bad) {
-        s_flags[2] = 1;
-        if (blockIdx.x == 0) set_status(p.status, DEV_BAD_ROUTE);
-      }
+      if (bad && blockIdx.x == 0) set_status(p.status, DEV_BAD_ROUTE);
     }
     if (bad)
       for (int e = lane; e < p.E; e += 32) s_gstart[e] = 0;
@@ -178,17 +238,21 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
   const int n_items = s_gstart[p.E] * p.RT * p.KS;
   const int kbi = p.KB / p.KS;
   const int nst = kbi / p.kbs;
-  const int S = p.T * p.topk;
 
   if (warp == SK_CONSUMER_WARPS) {
-    // ------------------------------------------------ producer
+    // ------------------------------------------------ producer: dynamic work queue
+    // With the test hook set the producer stays silent, so the consumers'
+    // bounded waits run out and report DEV_TIMEOUT.
     if (lane == 0 && !p.debug_no_copies) {
       const uint64_t pol = l2_policy_evict_first();
+      const int S = p.T * p.topk;
       int slot = 0;
       uint32_t ph = 0;
       int issued = 0;
       bool aborted = false;
-      for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x) {
+      while (!aborted) {
+        const int i = atomicAdd(p.queue, 1);
+        if (i >= n_items) break;
         const SkItem it = decode_item(p, s_gstart, i);
         const int fmt = expert_fmt(p, it.e);
         const size_t tb = (size_t)tile_bytes(fmt);
@@ -210,7 +274,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
           }
         }
         for (int st = 0; st < nst; ++st) {
-          if (!mbar_wait(&empty[slot], ph ^ 1u, s_flags, p.wait_limit_ns)) {
+          if (!mbar_wait(&empty[slot], ph ^ 1u, s_flags, lim)) {
             aborted = true;
             s_flags[0] = 1;
             set_status(p.status, DEV_TIMEOUT);
@@ -221,6 +285,9 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
           const uint32_t xbytes = (uint32_t)(p.kbs * 128);
           uint8_t* sw = smem + slot * SK_STAGE_BYTES;
           uint8_t* sx = sw + SK_W_BYTES;
+          int* hdr = reinterpret_cast<int*>(sx + SK_X_BYTES);
+          hdr[0] = i;
+          hdr[1] = st;
           mbar_arrive_expect_tx(&full[slot], wbytes + (uint32_t)it.n * xbytes);
           bulk_g2s_stream(sw, base + ((size_t)it.rt * p.KB + kbA) * tb, wbytes, &full[slot], pol);
           for (int j = 0; j < it.n; ++j)
@@ -233,6 +300,18 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
           }
         }
       }
+      if (!aborted) {
+        // Terminator stage: item -1, no bytes.
+        if (mbar_wait(&empty[slot], ph ^ 1u, s_flags, lim)) {
+          int* hdr = reinterpret_cast<int*>(smem + slot * SK_STAGE_BYTES + SK_W_BYTES + SK_X_BYTES);
+          hdr[0] = -1;
+          mbar_arrive(&full[slot]);
+        } else {
+          aborted = true;
+          s_flags[0] = 1;
+          set_status(p.status, DEV_TIMEOUT);
+        }
+      }
       if (aborted) {
         // Drain copies still in flight before the CTA may exit (bounded).
         volatile int never = 0;
@@ -241,96 +320,116 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
             slot = SK_STAGES - 1;
             ph ^= 1u;
           }
-          mbar_wait(&full[slot], ph, &never, p.wait_limit_ns);
+          mbar_wait(&full[slot], ph, &never, lim);
         }
+        s_flags[0] = 1;
       }
     }
   } else {
     // ------------------------------------------------ consumers
     const int rg = warp, g = lane >> 2, q = lane & 3;
     int slot = 0;
-    uint32_t ph = 0;
-    bool aborted = false;
-    for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
-      const SkItem it = decode_item(p, s_gstart, i);
-      const int fmt = expert_fmt(p, it.e);
-      const int tb = tile_bytes(fmt);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int st = 0; st < nst; ++st) {
-        if (!aborted) {
-          // Warp-uniform outcome: the MMAs below are .aligned warp collectives.
-          const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[slot], ph, s_flags, p.wait_limit_ns));
-          if (!ok) {
-            aborted = true;
-            if (lane == 0) {
-              s_flags[0] = 1;
-              set_status(p.status, DEV_TIMEOUT);
-            }
-          }
+    uint32_t ph = 0, eph = 0;
+    SkItem it{};
+    int fmt = FMT_NF3;
+    float accA[4], accB[4];
+    while (true) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], ph, s_flags, lim))) {
+        if (lane == 0) {
+          s_flags[0] = 1;
+          set_status(p.status, DEV_TIMEOUT);
         }
-        if (!aborted) {
-          const uint8_t* sw = smem + slot * SK_STAGE_BYTES;
-          const uint8_t* sx = sw + SK_W_BYTES + g * SK_XROW + q * 32;
-          for (int j = 0; j < p.kbs; ++j) {
-            if (fmt == FMT_NVFP4)
-              sk_consume_kblock<FMT_NVFP4>(sw + j * tb, sx + j * 128, rg, lane, acc);
-            else if (fmt == FMT_MXFP4)
-              sk_consume_kblock<FMT_MXFP4>(sw + j * tb, sx + j * 128, rg, lane, acc);
-            else
-              sk_consume_kblock<FMT_NF3>(sw + j * tb, sx + j * 128, rg, lane, acc);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        if (++slot == SK_STAGES) {
-          slot = 0;
-          ph ^= 1u;
-        }
+        break;
       }
-      // ---------------- epilogue
+      const uint8_t* sw = smem + slot * SK_STAGE_BYTES;
+      const int* hdr = reinterpret_cast<const int*>(sw + SK_W_BYTES + SK_X_BYTES);
+      const int i = hdr[0], st = hdr[1];
+      if (i < 0) break;
+      if (st == 0) {
+        it = decode_item(p, s_gstart, i);
+        fmt = expert_fmt(p, it.e);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) accA[r] = accB[r] = 0.f;
+      }
+      const uint8_t* sx = sw + SK_W_BYTES + g * SK_XROW + q * 32;
+      if (fmt == FMT_NVFP4) sk_stage<FMT_NVFP4>(sw, sx, p.kbs, rg, lane, s_e4m3, accA, accB);
+      else if (fmt == FMT_MXFP4) sk_stage<FMT_MXFP4>(sw, sx, p.kbs, rg, lane, s_e4m3, accA, accB);
+      else sk_stage<FMT_NF3>(sw, sx, p.kbs, rg, lane, s_e4m3, accA, accB);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+      if (++slot == SK_STAGES) {
+        slot = 0;
+        ph ^= 1u;
+      }
+      if (st != nst - 1) continue;
+      // ---------------- item epilogue
+      float acc[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[r] = accA[r] + accB[r];
       if (p.KS == 1) {
-        if (!aborted) sk_emit(p, it, rg, g, q, acc);
+        sk_emit(p, it, rg, g, q, acc);
         continue;
       }
-      const int rowA = it.rt * 128 + rg * 16 + g, rowB = rowA + 8;
-      float* pb = p.part + (size_t)it.ks * S * p.rows;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c = 2 * q + h;
-        if (c < it.n) {
-          pb[(size_t)(it.p0 + c) * p.rows + rowA] = acc[h];
-          pb[(size_t)(it.p0 + c) * p.rows + rowB] = acc[2 + h];
+      // Split-K: write this split's float4, count arrivals, the last split sums in order.
+      const size_t cell = ((size_t)it.grp * p.RT + it.rt) * 256 + rg * 32 + lane;
+      const size_t split_stride = (size_t)p.gmax * p.RT * 256;
+      reinterpret_cast<float4*>(p.part)[(size_t)it.ks * split_stride + cell] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(epi_a);
+      if (warp == 0) {
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(epi_a, eph, s_flags, lim));
+        if (lane == 0) {
+          int last = 0;
+          if (ok) {
+            __threadfence();
+            const int old = atomicAdd(&p.counters[it.grp * p.RT + it.rt], 1);
+            last = (old == p.KS - 1);
+            if (last) p.counters[it.grp * p.RT + it.rt] = 0;
+          } else {
+            s_flags[0] = 1;
+            set_status(p.status, DEV_TIMEOUT);
+          }
+          s_flags[1] = last;
+          mbar_arrive(epi_b);
         }
       }
-      __threadfence();
-      named_bar_sync(1, SK_CONSUMER_WARPS * 32);
-      if (tid == 0) {
-        const int old = atomicAdd(&p.counters[it.grp * p.RT + it.rt], 1);
-        s_flags[1] = (old == p.KS - 1);
+      const bool ok2 = __all_sync(0xffffffffu, mbar_wait(epi_b, eph, s_flags, lim));
+      eph ^= 1u;
+      if (!ok2) {
+        if (lane == 0) {
+          s_flags[0] = 1;
+          set_status(p.status, DEV_TIMEOUT);
+        }
+        break;
       }
-      named_bar_sync(1, SK_CONSUMER_WARPS * 32);
       if (s_flags[1]) {
         __threadfence();
-        float sum[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int k2 = 0; k2 < p.KS; ++k2) {
-          const float* pk = p.part + (size_t)k2 * S * p.rows;
+        float4 v[8];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int c = 2 * q + h;
-            if (c < it.n) {
-              const float a = (k2 == it.ks) ? acc[h] : __ldcg(pk + (size_t)(it.p0 + c) * p.rows + rowA);
-              const float b = (k2 == it.ks) ? acc[2 + h] : __ldcg(pk + (size_t)(it.p0 + c) * p.rows + rowB);
-              sum[h] += a;
-              sum[2 + h] += b;
-            }
+        for (int k2 = 0; k2 < 8; ++k2)
+          if (k2 < p.KS) v[k2] = __ldcg(reinterpret_cast<const float4*>(p.part) + (size_t)k2 * split_stride + cell);
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k2 = 0; k2 < 8; ++k2)
+          if (k2 < p.KS) {
+            sum[0] += v[k2].x;
+            sum[1] += v[k2].y;
+            sum[2] += v[k2].z;
+            sum[3] += v[k2].w;
           }
-        }
-        if (!aborted) sk_emit(p, it, rg, g, q, sum);
-        if (tid == 0) p.counters[it.grp * p.RT + it.rt] = 0;
+        sk_emit(p, it, rg, g, q, sum);
       }
     }
   }
   __syncthreads();
+  if (tid == 0) {
+    // The last CTA to leave resets the work queue for the next launch.
+    if (atomicAdd(p.queue + 1, 1) == (int)gridDim.x - 1) {
+      p.queue[0] = 0;
+      p.queue[1] = 0;
+      __threadfence();
+    }
+  }
 }
 
 int stream_grid(int num_sms) { return 2 * num_sms; }
@@ -343,7 +442,8 @@ cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st)
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  if (p.kbs < 1 || p.kbs > SK_MAX_KBS || p.group_tokens < 1 || p.group_tokens > 8) return cudaErrorInvalidValue;
+  if (p.kbs < 1 || p.kbs > SK_MAX_KBS || p.group_tokens < 1 || p.group_tokens > 8 || p.KS < 1 || p.KS > 8)
+    return cudaErrorInvalidValue;
   stream_gemm_kernel<<<grid, SK_THREADS, SK_SMEM_BYTES, st>>>(p);
   count_launches(1);
   return cudaGetLastError();

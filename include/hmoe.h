@@ -196,6 +196,39 @@ hmoe_status hmoe_forward_ex(const hmoe_layer* layer, const void* x, int T, const
                             void* out, void* ws, size_t ws_bytes, const hmoe_forward_opts* opts,
                             hmoe_stream_t stream);
 
+/* The same layer forward as hmoe_forward, for callers that cannot allocate
+ * device memory and so cannot provide a workspace. Examples are hosts that
+ * give a library only its input and output buffers under a fixed
+ * device-memory plan (some serving engines and plugin interfaces), and code
+ * that must never reach the allocator or cudaFree's implicit device-wide
+ * synchronisation. The pages have no counterpart; this is a library
+ * convenience.
+ *
+ * Instead of a caller workspace, the call uses a file-scope device array of
+ * HMOE_STATIC_SCRATCH_BYTES (16 MiB). Every GPU that loads the library
+ * holds that array until the process exits. The call allocates nothing: no
+ * cudaMalloc, no cudaFree, and no allocating library routine.
+ * - Set-up: the first call on each device looks up the array's device
+ *   address while that device is current. Make that first call before any
+ *   stream capture begins.
+ * - Size limit: a batch whose scratch would exceed the array returns
+ *   HMOE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued. For the
+ *   256-expert layer (H=6144, I=2048, top-8) every T <= 8 fits.
+ * - Sharing: all calls share the one array per device, and it keeps the
+ *   last call's contents. Each call first clears, on the stream, the part
+ *   that must start at zero. Calls that overlap on the GPU (other streams,
+ *   other threads) race on the array. Serialise them.
+ * - Arguments and results are as in hmoe_forward. Device faults are read
+ *   with hmoe_check_device_status_static. */
+#define HMOE_STATIC_SCRATCH_BYTES (16u << 20)
+hmoe_status hmoe_forward_static(const hmoe_layer* layer, const void* x, int T, const int32_t* ids,
+                                const float* gates, const int32_t* perm, const int32_t* offsets, void* out,
+                                hmoe_stream_t stream);
+
+/* hmoe_check_device_status for the array used by hmoe_forward_static on the
+ * current device. It synchronises the stream. */
+hmoe_status hmoe_check_device_status_static(hmoe_stream_t stream);
+
 /* Synchronise the stream and read the device status word the kernels write
  * into the workspace. Returns HMOE_OK, HMOE_ERR_BAD_ROUTE or
  * HMOE_ERR_DEVICE_TIMEOUT, then clears the word. */

@@ -175,3 +175,15 @@ class HybridMoELayer:
             out = torch.empty((x.shape[0], self.H), dtype=torch.bfloat16, device=x.device)
         hmoe_forward(self.layer, x, ids, gates, perm, offsets, out, self.ws, tier_order=tier_order, path=path)
         return out
+
+
+def hmoe_forward_static(layer, x, ids, gates, perm, offsets, out, stream=None):
+    """hmoe_forward without a caller workspace (see include/hmoe.h): the scratch is a fixed
+    per-device array inside the library, so the call allocates no device memory."""
+    T = x.shape[0]
+    _lib.check(_lib.lib().hmoe_forward_static(layer.handle, _ptr(x), T, _ptr(ids), _ptr(gates), _ptr(perm),
+                                              _ptr(offsets), _ptr(out), _stream(stream)))
+
+
+def hmoe_check_device_status_static(stream=None):
+    _lib.check(_lib.lib().hmoe_check_device_status_static(_stream(stream)))

@@ -27,7 +27,7 @@ EXPORTS = (
     "hmoe_packed_size", "hmoe_workspace_size", "hmoe_workspace_init", "hmoe_pack_weights",
     "hmoe_plan_routes", "hmoe_forward", "hmoe_forward_ex", "hmoe_check_device_status",
     "hmoe_debug_dequant", "hmoe_layer_expert_info", "hmoe_layer_destroy", "hmoe_last_error",
-    "hmoe_launch_count", "hmoe_version",
+    "hmoe_launch_count", "hmoe_version", "hmoe_forward_static", "hmoe_check_device_status_static",
 )
 
 
@@ -73,6 +73,8 @@ def load(path=LIB_PATH):
         "hmoe_layer_destroy": (None, [vp]),
         "hmoe_last_error": (ctypes.c_char_p, []),
         "hmoe_launch_count": (ctypes.c_uint64, []),
+        "hmoe_forward_static": (i, [vp, vp, i, vp, vp, vp, vp, vp, vp]),
+        "hmoe_check_device_status_static": (i, [vp]),
         "hmoe_version": (i, []),
     }
     for name, (res, args) in sig.items():

@@ -11,6 +11,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 
@@ -490,6 +491,67 @@ hmoe_status hmoe_debug_dequant(const hmoe_layer* L, int expert, int which, void*
                                        (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "debug dequant launch");
   return HMOE_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------ allocation-free forward
+// The scratch of hmoe_forward_static: one file-scope device array per GPU
+// that loads the library. Host code must not use the symbol as an address.
+// The device address is looked up once per device with
+// cudaGetSymbolAddress while that device is current, and passed to the
+// kernels like any caller workspace.
+static __device__ __align__(256) unsigned char g_hmoe_static_scratch[HMOE_STATIC_SCRATCH_BYTES];
+
+namespace {
+constexpr int STATIC_MAX_DEVICES = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[STATIC_MAX_DEVICES] = {};
+
+hmoe_status static_scratch(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= STATIC_MAX_DEVICES)
+    return fail(HMOE_ERR_INVALID_ARG, "device ordinal %d beyond the %d supported", dev, STATIC_MAX_DEVICES);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_hmoe_static_scratch);
+    if (e != cudaSuccess || !p) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return HMOE_OK;
+}
+}  // namespace
+
+extern "C" {
+
+hmoe_status hmoe_forward_static(const hmoe_layer* L, const void* x, int T, const int32_t* ids, const float* gates,
+                                const int32_t* perm, const int32_t* offsets, void* out, hmoe_stream_t stream) {
+  if (!L) return fail(HMOE_ERR_INVALID_ARG, "layer is NULL");
+  if (T < 0) return fail(HMOE_ERR_INVALID_ARG, "T=%d < 0", T);
+  const WsLayout w = ws_layout(L->d, T);
+  if (w.total > (size_t)HMOE_STATIC_SCRATCH_BYTES)
+    return fail(HMOE_ERR_WORKSPACE_TOO_SMALL,
+                "T=%d needs %zu bytes of scratch; the static scratch of hmoe_forward_static holds %u", T, w.total,
+                (unsigned)HMOE_STATIC_SCRATCH_BYTES);
+  void* ws = nullptr;
+  hmoe_status s = static_scratch(&ws);
+  if (s != HMOE_OK) return s;
+  // The array keeps the previous call's contents: clear the part that must
+  // start at zero (status word, work queues, split-K arrival counters).
+  cudaError_t e = cudaMemsetAsync(ws, 0, w.part13, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch");
+  return hmoe_forward_ex(L, x, T, ids, gates, perm, offsets, out, ws, HMOE_STATIC_SCRATCH_BYTES, nullptr, stream);
+}
+
+hmoe_status hmoe_check_device_status_static(hmoe_stream_t stream) {
+  void* ws = nullptr;
+  hmoe_status s = static_scratch(&ws);
+  if (s != HMOE_OK) return s;
+  return hmoe_check_device_status(ws, HMOE_STATIC_SCRATCH_BYTES, stream);
 }
 
 }  // extern "C"

@@ -78,21 +78,6 @@ hmoe_status check_bitmap(const hmoe_layer_desc* d, const int8_t* bit_map) {
   return HMOE_OK;
 }
 
-// Split of the K extent for small batches. The smallest divisor ks of KB
-// (ks <= cap, at least 2 k-blocks per split) whose item count
-// groups * RT * ks reaches 4 items per CTA of a reference grid (2 CTAs on
-// each of 152 SMs). It depends only on the shape and T, so the workspace
-// size is fixed before any device is known.
-constexpr int REF_STREAM_CTAS = 304;
-int pick_split(int groups, int RT, int KB, int cap) {
-  int best = 1;
-  for (int ks = 1; ks <= cap; ++ks) {
-    if (KB % ks != 0 || KB / ks < 2) continue;
-    best = ks;
-    if ((long long)groups * RT * ks >= 4LL * REF_STREAM_CTAS) return ks;
-  }
-  return best;
-}
 int pick_stage(int kbi) {
   for (int s = 4; s > 1; s >>= 1)
     if (kbi % s == 0) return s;
@@ -102,35 +87,19 @@ int pick_stage(int kbi) {
 constexpr int DECODE_MAX_T = 8;
 
 struct WsLayout {
-  size_t status, queues, counters13, counters2, part13, part2, chunk_cnt, chunk_base, xg, h, y, total;
-  int KS13, KS2, gmax;
+  size_t status, queues, chunk_cnt, chunk_base, xg, h, y, total;
 };
 
-// Fixed prefix (status, counters) first, so that the counters stay at the
+// Fixed prefix (status word, work queues) first, so that it stays at the
 // same place for every T.
 WsLayout ws_layout(const hmoe_layer_desc& d, int T) {
   WsLayout w{};
-  const int RT13 = 2 * d.I / TILE_ROWS, RT2 = d.H / TILE_ROWS;
-  const int KB13 = d.H / TILE_K, KB2 = d.I / TILE_K;
-  const int cmax = d.E < DECODE_MAX_T * d.topk ? d.E : DECODE_MAX_T * d.topk;  // groups when T <= 8
   size_t off = 0;
   w.status = off;
   off += 256;
   w.queues = off;                       // 4 launch slots x {head, finished}
   off += 256;
-  w.counters13 = off;
-  off += align256((size_t)cmax * RT13 * 4);
-  w.counters2 = off;
-  off += align256((size_t)cmax * RT2 * 4);
   // T-dependent regions from here on.
-  const int Td = T < DECODE_MAX_T ? T : DECODE_MAX_T;
-  w.gmax = d.E < Td * d.topk ? d.E : Td * d.topk;
-  w.KS13 = T <= DECODE_MAX_T ? pick_split(w.gmax, RT13, KB13, 8) : 1;
-  w.KS2 = T <= DECODE_MAX_T ? pick_split(w.gmax, RT2, KB2, 8) : 1;
-  w.part13 = off;
-  off += align256(w.KS13 > 1 ? (size_t)w.KS13 * w.gmax * RT13 * 256 * 16 : 0);
-  w.part2 = off;
-  off += align256(w.KS2 > 1 ? (size_t)w.KS2 * w.gmax * RT2 * 256 * 16 : 0);
   const size_t nch = (size_t)route_chunks(T);
   w.chunk_cnt = off;
   off += align256(nch * d.E * 4);
@@ -187,8 +156,8 @@ hmoe_status hmoe_workspace_size(const hmoe_layer_desc* desc, int max_tokens, siz
   hmoe_status s = check_desc(desc);
   if (s != HMOE_OK) return s;
   if (!bytes || max_tokens < 0) return fail(HMOE_ERR_INVALID_ARG, "bytes NULL or max_tokens < 0");
-  // Every T <= max_tokens must fit. Small T may need more split-K
-  // partials than larger T; above DECODE_MAX_T the need grows with T.
+  // Every T <= max_tokens must fit (the layout grows with T; the loop keeps
+  // that true however the layout changes).
   size_t need = ws_layout(*desc, max_tokens).total;
   for (int t = 0; t <= max_tokens && t <= DECODE_MAX_T; ++t) {
     const size_t n = ws_layout(*desc, t).total;
@@ -333,7 +302,7 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
   const int grid = stream_grid(L->num_sms);
   auto mark = [&](int i) -> cudaError_t {
     if (o.stage_events && i < o.n_stage_events && o.stage_events[i])
-      return cudaEventRecord((cudaEvent_t)o.stage_events[i], st);
+      return cudaEventRecordWithFlags((cudaEvent_t)o.stage_events[i], st, cudaEventRecordExternal);
     return cudaSuccess;
   };
   if (mark(0) != cudaSuccess) return cuda_fail(cudaGetLastError(), "stage event record");
@@ -343,13 +312,9 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
     p.K = which == 13 ? d.H : d.I;
     p.RT = p.rows / TILE_ROWS;
     p.KB = p.K / TILE_K;
-    p.KS = which == 13 ? w.KS13 : w.KS2;
-    p.gmax = w.gmax;
-    p.kbs = pick_stage(p.KB / p.KS);
+    p.kbs = pick_stage(p.KB);
     p.act = which == 13 ? static_cast<const __nv_bfloat16*>(x) : p.h_out;
     p.act_stride = which == 13 ? d.H : d.I;
-    p.part = reinterpret_cast<float*>(wsb + (which == 13 ? w.part13 : w.part2));
-    p.counters = reinterpret_cast<int*>(wsb + (which == 13 ? w.counters13 : w.counters2));
     for (int li = 0; li < 2; ++li) {
       const int m = masks[li];
       if (!m) continue;
@@ -395,7 +360,7 @@ static hmoe_status run_grouped_path(const hmoe_layer* L, const void* x, int T, c
   __nv_bfloat16* xg = reinterpret_cast<__nv_bfloat16*>(wsb + w.xg);
   auto mark = [&](int i) -> cudaError_t {
     if (o.stage_events && i < o.n_stage_events && o.stage_events[i])
-      return cudaEventRecord((cudaEvent_t)o.stage_events[i], st);
+      return cudaEventRecordWithFlags((cudaEvent_t)o.stage_events[i], st, cudaEventRecordExternal);
     return cudaSuccess;
   };
   int masks[2] = {3, 0};
@@ -541,8 +506,8 @@ hmoe_status hmoe_forward_static(const hmoe_layer* L, const void* x, int T, const
   hmoe_status s = static_scratch(&ws);
   if (s != HMOE_OK) return s;
   // The array keeps the previous call's contents: clear the part that must
-  // start at zero (status word, work queues, split-K arrival counters).
-  cudaError_t e = cudaMemsetAsync(ws, 0, w.part13, (cudaStream_t)stream);
+  // start at zero (status word and work queues).
+  cudaError_t e = cudaMemsetAsync(ws, 0, w.chunk_cnt, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch");
   return hmoe_forward_ex(L, x, T, ids, gates, perm, offsets, out, ws, HMOE_STATIC_SCRATCH_BYTES, nullptr, stream);
 }

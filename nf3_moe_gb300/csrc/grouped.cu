@@ -6,29 +6,36 @@
 // fused MoE", Summary. W4A16: weights dequantised to the 16-bit activation
 // type, with no activation quantisation.
 //
-// One persistent CTA per SM takes work items (expert e, weight row tile rt
-// of 128 rows, token tile nt of up to 128 permuted slots). For one expert,
-// the token tiles of a row tile are consecutive items, so the CTAs that
-// run them at the same time share that weight tile through L2.
+// One persistent CTA per SM takes work items (expert e, token tile nt of up
+// to 128 permuted slots, a pair of weight row tiles rt, rt+1 of 128 rows
+// each), with row-tile pairs fastest. Both row tiles of an item multiply
+// the same activation tile, so each activation tile is read from L2 once per
+// 256 weight rows; the CTAs running together also share it through L2. An
+// expert's token tiles follow each other, so its weight tiles are re-read
+// from L2 rather than HBM.
 //
-// Warp roles (14 warps):
-//   warp 0      producer. Per k-block (64 K) it bulk-copies the packed
-//               weight tile, and loads the activation tile (128 rows x 64
-//               bf16) with a 2D TMA tensor load in 128B-swizzled layout.
-//   warp 1      TMEM allocator and MMA issuer. One lane issues 4
-//               tcgen05.mma.kind::f16 (M=128, N = token count rounded up
-//               to 16, K=16) per k-block into a double-buffered fp32
-//               accumulator in TMEM, then tcgen05.commit to free the stage.
-//   warps 2..9  dequantisers. Each thread expands one tile slot (2 rows x
-//               16 K) to bf16 (E2M1 x E4M3, E2M1 x 2^e, or
-//               bf16_rne(NF3 codebook x scale)). It writes the values into
-//               the canonical K-major SWIZZLE_128B operand layout, then
-//               fences the async proxy.
-//   warps 10..13 epilogue. tcgen05.ld of the accumulator (each warp owns 32
-//               TMEM lanes, i.e. 32 weight rows).
-//               W13: rows come in gate/up pairs 8 lanes apart, so one
-//               shuffle gives h = bf16(silu(g13*gate) * (g13*up)).
-//               W2: y[s][row] = g2 * acc for the flat slot s = perm[p].
+// Warp roles (23 warps):
+//   warp 0       packed-weight producer. 1D bulk copies of each k-block's
+//                two packed tiles (64 K each) into a 4-deep ring.
+//   warp 2       activation producer. A 2D TMA tensor load (128 rows x 64
+//                bf16, 128B swizzle) into a 5-deep ring, plus an L2 prefetch
+//                of the tile needed 8 k-blocks later.
+//   warp 1       TMEM allocator (512 columns) and MMA issuer. One lane
+//                issues, per k-block and row tile, 4 tcgen05.mma.kind::f16
+//                (M=128, N = token count rounded up to 16, K=16) into a
+//                double-buffered fp32 accumulator pair in TMEM. The
+//                shared-memory descriptors are precomputed per ring slot.
+//                tcgen05.commits then free the operand and activation slots.
+//   warps 3..18  dequantisers, in two groups of 8; group r expands row tile
+//                r of the item. Each thread expands one tile slot (2 rows x
+//                16 K) to bf16 (E2M1 x E4M3, E2M1 x 2^e, or bf16_rne(NF3
+//                codebook x scale)) into the canonical K-major SWIZZLE_128B
+//                operand layout of a 3-deep ring, then fences the async proxy.
+//   warps 19..22 epilogue. tcgen05.ld of the accumulators (each warp owns 32
+//                TMEM lanes, i.e. 32 weight rows of each row tile).
+//                W13: rows come in gate/up pairs 8 lanes apart, so one
+//                shuffle gives h = bf16(silu(g13*gate) * (g13*up)).
+//                W2: y[s][row] = g2 * acc for the flat slot s = perm[p].
 // Every mbarrier wait is bounded. On a timeout the CTA records
 // DEV_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -40,17 +47,34 @@
 namespace hmoe {
 
 constexpr int GT_N = 128;                 // token tile
-constexpr int GT_STAGES = 5;
-constexpr int GT_A_BYTES = 128 * 128;     // bf16 A tile 128 x 64
+constexpr int GT_R = 2;                   // weight row tiles per item (they share the activation tile)
+constexpr int GT_A_TILE = 128 * 128;      // bf16 A tile 128 x 64
+constexpr int GT_A_BYTES = GT_R * GT_A_TILE;
 constexpr int GT_B_BYTES = GT_N * 128;    // bf16 B tile GT_N x 64
-constexpr int GT_P_BYTES = 4608;          // largest packed tile
-constexpr int GT_STAGE_BYTES = ((GT_A_BYTES + GT_B_BYTES + GT_P_BYTES + 1023) / 1024) * 1024;
-constexpr int GT_DQ_WARPS = 8;
+constexpr int GT_P_TILE = 4608;           // largest packed tile
+constexpr int GT_P_BYTES = GT_R * GT_P_TILE;
+constexpr int GT_PSTAGES = 4;             // packed weight tiles in flight
+constexpr int GT_BSTAGES = 5;             // activation tiles in flight
+constexpr int GT_ASTAGES = 3;             // dequantised operand tiles between dequant and MMA
+constexpr int GT_BPREFETCH = 8;           // B tiles prefetched into L2 ahead of the TMA loads
+constexpr int GT_DQ_GROUPS = GT_R;        // dequant group r expands row tile r of the item
+constexpr int GT_DQ_WARPS = 8 * GT_DQ_GROUPS;
 constexpr int GT_EPI_WARPS = 4;
-constexpr int GT_THREADS = (2 + GT_DQ_WARPS + GT_EPI_WARPS) * 32;
-constexpr int GT_TMEM_COLS = 2 * GT_N;
-constexpr int GT_SMEM_BYTES = 1024 + GT_STAGES * GT_STAGE_BYTES + 1024 + (MAX_E + 1) * 4 + 256 * 2;
+constexpr int GT_WARP_PPROD = 0, GT_WARP_MMA = 1, GT_WARP_BPROD = 2, GT_WARP_DQ0 = 3;
+constexpr int GT_WARP_EPI0 = GT_WARP_DQ0 + GT_DQ_WARPS;
+constexpr int GT_THREADS = (GT_WARP_EPI0 + GT_EPI_WARPS) * 32;
+constexpr int GT_TMEM_COLS = 2 * GT_R * GT_N;   // [buffer][row tile] accumulators
+// Shared memory map (offsets from the 1024-aligned base).
+constexpr int GT_OFF_A = 0;
+constexpr int GT_OFF_B = GT_OFF_A + GT_ASTAGES * GT_A_BYTES;
+constexpr int GT_OFF_P = GT_OFF_B + GT_BSTAGES * GT_B_BYTES;
+constexpr int GT_OFF_BAR = GT_OFF_P + GT_PSTAGES * GT_P_BYTES;
+constexpr int GT_NBAR = 2 * (GT_PSTAGES + GT_BSTAGES + GT_ASTAGES) + 4 + 1;
+constexpr int GT_OFF_MISC = GT_OFF_BAR + ((GT_NBAR * 8 + 16 + 127) / 128) * 128;
+constexpr int GT_SMEM_BYTES = 1024 + GT_OFF_MISC + 2 * (MAX_E + 1) * 4 + 256 * 2;
 static_assert(GT_SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(GT_OFF_P % 16 == 0 && GT_OFF_B % 1024 == 0, "alignment");
+static_assert(GT_TMEM_COLS <= 512, "TMEM columns");
 
 // ------------------------------------------------------------ tcgen05 / TMA wrappers
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
@@ -70,6 +94,15 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// The same MMA with the accumulate flag known to be set (k-steps after the first).
+__device__ __forceinline__ void umma_bf16_acc(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.eq.u32 p, 1, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc)
       : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -101,6 +134,11 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+               : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 bytes apart (SBO), version 1, base offset 0 (atoms 1024-aligned).
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
@@ -111,20 +149,29 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   d |= (uint64_t)2u << 61;                 // SWIZZLE_128B
   return d;
 }
+// The descriptor above as (low word, high word). The low word holds the start
+// address (>> 4) and the leading byte offset; the high word is constant.
+// Advancing 32 bytes along K adds 2 to the low word.
+constexpr uint32_t SW128_DESC_HI = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t smem_desc_sw128_lo(uint32_t addr) { return ((addr >> 4) & 0x3FFFu) | (1u << 16); }
+__device__ __forceinline__ uint64_t desc_from_lo(uint32_t lo) {
+  return ((uint64_t)SW128_DESC_HI << 32) | (uint64_t)lo;
+}
+
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
 __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 struct GtItem {
-  int e, p0, n, rt;
+  int e, p0, n, rt, nr;  // row tiles rt .. rt + nr - 1 (nr = 1 or 2)
 };
 
 __device__ __forceinline__ int gt_expert_fmt(const GroupedParams& p, int e) {
   return (p.tab.loc[e] & LOC_NF3) ? FMT_NF3 : p.kept_fmt;
 }
 
-__device__ __forceinline__ GtItem gt_decode(const GroupedParams& p, const int* s_istart, int i) {
+__device__ __forceinline__ GtItem gt_decode(const GroupedParams& p, const int* s_istart, const int* s_off, int i) {
   int lo = 0, hi = p.E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -132,11 +179,15 @@ __device__ __forceinline__ GtItem gt_decode(const GroupedParams& p, const int* s
   }
   GtItem it;
   it.e = lo;
-  const int o0 = p.offsets[lo], ne = p.offsets[lo + 1] - o0;
-  const int ntile = (ne + GT_N - 1) / GT_N;
+  const int o0 = s_off[lo], ne = s_off[lo + 1] - o0;
+  // Row-tile pairs fastest: the CTAs that run together share one activation
+  // tile through L2, and an expert's token tiles follow each other, so its
+  // weight tiles are re-read from L2 rather than HBM.
+  const int RP = (p.RT + GT_R - 1) / GT_R;
   const int local = i - s_istart[lo];
-  it.rt = local / ntile;
-  const int nt = local % ntile;
+  it.rt = (local % RP) * GT_R;
+  it.nr = min(GT_R, p.RT - it.rt);
+  const int nt = local / RP;
   it.p0 = o0 + nt * GT_N;
   it.n = min(GT_N, ne - nt * GT_N);
   return it;
@@ -166,25 +217,35 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GT_STAGES * GT_STAGE_BYTES);
-  uint64_t* full = bars;                       // [STAGES] producer -> dequant/MMA (tx bytes)
-  uint64_t* aready = bars + GT_STAGES;         // [STAGES] dequant warps -> MMA
-  uint64_t* empty = bars + 2 * GT_STAGES;      // [STAGES] MMA commit -> producer
-  uint64_t* acc_full = bars + 3 * GT_STAGES;   // [2] MMA commit -> epilogue
-  uint64_t* acc_empty = acc_full + 2;          // [2] epilogue -> MMA
-  uint64_t* mma_done = acc_empty + 2;          // [1] final drain
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GT_OFF_BAR);
+  uint64_t* pfull = bars;                              // packed tile landed (tx)
+  uint64_t* pempty = pfull + GT_PSTAGES;               // dequant warps done reading it
+  uint64_t* bfull = pempty + GT_PSTAGES;               // activation tile landed (tx)
+  uint64_t* bempty = bfull + GT_BSTAGES;               // MMAs that read it completed
+  uint64_t* afull = bempty + GT_BSTAGES;               // dequant warps wrote the operand tile
+  uint64_t* aempty = afull + GT_ASTAGES;               // MMAs that read it completed
+  uint64_t* acc_full = aempty + GT_ASTAGES;            // [2] accumulator ready for the epilogue
+  uint64_t* acc_empty = acc_full + 2;                  // [2] epilogue drained it
+  uint64_t* mma_done = acc_empty + 2;                  // final drain before TMEM release
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* s_flags = reinterpret_cast<volatile int*>(s_tmem + 1);  // [0] abort
-  int* s_istart = reinterpret_cast<int*>(smem + GT_STAGES * GT_STAGE_BYTES + 1024);
-  uint16_t* s_e4m3 = reinterpret_cast<uint16_t*>(s_istart + MAX_E + 1);
+  int* s_istart = reinterpret_cast<int*>(smem + GT_OFF_MISC);
+  int* s_off = s_istart + MAX_E + 1;
+  uint16_t* s_e4m3 = reinterpret_cast<uint16_t*>(s_off + MAX_E + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < GT_STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&aready[s], GT_DQ_WARPS);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < GT_PSTAGES; ++s) {
+      mbar_init(&pfull[s], 1);
+      mbar_init(&pempty[s], GT_DQ_WARPS);
+    }
+    for (int s = 0; s < GT_BSTAGES; ++s) {
+      mbar_init(&bfull[s], 1);
+      mbar_init(&bempty[s], 1);
+    }
+    for (int s = 0; s < GT_ASTAGES; ++s) {
+      mbar_init(&afull[s], GT_DQ_WARPS);
+      mbar_init(&aempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -194,25 +255,27 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     fence_mbar_init();
     s_flags[0] = 0;
   }
-  if (warp == 1) {
+  if (warp == GT_WARP_MMA) {
     tmem_alloc(s_tmem, GT_TMEM_COLS);
     tmem_relinquish();
   }
-  if (tid >= 64 && tid < 64 + 256) s_e4m3[tid - 64] = e4m3_to_bf16((uint32_t)(tid - 64));
+  if (tid >= 96 && tid < 96 + 256) s_e4m3[tid - 96] = e4m3_to_bf16((uint32_t)(tid - 96));
+  for (int e = tid; e <= p.E; e += blockDim.x) s_off[e] = p.offsets[e];
+  __syncthreads();
   if (warp == 0) {
     // Item prefix over the experts of the selected tiers.
     const int S = p.T * p.topk;
-    bool bad = (p.offsets[0] != 0) || (p.offsets[p.E] != S);
+    bool bad = (s_off[0] != 0) || (s_off[p.E] != S);
     int run = 0;
     for (int e0 = 0; e0 < p.E; e0 += 32) {
       const int e = e0 + lane;
       int ni = 0;
       if (e < p.E) {
-        const int ne = p.offsets[e + 1] - p.offsets[e];
+        const int ne = s_off[e + 1] - s_off[e];
         if (ne < 0) bad = true;
         const bool nf3 = (p.tab.loc[e] & LOC_NF3) != 0;
         const bool sel = nf3 ? (p.tier_mask & 2) : (p.tier_mask & 1);
-        ni = (sel && ne > 0) ? ((ne + GT_N - 1) / GT_N) * p.RT : 0;
+        ni = (sel && ne > 0) ? ((ne + GT_N - 1) / GT_N) * ((p.RT + GT_R - 1) / GT_R) : 0;
       }
       int incl = ni;
 #pragma unroll
@@ -238,16 +301,15 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
   const int n_items = s_istart[p.E];
   const uint64_t lim = p.wait_limit_ns;
 
-  if (warp == 0) {
-    // ------------------------------------------------ producer
+  if (warp == GT_WARP_PPROD) {
+    // ------------------------------------------------ packed weight tiles (HBM)
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      int slot = 0;
+      int slot = 0, issued = 0;
       uint32_t ph = 0;
-      int issued = 0;
       bool aborted = false;
       for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x) {
-        const GtItem it = gt_decode(p, s_istart, i);
+        const GtItem it = gt_decode(p, s_istart, s_off, i);
         const int fmt = gt_expert_fmt(p, it.e);
         const uint32_t tb = (uint32_t)tile_bytes(fmt);
         const uint8_t* base = (fmt == FMT_NF3 ? p.nf3_buf : p.kept_buf) +
@@ -255,70 +317,119 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
                                   (fmt == FMT_NF3 ? p.nf3_expert_bytes : p.kept_expert_bytes) +
                               (p.which == 2 ? (fmt == FMT_NF3 ? p.nf3_w2_off : p.kept_w2_off) : 0) +
                               (size_t)it.rt * p.KB * tb;
+        const size_t rt_stride = (size_t)p.KB * tb;
         for (int kb = 0; kb < p.KB; ++kb) {
-          if (!mbar_wait(&empty[slot], ph ^ 1u, s_flags, lim)) {
+          if (!mbar_wait(&pempty[slot], ph ^ 1u, s_flags, lim)) {
             aborted = true;
-            s_flags[0] = 1;
-            set_status(p.status, DEV_TIMEOUT);
             break;
           }
-          uint8_t* st = stages + slot * GT_STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[slot], tb + GT_B_BYTES);
-          bulk_g2s_stream(st + GT_A_BYTES + GT_B_BYTES, base + (size_t)kb * tb, tb, &full[slot], pol);
-          tma_load_2d(st + GT_A_BYTES, &tmap_b, kb * TILE_K, it.p0, &full[slot]);
+          mbar_arrive_expect_tx(&pfull[slot], tb * (uint32_t)it.nr);
+          for (int r = 0; r < it.nr; ++r)
+            bulk_g2s_stream(smem + GT_OFF_P + slot * GT_P_BYTES + r * GT_P_TILE, base + r * rt_stride + (size_t)kb * tb,
+                            tb, &pfull[slot], pol);
           ++issued;
-          if (++slot == GT_STAGES) {
+          if (++slot == GT_PSTAGES) {
             slot = 0;
             ph ^= 1u;
           }
         }
       }
       if (aborted) {
+        s_flags[0] = 1;
+        set_status(p.status, DEV_TIMEOUT);
         volatile int never = 0;
-        for (int b = 0; b < GT_STAGES && b < issued; ++b) {
+        for (int b = 0; b < GT_PSTAGES && b < issued; ++b) {
           if (--slot < 0) {
-            slot = GT_STAGES - 1;
+            slot = GT_PSTAGES - 1;
             ph ^= 1u;
           }
-          mbar_wait(&full[slot], ph, &never, lim);
+          mbar_wait(&pfull[slot], ph, &never, lim);
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == GT_WARP_BPROD) {
+    // ------------------------------------------------ activation tiles (L2), TMA tensor loads
+    if (lane == 0) {
+      int slot = 0, issued = 0;
+      uint32_t ph = 0;
+      bool aborted = false;
+      for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x) {
+        const GtItem it = gt_decode(p, s_istart, s_off, i);
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!mbar_wait(&bempty[slot], ph ^ 1u, s_flags, lim)) {
+            aborted = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&bfull[slot], GT_B_BYTES);
+          tma_load_2d(smem + GT_OFF_B + slot * GT_B_BYTES, &tmap_b, kb * TILE_K, it.p0, &bfull[slot]);
+          // Warm L2 with a tile needed a few loads from now (same token tile).
+          if (kb + GT_BPREFETCH < p.KB) tma_prefetch_2d(&tmap_b, (kb + GT_BPREFETCH) * TILE_K, it.p0);
+          ++issued;
+          if (++slot == GT_BSTAGES) {
+            slot = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (aborted) {
+        s_flags[0] = 1;
+        set_status(p.status, DEV_TIMEOUT);
+        volatile int never = 0;
+        for (int b = 0; b < GT_BSTAGES && b < issued; ++b) {
+          if (--slot < 0) {
+            slot = GT_BSTAGES - 1;
+            ph ^= 1u;
+          }
+          mbar_wait(&bfull[slot], ph, &never, lim);
+        }
+      }
+    }
+  } else if (warp == GT_WARP_MMA) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int slot = 0;
-      uint32_t ph = 0;
+      const uint32_t a_lo0 = smem_desc_sw128_lo(smem_u32(smem + GT_OFF_A));
+      const uint32_t b_lo0 = smem_desc_sw128_lo(smem_u32(smem + GT_OFF_B));
+      int as = 0, bs = 0;
+      uint32_t aph = 0, bph = 0;
       bool aborted = false;
       int j = 0;
       for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x, ++j) {
-        const GtItem it = gt_decode(p, s_istart, i);
+        const GtItem it = gt_decode(p, s_istart, s_off, i);
         const int buf = j & 1;
-        const uint32_t aph = (uint32_t)((j >> 1) & 1);
-        if (!mbar_wait(&acc_empty[buf], aph ^ 1u, s_flags, lim)) {
+        if (!mbar_wait(&acc_empty[buf], ((uint32_t)(j >> 1) & 1u) ^ 1u, s_flags, lim)) {
           aborted = true;
           break;
         }
         tc_fence_after();
         const int npad = max(16, (it.n + 15) & ~15);
         const uint32_t idesc = idesc_bf16(128, npad);
-        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * GT_N);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * GT_R * GT_N);
         for (int kb = 0; kb < p.KB; ++kb) {
-          if (!mbar_wait(&full[slot], ph, s_flags, lim) || !mbar_wait(&aready[slot], ph, s_flags, lim)) {
+          if (!mbar_wait(&afull[as], aph, s_flags, lim) || !mbar_wait(&bfull[bs], bph, s_flags, lim)) {
             aborted = true;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(stages + slot * GT_STAGE_BYTES);
-          const uint32_t b_addr = a_addr + GT_A_BYTES;
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(d_tmem, smem_desc_sw128(a_addr + ks * 32), smem_desc_sw128(b_addr + ks * 32), idesc,
-                      (kb | ks) ? 1u : 0u);
-          umma_commit(&empty[slot]);
-          if (++slot == GT_STAGES) {
-            slot = 0;
-            ph ^= 1u;
+          // Descriptor low words of this stage's A and B tiles (k-step 0).
+          const uint32_t a_lo = a_lo0 + (uint32_t)as * (GT_A_BYTES >> 4);
+          const uint32_t b_lo = b_lo0 + (uint32_t)bs * (GT_B_BYTES >> 4);
+          for (int r = 0; r < it.nr; ++r) {
+            const uint32_t ar = a_lo + (uint32_t)r * (GT_A_TILE >> 4);
+            const uint32_t dr = d_tmem + (uint32_t)(r * GT_N);
+            umma_bf16(dr, desc_from_lo(ar), desc_from_lo(b_lo), idesc, kb ? 1u : 0u);
+            umma_bf16_acc(dr, desc_from_lo(ar + 2), desc_from_lo(b_lo + 2), idesc);
+            umma_bf16_acc(dr, desc_from_lo(ar + 4), desc_from_lo(b_lo + 4), idesc);
+            umma_bf16_acc(dr, desc_from_lo(ar + 6), desc_from_lo(b_lo + 6), idesc);
+          }
+          umma_commit(&aempty[as]);
+          umma_commit(&bempty[bs]);
+          if (++as == GT_ASTAGES) {
+            as = 0;
+            aph ^= 1u;
+          }
+          if (++bs == GT_BSTAGES) {
+            bs = 0;
+            bph ^= 1u;
           }
         }
         if (!aborted) umma_commit(&acc_full[buf]);
@@ -332,37 +443,49 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
       volatile int never = 0;
       mbar_wait(mma_done, 0, &never, lim);
     }
-  } else if (warp < 2 + GT_DQ_WARPS) {
-    // ------------------------------------------------ dequantisers
-    const int rg = warp - 2;
-    int slot = 0;
-    uint32_t ph = 0;
-    bool aborted = false;
-    for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x) {
-      const GtItem it = gt_decode(p, s_istart, i);
+  } else if (warp < GT_WARP_EPI0) {
+    // ------------------------------------------------ dequantisers: packed tile -> bf16 operand tile
+    // Group r (8 warps, one per 16-row group) expands row tile r of each
+    // k-block. For an item with one row tile, group 1 only arrives.
+    const int dq = warp - GT_WARP_DQ0;
+    const int grp = dq >> 3, rg = dq & 7;
+    int ps = 0, as = 0;
+    uint32_t pph = 0, aph = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      const GtItem it = gt_decode(p, s_istart, s_off, i);
       const int fmt = gt_expert_fmt(p, it.e);
+      const bool mine = grp < it.nr;
       for (int kb = 0; kb < p.KB; ++kb) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], ph, s_flags, lim))) {
-          aborted = true;
-          if (lane == 0) {
-            s_flags[0] = 1;
-            set_status(p.status, DEV_TIMEOUT);
-          }
-          break;
+        ok = __all_sync(0xffffffffu, mbar_wait(&pfull[ps], pph, s_flags, lim)) &&
+             __all_sync(0xffffffffu, mbar_wait(&aempty[as], aph ^ 1u, s_flags, lim));
+        if (!ok) break;
+        if (mine) {
+          const uint8_t* pt = smem + GT_OFF_P + ps * GT_P_BYTES + grp * GT_P_TILE;
+          uint8_t* at = smem + GT_OFF_A + as * GT_A_BYTES + grp * GT_A_TILE;
+          if (fmt == FMT_NVFP4) gt_dequant_slot<FMT_NVFP4>(pt, at, rg, lane, s_e4m3);
+          else if (fmt == FMT_MXFP4) gt_dequant_slot<FMT_MXFP4>(pt, at, rg, lane, s_e4m3);
+          else gt_dequant_slot<FMT_NF3>(pt, at, rg, lane, s_e4m3);
+          fence_async_smem();
         }
-        uint8_t* st = stages + slot * GT_STAGE_BYTES;
-        const uint8_t* pt = st + GT_A_BYTES + GT_B_BYTES;
-        if (fmt == FMT_NVFP4) gt_dequant_slot<FMT_NVFP4>(pt, st, rg, lane, s_e4m3);
-        else if (fmt == FMT_MXFP4) gt_dequant_slot<FMT_MXFP4>(pt, st, rg, lane, s_e4m3);
-        else gt_dequant_slot<FMT_NF3>(pt, st, rg, lane, s_e4m3);
-        fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&aready[slot]);
-        if (++slot == GT_STAGES) {
-          slot = 0;
-          ph ^= 1u;
+        if (lane == 0) {
+          mbar_arrive(&pempty[ps]);
+          mbar_arrive(&afull[as]);
+        }
+        if (++ps == GT_PSTAGES) {
+          ps = 0;
+          pph ^= 1u;
+        }
+        if (++as == GT_ASTAGES) {
+          as = 0;
+          aph ^= 1u;
         }
       }
+    }
+    if (!ok && lane == 0) {
+      s_flags[0] = 1;
+      set_status(p.status, DEV_TIMEOUT);
     }
   } else {
     // ------------------------------------------------ epilogue
@@ -371,10 +494,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     const int S = p.T * p.topk;
     int j = 0;
     for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++j) {
-      const GtItem it = gt_decode(p, s_istart, i);
+      const GtItem it = gt_decode(p, s_istart, s_off, i);
       const int buf = j & 1;
-      const uint32_t aph = (uint32_t)((j >> 1) & 1);
-      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], aph, s_flags, lim))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (uint32_t)(j >> 1) & 1u, s_flags, lim))) {
         if (lane == 0) {
           s_flags[0] = 1;
           set_status(p.status, DEV_TIMEOUT);
@@ -382,32 +504,37 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * GT_N);
-      for (int c0 = 0; c0 < it.n; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(taddr + (uint32_t)c0, v);
-        tmem_wait_ld();
-        if (p.which == 13) {
-          const float gsc = p.tab.g13[it.e];
-          const int w = row & 15;
-          const int ch = it.rt * 64 + (row >> 4) * 8 + (w & 7);
+      for (int r = 0; r < it.nr; ++r) {
+        const int rt = it.rt + r;
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((buf * GT_R + r) * GT_N);
+        for (int c0 = 0; c0 < it.n; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + (uint32_t)c0, v);
+          tmem_wait_ld();
+          if (p.which == 13) {
+            const float gsc = p.tab.g13[it.e];
+            const int w = row & 15;
+            const int ch = rt * 64 + (row >> 4) * 8 + (w & 7);
+            __nv_bfloat16* hrow = p.h_out + (size_t)(it.p0 + c0) * p.I + ch;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float up = __shfl_down_sync(0xffffffffu, __uint_as_float(v[c]), 8);
-            if (w < 8 && c0 + c < it.n) {
-              const float gate = __uint_as_float(v[c]) * gsc;
-              p.h_out[(size_t)(it.p0 + c0 + c) * p.I + ch] = __float2bfloat16_rn(silu_f(gate) * (up * gsc));
+            for (int c = 0; c < 32; ++c) {
+              const float up = __shfl_down_sync(0xffffffffu, __uint_as_float(v[c]), 8);
+              if (w < 8 && c0 + c < it.n)
+                hrow[(size_t)c * p.I] = __float2bfloat16_rn(silu_f(__uint_as_float(v[c]) * gsc) * (up * gsc));
             }
-          }
-        } else {
-          const float gsc = p.tab.g2[it.e];
-          const int orow = it.rt * 128 + row;
+          } else {
+            const float gsc = p.tab.g2[it.e];
+            const int orow = rt * 128 + row;
+            // slot of column c0 + lane, broadcast per column below
+            int my_s = -1;
+            if (c0 + lane < it.n) my_s = p.perm[it.p0 + c0 + lane];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            if (c0 + c < it.n) {
-              const int s = p.perm[it.p0 + c0 + c];
-              if (s >= 0 && s < S) p.y_out[(size_t)s * p.H + orow] = __uint_as_float(v[c]) * gsc;
-              else if (lane == 0) set_status(p.status, DEV_BAD_ROUTE);
+            for (int c = 0; c < 32; ++c) {
+              const int s = __shfl_sync(0xffffffffu, my_s, c);
+              if (c0 + c < it.n) {
+                if (s >= 0 && s < S) p.y_out[(size_t)s * p.H + orow] = __uint_as_float(v[c]) * gsc;
+                else if (lane == 0) set_status(p.status, DEV_BAD_ROUTE);
+              }
             }
           }
         }
@@ -419,7 +546,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == GT_WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem_base, GT_TMEM_COLS);
   }

@@ -40,7 +40,6 @@ struct StreamParams {
   int H, I, E, topk, T;
   int rows, K;         // this matrix: rows = 2I or H, K = H or I
   int RT, KB;          // row tiles, k-blocks
-  int KS;              // k-splits per (group, row tile); 1 = no split
   int kbs;             // k-blocks per pipeline stage
   int group_tokens;    // tokens per token group (<= 8)
   int tier_mask;       // bit 0: kept experts, bit 1: NF3 experts
@@ -50,9 +49,6 @@ struct StreamParams {
   const int* perm;
   const __nv_bfloat16* act;  // x [T][H] or h [S][I]
   int act_stride;
-  float* part;               // [KS][gmax][RT][256 slots] float4 split partials (KS > 1)
-  int gmax;                  // token groups the partial buffer holds (KS > 1)
-  int* counters;             // [gmax][RT] split arrivals, self-cleaning
   int* queue;                // [2] work-queue head and finished-CTA count, self-cleaning
   __nv_bfloat16* h_out;      // which == 13: [S][I] bf16, row = permuted position p
   float* y_out;              // which == 2:  [S][H] fp32, row = flat slot s

@@ -6,33 +6,32 @@
 // launch accumulates instead of zeroing. Here each routed expert's packed
 // weights are streamed from HBM once per group of up to 8 of its tokens.
 //
-// Work item = (token group, row tile of 128 weight rows, k-split). A token
-// group is up to 8 consecutive permuted slots of one expert, so at T <= 8
-// there is exactly one group per touched expert. Persistent CTAs pull
-// items from a global work queue that resets itself. One producer lane
-// streams each item's packed tiles and the group's activation rows into a
-// 4-stage shared-memory ring with 1D bulk copies (TMA engine). It writes
-// the item number into each stage header, and a terminator stage ends the
-// consumers' loop. Eight consumer warps, one per 16-row group, dequantise
-// in registers (prmt byte-table lookups; E4M3 scales from a shared table;
-// bf16x2 scale multiply) and issue m16n8k16 bf16 MMAs with the tokens as
-// the N=8 side. Accumulation is fp32, with two accumulator sets per thread.
-//
-// Split-K is used only when there are too few items to fill the GPU (the
-// host chooses it from T). Partials are combined without atomics on data.
-// Each split writes a float4 per thread. One thread per CTA counts arrivals
-// at a per-(group, row tile) counter. The last split sums all partials in
-// split order, which is deterministic, and runs the epilogue:
+// Work item = (token group, row tile of 128 weight rows), over the whole K
+// extent. A token group is up to 8 consecutive permuted slots of one expert,
+// so at T <= 8 there is exactly one group per touched expert. Persistent
+// CTAs (2 per SM) pull items from a global work queue that resets itself.
+// One producer lane streams each item's packed tiles and the group's
+// activation rows into a 4-stage shared-memory ring with 1D bulk copies
+// (TMA engine). It writes the item number into each stage header, and a
+// terminator stage ends the consumers' loop. Eight consumer warps, one per
+// 16-row group, dequantise in registers (prmt byte-table lookups; E4M3
+// scales from a shared table; bf16x2 scale multiply) and issue m16n8k16
+// bf16 MMAs with the tokens as the N=8 side. Accumulation is fp32, with two
+// accumulator sets per thread. The epilogue writes straight from registers:
 //   W13: h[p][c] = bf16(silu(g13 * gate) * (g13 * up)), SwiGLU fused.
 //   W2:  y[s][r] = g2 * sum, fp32, indexed by the flat slot s.
 // The finalize kernel then applies the gates and sums each token's k slots
-// in slot order.
+// in slot order, so every output element is summed in a fixed order.
+// Splitting K across CTAs was measured slower at every batch size (the
+// cross-CTA reduction costs more than the idle SMs it fills), so items
+// always cover the whole K extent.
 #include "common.cuh"
 #include "internal.h"
 
 namespace hmoe {
 
 constexpr int SK_CONSUMER_WARPS = 8;
+constexpr int SK_WARP_PRODUCER = SK_CONSUMER_WARPS;       // warp 8
 constexpr int SK_THREADS = (SK_CONSUMER_WARPS + 1) * 32;
 constexpr int SK_STAGES = 4;
 constexpr int SK_MAX_KBS = 4;
@@ -42,12 +41,12 @@ constexpr int SK_X_BYTES = 8 * SK_XROW;
 constexpr int SK_HDR_BYTES = 16;                           // {item, stage} written by the producer
 constexpr int SK_STAGE_BYTES = SK_W_BYTES + SK_X_BYTES + SK_HDR_BYTES;
 constexpr int SK_SMEM_DATA = SK_STAGES * SK_STAGE_BYTES;
-constexpr int SK_NBAR = 2 * SK_STAGES + 2;
+constexpr int SK_NBAR = 2 * SK_STAGES;
 constexpr int SK_SMEM_BYTES = SK_SMEM_DATA + SK_NBAR * 8 + (MAX_E + 1) * 4 + 4 * 4 + 256 * 2;
 static_assert(SK_STAGE_BYTES % 16 == 0, "stage alignment");
 
 struct SkItem {
-  int e, p0, n, rt, ks, grp;
+  int e, p0, n, rt, grp;
 };
 
 __device__ __forceinline__ int expert_fmt(const StreamParams& p, int e) {
@@ -56,10 +55,8 @@ __device__ __forceinline__ int expert_fmt(const StreamParams& p, int e) {
 
 __device__ __forceinline__ SkItem decode_item(const StreamParams& p, const int* s_gstart, int i) {
   SkItem it;
-  it.ks = i % p.KS;
-  const int r = i / p.KS;
-  it.rt = r % p.RT;
-  it.grp = r / p.RT;
+  it.rt = i % p.RT;
+  it.grp = i / p.RT;
   int lo = 0, hi = p.E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -180,10 +177,8 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SK_SMEM_DATA);
   uint64_t* empty = full + SK_STAGES;
-  uint64_t* epi_a = empty + SK_STAGES;     // consumer warps -> warp 0 (partials written)
-  uint64_t* epi_b = epi_a + 1;             // warp 0 -> consumer warps (arrival counted)
-  int* s_gstart = reinterpret_cast<int*>(epi_b + 1);
-  volatile int* s_flags = s_gstart + MAX_E + 1;  // [0] abort, [1] last-arriver
+  int* s_gstart = reinterpret_cast<int*>(empty + SK_STAGES);
+  volatile int* s_flags = s_gstart + MAX_E + 1;  // [0] abort
   uint16_t* s_e4m3 = reinterpret_cast<uint16_t*>(const_cast<int*>(s_flags) + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint64_t lim = p.wait_limit_ns;
@@ -193,15 +188,12 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], SK_CONSUMER_WARPS);
     }
-    mbar_init(epi_a, SK_CONSUMER_WARPS);
-    mbar_init(epi_b, 1);
     fence_mbar_init();
     s_flags[0] = 0;
-    s_flags[1] = 0;
   }
   if (tid < 256) s_e4m3[tid] = e4m3_to_bf16((uint32_t)tid);
   // Group prefix over experts of the selected tiers, from the caller's offsets.
-  if (warp == SK_CONSUMER_WARPS) {
+  if (warp == SK_WARP_PRODUCER) {
     const int S = p.T * p.topk;
     bool bad = (p.offsets[0] != 0) || (p.offsets[p.E] != S);
     int run = 0;
@@ -225,7 +217,6 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
     bad = __any_sync(0xffffffffu, bad);
-    if (p.KS > 1 && run > p.gmax) bad = true;
     if (lane == 0) {
       s_gstart[p.E] = bad ? 0 : run;
       if (bad && blockIdx.x == 0) set_status(p.status, DEV_BAD_ROUTE);
@@ -235,11 +226,10 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
   }
   __syncthreads();
 
-  const int n_items = s_gstart[p.E] * p.RT * p.KS;
-  const int kbi = p.KB / p.KS;
-  const int nst = kbi / p.kbs;
+  const int n_items = s_gstart[p.E] * p.RT;
+  const int nst = p.KB / p.kbs;
 
-  if (warp == SK_CONSUMER_WARPS) {
+  if (warp == SK_WARP_PRODUCER) {
     // ------------------------------------------------ producer: dynamic work queue
     // With the test hook set the producer stays silent, so the consumers'
     // bounded waits run out and report DEV_TIMEOUT.
@@ -280,7 +270,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
             set_status(p.status, DEV_TIMEOUT);
             break;
           }
-          const int kbA = it.ks * kbi + st * p.kbs;
+          const int kbA = st * p.kbs;
           const uint32_t wbytes = (uint32_t)(p.kbs * tb);
           const uint32_t xbytes = (uint32_t)(p.kbs * 128);
           uint8_t* sw = smem + slot * SK_STAGE_BYTES;
@@ -329,7 +319,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
     // ------------------------------------------------ consumers
     const int rg = warp, g = lane >> 2, q = lane & 3;
     int slot = 0;
-    uint32_t ph = 0, eph = 0;
+    uint32_t ph = 0;
     SkItem it{};
     int fmt = FMT_NF3;
     float accA[4], accB[4];
@@ -366,59 +356,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
       float acc[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) acc[r] = accA[r] + accB[r];
-      if (p.KS == 1) {
-        sk_emit(p, it, rg, g, q, acc);
-        continue;
-      }
-      // Split-K: write this split's float4, count arrivals, the last split sums in order.
-      const size_t cell = ((size_t)it.grp * p.RT + it.rt) * 256 + rg * 32 + lane;
-      const size_t split_stride = (size_t)p.gmax * p.RT * 256;
-      reinterpret_cast<float4*>(p.part)[(size_t)it.ks * split_stride + cell] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(epi_a);
-      if (warp == 0) {
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(epi_a, eph, s_flags, lim));
-        if (lane == 0) {
-          int last = 0;
-          if (ok) {
-            __threadfence();
-            const int old = atomicAdd(&p.counters[it.grp * p.RT + it.rt], 1);
-            last = (old == p.KS - 1);
-            if (last) p.counters[it.grp * p.RT + it.rt] = 0;
-          } else {
-            s_flags[0] = 1;
-            set_status(p.status, DEV_TIMEOUT);
-          }
-          s_flags[1] = last;
-          mbar_arrive(epi_b);
-        }
-      }
-      const bool ok2 = __all_sync(0xffffffffu, mbar_wait(epi_b, eph, s_flags, lim));
-      eph ^= 1u;
-      if (!ok2) {
-        if (lane == 0) {
-          s_flags[0] = 1;
-          set_status(p.status, DEV_TIMEOUT);
-        }
-        break;
-      }
-      if (s_flags[1]) {
-        __threadfence();
-        float4 v[8];
-#pragma unroll
-        for (int k2 = 0; k2 < 8; ++k2)
-          if (k2 < p.KS) v[k2] = __ldcg(reinterpret_cast<const float4*>(p.part) + (size_t)k2 * split_stride + cell);
-        float sum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k2 = 0; k2 < 8; ++k2)
-          if (k2 < p.KS) {
-            sum[0] += v[k2].x;
-            sum[1] += v[k2].y;
-            sum[2] += v[k2].z;
-            sum[3] += v[k2].w;
-          }
-        sk_emit(p, it, rg, g, q, sum);
-      }
+      sk_emit(p, it, rg, g, q, acc);
     }
   }
   __syncthreads();
@@ -442,7 +380,7 @@ cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st)
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  if (p.kbs < 1 || p.kbs > SK_MAX_KBS || p.group_tokens < 1 || p.group_tokens > 8 || p.KS < 1 || p.KS > 8)
+  if (p.kbs < 1 || p.kbs > SK_MAX_KBS || p.group_tokens < 1 || p.group_tokens > 8)
     return cudaErrorInvalidValue;
   stream_gemm_kernel<<<grid, SK_THREADS, SK_SMEM_BYTES, st>>>(p);
   count_launches(1);

@@ -260,6 +260,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     tmem_relinquish();
   }
   if (tid >= 96 && tid < 96 + 256) s_e4m3[tid - 96] = e4m3_to_bf16((uint32_t)(tid - 96));
+  pdl_wait();  // everything below reads or writes global memory
+  pdl_trigger();
   for (int e = tid; e <= p.E; e += blockDim.x) s_off[e] = p.offsets[e];
   __syncthreads();
   if (warp == 0) {
@@ -555,6 +557,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
 // ------------------------------------------------------------ gather of activation rows
 __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict__ perm, int S, int k,
                                    int T, int H, __nv_bfloat16* __restrict__ xg, int* status) {
+  pdl_wait();
+  pdl_trigger();
   const int vec = H / 8;  // 16-byte vectors per row
   const long long n = (long long)S * vec;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
@@ -578,9 +582,9 @@ cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int* perm, int S, i
   const long long n = (long long)S * (H / 8);
   const long long blocks = (n + 255) / 256;
   const int grid = (int)(blocks < (long long)num_sms * 8 ? blocks : (long long)num_sms * 8);
-  gather_rows_kernel<<<grid, 256, 0, st>>>(x, perm, S, k, T, H, xg, status);
+  cudaError_t e = launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, st, x, perm, S, k, T, H, xg, status);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 // ------------------------------------------------------------ host side
@@ -619,9 +623,9 @@ cudaError_t launch_grouped_gemm(const GroupedParams& p, const __nv_bfloat16* b_s
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  grouped_gemm_kernel<<<num_sms, GT_THREADS, GT_SMEM_BYTES, st>>>(p, map);
+  cudaError_t e = launch_pdl(grouped_gemm_kernel, dim3(num_sms), dim3(GT_THREADS), GT_SMEM_BYTES, st, p, map);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace hmoe

@@ -75,6 +75,8 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const float* __restri
                                                            int* __restrict__ ids, float* __restrict__ gates,
                                                            int* __restrict__ perm, int* __restrict__ offsets) {
   extern __shared__ int sm[];
+  pdl_wait();
+  pdl_trigger();
   const int S = T * k;
   int* s_ids = sm;
   int* s_cnt = sm + S;
@@ -132,6 +134,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   __shared__ int s_cnt[MAX_E];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   const int t0 = blockIdx.x * ROUTE_CHUNK_TOKENS;
   for (int i = 0; i < ROUTE_CHUNK_TOKENS / 8; ++i) {
@@ -157,6 +161,8 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int* __restrict_
                                                           int* __restrict__ offsets) {
   __shared__ int s_tot[MAX_E + 1];
   __shared__ int s_wsum[32];
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x;
   if (tid < E) {
     int run = 0;
@@ -223,6 +229,8 @@ __global__ void __launch_bounds__(256) route_place_kernel(const int* __restrict_
     s_run[e] = 0;
     for (int w = 0; w < 8; ++w) s_w[w][e] = 0;
   }
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   for (int base = s_begin; base < s_end; base += 256) {
     const int s = base + tid;
@@ -258,16 +266,21 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int* ids, flo
   const int S = T * k;
   if (S <= 1024) {
     const size_t smem = (size_t)(S + 2 * E + 1) * sizeof(int);
-    route_small_kernel<<<1, 1024, smem, st>>>(logits, T, E, k, ids, gates, perm, offsets);
+    cudaError_t e = launch_pdl(route_small_kernel, dim3(1), dim3(1024), smem, st, logits, T, E, k, ids, gates, perm,
+                               offsets);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
   }
   const int nch = route_chunks(T);
-  route_topk_kernel<<<nch, 256, 0, st>>>(logits, T, E, k, ids, gates, chunk_cnt);
-  route_scan_kernel<<<1, 1024, 0, st>>>(chunk_cnt, nch, E, S, chunk_base, offsets);
-  route_place_kernel<<<nch, 256, 0, st>>>(ids, T, E, k, chunk_base, offsets, perm);
+  cudaError_t e = launch_pdl(route_topk_kernel, dim3(nch), dim3(256), 0, st, logits, T, E, k, ids, gates, chunk_cnt);
+  if (e == cudaSuccess)
+    e = launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, st, (const int*)chunk_cnt, nch, E, S, chunk_base,
+                   offsets);
+  if (e == cudaSuccess)
+    e = launch_pdl(route_place_kernel, dim3(nch), dim3(256), 0, st, (const int*)ids, T, E, k,
+                   (const int*)chunk_base, (const int*)offsets, perm);
   count_launches(3);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace hmoe

@@ -192,6 +192,8 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
     s_flags[0] = 0;
   }
   if (tid < 256) s_e4m3[tid] = e4m3_to_bf16((uint32_t)tid);
+  pdl_wait();  // everything below reads or writes global memory
+  pdl_trigger();
   // Group prefix over experts of the selected tiers, from the caller's offsets.
   if (warp == SK_WARP_PRODUCER) {
     const int S = p.T * p.topk;
@@ -382,14 +384,16 @@ cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st)
   }
   if (p.kbs < 1 || p.kbs > SK_MAX_KBS || p.group_tokens < 1 || p.group_tokens > 8)
     return cudaErrorInvalidValue;
-  stream_gemm_kernel<<<grid, SK_THREADS, SK_SMEM_BYTES, st>>>(p);
+  cudaError_t e = launch_pdl(stream_gemm_kernel, dim3(grid), dim3(SK_THREADS), SK_SMEM_BYTES, st, p);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 // ------------------------------------------------------------ finalize
 __global__ void finalize_kernel(const float* __restrict__ y, const float* __restrict__ gates, int T, int k, int H,
                                 __nv_bfloat16* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int half = H / 2;
   const long long n = (long long)T * half;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
@@ -411,9 +415,10 @@ cudaError_t launch_finalize(const float* y, const float* gates, int T, int k, in
   if (n == 0) return cudaSuccess;
   const int threads = 256;
   const long long blocks = (n + threads - 1) / threads;
-  finalize_kernel<<<(int)(blocks < 4096 ? blocks : 4096), threads, 0, st>>>(y, gates, T, k, H, out);
+  cudaError_t e = launch_pdl(finalize_kernel, dim3((unsigned)(blocks < 4096 ? blocks : 4096)), dim3(threads), 0, st, y,
+                             gates, T, k, H, out);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace hmoe

@@ -173,7 +173,9 @@ typedef struct {
                         HMOE_ERR_DEVICE_TIMEOUT through hmoe_check_device_status. 0 in normal use. */
   void* const* stage_events; /* optional cudaEvent_t[n_stage_events], recorded on the stream at
                                 the stage boundaries: [0] before the W13 GEMM, [1] after it,
-                                [2] after the W2 GEMM, [3] after the finalize. NULL = none. */
+                                [2] after the W2 GEMM, [3] after the finalize. NULL = none.
+                                Where one launch runs both GEMMs (the streaming path at
+                                small T), [1] and [2] are both recorded after that launch. */
   int n_stage_events;
 } hmoe_forward_opts;
 

@@ -7,6 +7,7 @@
 // token count). "quant: add native mixed NVFP4/MXFP4 plus NF3 MoE serving",
 // Summary (hybrid_bit_map 4 = kept, 3 = NF3; kept_format; the metadata is
 // validated).
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -85,9 +86,12 @@ int pick_stage(int kbi) {
 }
 
 constexpr int DECODE_MAX_T = 8;
+// Token groups the fixed counter array holds. A stream-path forward whose
+// group bound exceeds it runs W13 and W2 as two launches instead of one.
+constexpr int STREAM_FUSED_MAX_GROUPS = 1024;
 
 struct WsLayout {
-  size_t status, queues, chunk_cnt, chunk_base, xg, h, y, total;
+  size_t status, queues, done13, chunk_cnt, chunk_base, xg, h, y, total;
 };
 
 // Fixed prefix (status word, work queues) first, so that it stays at the
@@ -99,6 +103,8 @@ WsLayout ws_layout(const hmoe_layer_desc& d, int T) {
   off += 256;
   w.queues = off;                       // 4 launch slots x {head, finished}
   off += 256;
+  w.done13 = off;                       // per-group W13 completion counts (fused stream launch)
+  off += align256((size_t)STREAM_FUSED_MAX_GROUPS * 4);
   // T-dependent regions from here on.
   const size_t nch = (size_t)route_chunks(T);
   w.chunk_cnt = off;
@@ -269,6 +275,7 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
                                    const WsLayout& w, const hmoe_forward_opts& o, cudaStream_t st) {
   const int tier_order = o.tier_order;
   const hmoe_layer_desc& d = L->d;
+  const int S = T * d.topk;
   StreamParams p{};
   p.kept_buf = L->kept_buf;
   p.nf3_buf = L->nf3_buf;
@@ -281,11 +288,10 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
   p.group_tokens = 8;
   p.kept_expert_bytes = L->gk.expert_bytes;
   p.nf3_expert_bytes = L->gn.expert_bytes;
-  p.kept_w2_off = L->gk.w13_bytes;
-  p.nf3_w2_off = L->gn.w13_bytes;
   p.offsets = offsets;
   p.perm = perm;
   p.status = reinterpret_cast<int*>(wsb + w.status);
+  p.done13 = reinterpret_cast<int*>(wsb + w.done13);
   p.h_out = reinterpret_cast<__nv_bfloat16*>(wsb + w.h);
   p.y_out = reinterpret_cast<float*>(wsb + w.y);
   p.tab = L->tab;
@@ -306,24 +312,38 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
     return cudaSuccess;
   };
   if (mark(0) != cudaSuccess) return cuda_fail(cudaGetLastError(), "stage event record");
-  for (int which : {13, 2}) {
-    p.which = which;
-    p.rows = which == 13 ? 2 * d.I : d.H;
-    p.K = which == 13 ? d.H : d.I;
-    p.RT = p.rows / TILE_ROWS;
-    p.KB = p.K / TILE_K;
-    p.kbs = pick_stage(p.KB);
-    p.act = which == 13 ? static_cast<const __nv_bfloat16*>(x) : p.h_out;
-    p.act_stride = which == 13 ? d.H : d.I;
+  for (int f = 0; f < 2; ++f) {
+    StreamPhase& P = p.ph[f];
+    P.rows = f == 0 ? 2 * d.I : d.H;
+    P.K = f == 0 ? d.H : d.I;
+    P.RT = P.rows / TILE_ROWS;
+    P.KB = P.K / TILE_K;
+    P.kbs = pick_stage(P.KB);
+    P.act = f == 0 ? static_cast<const __nv_bfloat16*>(x) : p.h_out;
+    P.act_stride = f == 0 ? d.H : d.I;
+    P.kept_off = f == 0 ? 0 : L->gk.w13_bytes;
+    P.nf3_off = f == 0 ? 0 : L->gn.w13_bytes;
+  }
+  // Upper bound on the token groups of one launch: every slot of an expert
+  // goes to one group of up to 8, so G <= min(S, ceil(S / 8) + E).
+  const long long g_bound = std::min<long long>(S, (S + 7) / 8 + d.E);
+  const bool fused = g_bound <= STREAM_FUSED_MAX_GROUPS;
+  // Fused: W13 and W2 run in one launch per tier selection, and the events
+  // that follow W13 and W2 are both recorded after it.
+  const int ranges[2][2] = {{0, fused ? 2 : 1}, {1, 2}};
+  for (int r = 0; r < (fused ? 1 : 2); ++r) {
+    p.ph_begin = ranges[r][0];
+    p.ph_end = ranges[r][1];
     for (int li = 0; li < 2; ++li) {
       const int m = masks[li];
       if (!m) continue;
       p.tier_mask = m;
-      p.queue = reinterpret_cast<int*>(wsb + w.queues) + 2 * ((which == 13 ? 0 : 2) + li);
+      p.queue = reinterpret_cast<int*>(wsb + w.queues) + 2 * (2 * r + li);
       cudaError_t e = launch_stream_gemm(p, grid, st);
       if (e != cudaSuccess) return cuda_fail(e, "stream GEMM launch");
     }
-    cudaError_t e = mark(which == 13 ? 1 : 2);
+    cudaError_t e = mark(fused || r == 0 ? 1 : 2);
+    if (e == cudaSuccess && fused) e = mark(2);
     if (e != cudaSuccess) return cuda_fail(e, "stage event record");
   }
   cudaError_t e = launch_finalize(p.y_out, gates, T, d.topk, d.H, static_cast<__nv_bfloat16*>(out), st);

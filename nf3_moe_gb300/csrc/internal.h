@@ -32,28 +32,34 @@ cudaError_t launch_debug_dequant(int fmt, int which, const uint8_t* src, int N, 
                                  cudaStream_t st);
 
 // ---------------------------------------------------------------- streaming GEMM (any T; the decode path)
+// One matrix of the expert FFN as the streaming kernel sees it.
+struct StreamPhase {
+  int rows, K;               // rows = 2I (W13) or H (W2); K = H or I
+  int RT, KB;                // row tiles, k-blocks
+  int kbs;                   // k-blocks per pipeline stage
+  const __nv_bfloat16* act;  // W13: x [T][H] by token; W2: h [S][I] by permuted position
+  int act_stride;
+  size_t kept_off, nf3_off;  // byte offset of this matrix inside an expert's block
+};
+
 struct StreamParams {
   const uint8_t* kept_buf;
   const uint8_t* nf3_buf;
   int kept_fmt;
-  int which;           // 13: act = x rows by token, output h;  2: act = h rows by slot, output y
   int H, I, E, topk, T;
-  int rows, K;         // this matrix: rows = 2I or H, K = H or I
-  int RT, KB;          // row tiles, k-blocks
-  int kbs;             // k-blocks per pipeline stage
-  int group_tokens;    // tokens per token group (<= 8)
-  int tier_mask;       // bit 0: kept experts, bit 1: NF3 experts
+  StreamPhase ph[2];     // [0] W13 (output h), [1] W2 (output y)
+  int ph_begin, ph_end;  // phases this launch runs: [0,2) both (W2 items wait on done13), [0,1) or [1,2)
+  int group_tokens;      // tokens per token group (<= 8)
+  int tier_mask;         // bit 0: kept experts, bit 1: NF3 experts
   size_t kept_expert_bytes, nf3_expert_bytes;
-  size_t kept_w2_off, nf3_w2_off;
   const int* offsets;
   const int* perm;
-  const __nv_bfloat16* act;  // x [T][H] or h [S][I]
-  int act_stride;
   int* queue;                // [2] work-queue head and finished-CTA count, self-cleaning
-  __nv_bfloat16* h_out;      // which == 13: [S][I] bf16, row = permuted position p
-  float* y_out;              // which == 2:  [S][H] fp32, row = flat slot s
+  int* done13;               // [token groups] finished W13 warp-items per group, self-cleaning ([0,2) only)
+  __nv_bfloat16* h_out;      // W13 output: [S][I] bf16, row = permuted position p
+  float* y_out;              // W2 output:  [S][H] fp32, row = flat slot s
   int* status;
-  unsigned long long wait_limit_ns;  // bound on every mbarrier wait
+  unsigned long long wait_limit_ns;  // bound on every wait
   int debug_no_copies;               // test hook: the producer issues nothing
   ExpertTable tab;
 };

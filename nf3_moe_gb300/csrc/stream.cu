@@ -6,18 +6,29 @@
 // launch accumulates instead of zeroing. Here each routed expert's packed
 // weights are streamed from HBM once per group of up to 8 of its tokens.
 //
-// Work item = (token group, row tile of 128 weight rows), over the whole K
-// extent. A token group is up to 8 consecutive permuted slots of one expert,
-// so at T <= 8 there is exactly one group per touched expert. Persistent
-// CTAs (2 per SM) pull items from a global work queue that resets itself.
+// One launch runs both matrices of the expert FFN. Work items are first
+// every (token group, W13 row tile), then every (token group, W2 row tile),
+// each over the whole K extent. A token group is up to 8 consecutive
+// permuted slots of one expert, so at T <= 8 there is exactly one group per
+// touched expert. Persistent CTAs (2 per SM) pull items from a global work
+// queue that resets itself. A W2 item reads the group's h rows, so its
+// producer first waits (bounded) until every W13 item of that group has
+// been written: each consumer warp counts its finished W13 items into a
+// per-group counter with release semantics. W13 items never wait on
+// anything, and every W13 item is dequeued before any W2 item, so the waits
+// always end. The W13 tail overlaps the W2 start, and there is one launch
+// instead of two. (Past the counter array's capacity the host runs the two
+// phases as two launches of the same kernel.)
+//
 // One producer lane streams each item's packed tiles and the group's
 // activation rows into a 4-stage shared-memory ring with 1D bulk copies
 // (TMA engine). It writes the item number into each stage header, and a
 // terminator stage ends the consumers' loop. Eight consumer warps, one per
 // 16-row group, dequantise in registers (prmt byte-table lookups; E4M3
-// scales from a shared table; bf16x2 scale multiply) and issue m16n8k16
-// bf16 MMAs with the tokens as the N=8 side. Accumulation is fp32, with two
-// accumulator sets per thread. The epilogue writes straight from registers:
+// scales from a shared table of bf16 pairs; bf16x2 scale multiply) and
+// issue m16n8k16 bf16 MMAs with the tokens as the N=8 side. Accumulation is
+// fp32, with two accumulator sets per thread. The epilogue writes straight
+// from registers:
 //   W13: h[p][c] = bf16(silu(g13 * gate) * (g13 * up)), SwiGLU fused.
 //   W2:  y[s][r] = g2 * sum, fp32, indexed by the flat slot s.
 // The finalize kernel then applies the gates and sums each token's k slots
@@ -42,11 +53,11 @@ constexpr int SK_HDR_BYTES = 16;                           // {item, stage} writ
 constexpr int SK_STAGE_BYTES = SK_W_BYTES + SK_X_BYTES + SK_HDR_BYTES;
 constexpr int SK_SMEM_DATA = SK_STAGES * SK_STAGE_BYTES;
 constexpr int SK_NBAR = 2 * SK_STAGES;
-constexpr int SK_SMEM_BYTES = SK_SMEM_DATA + SK_NBAR * 8 + (MAX_E + 1) * 4 + 4 * 4 + 256 * 2;
+constexpr int SK_SMEM_BYTES = SK_SMEM_DATA + SK_NBAR * 8 + (MAX_E + 1) * 4 + 4 * 4 + 256 * 4;
 static_assert(SK_STAGE_BYTES % 16 == 0, "stage alignment");
 
 struct SkItem {
-  int e, p0, n, rt, grp;
+  int e, p0, n, rt, grp, ph;  // ph: 0 = W13, 1 = W2
 };
 
 __device__ __forceinline__ int expert_fmt(const StreamParams& p, int e) {
@@ -55,8 +66,12 @@ __device__ __forceinline__ int expert_fmt(const StreamParams& p, int e) {
 
 __device__ __forceinline__ SkItem decode_item(const StreamParams& p, const int* s_gstart, int i) {
   SkItem it;
-  it.rt = i % p.RT;
-  it.grp = i / p.RT;
+  const int n13 = p.ph_begin == 0 ? s_gstart[p.E] * p.ph[0].RT : 0;
+  it.ph = i >= n13 ? 1 : 0;
+  const int local = it.ph ? i - n13 : i;
+  const int RT = p.ph[it.ph].RT;
+  it.rt = local % RT;
+  it.grp = local / RT;
   int lo = 0, hi = p.E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -79,7 +94,7 @@ __device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it,
     const int c = 2 * q + h;
     if (c >= it.n) continue;
     const int pp = it.p0 + c;
-    if (p.which == 13) {
+    if (it.ph == 0) {
       const float gsc = p.tab.g13[it.e];
       const int ch = it.rt * 64 + rg * 8 + g;
       const float gate = v[h] * gsc, up = v[2 + h] * gsc;
@@ -102,7 +117,7 @@ __device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it,
 // shared lookup table, NF3 scale applied to the fp32 sum) and 4 MMAs.
 template <int FMT>
 __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xrow, int rg, int lane,
-                                          const uint16_t* s_e4m3, float* acc) {
+                                          const uint32_t* s_e4m3, float* acc) {
   const uint4 xa = *reinterpret_cast<const uint4*>(xrow);
   const uint4 xb = *reinterpret_cast<const uint4*>(xrow + 16);
   const uint32_t xr[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
@@ -110,15 +125,14 @@ __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xr
   uint32_t r0[8], r1[8];
   if constexpr (FMT == FMT_NVFP4 || FMT == FMT_MXFP4) {
     const uint4 q = *reinterpret_cast<const uint4*>(tile + slot * 16);
-    uint32_t sc;
     uint32_t s0, s1;
     if constexpr (FMT == FMT_NVFP4) {
-      sc = *reinterpret_cast<const uint16_t*>(tile + 4096 + slot * 2);
-      s0 = bf16_bcast(s_e4m3[sc & 0xFFu]);
-      s1 = bf16_bcast(s_e4m3[sc >> 8]);
+      // Byte loads index a table of bf16 pairs directly: no extract, no broadcast.
+      s0 = s_e4m3[tile[4096 + slot * 2]];
+      s1 = s_e4m3[tile[4096 + slot * 2 + 1]];
     } else {
       const int g = lane >> 2, hq = (lane & 3) >> 1;
-      sc = *reinterpret_cast<const uint16_t*>(tile + 4096 + (rg * 16 + g * 2 + hq) * 2);
+      const uint32_t sc = *reinterpret_cast<const uint16_t*>(tile + 4096 + (rg * 16 + g * 2 + hq) * 2);
       s0 = bf16_bcast(e8m0_to_bf16(sc & 0xFFu));
       s1 = bf16_bcast(e8m0_to_bf16(sc >> 8));
     }
@@ -147,9 +161,10 @@ __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xr
     nf3x8_to_bf16x2(sel[1], r0 + 4);
     nf3x8_to_bf16x2(sel[2], r1);
     nf3x8_to_bf16x2(sel[3], r1 + 4);
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    float d[4];
+    mma_bf16_16816_zc(d, r0[0], r1[0], r0[1], r1[1], xr[0], xr[1]);
 #pragma unroll
-    for (int s = 0; s < 4; ++s)
+    for (int s = 1; s < 4; ++s)
       mma_bf16_16816(d, r0[2 * s], r1[2 * s], r0[2 * s + 1], r1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
     acc[0] = fmaf(sc0, d[0], acc[0]);
     acc[1] = fmaf(sc0, d[1], acc[1]);
@@ -161,7 +176,7 @@ __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xr
 // All k-blocks of one stage, two accumulator sets to break the MMA chain.
 template <int FMT>
 __device__ __forceinline__ void sk_stage(const uint8_t* sw, const uint8_t* sx, int kbs, int rg, int lane,
-                                         const uint16_t* s_e4m3, float* accA, float* accB) {
+                                         const uint32_t* s_e4m3, float* accA, float* accB) {
   constexpr int TB = tile_bytes(FMT);
   if (kbs == 4) {
     sk_kblock<FMT>(sw, sx, rg, lane, s_e4m3, accA);
@@ -179,7 +194,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
   uint64_t* empty = full + SK_STAGES;
   int* s_gstart = reinterpret_cast<int*>(empty + SK_STAGES);
   volatile int* s_flags = s_gstart + MAX_E + 1;  // [0] abort
-  uint16_t* s_e4m3 = reinterpret_cast<uint16_t*>(const_cast<int*>(s_flags) + 4);
+  uint32_t* s_e4m3 = reinterpret_cast<uint32_t*>(const_cast<int*>(s_flags) + 4);  // E4M3 -> bf16 pair
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint64_t lim = p.wait_limit_ns;
 
@@ -191,7 +206,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
     fence_mbar_init();
     s_flags[0] = 0;
   }
-  if (tid < 256) s_e4m3[tid] = e4m3_to_bf16((uint32_t)tid);
+  if (tid < 256) s_e4m3[tid] = bf16_bcast(e4m3_to_bf16((uint32_t)tid));
   pdl_wait();  // everything below reads or writes global memory
   pdl_trigger();
   // Group prefix over experts of the selected tiers, from the caller's offsets.
@@ -228,8 +243,11 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
   }
   __syncthreads();
 
-  const int n_items = s_gstart[p.E] * p.RT;
-  const int nst = p.KB / p.kbs;
+  const int n_groups = s_gstart[p.E];
+  int rt_sum = 0;
+  for (int f = p.ph_begin; f < p.ph_end; ++f) rt_sum += p.ph[f].RT;
+  const int n_items = n_groups * rt_sum;
+  const bool fused = p.ph_begin == 0 && p.ph_end == 2;
 
   if (warp == SK_WARP_PRODUCER) {
     // ------------------------------------------------ producer: dynamic work queue
@@ -246,15 +264,16 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
         const int i = atomicAdd(p.queue, 1);
         if (i >= n_items) break;
         const SkItem it = decode_item(p, s_gstart, i);
+        const StreamPhase& P = p.ph[it.ph];
         const int fmt = expert_fmt(p, it.e);
         const size_t tb = (size_t)tile_bytes(fmt);
         const uint8_t* base = (fmt == FMT_NF3 ? p.nf3_buf : p.kept_buf) +
                               (size_t)(p.tab.loc[it.e] & 0x7FFF) *
                                   (fmt == FMT_NF3 ? p.nf3_expert_bytes : p.kept_expert_bytes) +
-                              (p.which == 2 ? (fmt == FMT_NF3 ? p.nf3_w2_off : p.kept_w2_off) : 0);
+                              (fmt == FMT_NF3 ? P.nf3_off : P.kept_off);
         int rows[8];
         for (int j = 0; j < it.n; ++j) {
-          if (p.which == 13) {
+          if (it.ph == 0) {
             int s = p.perm[it.p0 + j];
             if (s < 0 || s >= S) {
               set_status(p.status, DEV_BAD_ROUTE);
@@ -265,6 +284,18 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
             rows[j] = it.p0 + j;
           }
         }
+        if (fused && it.ph == 1) {
+          // The group's h rows come from its W13 items (any CTA): wait until
+          // all of them are written, then order the bulk copies after.
+          if (!wait_count_at_least(p.done13 + it.grp, SK_CONSUMER_WARPS * p.ph[0].RT, s_flags, lim)) {
+            aborted = true;
+            s_flags[0] = 1;
+            set_status(p.status, DEV_TIMEOUT);
+            break;
+          }
+          fence_proxy_async_global();
+        }
+        const int nst = P.KB / P.kbs;
         for (int st = 0; st < nst; ++st) {
           if (!mbar_wait(&empty[slot], ph ^ 1u, s_flags, lim)) {
             aborted = true;
@@ -272,18 +303,18 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
             set_status(p.status, DEV_TIMEOUT);
             break;
           }
-          const int kbA = st * p.kbs;
-          const uint32_t wbytes = (uint32_t)(p.kbs * tb);
-          const uint32_t xbytes = (uint32_t)(p.kbs * 128);
+          const int kbA = st * P.kbs;
+          const uint32_t wbytes = (uint32_t)(P.kbs * tb);
+          const uint32_t xbytes = (uint32_t)(P.kbs * 128);
           uint8_t* sw = smem + slot * SK_STAGE_BYTES;
           uint8_t* sx = sw + SK_W_BYTES;
           int* hdr = reinterpret_cast<int*>(sx + SK_X_BYTES);
           hdr[0] = i;
           hdr[1] = st;
           mbar_arrive_expect_tx(&full[slot], wbytes + (uint32_t)it.n * xbytes);
-          bulk_g2s_stream(sw, base + ((size_t)it.rt * p.KB + kbA) * tb, wbytes, &full[slot], pol);
+          bulk_g2s_stream(sw, base + ((size_t)it.rt * P.KB + kbA) * tb, wbytes, &full[slot], pol);
           for (int j = 0; j < it.n; ++j)
-            bulk_g2s(sx + j * SK_XROW, p.act + (size_t)rows[j] * p.act_stride + (size_t)kbA * 64, xbytes,
+            bulk_g2s(sx + j * SK_XROW, P.act + (size_t)rows[j] * P.act_stride + (size_t)kbA * 64, xbytes,
                      &full[slot]);
           ++issued;
           if (++slot == SK_STAGES) {
@@ -323,7 +354,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
     int slot = 0;
     uint32_t ph = 0;
     SkItem it{};
-    int fmt = FMT_NF3;
+    int fmt = FMT_NF3, kbs = 1, nst = 1;
     float accA[4], accB[4];
     while (true) {
       if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], ph, s_flags, lim))) {
@@ -340,13 +371,15 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
       if (st == 0) {
         it = decode_item(p, s_gstart, i);
         fmt = expert_fmt(p, it.e);
+        kbs = p.ph[it.ph].kbs;
+        nst = p.ph[it.ph].KB / kbs;
 #pragma unroll
         for (int r = 0; r < 4; ++r) accA[r] = accB[r] = 0.f;
       }
       const uint8_t* sx = sw + SK_W_BYTES + g * SK_XROW + q * 32;
-      if (fmt == FMT_NVFP4) sk_stage<FMT_NVFP4>(sw, sx, p.kbs, rg, lane, s_e4m3, accA, accB);
-      else if (fmt == FMT_MXFP4) sk_stage<FMT_MXFP4>(sw, sx, p.kbs, rg, lane, s_e4m3, accA, accB);
-      else sk_stage<FMT_NF3>(sw, sx, p.kbs, rg, lane, s_e4m3, accA, accB);
+      if (fmt == FMT_NVFP4) sk_stage<FMT_NVFP4>(sw, sx, kbs, rg, lane, s_e4m3, accA, accB);
+      else if (fmt == FMT_MXFP4) sk_stage<FMT_MXFP4>(sw, sx, kbs, rg, lane, s_e4m3, accA, accB);
+      else sk_stage<FMT_NF3>(sw, sx, kbs, rg, lane, s_e4m3, accA, accB);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
       if (++slot == SK_STAGES) {
@@ -359,12 +392,28 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
 #pragma unroll
       for (int r = 0; r < 4; ++r) acc[r] = accA[r] + accB[r];
       sk_emit(p, it, rg, g, q, acc);
+      if (fused && it.ph == 0) {
+        // Publish this warp's h rows to the W2 producers, whose bulk copies
+        // (async proxy) may run on any SM: every lane fences its own stores
+        // (proxy, then gpu scope), the warp synchronises, and lane 0 fences
+        // again before one count per warp.
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          atomicAdd(p.done13 + it.grp, 1);
+        }
+      }
     }
   }
   __syncthreads();
   if (tid == 0) {
-    // The last CTA to leave resets the work queue for the next launch.
+    // The last CTA to leave resets the work queue and the group counters
+    // for the next launch.
     if (atomicAdd(p.queue + 1, 1) == (int)gridDim.x - 1) {
+      if (fused)
+        for (int g = 0; g < n_groups; ++g) p.done13[g] = 0;
       p.queue[0] = 0;
       p.queue[1] = 0;
       __threadfence();
@@ -382,8 +431,11 @@ cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st)
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  if (p.kbs < 1 || p.kbs > SK_MAX_KBS || p.group_tokens < 1 || p.group_tokens > 8)
-    return cudaErrorInvalidValue;
+  if (p.ph_begin < 0 || p.ph_begin >= p.ph_end || p.ph_end > 2) return cudaErrorInvalidValue;
+  if (p.ph_begin == 0 && p.ph_end == 2 && !p.done13) return cudaErrorInvalidValue;
+  for (const StreamPhase& P : p.ph)
+    if (P.kbs < 1 || P.kbs > SK_MAX_KBS || P.KB % P.kbs != 0) return cudaErrorInvalidValue;
+  if (p.group_tokens < 1 || p.group_tokens > 8) return cudaErrorInvalidValue;
   cudaError_t e = launch_pdl(stream_gemm_kernel, dim3(grid), dim3(SK_THREADS), SK_SMEM_BYTES, st, p);
   count_launches(1);
   return e;

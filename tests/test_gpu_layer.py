@@ -138,3 +138,23 @@ def test_full_size_hybrid_decode(hybrid256, T):
     assert torch.isfinite(out.float()).all()
     out2, _ = U.run(moe, x, logits, tier_order=hm.TIERS_NF3_FIRST)
     assert torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("T", [8, 4200])
+def test_stream_path_one_and_two_launch_forms(tiny, T):
+    """The streaming path runs W13 and W2 in one launch while its token groups fit the counter
+    array, and as two launches past it (T=4200 on this layer). Both match the oracle on sampled
+    rows and the grouped path within tolerance, in every tier order."""
+    L, _ = tiny
+    moe = U.build(L, T)
+    x = synth.gen_x(T, L.H, seed=7, device="cuda")
+    logits = synth.gen_logits(T, L.E, seed=7, device="cuda")
+    s, (ids, gates, _, _) = U.run(moe, x, logits, path=hm.PATH_STREAM)
+    tokens = sorted({0, 1, T // 2, T - 1})
+    U.assert_rows_close(s.float().cpu().numpy()[tokens], U.oracle_out(L, x, ids, gates, tokens=tokens))
+    for order in (hm.TIERS_KEPT_FIRST, hm.TIERS_NF3_FIRST):
+        o, _ = U.run(moe, x, logits, path=hm.PATH_STREAM, tier_order=order)
+        assert torch.equal(o, s)
+    if T > 8:
+        g, _ = U.run(moe, x, logits, path=hm.PATH_GROUPED)
+        U.assert_rows_close(s.float().cpu().numpy(), g.float().cpu().numpy())

@@ -270,6 +270,16 @@ hmoe_status hmoe_plan_routes(const hmoe_layer* L, const float* logits, int T, in
   return HMOE_OK;
 }
 
+// Records a caller's stage event. Inside a stream capture the record must
+// become an event-record node (external flag); outside one, a plain record.
+static cudaError_t record_stage_event(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal)
+                                             : cudaEventRecord(ev, st);
+}
+
 static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, const float* gates,
                                    const int32_t* perm, const int32_t* offsets, void* out, uint8_t* wsb,
                                    const WsLayout& w, const hmoe_forward_opts& o, cudaStream_t st) {
@@ -308,7 +318,7 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
   const int grid = stream_grid(L->num_sms);
   auto mark = [&](int i) -> cudaError_t {
     if (o.stage_events && i < o.n_stage_events && o.stage_events[i])
-      return cudaEventRecordWithFlags((cudaEvent_t)o.stage_events[i], st, cudaEventRecordExternal);
+      return record_stage_event((cudaEvent_t)o.stage_events[i], st);
     return cudaSuccess;
   };
   if (mark(0) != cudaSuccess) return cuda_fail(cudaGetLastError(), "stage event record");
@@ -380,7 +390,7 @@ static hmoe_status run_grouped_path(const hmoe_layer* L, const void* x, int T, c
   __nv_bfloat16* xg = reinterpret_cast<__nv_bfloat16*>(wsb + w.xg);
   auto mark = [&](int i) -> cudaError_t {
     if (o.stage_events && i < o.n_stage_events && o.stage_events[i])
-      return cudaEventRecordWithFlags((cudaEvent_t)o.stage_events[i], st, cudaEventRecordExternal);
+      return record_stage_event((cudaEvent_t)o.stage_events[i], st);
     return cudaSuccess;
   };
   int masks[2] = {3, 0};

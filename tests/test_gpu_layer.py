@@ -158,3 +158,22 @@ def test_stream_path_one_and_two_launch_forms(tiny, T):
     if T > 8:
         g, _ = U.run(moe, x, logits, path=hm.PATH_GROUPED)
         U.assert_rows_close(s.float().cpu().numpy(), g.float().cpu().numpy())
+
+
+@pytest.mark.parametrize("T", [4, 300])
+def test_stage_events_outside_capture(tiny, T):
+    """Stage events given to an eager (not captured) forward are recorded in order on its stream."""
+    L, _ = tiny
+    moe = U.build(L, T)
+    x = synth.gen_x(T, L.H, device="cuda")
+    ids, gates, perm, offsets = moe.plan(synth.gen_logits(T, L.E, device="cuda"))
+    out = torch.empty((T, L.H), dtype=torch.bfloat16, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for e in ev:
+        e.record()  # creates the events; the library records them again below
+    ev[0].record()
+    hm.hmoe_forward(moe.layer, x, ids, gates, perm, offsets, out, moe.ws, stage_events=ev[1:])
+    torch.cuda.synchronize()
+    hm.hmoe_check_device_status(moe.ws)
+    for a, b in zip(ev[:-1], ev[1:]):
+        assert a.elapsed_time(b) >= 0.0

@@ -476,7 +476,10 @@ def run_profile_case(args):
         hm.hmoe_forward(moe.layer, x, ids, gates, perm, off, out, moe.ws)
     torch.cuda.synchronize()
     hm.hmoe_check_device_status(moe.ws)
-    print(json.dumps({"profile_case": {"experts": E, "m": M, "steps": args.steps}}))
+    fmts = [moe.layer.expert_info(e)[0] for e in range(E)]
+    tb, _, ne = touched(ids.cpu().numpy(), fmts)
+    print(json.dumps({"profile_case": {"experts": E, "m": M, "steps": args.steps, "touched_experts": ne,
+                                       "touched_packed_bytes": tb}}))
 
 
 def main():

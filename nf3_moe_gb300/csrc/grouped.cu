@@ -62,14 +62,18 @@ constexpr int GT_DQ_WARPS = 8 * GT_DQ_GROUPS;
 constexpr int GT_EPI_WARPS = 4;
 constexpr int GT_WARP_PPROD = 0, GT_WARP_MMA = 1, GT_WARP_BPROD = 2, GT_WARP_DQ0 = 3;
 constexpr int GT_WARP_EPI0 = GT_WARP_DQ0 + GT_DQ_WARPS;
-constexpr int GT_THREADS = (GT_WARP_EPI0 + GT_EPI_WARPS) * 32;
+// A second MMA-issuing warp: each issuer drives one row tile's accumulator.
+constexpr int GT_WARP_MMA2 = GT_WARP_EPI0 + GT_EPI_WARPS;
+constexpr int GT_MMA_ISSUERS = GT_R;
+static_assert(GT_MMA_ISSUERS == 2, "issuer r drives row tile r");
+constexpr int GT_THREADS = (GT_WARP_MMA2 + 1) * 32;
 constexpr int GT_TMEM_COLS = 2 * GT_R * GT_N;   // [buffer][row tile] accumulators
 // Shared memory map (offsets from the 1024-aligned base).
 constexpr int GT_OFF_A = 0;
 constexpr int GT_OFF_B = GT_OFF_A + GT_ASTAGES * GT_A_BYTES;
 constexpr int GT_OFF_P = GT_OFF_B + GT_BSTAGES * GT_B_BYTES;
 constexpr int GT_OFF_BAR = GT_OFF_P + GT_PSTAGES * GT_P_BYTES;
-constexpr int GT_NBAR = 2 * (GT_PSTAGES + GT_BSTAGES + GT_ASTAGES) + 4 + 1;
+constexpr int GT_NBAR = 2 * (GT_PSTAGES + GT_BSTAGES + GT_ASTAGES) + 4 + GT_MMA_ISSUERS;
 constexpr int GT_OFF_MISC = GT_OFF_BAR + ((GT_NBAR * 8 + 16 + 127) / 128) * 128;
 constexpr int GT_SMEM_BYTES = 1024 + GT_OFF_MISC + 2 * (MAX_E + 1) * 4 + 256 * 2;
 static_assert(GT_SMEM_BYTES <= 232448, "shared memory budget");
@@ -226,8 +230,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
   uint64_t* aempty = afull + GT_ASTAGES;               // MMAs that read it completed
   uint64_t* acc_full = aempty + GT_ASTAGES;            // [2] accumulator ready for the epilogue
   uint64_t* acc_empty = acc_full + 2;                  // [2] epilogue drained it
-  uint64_t* mma_done = acc_empty + 2;                  // final drain before TMEM release
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* mma_done = acc_empty + 2;                  // [issuer] final drain before TMEM release
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mma_done + GT_MMA_ISSUERS);
   volatile int* s_flags = reinterpret_cast<volatile int*>(s_tmem + 1);  // [0] abort
   int* s_istart = reinterpret_cast<int*>(smem + GT_OFF_MISC);
   int* s_off = s_istart + MAX_E + 1;
@@ -241,17 +245,17 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     }
     for (int s = 0; s < GT_BSTAGES; ++s) {
       mbar_init(&bfull[s], 1);
-      mbar_init(&bempty[s], 1);
+      mbar_init(&bempty[s], GT_MMA_ISSUERS);
     }
     for (int s = 0; s < GT_ASTAGES; ++s) {
       mbar_init(&afull[s], GT_DQ_WARPS);
-      mbar_init(&aempty[s], 1);
+      mbar_init(&aempty[s], GT_MMA_ISSUERS);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_full[b], GT_MMA_ISSUERS);
       mbar_init(&acc_empty[b], GT_EPI_WARPS);
     }
-    mbar_init(mma_done, 1);
+    for (int r = 0; r < GT_MMA_ISSUERS; ++r) mbar_init(&mma_done[r], 1);
     fence_mbar_init();
     s_flags[0] = 0;
   }
@@ -386,8 +390,13 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         }
       }
     }
-  } else if (warp == GT_WARP_MMA) {
-    // ------------------------------------------------ MMA issuer
+  } else if (warp == GT_WARP_MMA || warp == GT_WARP_MMA2) {
+    // ------------------------------------------------ MMA issuers
+    // Issuing one tcgen05.mma costs the issuing thread about 100 cycles, so
+    // two threads in different warps (and SM sub-partitions) issue: issuer r
+    // drives row tile r's accumulator. Both wait for the same operand stages
+    // and both commit to the barriers that free them (two arrivals each).
+    const int my_r = warp == GT_WARP_MMA ? 0 : 1;
     if (lane == 0) {
       const uint32_t a_lo0 = smem_desc_sw128_lo(smem_u32(smem + GT_OFF_A));
       const uint32_t b_lo0 = smem_desc_sw128_lo(smem_u32(smem + GT_OFF_B));
@@ -415,9 +424,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
           // Descriptor low words of this stage's A and B tiles (k-step 0).
           const uint32_t a_lo = a_lo0 + (uint32_t)as * (GT_A_BYTES >> 4);
           const uint32_t b_lo = b_lo0 + (uint32_t)bs * (GT_B_BYTES >> 4);
-          for (int r = 0; r < it.nr; ++r) {
-            const uint32_t ar = a_lo + (uint32_t)r * (GT_A_TILE >> 4);
-            const uint32_t dr = d_tmem + (uint32_t)(r * GT_N);
+          if (my_r < it.nr) {
+            const uint32_t ar = a_lo + (uint32_t)my_r * (GT_A_TILE >> 4);
+            const uint32_t dr = d_tmem + (uint32_t)(my_r * GT_N);
             umma_bf16(dr, desc_from_lo(ar), desc_from_lo(b_lo), idesc, kb ? 1u : 0u);
             umma_bf16_acc(dr, desc_from_lo(ar + 2), desc_from_lo(b_lo + 2), idesc);
             umma_bf16_acc(dr, desc_from_lo(ar + 4), desc_from_lo(b_lo + 4), idesc);
@@ -441,9 +450,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         set_status(p.status, DEV_TIMEOUT);
       }
       // Drain every MMA this thread issued before TMEM can be released.
-      umma_commit(mma_done);
+      umma_commit(&mma_done[my_r]);
       volatile int never = 0;
-      mbar_wait(mma_done, 0, &never, lim);
+      mbar_wait(&mma_done[my_r], 0, &never, lim);
     }
   } else if (warp < GT_WARP_EPI0) {
     // ------------------------------------------------ dequantisers: packed tile -> bf16 operand tile

@@ -14,18 +14,20 @@
 // expert's token tiles follow each other, so its weight tiles are re-read
 // from L2 rather than HBM.
 //
-// Warp roles (23 warps):
+// Warp roles (24 warps):
 //   warp 0       packed-weight producer. 1D bulk copies of each k-block's
 //                two packed tiles (64 K each) into a 4-deep ring.
 //   warp 2       activation producer. A 2D TMA tensor load (128 rows x 64
 //                bf16, 128B swizzle) into a 5-deep ring, plus an L2 prefetch
 //                of the tile needed 8 k-blocks later.
-//   warp 1       TMEM allocator (512 columns) and MMA issuer. One lane
-//                issues, per k-block and row tile, 4 tcgen05.mma.kind::f16
-//                (M=128, N = token count rounded up to 16, K=16) into a
-//                double-buffered fp32 accumulator pair in TMEM. The
-//                shared-memory descriptors are precomputed per ring slot.
-//                tcgen05.commits then free the operand and activation slots.
+//   warps 1, 23  MMA issuers (warp 1 also allocates 512 TMEM columns).
+//                Issuing a tcgen05.mma costs the issuing thread about 100
+//                cycles, so each row tile has its own issuing lane: per
+//                k-block it issues 4 tcgen05.mma.kind::f16 (M=128, N = token
+//                count rounded up to 16, K=16) into its row tile's fp32
+//                accumulator, double-buffered in TMEM. The shared-memory
+//                descriptors are precomputed per ring slot. Both issuers'
+//                tcgen05.commits free the operand and activation slots.
 //   warps 3..18  dequantisers, in two groups of 8; group r expands row tile
 //                r of the item. Each thread expands one tile slot (2 rows x
 //                16 K) to bf16 (E2M1 x E4M3, E2M1 x 2^e, or bf16_rne(NF3

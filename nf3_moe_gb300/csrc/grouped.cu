@@ -218,6 +218,40 @@ __device__ __forceinline__ void gt_dequant_slot(const uint8_t* ptile, uint8_t* a
   *reinterpret_cast<uint4*>(a1 + c1) = make_uint4(r1[4], r1[5], r1[6], r1[7]);
 }
 
+// The k-block loop of one dequantising warp over one item, for one format
+// (the format branch is taken once per item, not once per k-block).
+// Returns false if a bounded wait gave up.
+template <int FMT>
+__device__ __forceinline__ bool gt_dequant_item(int KB, bool mine, const uint8_t* p_base, uint8_t* a_base,
+                                                uint64_t* pfull, uint64_t* pempty, uint64_t* afull,
+                                                uint64_t* aempty, const uint32_t* s_e4m3, int rg, int lane,
+                                                volatile int* s_flags, uint64_t lim, int& ps, uint32_t& pph,
+                                                int& as, uint32_t& aph) {
+  for (int kb = 0; kb < KB; ++kb) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&pfull[ps], pph, s_flags, lim)) ||
+        !__all_sync(0xffffffffu, mbar_wait(&aempty[as], aph ^ 1u, s_flags, lim)))
+      return false;
+    if (mine) {
+      gt_dequant_slot<FMT>(p_base + ps * GT_P_BYTES, a_base + as * GT_A_BYTES, rg, lane, s_e4m3);
+      fence_async_smem();
+    }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&pempty[ps]);
+      mbar_arrive(&afull[as]);
+    }
+    if (++ps == GT_PSTAGES) {
+      ps = 0;
+      pph ^= 1u;
+    }
+    if (++as == GT_ASTAGES) {
+      as = 0;
+      aph ^= 1u;
+    }
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(GT_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ GroupedParams p, const __grid_constant__ CUtensorMap tmap_b) {
   extern __shared__ uint8_t smem_raw[];
@@ -467,36 +501,21 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     int ps = 0, as = 0;
     uint32_t pph = 0, aph = 0;
     bool ok = true;
+    const uint8_t* p_base = smem + GT_OFF_P + grp * GT_P_TILE;
+    uint8_t* a_base = smem + GT_OFF_A + grp * GT_A_TILE;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       const GtItem it = gt_decode(p, s_istart, s_off, i);
       const int fmt = gt_expert_fmt(p, it.e);
       const bool mine = grp < it.nr;
-      for (int kb = 0; kb < p.KB; ++kb) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&pfull[ps], pph, s_flags, lim)) &&
-             __all_sync(0xffffffffu, mbar_wait(&aempty[as], aph ^ 1u, s_flags, lim));
-        if (!ok) break;
-        if (mine) {
-          const uint8_t* pt = smem + GT_OFF_P + ps * GT_P_BYTES + grp * GT_P_TILE;
-          uint8_t* at = smem + GT_OFF_A + as * GT_A_BYTES + grp * GT_A_TILE;
-          if (fmt == FMT_NVFP4) gt_dequant_slot<FMT_NVFP4>(pt, at, rg, lane, s_e4m3);
-          else if (fmt == FMT_MXFP4) gt_dequant_slot<FMT_MXFP4>(pt, at, rg, lane, s_e4m3);
-          else gt_dequant_slot<FMT_NF3>(pt, at, rg, lane, s_e4m3);
-          fence_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&pempty[ps]);
-          mbar_arrive(&afull[as]);
-        }
-        if (++ps == GT_PSTAGES) {
-          ps = 0;
-          pph ^= 1u;
-        }
-        if (++as == GT_ASTAGES) {
-          as = 0;
-          aph ^= 1u;
-        }
-      }
+      if (fmt == FMT_NVFP4)
+        ok = gt_dequant_item<FMT_NVFP4>(p.KB, mine, p_base, a_base, pfull, pempty, afull, aempty, s_e4m3, rg, lane,
+                                        s_flags, lim, ps, pph, as, aph);
+      else if (fmt == FMT_MXFP4)
+        ok = gt_dequant_item<FMT_MXFP4>(p.KB, mine, p_base, a_base, pfull, pempty, afull, aempty, s_e4m3, rg, lane,
+                                        s_flags, lim, ps, pph, as, aph);
+      else
+        ok = gt_dequant_item<FMT_NF3>(p.KB, mine, p_base, a_base, pfull, pempty, afull, aempty, s_e4m3, rg, lane,
+                                      s_flags, lim, ps, pph, as, aph);
     }
     if (!ok && lane == 0) {
       s_flags[0] = 1;

@@ -21,8 +21,10 @@
 // phases as two launches of the same kernel.)
 //
 // One producer lane streams each item's packed tiles and the group's
-// activation rows into a 4-stage shared-memory ring with 1D bulk copies
-// (TMA engine). It writes the item number into each stage header, and a
+// activation rows into a 2-stage shared-memory ring of up to 8 k-blocks per
+// stage with 1D bulk copies (TMA engine). Eight k-blocks per stage instead of
+// four halve the per-stage waits and bookkeeping of the consumers; measured
+// 308 -> 284 us at M=8. It writes the item number into each stage header, and a
 // terminator stage ends the consumers' loop. Eight consumer warps, one per
 // 16-row group, dequantise in registers (prmt byte-table lookups; E4M3
 // scales from a shared table of bf16 pairs; bf16x2 scale multiply) and
@@ -44,8 +46,8 @@ namespace hmoe {
 constexpr int SK_CONSUMER_WARPS = 8;
 constexpr int SK_WARP_PRODUCER = SK_CONSUMER_WARPS;       // warp 8
 constexpr int SK_THREADS = (SK_CONSUMER_WARPS + 1) * 32;
-constexpr int SK_STAGES = 4;
-constexpr int SK_MAX_KBS = 4;
+constexpr int SK_STAGES = 2;
+constexpr int SK_MAX_KBS = 8;
 constexpr int SK_XROW = SK_MAX_KBS * 128 + 16;            // padded token row, bytes
 constexpr int SK_W_BYTES = SK_MAX_KBS * 4608;
 constexpr int SK_X_BYTES = 8 * SK_XROW;
@@ -178,7 +180,10 @@ template <int FMT>
 __device__ __forceinline__ void sk_stage(const uint8_t* sw, const uint8_t* sx, int kbs, int rg, int lane,
                                          const uint32_t* s_e4m3, float* accA, float* accB) {
   constexpr int TB = tile_bytes(FMT);
-  if (kbs == 4) {
+  if (kbs == 8) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sk_kblock<FMT>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, (j & 1) ? accB : accA);
+  } else if (kbs == 4) {
     sk_kblock<FMT>(sw, sx, rg, lane, s_e4m3, accA);
     sk_kblock<FMT>(sw + TB, sx + 128, rg, lane, s_e4m3, accB);
     sk_kblock<FMT>(sw + 2 * TB, sx + 256, rg, lane, s_e4m3, accA);

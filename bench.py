@@ -404,6 +404,22 @@ def run_ours(args, rank, world):
                    "tflops": round(tfs, 2), "frac_bf16_peak": round(tfs / pk["bf16_tflops_sustained"], 4),
                    "peak_used": "bf16_tflops_sustained (" + pk["source"] + ")",
                    "path": {0: "auto", 1: "stream", 2: "grouped"}[args.prefill_path]}
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            # The oracle on a bounded sample of the same batch: its first two tokens.
+            from oracle import layer as olayer
+            nt = 2
+            ids_p = bp["ids"][:nt].cpu().numpy()
+            g_p = bp["gates"][:nt].cpu().numpy().astype(np.float64)
+            x_p = xp[:nt].float().cpu().numpy().astype(np.float64)
+            exps_p = host_experts(L, ids_p)
+            t0 = time.perf_counter()
+            olayer.moe_forward(x_p, ids_p, g_p, lambda e: exps_p[e], H, I)
+            dt = time.perf_counter() - t0
+            prefill["cpu_baseline"] = {
+                "value": round(nt / dt, 4), "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+                "kind": "oracle", "tflops": round(2.0 * k * 3 * H * I * nt / dt / 1e12, 6),
+                "sample": f"the first {nt} tokens of the M={Mp} batch ({len(exps_p)} experts), float64 NumPy "
+                          f"dequantise-then-matmul, {dt:.1f} s"}
 
     # CPU oracle on a bounded sample (rank 0, N=1 only)
     cpu = None

@@ -132,6 +132,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
       : "memory");
 }
 
+// 16 lanes x 256 bits, four times along the columns: thread t gets rows
+// base + t/4 (regs 4j, 4j+1) and base + t/4 + 8 (regs 4j+2, 4j+3) at
+// columns 8j + 2(t % 4) and + 1 of repetition j.
+__device__ __forceinline__ void tmem_ld16x256x4(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -541,22 +554,41 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
       for (int r = 0; r < it.nr; ++r) {
         const int rt = it.rt + r;
         const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((buf * GT_R + r) * GT_N);
+        if (p.which == 13) {
+          // A 16-row group holds 8 gate rows then the 8 up rows of the same
+          // channels, so the 16x256b load gives each thread gate and up of
+          // one channel (row 16j + lane/4) for 8 token columns: SwiGLU in
+          // registers, every lane busy. The quarter holds groups 2q, 2q + 1.
+          const float gsc = p.tab.g13[it.e];
+          const int g = lane >> 2, qq = lane & 3;
+          for (int h = 0; h < 2; ++h) {
+            const int grp16 = 2 * quarter + h;
+            const int ch = rt * 64 + grp16 * 8 + g;
+            const uint32_t ta = tmem_base + ((uint32_t)(quarter * 32 + 16 * h) << 16) +
+                                (uint32_t)((buf * GT_R + r) * GT_N);
+            for (int c0 = 0; c0 < it.n; c0 += 32) {
+              uint32_t v[16];
+              tmem_ld16x256x4(ta + (uint32_t)c0, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int rep = 0; rep < 4; ++rep) {
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                  const int col = c0 + 8 * rep + 2 * qq + b;
+                  const float gate = __uint_as_float(v[4 * rep + b]) * gsc;
+                  const float up = __uint_as_float(v[4 * rep + 2 + b]) * gsc;
+                  if (col < it.n)
+                    p.h_out[(size_t)(it.p0 + col) * p.I + ch] = __float2bfloat16_rn(silu_fast(gate) * up);
+                }
+              }
+            }
+          }
+        } else {
         for (int c0 = 0; c0 < it.n; c0 += 32) {
           uint32_t v[32];
           tmem_ld32(taddr + (uint32_t)c0, v);
           tmem_wait_ld();
-          if (p.which == 13) {
-            const float gsc = p.tab.g13[it.e];
-            const int w = row & 15;
-            const int ch = rt * 64 + (row >> 4) * 8 + (w & 7);
-            __nv_bfloat16* hrow = p.h_out + (size_t)(it.p0 + c0) * p.I + ch;
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const float up = __shfl_down_sync(0xffffffffu, __uint_as_float(v[c]), 8);
-              if (w < 8 && c0 + c < it.n)
-                hrow[(size_t)c * p.I] = __float2bfloat16_rn(silu_f(__uint_as_float(v[c]) * gsc) * (up * gsc));
-            }
-          } else {
+          {
             const float gsc = p.tab.g2[it.e];
             const int orow = rt * 128 + row;
             // slot of column c0 + lane, broadcast per column below
@@ -571,6 +603,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
               }
             }
           }
+        }
         }
       }
       tc_fence_before();

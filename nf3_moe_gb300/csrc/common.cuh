@@ -250,6 +250,21 @@ __device__ __forceinline__ void e2m1x8_to_bf16x2(uint32_t w, uint32_t* p) {
   p[3] = __byte_perm(lo, hi, 0x7362);
 }
 
+// 8 NVFP4 codes (the shift-and-mask word layout written by the packer) ->
+// 4 bf16x2 holding 2^-126 times the E2M1 values. Multiplied by a scale that
+// carries 2^63 (an exact bf16 product: at most 6 significant bits, never
+// below the normal range), they give 2^-63 times the dequantised weights;
+// the factor 2^63 returns with the global scale after the fp32 accumulation.
+constexpr float NVFP4_UNSCALE = 9.223372036854775808e18f;  // 2^63
+constexpr uint32_t BF16X2_2P63 = 0x5F005F00u;               // bf16 pair of 2^63
+__device__ __forceinline__ void e2m1s_to_bf16x2(uint32_t w, uint32_t* p) {
+  constexpr uint32_t M = 0x81C081C0u;
+  p[0] = w & M;
+  p[1] = (w << 3) & M;
+  p[2] = (w << 6) & M;
+  p[3] = ((w >> 4) & 0x00C000C0u) | ((w >> 5) & 0x01000100u) | ((w << 1) & 0x80008000u);
+}
+
 // 8 NF3 codes held as selector nibbles (bit 3 of each nibble clear) -> 4 bf16x2.
 __device__ __forceinline__ void nf3x8_to_bf16x2(uint32_t sel, uint32_t* p) {
   uint32_t lo = __byte_perm(NF3_LO0, NF3_LO1, sel);
@@ -278,10 +293,11 @@ __device__ __forceinline__ void nf3_selectors(uint32_t A, uint32_t B, uint32_t C
 // order) and r1[8] for row R1. With with_nf3_scale == false the NF3 values
 // are raw codebook entries, and scale0/scale1 return the two row scales as
 // floats for the caller to apply to fp32 sums. Otherwise every format's
-// values come out multiplied by their scale in bf16 (the "tile" values).
-// e4m3_lut: optional 256-entry table of E4M3 -> bf16 pairs (the value in both
-// halves; shared memory), indexed by the scale bytes directly; NULL converts
-// arithmetically.
+// values come out multiplied by their scale in bf16 (the "tile" values);
+// NVFP4 tile values come out times 2^-63 (see e2m1s_to_bf16x2).
+// e4m3_lut: optional 256-entry table of E4M3 -> bf16 pairs times 2^63 (the
+// value in both halves; shared memory), indexed by the scale bytes directly;
+// NULL converts arithmetically.
 template <int FMT, bool WITH_NF3_SCALE>
 __device__ __forceinline__ void dequant_slot(const uint8_t* tile, int rg, int lane, uint32_t* r0, uint32_t* r1,
                                              float* scale0, float* scale1, const uint32_t* e4m3_lut = nullptr) {
@@ -290,13 +306,14 @@ __device__ __forceinline__ void dequant_slot(const uint8_t* tile, int rg, int la
     const uint4 q = *reinterpret_cast<const uint4*>(tile + slot * 16);
     uint32_t s0, s1;
     if constexpr (FMT == FMT_NVFP4) {
+      // Scales carry the factor 2^63 (see e2m1s_to_bf16x2).
       if (e4m3_lut) {
         s0 = e4m3_lut[tile[4096 + slot * 2]];
         s1 = e4m3_lut[tile[4096 + slot * 2 + 1]];
       } else {
         const uint32_t sc = *reinterpret_cast<const uint16_t*>(tile + 4096 + slot * 2);
-        s0 = bf16_bcast(e4m3_to_bf16(sc & 0xFFu));
-        s1 = bf16_bcast(e4m3_to_bf16(sc >> 8));
+        s0 = bf16x2_mul(bf16_bcast(e4m3_to_bf16(sc & 0xFFu)), BF16X2_2P63);
+        s1 = bf16x2_mul(bf16_bcast(e4m3_to_bf16(sc >> 8)), BF16X2_2P63);
       }
     } else {
       const int g = lane >> 2, hq = (lane & 3) >> 1;
@@ -304,10 +321,17 @@ __device__ __forceinline__ void dequant_slot(const uint8_t* tile, int rg, int la
       s0 = bf16_bcast(e8m0_to_bf16(sc & 0xFFu));
       s1 = bf16_bcast(e8m0_to_bf16(sc >> 8));
     }
-    e2m1x8_to_bf16x2(q.x, r0);
-    e2m1x8_to_bf16x2(q.y, r0 + 4);
-    e2m1x8_to_bf16x2(q.z, r1);
-    e2m1x8_to_bf16x2(q.w, r1 + 4);
+    if constexpr (FMT == FMT_NVFP4) {
+      e2m1s_to_bf16x2(q.x, r0);
+      e2m1s_to_bf16x2(q.y, r0 + 4);
+      e2m1s_to_bf16x2(q.z, r1);
+      e2m1s_to_bf16x2(q.w, r1 + 4);
+    } else {
+      e2m1x8_to_bf16x2(q.x, r0);
+      e2m1x8_to_bf16x2(q.y, r0 + 4);
+      e2m1x8_to_bf16x2(q.z, r1);
+      e2m1x8_to_bf16x2(q.w, r1 + 4);
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       r0[i] = bf16x2_mul(r0[i], s0);

@@ -312,7 +312,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     tmem_alloc(s_tmem, GT_TMEM_COLS);
     tmem_relinquish();
   }
-  if (tid >= 96 && tid < 96 + 256) s_e4m3[tid - 96] = bf16_bcast(e4m3_to_bf16((uint32_t)(tid - 96)));
+  if (tid >= 96 && tid < 96 + 256)
+    s_e4m3[tid - 96] = bf16x2_mul(bf16_bcast(e4m3_to_bf16((uint32_t)(tid - 96))), BF16X2_2P63);
   pdl_wait();  // everything below reads or writes global memory
   pdl_trigger();
   for (int e = tid; e <= p.E; e += blockDim.x) s_off[e] = p.offsets[e];
@@ -559,7 +560,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
           // channels, so the 16x256b load gives each thread gate and up of
           // one channel (row 16j + lane/4) for 8 token columns: SwiGLU in
           // registers, every lane busy. The quarter holds groups 2q, 2q + 1.
-          const float gsc = p.tab.g13[it.e];
+          const float gsc = p.tab.g13[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
           const int g = lane >> 2, qq = lane & 3;
           for (int h = 0; h < 2; ++h) {
             const int grp16 = 2 * quarter + h;
@@ -589,7 +590,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
           tmem_ld32(taddr + (uint32_t)c0, v);
           tmem_wait_ld();
           {
-            const float gsc = p.tab.g2[it.e];
+            const float gsc = p.tab.g2[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
             const int orow = rt * 128 + row;
             // slot of column c0 + lane, broadcast per column below
             int my_s = -1;

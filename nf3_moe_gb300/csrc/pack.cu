@@ -33,6 +33,35 @@ __device__ __forceinline__ int logical_row(int which, int I, int rt, int r) {
   return (w < 8) ? ch : I + ch;
 }
 
+// NVFP4 code word: 8 codes laid out so that one AND (after a left shift of 0,
+// 3 or 6 bits) puts a code pair's magnitude bits at bf16 bits 6..8 / 22..24
+// and its sign at bit 15 / 31, i.e. a bf16 pair equal to 2^-126 times the
+// E2M1 values (exponent field e, mantissa top bit m; e = 0 gives the
+// subnormal m * 2^-127 = 0.5m * 2^-126). Pair (0,1) sits there unshifted,
+// pair (2,3) 3 bits lower, pair (4,5) 6 bits lower; pair (6,7) fills the
+// remaining bits: magnitude bits 0,1 at 10,11 / 26,27, bit 2 at 13 / 29,
+// sign at 14 / 30.
+__device__ __forceinline__ uint32_t e2m1s_word(const uint32_t* d) {
+  uint32_t w = 0;
+  const int base[3] = {6, 3, 0};
+#pragma unroll
+  for (int pr = 0; pr < 3; ++pr) {
+    const uint32_t a = d[2 * pr], b = d[2 * pr + 1];
+    w |= (a & 7u) << base[pr];
+    w |= ((a >> 3) & 1u) << (base[pr] + 9);
+    w |= (b & 7u) << (base[pr] + 16);
+    w |= ((b >> 3) & 1u) << (base[pr] + 25);
+  }
+  const uint32_t a = d[6], b = d[7];
+  w |= (a & 3u) << 10;
+  w |= ((a >> 2) & 1u) << 13;
+  w |= ((a >> 3) & 1u) << 14;
+  w |= (b & 3u) << 26;
+  w |= ((b >> 2) & 1u) << 29;
+  w |= ((b >> 3) & 1u) << 30;
+  return w;
+}
+
 __device__ __forceinline__ uint32_t e2m1_word(const uint32_t* d) {
   // d[0..7]: 4-bit codes. Layout: magnitudes in nibbles 0..7; signs of codes
   // 0..3 at bits 7,15,23,31 and of codes 4..7 at bits 3,11,19,27.
@@ -70,10 +99,17 @@ __global__ void pack_matrix_kernel(int fmt, int which, const uint8_t* __restrict
       c1[2 * m + 1] = s1[m] >> 4;
     }
     uint4 v;
-    v.x = e2m1_word(c0);
-    v.y = e2m1_word(c0 + 8);
-    v.z = e2m1_word(c1);
-    v.w = e2m1_word(c1 + 8);
+    if (fmt == FMT_NVFP4) {
+      v.x = e2m1s_word(c0);
+      v.y = e2m1s_word(c0 + 8);
+      v.z = e2m1s_word(c1);
+      v.w = e2m1s_word(c1 + 8);
+    } else {
+      v.x = e2m1_word(c0);
+      v.y = e2m1_word(c0 + 8);
+      v.z = e2m1_word(c1);
+      v.w = e2m1_word(c1 + 8);
+    }
     *reinterpret_cast<uint4*>(tile + slot * 16) = v;
     if (fmt == FMT_NVFP4) {
       const uint32_t a = scales[(size_t)L0 * (K / 16) + k0 / 16];
@@ -140,7 +176,15 @@ __global__ void debug_dequant_kernel(int fmt, int which, const uint8_t* __restri
   const int tid = threadIdx.x, rg = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
   const uint8_t* tile = src + ((size_t)rt * KB + kb) * tile_bytes(fmt);
   uint32_t r0[8], r1[8];
-  if (fmt == FMT_NVFP4) debug_tile<FMT_NVFP4>(tile, rg, lane, r0, r1);
+  if (fmt == FMT_NVFP4) {
+    debug_tile<FMT_NVFP4>(tile, rg, lane, r0, r1);
+    // The kernels carry NVFP4 tiles times 2^-63; the export is the tile itself.
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      r0[i] = bf16x2_mul(r0[i], BF16X2_2P63);
+      r1[i] = bf16x2_mul(r1[i], BF16X2_2P63);
+    }
+  }
   else if (fmt == FMT_MXFP4) debug_tile<FMT_MXFP4>(tile, rg, lane, r0, r1);
   else debug_tile<FMT_NF3>(tile, rg, lane, r0, r1);
   const int L0 = logical_row(which, I, rt, rg * 16 + g), L1 = logical_row(which, I, rt, rg * 16 + g + 8);

@@ -97,12 +97,12 @@ __device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it,
     if (c >= it.n) continue;
     const int pp = it.p0 + c;
     if (it.ph == 0) {
-      const float gsc = p.tab.g13[it.e];
+      const float gsc = p.tab.g13[it.e] * (expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
       const int ch = it.rt * 64 + rg * 8 + g;
       const float gate = v[h] * gsc, up = v[2 + h] * gsc;
       p.h_out[(size_t)pp * p.I + ch] = __float2bfloat16_rn(silu_f(gate) * up);
     } else {
-      const float gsc = p.tab.g2[it.e];
+      const float gsc = p.tab.g2[it.e] * (expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
       const int s = p.perm[pp];
       if (s < 0 || s >= S) {
         set_status(p.status, DEV_BAD_ROUTE);
@@ -138,10 +138,17 @@ __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xr
       s0 = bf16_bcast(e8m0_to_bf16(sc & 0xFFu));
       s1 = bf16_bcast(e8m0_to_bf16(sc >> 8));
     }
-    e2m1x8_to_bf16x2(q.x, r0);
-    e2m1x8_to_bf16x2(q.y, r0 + 4);
-    e2m1x8_to_bf16x2(q.z, r1);
-    e2m1x8_to_bf16x2(q.w, r1 + 4);
+    if constexpr (FMT == FMT_NVFP4) {
+      e2m1s_to_bf16x2(q.x, r0);
+      e2m1s_to_bf16x2(q.y, r0 + 4);
+      e2m1s_to_bf16x2(q.z, r1);
+      e2m1s_to_bf16x2(q.w, r1 + 4);
+    } else {
+      e2m1x8_to_bf16x2(q.x, r0);
+      e2m1x8_to_bf16x2(q.y, r0 + 4);
+      e2m1x8_to_bf16x2(q.z, r1);
+      e2m1x8_to_bf16x2(q.w, r1 + 4);
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       r0[i] = bf16x2_mul(r0[i], s0);
@@ -211,7 +218,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
     fence_mbar_init();
     s_flags[0] = 0;
   }
-  if (tid < 256) s_e4m3[tid] = bf16_bcast(e4m3_to_bf16((uint32_t)tid));
+  if (tid < 256) s_e4m3[tid] = bf16x2_mul(bf16_bcast(e4m3_to_bf16((uint32_t)tid)), BF16X2_2P63);
   pdl_wait();  // everything below reads or writes global memory
   pdl_trigger();
   // Group prefix over experts of the selected tiers, from the caller's offsets.

@@ -59,7 +59,7 @@ constexpr int GT_PSTAGES = 4;             // packed weight tiles in flight
 constexpr int GT_BSTAGES = 5;             // activation tiles in flight
 constexpr int GT_ASTAGES = 3;             // dequantised operand tiles between dequant and MMA
 constexpr int GT_BPREFETCH = 8;           // B tiles prefetched into L2 ahead of the TMA loads
-constexpr int GT_DQ_GROUPS = GT_R;        // dequant group r expands row tile r of the item
+constexpr int GT_DQ_GROUPS = 2;           // dequant group g expands the k-blocks of parity g
 constexpr int GT_DQ_WARPS = 8 * GT_DQ_GROUPS;
 constexpr int GT_EPI_WARPS = 4;
 constexpr int GT_WARP_PPROD = 0, GT_WARP_MMA = 1, GT_WARP_BPROD = 2, GT_WARP_DQ0 = 3;
@@ -232,26 +232,32 @@ __device__ __forceinline__ void gt_dequant_slot(const uint8_t* ptile, uint8_t* a
 }
 
 // The k-block loop of one dequantising warp over one item, for one format
-// (the format branch is taken once per item, not once per k-block).
-// Returns false if a bounded wait gave up.
+// (the format branch is taken once per item, not once per k-block). The two
+// groups of 8 warps take alternate k-blocks (par = parity of the running
+// k-block count gk), and a warp expands its 16-row group of every row tile
+// of its k-blocks: the waits, fence and arrivals are paid once per two slots
+// while all 16 warps stay busy. Returns false if a bounded wait gave up.
 template <int FMT>
-__device__ __forceinline__ bool gt_dequant_item(int KB, bool mine, const uint8_t* p_base, uint8_t* a_base,
+__device__ __forceinline__ bool gt_dequant_item(int KB, int nr, int par, const uint8_t* p_base, uint8_t* a_base,
                                                 uint64_t* pfull, uint64_t* pempty, uint64_t* afull,
                                                 uint64_t* aempty, const uint32_t* s_e4m3, int rg, int lane,
-                                                volatile int* s_flags, uint64_t lim, int& ps, uint32_t& pph,
-                                                int& as, uint32_t& aph) {
-  for (int kb = 0; kb < KB; ++kb) {
-    if (!__all_sync(0xffffffffu, mbar_wait(&pfull[ps], pph, s_flags, lim)) ||
-        !__all_sync(0xffffffffu, mbar_wait(&aempty[as], aph ^ 1u, s_flags, lim)))
-      return false;
-    if (mine) {
-      gt_dequant_slot<FMT>(p_base + ps * GT_P_BYTES, a_base + as * GT_A_BYTES, rg, lane, s_e4m3);
+                                                volatile int* s_flags, uint64_t lim, uint32_t& gk, int& ps,
+                                                uint32_t& pph, int& as, uint32_t& aph) {
+  for (int kb = 0; kb < KB; ++kb, ++gk) {
+    if ((int)(gk & 1u) == par) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&pfull[ps], pph, s_flags, lim)) ||
+          !__all_sync(0xffffffffu, mbar_wait(&aempty[as], aph ^ 1u, s_flags, lim)))
+        return false;
+      const uint8_t* pt = p_base + ps * GT_P_BYTES;
+      uint8_t* at = a_base + as * GT_A_BYTES;
+      gt_dequant_slot<FMT>(pt, at, rg, lane, s_e4m3);
+      if (nr > 1) gt_dequant_slot<FMT>(pt + GT_P_TILE, at + GT_A_TILE, rg, lane, s_e4m3);
       fence_async_smem();
-    }
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&pempty[ps]);
-      mbar_arrive(&afull[as]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&pempty[ps]);
+        mbar_arrive(&afull[as]);
+      }
     }
     if (++ps == GT_PSTAGES) {
       ps = 0;
@@ -290,14 +296,14 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
   if (tid == 0) {
     for (int s = 0; s < GT_PSTAGES; ++s) {
       mbar_init(&pfull[s], 1);
-      mbar_init(&pempty[s], GT_DQ_WARPS);
+      mbar_init(&pempty[s], GT_DQ_WARPS / 2);
     }
     for (int s = 0; s < GT_BSTAGES; ++s) {
       mbar_init(&bfull[s], 1);
       mbar_init(&bempty[s], GT_MMA_ISSUERS);
     }
     for (int s = 0; s < GT_ASTAGES; ++s) {
-      mbar_init(&afull[s], GT_DQ_WARPS);
+      mbar_init(&afull[s], GT_DQ_WARPS / 2);
       mbar_init(&aempty[s], GT_MMA_ISSUERS);
     }
     for (int b = 0; b < 2; ++b) {
@@ -506,30 +512,28 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     }
   } else if (warp < GT_WARP_EPI0) {
     // ------------------------------------------------ dequantisers: packed tile -> bf16 operand tile
-    // Group r (8 warps, one per 16-row group) expands row tile r of each
-    // k-block. For an item with one row tile, group 1 only arrives. (One
-    // warp per 16-row group expanding both row tiles was measured slower:
-    // 4.18 against 4.03 ms at M=4096.)
+    // Group par (8 warps, one per 16-row group) expands the k-blocks of
+    // parity par, both row tiles. (Eight warps each expanding both row tiles
+    // of every k-block was measured slower: 4.18 against 4.03 ms at M=4096.)
     const int dq = warp - GT_WARP_DQ0;
-    const int grp = dq >> 3, rg = dq & 7;
+    const int par = dq >> 3, rg = dq & 7;
     int ps = 0, as = 0;
-    uint32_t pph = 0, aph = 0;
+    uint32_t pph = 0, aph = 0, gk = 0;
     bool ok = true;
-    const uint8_t* p_base = smem + GT_OFF_P + grp * GT_P_TILE;
-    uint8_t* a_base = smem + GT_OFF_A + grp * GT_A_TILE;
+    const uint8_t* p_base = smem + GT_OFF_P;
+    uint8_t* a_base = smem + GT_OFF_A;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       const GtItem it = gt_decode(p, s_istart, s_off, i);
       const int fmt = gt_expert_fmt(p, it.e);
-      const bool mine = grp < it.nr;
       if (fmt == FMT_NVFP4)
-        ok = gt_dequant_item<FMT_NVFP4>(p.KB, mine, p_base, a_base, pfull, pempty, afull, aempty, s_e4m3, rg, lane,
-                                        s_flags, lim, ps, pph, as, aph);
+        ok = gt_dequant_item<FMT_NVFP4>(p.KB, it.nr, par, p_base, a_base, pfull, pempty, afull, aempty, s_e4m3, rg,
+                                        lane, s_flags, lim, gk, ps, pph, as, aph);
       else if (fmt == FMT_MXFP4)
-        ok = gt_dequant_item<FMT_MXFP4>(p.KB, mine, p_base, a_base, pfull, pempty, afull, aempty, s_e4m3, rg, lane,
-                                        s_flags, lim, ps, pph, as, aph);
+        ok = gt_dequant_item<FMT_MXFP4>(p.KB, it.nr, par, p_base, a_base, pfull, pempty, afull, aempty, s_e4m3, rg,
+                                        lane, s_flags, lim, gk, ps, pph, as, aph);
       else
-        ok = gt_dequant_item<FMT_NF3>(p.KB, mine, p_base, a_base, pfull, pempty, afull, aempty, s_e4m3, rg, lane,
-                                      s_flags, lim, ps, pph, as, aph);
+        ok = gt_dequant_item<FMT_NF3>(p.KB, it.nr, par, p_base, a_base, pfull, pempty, afull, aempty, s_e4m3, rg,
+                                      lane, s_flags, lim, gk, ps, pph, as, aph);
     }
     if (!ok && lane == 0) {
       s_flags[0] = 1;

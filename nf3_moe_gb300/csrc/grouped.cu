@@ -59,8 +59,16 @@ constexpr int GT_PSTAGES = 4;             // packed weight tiles in flight
 constexpr int GT_BSTAGES = 5;             // activation tiles in flight
 constexpr int GT_ASTAGES = 3;             // dequantised operand tiles between dequant and MMA
 constexpr int GT_BPREFETCH = 8;           // B tiles prefetched into L2 ahead of the TMA loads
-constexpr int GT_DQ_GROUPS = 2;           // dequant group g expands the k-blocks of parity g
-constexpr int GT_DQ_WARPS = 8 * GT_DQ_GROUPS;
+constexpr int GT_DQ_GROUPS = 2;           // dequant group g expands the k-blocks k with k % 2 == g
+constexpr int GT_DQ_WARPS = 16;           // 8 per group, one per 16-row group of every row tile
+constexpr int GT_DQ_PER_GROUP = GT_DQ_WARPS / GT_DQ_GROUPS;
+// The waits track mbarrier phases by parity, which is only sound while a
+// waiter is never two phases behind. A group revisits a ring slot after
+// GT_DQ_GROUPS * (ring depth) k-blocks, and its own previous wait has already
+// forced progress up to GT_DQ_GROUPS k-blocks back; with more than two groups
+// a slot can be two phases behind the one awaited and the parity test passes
+// early (measured: bounded waits timed out with four groups).
+static_assert(GT_DQ_GROUPS <= 2, "parity-tracked waits need at most two dequant groups");
 constexpr int GT_EPI_WARPS = 4;
 constexpr int GT_WARP_PPROD = 0, GT_WARP_MMA = 1, GT_WARP_BPROD = 2, GT_WARP_DQ0 = 3;
 constexpr int GT_WARP_EPI0 = GT_WARP_DQ0 + GT_DQ_WARPS;
@@ -232,11 +240,12 @@ __device__ __forceinline__ void gt_dequant_slot(const uint8_t* ptile, uint8_t* a
 }
 
 // The k-block loop of one dequantising warp over one item, for one format
-// (the format branch is taken once per item, not once per k-block). The two
-// groups of 8 warps take alternate k-blocks (par = parity of the running
-// k-block count gk), and a warp expands its 16-row group of every row tile
-// of its k-blocks: the waits, fence and arrivals are paid once per two slots
-// while all 16 warps stay busy. Returns false if a bounded wait gave up.
+// (the format branch is taken once per item, not once per k-block). The
+// groups of warps take turns by k-block (group par takes the k-blocks whose
+// running count gk is par modulo the group count), and a warp expands its
+// row groups rg, rg + 1, ... of every row tile of its k-blocks: the waits,
+// fence and arrivals are paid once per several slots while all the warps
+// stay busy. Returns false if a bounded wait gave up.
 template <int FMT>
 __device__ __forceinline__ bool gt_dequant_item(int KB, int nr, int par, const uint8_t* p_base, uint8_t* a_base,
                                                 uint64_t* pfull, uint64_t* pempty, uint64_t* afull,
@@ -244,14 +253,17 @@ __device__ __forceinline__ bool gt_dequant_item(int KB, int nr, int par, const u
                                                 volatile int* s_flags, uint64_t lim, uint32_t& gk, int& ps,
                                                 uint32_t& pph, int& as, uint32_t& aph) {
   for (int kb = 0; kb < KB; ++kb, ++gk) {
-    if ((int)(gk & 1u) == par) {
+    if ((int)(gk % GT_DQ_GROUPS) == par) {
       if (!__all_sync(0xffffffffu, mbar_wait(&pfull[ps], pph, s_flags, lim)) ||
           !__all_sync(0xffffffffu, mbar_wait(&aempty[as], aph ^ 1u, s_flags, lim)))
         return false;
       const uint8_t* pt = p_base + ps * GT_P_BYTES;
       uint8_t* at = a_base + as * GT_A_BYTES;
-      gt_dequant_slot<FMT>(pt, at, rg, lane, s_e4m3);
-      if (nr > 1) gt_dequant_slot<FMT>(pt + GT_P_TILE, at + GT_A_TILE, rg, lane, s_e4m3);
+#pragma unroll
+      for (int h = 0; h < 8 / GT_DQ_PER_GROUP; ++h) {
+        gt_dequant_slot<FMT>(pt, at, rg + h, lane, s_e4m3);
+        if (nr > 1) gt_dequant_slot<FMT>(pt + GT_P_TILE, at + GT_A_TILE, rg + h, lane, s_e4m3);
+      }
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -296,14 +308,14 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
   if (tid == 0) {
     for (int s = 0; s < GT_PSTAGES; ++s) {
       mbar_init(&pfull[s], 1);
-      mbar_init(&pempty[s], GT_DQ_WARPS / 2);
+      mbar_init(&pempty[s], GT_DQ_PER_GROUP);
     }
     for (int s = 0; s < GT_BSTAGES; ++s) {
       mbar_init(&bfull[s], 1);
       mbar_init(&bempty[s], GT_MMA_ISSUERS);
     }
     for (int s = 0; s < GT_ASTAGES; ++s) {
-      mbar_init(&afull[s], GT_DQ_WARPS / 2);
+      mbar_init(&afull[s], GT_DQ_PER_GROUP);
       mbar_init(&aempty[s], GT_MMA_ISSUERS);
     }
     for (int b = 0; b < 2; ++b) {
@@ -512,11 +524,12 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     }
   } else if (warp < GT_WARP_EPI0) {
     // ------------------------------------------------ dequantisers: packed tile -> bf16 operand tile
-    // Group par (8 warps, one per 16-row group) expands the k-blocks of
-    // parity par, both row tiles. (Eight warps each expanding both row tiles
-    // of every k-block was measured slower: 4.18 against 4.03 ms at M=4096.)
+    // Group par expands the k-blocks k with k % GT_DQ_GROUPS == par, every
+    // row tile; its warps split the 8 row groups. (Eight warps each expanding
+    // both row tiles of every k-block was measured slower: 4.18 against 4.03
+    // ms at M=4096.)
     const int dq = warp - GT_WARP_DQ0;
-    const int par = dq >> 3, rg = dq & 7;
+    const int par = dq / GT_DQ_PER_GROUP, rg = (dq % GT_DQ_PER_GROUP) * (8 / GT_DQ_PER_GROUP);
     int ps = 0, as = 0;
     uint32_t pph = 0, aph = 0, gk = 0;
     bool ok = true;
@@ -556,6 +569,18 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         break;
       }
       tc_fence_after();
+      // W2: the flat slot of each of the item's token columns (column
+      // 32u + lane in item_slot[u]); -1 past the item or for a bad entry.
+      int item_slot[GT_N / 32];
+#pragma unroll
+      for (int u = 0; u < GT_N / 32; ++u) {
+        item_slot[u] = -1;
+        if (p.which != 13 && 32 * u + lane < it.n) {
+          const int sc = p.perm[it.p0 + 32 * u + lane];
+          if (sc >= 0 && sc < S) item_slot[u] = sc;
+          else set_status(p.status, DEV_BAD_ROUTE);
+        }
+      }
       for (int r = 0; r < it.nr; ++r) {
         const int rt = it.rt + r;
         const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((buf * GT_R + r) * GT_N);
@@ -589,26 +614,23 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
             }
           }
         } else {
-        for (int c0 = 0; c0 < it.n; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(taddr + (uint32_t)c0, v);
-          tmem_wait_ld();
-          {
-            const float gsc = p.tab.g2[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
-            const int orow = rt * 128 + row;
-            // slot of column c0 + lane, broadcast per column below
-            int my_s = -1;
-            if (c0 + lane < it.n) my_s = p.perm[it.p0 + c0 + lane];
+          // W2: lanes are output rows, so each column's store is one
+          // coalesced row segment of slot s = perm[p0 + column].
+          const float gsc = p.tab.g2[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
+          const int orow = rt * 128 + row;
+#pragma unroll
+          for (int u = 0; u < GT_N / 32; ++u) {
+            if (32 * u >= it.n) break;
+            uint32_t v[32];
+            tmem_ld32(taddr + (uint32_t)(32 * u), v);
+            tmem_wait_ld();
+            const int my_s = item_slot[u];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-              const int s = __shfl_sync(0xffffffffu, my_s, c);
-              if (c0 + c < it.n) {
-                if (s >= 0 && s < S) p.y_out[(size_t)s * p.H + orow] = __uint_as_float(v[c]) * gsc;
-                else if (lane == 0) set_status(p.status, DEV_BAD_ROUTE);
-              }
+              const int sc = __shfl_sync(0xffffffffu, my_s, c);
+              if (sc >= 0) p.y_out[(size_t)sc * p.H + orow] = __uint_as_float(v[c]) * gsc;
             }
           }
-        }
         }
       }
       tc_fence_before();

@@ -98,14 +98,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// The suspend-time hint lets a waiting thread sleep inside the instruction
+// (up to the hint, in ns; the phase completing wakes it) instead of spinning
+// on short polls that take issue slots from the working warps. Measured on
+// the prefill kernel: 3.37 -> 3.30 ms at M=4096 for any hint of 20 ns to 2 us.
+constexpr uint32_t MBAR_SUSPEND_HINT_NS = 500;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(MBAR_SUSPEND_HINT_NS)
       : "memory");
   return ok != 0;
 }

@@ -18,25 +18,29 @@
 //   warp 0       packed-weight producer. 1D bulk copies of each k-block's
 //                two packed tiles (64 K each) into a 4-deep ring.
 //   warp 2       activation producer. A 2D TMA tensor load (128 rows x 64
-//                bf16, 128B swizzle) into a 5-deep ring, plus an L2 prefetch
-//                of the tile needed 8 k-blocks later.
+//                bf16, 128B swizzle) into the k-block's operand slot (a
+//                3-deep ring whose slots also hold the dequantised weight
+//                tiles), plus an L2 prefetch of the tile needed 8 k-blocks
+//                later.
 //   warps 1, 23  MMA issuers (warp 1 also allocates 512 TMEM columns).
 //                Issuing a tcgen05.mma costs the issuing thread about 100
 //                cycles, so each row tile has its own issuing lane: per
 //                k-block it issues 4 tcgen05.mma.kind::f16 (M=128, N = token
 //                count rounded up to 16, K=16) into its row tile's fp32
-//                accumulator, double-buffered in TMEM. The shared-memory
-//                descriptors are precomputed per ring slot. Both issuers'
-//                tcgen05.commits free the operand and activation slots.
-//   warps 3..18  dequantisers, in two groups of 8; group r expands row tile
-//                r of the item. Each thread expands one tile slot (2 rows x
-//                16 K) to bf16 (E2M1 x E4M3, E2M1 x 2^e, or bf16_rne(NF3
-//                codebook x scale)) into the canonical K-major SWIZZLE_128B
-//                operand layout of a 3-deep ring, then fences the async proxy.
+//                accumulator, double-buffered in TMEM. Both issuers'
+//                tcgen05.commits free the operand slot (one commit each per
+//                k-block).
+//   warps 3..18  dequantisers, in two groups of 8 that take alternate
+//                k-blocks. Per k-block each warp expands its 16-row group of
+//                both row tiles: each thread turns one tile slot (2 rows x
+//                16 K) of each into bf16 (E2M1 x E4M3, E2M1 x 2^e, or
+//                bf16_rne(NF3 codebook x scale)) in the canonical K-major
+//                SWIZZLE_128B operand layout, then fences the async proxy.
 //   warps 19..22 epilogue. tcgen05.ld of the accumulators (each warp owns 32
 //                TMEM lanes, i.e. 32 weight rows of each row tile).
-//                W13: rows come in gate/up pairs 8 lanes apart, so one
-//                shuffle gives h = bf16(silu(g13*gate) * (g13*up)).
+//                W13: rows come in gate/up pairs 8 lanes apart, and one
+//                16x256b load gives a thread both, so
+//                h = bf16(silu(g13*gate) * (g13*up)) needs no shuffle.
 //                W2: y[s][row] = g2 * acc for the flat slot s = perm[p].
 // Every mbarrier wait is bounded. On a timeout the CTA records
 // DEV_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
@@ -56,8 +60,11 @@ constexpr int GT_B_BYTES = GT_N * 128;    // bf16 B tile GT_N x 64
 constexpr int GT_P_TILE = 4608;           // largest packed tile
 constexpr int GT_P_BYTES = GT_R * GT_P_TILE;
 constexpr int GT_PSTAGES = 4;             // packed weight tiles in flight
-constexpr int GT_BSTAGES = 5;             // activation tiles in flight
-constexpr int GT_ASTAGES = 3;             // dequantised operand tiles between dequant and MMA
+// Operand stages: slot s holds one k-block's dequantised weight tiles (A)
+// and its activation tile (B). One barrier per slot frees both, so each
+// issuer commits once per k-block (measured 3.30 -> 3.21 ms at M=4096
+// against separate A and B rings of depth 3 and 5).
+constexpr int GT_OSTAGES = 3;
 constexpr int GT_BPREFETCH = 8;           // B tiles prefetched into L2 ahead of the TMA loads
 constexpr int GT_DQ_GROUPS = 2;           // dequant group g expands the k-blocks k with k % 2 == g
 constexpr int GT_DQ_WARPS = 16;           // 8 per group, one per 16-row group of every row tile
@@ -69,6 +76,13 @@ constexpr int GT_DQ_PER_GROUP = GT_DQ_WARPS / GT_DQ_GROUPS;
 // a slot can be two phases behind the one awaited and the parity test passes
 // early (measured: bounded waits timed out with four groups).
 static_assert(GT_DQ_GROUPS <= 2, "parity-tracked waits need at most two dequant groups");
+// That forced progress holds for the operand ring, whose slots are freed by
+// MMA commits in issue order, but not for the packed ring: bulk copies may
+// land out of order, so a group's earlier waits say nothing about a slot it
+// did not wait on. With a depth that is a multiple of the group count each
+// group owns its own packed slots and waits on each of them every time
+// (measured: a 3-deep packed ring with two groups gave wrong results).
+static_assert(GT_PSTAGES % GT_DQ_GROUPS == 0, "each dequant group owns its packed-ring slots");
 constexpr int GT_EPI_WARPS = 4;
 constexpr int GT_WARP_PPROD = 0, GT_WARP_MMA = 1, GT_WARP_BPROD = 2, GT_WARP_DQ0 = 3;
 constexpr int GT_WARP_EPI0 = GT_WARP_DQ0 + GT_DQ_WARPS;
@@ -80,10 +94,10 @@ constexpr int GT_THREADS = (GT_WARP_MMA2 + 1) * 32;
 constexpr int GT_TMEM_COLS = 2 * GT_R * GT_N;   // [buffer][row tile] accumulators
 // Shared memory map (offsets from the 1024-aligned base).
 constexpr int GT_OFF_A = 0;
-constexpr int GT_OFF_B = GT_OFF_A + GT_ASTAGES * GT_A_BYTES;
-constexpr int GT_OFF_P = GT_OFF_B + GT_BSTAGES * GT_B_BYTES;
+constexpr int GT_OFF_B = GT_OFF_A + GT_OSTAGES * GT_A_BYTES;
+constexpr int GT_OFF_P = GT_OFF_B + GT_OSTAGES * GT_B_BYTES;
 constexpr int GT_OFF_BAR = GT_OFF_P + GT_PSTAGES * GT_P_BYTES;
-constexpr int GT_NBAR = 2 * (GT_PSTAGES + GT_BSTAGES + GT_ASTAGES) + 4 + GT_MMA_ISSUERS;
+constexpr int GT_NBAR = 2 * GT_PSTAGES + 3 * GT_OSTAGES + 4 + GT_MMA_ISSUERS;
 constexpr int GT_OFF_MISC = GT_OFF_BAR + ((GT_NBAR * 8 + 16 + 127) / 128) * 128;
 constexpr int GT_SMEM_BYTES = 1024 + GT_OFF_MISC + 2 * (MAX_E + 1) * 4 + 256 * 4;
 static_assert(GT_SMEM_BYTES <= 232448, "shared memory budget");
@@ -249,13 +263,13 @@ __device__ __forceinline__ void gt_dequant_slot(const uint8_t* ptile, uint8_t* a
 template <int FMT>
 __device__ __forceinline__ bool gt_dequant_item(int KB, int nr, int par, const uint8_t* p_base, uint8_t* a_base,
                                                 uint64_t* pfull, uint64_t* pempty, uint64_t* afull,
-                                                uint64_t* aempty, const uint32_t* s_e4m3, int rg, int lane,
+                                                uint64_t* oempty, const uint32_t* s_e4m3, int rg, int lane,
                                                 volatile int* s_flags, uint64_t lim, uint32_t& gk, int& ps,
                                                 uint32_t& pph, int& as, uint32_t& aph) {
   for (int kb = 0; kb < KB; ++kb, ++gk) {
     if ((int)(gk % GT_DQ_GROUPS) == par) {
       if (!__all_sync(0xffffffffu, mbar_wait(&pfull[ps], pph, s_flags, lim)) ||
-          !__all_sync(0xffffffffu, mbar_wait(&aempty[as], aph ^ 1u, s_flags, lim)))
+          !__all_sync(0xffffffffu, mbar_wait(&oempty[as], aph ^ 1u, s_flags, lim)))
         return false;
       const uint8_t* pt = p_base + ps * GT_P_BYTES;
       uint8_t* at = a_base + as * GT_A_BYTES;
@@ -275,7 +289,7 @@ __device__ __forceinline__ bool gt_dequant_item(int KB, int nr, int par, const u
       ps = 0;
       pph ^= 1u;
     }
-    if (++as == GT_ASTAGES) {
+    if (++as == GT_OSTAGES) {
       as = 0;
       aph ^= 1u;
     }
@@ -292,10 +306,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
   uint64_t* pfull = bars;                              // packed tile landed (tx)
   uint64_t* pempty = pfull + GT_PSTAGES;               // dequant warps done reading it
   uint64_t* bfull = pempty + GT_PSTAGES;               // activation tile landed (tx)
-  uint64_t* bempty = bfull + GT_BSTAGES;               // MMAs that read it completed
-  uint64_t* afull = bempty + GT_BSTAGES;               // dequant warps wrote the operand tile
-  uint64_t* aempty = afull + GT_ASTAGES;               // MMAs that read it completed
-  uint64_t* acc_full = aempty + GT_ASTAGES;            // [2] accumulator ready for the epilogue
+  uint64_t* afull = bfull + GT_OSTAGES;                // dequant warps wrote the weight tiles
+  uint64_t* oempty = afull + GT_OSTAGES;               // MMAs that read the slot completed
+  uint64_t* acc_full = oempty + GT_OSTAGES;            // [2] accumulator ready for the epilogue
   uint64_t* acc_empty = acc_full + 2;                  // [2] epilogue drained it
   uint64_t* mma_done = acc_empty + 2;                  // [issuer] final drain before TMEM release
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mma_done + GT_MMA_ISSUERS);
@@ -310,13 +323,10 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
       mbar_init(&pfull[s], 1);
       mbar_init(&pempty[s], GT_DQ_PER_GROUP);
     }
-    for (int s = 0; s < GT_BSTAGES; ++s) {
+    for (int s = 0; s < GT_OSTAGES; ++s) {
       mbar_init(&bfull[s], 1);
-      mbar_init(&bempty[s], GT_MMA_ISSUERS);
-    }
-    for (int s = 0; s < GT_ASTAGES; ++s) {
       mbar_init(&afull[s], GT_DQ_PER_GROUP);
-      mbar_init(&aempty[s], GT_MMA_ISSUERS);
+      mbar_init(&oempty[s], GT_MMA_ISSUERS);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], GT_MMA_ISSUERS);
@@ -430,7 +440,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
       for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x) {
         const GtItem it = gt_decode(p, s_istart, s_off, i);
         for (int kb = 0; kb < p.KB; ++kb) {
-          if (!mbar_wait(&bempty[slot], ph ^ 1u, s_flags, lim)) {
+          if (!mbar_wait(&oempty[slot], ph ^ 1u, s_flags, lim)) {
             aborted = true;
             break;
           }
@@ -439,7 +449,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
           // Warm L2 with a tile needed a few loads from now (same token tile).
           if (kb + GT_BPREFETCH < p.KB) tma_prefetch_2d(&tmap_b, (kb + GT_BPREFETCH) * TILE_K, it.p0);
           ++issued;
-          if (++slot == GT_BSTAGES) {
+          if (++slot == GT_OSTAGES) {
             slot = 0;
             ph ^= 1u;
           }
@@ -449,9 +459,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         s_flags[0] = 1;
         set_status(p.status, DEV_TIMEOUT);
         volatile int never = 0;
-        for (int b = 0; b < GT_BSTAGES && b < issued; ++b) {
+        for (int b = 0; b < GT_OSTAGES && b < issued; ++b) {
           if (--slot < 0) {
-            slot = GT_BSTAGES - 1;
+            slot = GT_OSTAGES - 1;
             ph ^= 1u;
           }
           mbar_wait(&bfull[slot], ph, &never, lim);
@@ -468,8 +478,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     if (lane == 0) {
       const uint32_t a_lo0 = smem_desc_sw128_lo(smem_u32(smem + GT_OFF_A));
       const uint32_t b_lo0 = smem_desc_sw128_lo(smem_u32(smem + GT_OFF_B));
-      int as = 0, bs = 0;
-      uint32_t aph = 0, bph = 0;
+      int os = 0;
+      uint32_t oph = 0;
       bool aborted = false;
       int j = 0;
       for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x, ++j) {
@@ -484,14 +494,14 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         const uint32_t idesc = idesc_bf16(128, npad);
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * GT_R * GT_N);
         for (int kb = 0; kb < p.KB; ++kb) {
-          if (!mbar_wait(&afull[as], aph, s_flags, lim) || !mbar_wait(&bfull[bs], bph, s_flags, lim)) {
+          if (!mbar_wait(&afull[os], oph, s_flags, lim) || !mbar_wait(&bfull[os], oph, s_flags, lim)) {
             aborted = true;
             break;
           }
           tc_fence_after();
           // Descriptor low words of this stage's A and B tiles (k-step 0).
-          const uint32_t a_lo = a_lo0 + (uint32_t)as * (GT_A_BYTES >> 4);
-          const uint32_t b_lo = b_lo0 + (uint32_t)bs * (GT_B_BYTES >> 4);
+          const uint32_t a_lo = a_lo0 + (uint32_t)os * (GT_A_BYTES >> 4);
+          const uint32_t b_lo = b_lo0 + (uint32_t)os * (GT_B_BYTES >> 4);
           if (my_r < it.nr) {
             const uint32_t ar = a_lo + (uint32_t)my_r * (GT_A_TILE >> 4);
             const uint32_t dr = d_tmem + (uint32_t)(my_r * GT_N);
@@ -500,15 +510,10 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
             umma_bf16_acc(dr, desc_from_lo(ar + 4), desc_from_lo(b_lo + 4), idesc);
             umma_bf16_acc(dr, desc_from_lo(ar + 6), desc_from_lo(b_lo + 6), idesc);
           }
-          umma_commit(&aempty[as]);
-          umma_commit(&bempty[bs]);
-          if (++as == GT_ASTAGES) {
-            as = 0;
-            aph ^= 1u;
-          }
-          if (++bs == GT_BSTAGES) {
-            bs = 0;
-            bph ^= 1u;
+          umma_commit(&oempty[os]);
+          if (++os == GT_OSTAGES) {
+            os = 0;
+            oph ^= 1u;
           }
         }
         if (!aborted) umma_commit(&acc_full[buf]);
@@ -539,13 +544,13 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
       const GtItem it = gt_decode(p, s_istart, s_off, i);
       const int fmt = gt_expert_fmt(p, it.e);
       if (fmt == FMT_NVFP4)
-        ok = gt_dequant_item<FMT_NVFP4>(p.KB, it.nr, par, p_base, a_base, pfull, pempty, afull, aempty, s_e4m3, rg,
+        ok = gt_dequant_item<FMT_NVFP4>(p.KB, it.nr, par, p_base, a_base, pfull, pempty, afull, oempty, s_e4m3, rg,
                                         lane, s_flags, lim, gk, ps, pph, as, aph);
       else if (fmt == FMT_MXFP4)
-        ok = gt_dequant_item<FMT_MXFP4>(p.KB, it.nr, par, p_base, a_base, pfull, pempty, afull, aempty, s_e4m3, rg,
+        ok = gt_dequant_item<FMT_MXFP4>(p.KB, it.nr, par, p_base, a_base, pfull, pempty, afull, oempty, s_e4m3, rg,
                                         lane, s_flags, lim, gk, ps, pph, as, aph);
       else
-        ok = gt_dequant_item<FMT_NF3>(p.KB, it.nr, par, p_base, a_base, pfull, pempty, afull, aempty, s_e4m3, rg,
+        ok = gt_dequant_item<FMT_NF3>(p.KB, it.nr, par, p_base, a_base, pfull, pempty, afull, oempty, s_e4m3, rg,
                                       lane, s_flags, lim, gk, ps, pph, as, aph);
     }
     if (!ok && lane == 0) {

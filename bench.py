@@ -498,6 +498,71 @@ def run_profile_case(args):
                                        "touched_packed_bytes": tb}}))
 
 
+def run_sweep(args):
+    """The other configurations of the measurement table, timed one point at a time.
+
+    - the 256-expert shape with the kept tier in MXFP4 (64 MXFP4 + 192 NF3),
+      M in {64, 512}, uniform N(0,1) logits;
+    - the uniform NVFP4 layer (H=2048, I=768, E=128, top-8, no bit map),
+      M in {1, 8, 128, 1024, 8192}.
+    A step is plan + forward on the automatic path. Before every step a
+    512 MB buffer is written, outside the event bracket, so no step finds its
+    weights in L2. Prints one JSON object with one entry per point (median of
+    --steps steps).
+    """
+    import nf3_moe_gb300 as hm
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pk = peaks()
+    bpw = {FMT_NVFP4: 0.5625, 5: 0.53125, FMT_NF3: 0.40625}
+    cases = [
+        ("hybrid MXFP4 kept tier, H=6144 I=2048 E=256 top-8, 64 MXFP4 + 192 NF3",
+         dict(**SHAPE, kept=KEPT, kept_format=synth.FMT_MXFP4), (64, 512)),
+        ("uniform NVFP4, H=2048 I=768 E=128 top-8", dict(**synth.UNIFORM_128, uniform=True),
+         (1, 8, 128, 1024, 8192)),
+    ]
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    points = []
+    for name, kw, ms in cases:
+        L = synth.make_layer(device=dev, **kw)
+        bm = None if L.bit_map is None else [int(b) for b in L.bit_map]
+        moe = hm.HybridMoELayer(L.H, L.I, L.E, L.topk, bm, expert_tuples(L), kept_format=L.kept_format,
+                                max_tokens=max(ms))
+        fmts = [moe.layer.expert_info(e)[0] for e in range(L.E)]
+        per_w = 3 * L.H * L.I
+        for M in ms:
+            x = synth.gen_x(M, L.H, seed=4000 + M, device=dev)
+            lg = synth.gen_logits(M, L.E, seed=4000 + M, device=dev)
+            out = torch.empty((M, L.H), dtype=torch.bfloat16, device=dev)
+            ids = gates = None
+            ts = []
+            for i in range(args.warmup + args.steps):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                ids, gates, perm, off = moe.plan(lg)
+                hm.hmoe_forward(moe.layer, x, ids, gates, perm, off, out, moe.ws)
+                b.record()
+                torch.cuda.synchronize()
+                if i >= args.warmup:
+                    ts.append(a.elapsed_time(b))
+            hm.hmoe_check_device_status(moe.ws)
+            ms_ = statistics.median(ts)
+            es = np.unique(ids.cpu().numpy().reshape(-1))
+            byt = sum(per_w * bpw[fmts[int(e)]] for e in es)
+            tfs = 2.0 * L.topk * per_w * M / (ms_ * 1e-3) / 1e12
+            path = "stream" if M * L.topk <= 8 * L.E else "grouped"
+            points.append({"workload": f"{name}, M={M}", "path": path,
+                           "us_per_layer": round(ms_ * 1e3, 2), "touched_experts": int(len(es)),
+                           "touched_bytes": int(byt), "hbm_gbs": round(byt / (ms_ * 1e-3) / 1e9, 1),
+                           "frac_hbm": round(byt / (ms_ * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                           "tflops": round(tfs, 2), "frac_bf16_peak": round(tfs / pk["bf16_tflops_sustained"], 4)})
+        del moe, L
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": points, "steps": args.steps, "warmup": args.warmup, "peaks": pk,
+                      "timing": "plan + forward per step, CUDA events, L2 flushed before each step; median"}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -513,10 +578,16 @@ def main():
     ap.add_argument("--soak-s", type=float, default=1.0)
     ap.add_argument("--profile", action="store_true", help="run the small fixed case used for ncu captures")
     ap.add_argument("--experts", type=int, default=64, help="experts in the --profile case")
+    ap.add_argument("--sweep", action="store_true", help="time the MXFP4-kept and uniform NVFP4 configurations")
     args = ap.parse_args()
     if args.profile:
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         run_profile_case(args)
+        return
+    if args.sweep:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        args.warmup = max(args.warmup, 3)
+        run_sweep(args)
         return
     args.warmup = max(args.warmup, 3)
 

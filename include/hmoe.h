@@ -159,7 +159,8 @@ typedef enum {
 } hmoe_tier_order;
 
 typedef enum {
-  HMOE_PATH_AUTO = 0,     /* T <= 8 streams weights once per batch; larger T uses the grouped path */
+  HMOE_PATH_AUTO = 0,     /* streaming while T*topk <= 8*E (at most 8 routed slots per expert
+                             on average, every T <= 8 included); the grouped path above */
   HMOE_PATH_STREAM = 1,   /* weight-streaming path at any T (tokens in groups of 8) */
   HMOE_PATH_GROUPED = 2   /* tensor-core grouped GEMM path (tcgen05) */
 } hmoe_path;

@@ -86,6 +86,16 @@ int pick_stage(int kbi) {
 }
 
 constexpr int DECODE_MAX_T = 8;
+// The automatic path streams weights (stream.cu) while the batch routes at
+// most this many slots per expert on average, T * topk <= 8 * E, and uses the
+// tensor-core grouped kernel above. The streaming kernel reads each touched
+// expert once per group of 8 of its tokens, so its cost grows with the slots
+// per expert; the grouped kernel costs about the same per k-block whatever
+// its token count. Measured crossover (uniform routing, L2 flushed): at 8
+// slots per expert streaming wins (256 experts, H=6144, I=2048, T=256: 1.69
+// against 1.89 ms; 128 experts, H=2048, I=768, T=128: 146 against 164 us), at
+// 12 to 16 the grouped kernel wins (T=384: 1.90 against 2.31 ms).
+constexpr int STREAM_MAX_SLOTS_PER_EXPERT = 8;
 // Token groups the fixed counter array holds. A stream-path forward whose
 // group bound exceeds it runs W13 and W2 as two launches instead of one.
 constexpr int STREAM_FUSED_MAX_GROUPS = 1024;
@@ -443,7 +453,9 @@ hmoe_status hmoe_forward_ex(const hmoe_layer* L, const void* x, int T, const int
   if (!x || !ids || !gates || !perm || !offsets || !out) return fail(HMOE_ERR_INVALID_ARG, "a buffer is NULL");
   if (!aligned16(x) || !aligned16(out)) return fail(HMOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
   (void)ids;
-  const bool grouped = path == HMOE_PATH_GROUPED || (path == HMOE_PATH_AUTO && T > DECODE_MAX_T);
+  const bool grouped =
+      path == HMOE_PATH_GROUPED ||
+      (path == HMOE_PATH_AUTO && (long long)T * L->d.topk > (long long)STREAM_MAX_SLOTS_PER_EXPERT * L->d.E);
   if (grouped && T <= DECODE_MAX_T)
     return fail(HMOE_ERR_INVALID_ARG, "the grouped path needs T > %d (the workspace holds no gather buffer below)",
                 DECODE_MAX_T);

@@ -47,7 +47,8 @@ def test_bad_offsets_reported_and_context_survives(tiny):
     U.assert_rows_close(good.float().cpu().numpy(), U.oracle_out(L, x, i2, g2))
 
 
-def test_out_of_range_perm_reported(tiny):
+@pytest.mark.parametrize("path", [hm.PATH_AUTO, hm.PATH_STREAM, hm.PATH_GROUPED])
+def test_out_of_range_perm_reported(tiny, path):
     L, moe = tiny
     x, logits = _inputs(L, 37)
     ids, gates, perm, offsets = moe.plan(logits)
@@ -55,7 +56,7 @@ def test_out_of_range_perm_reported(tiny):
     bad[3] = 10_000
     bad[5] = -4
     out = torch.empty((37, L.H), dtype=torch.bfloat16, device="cuda")
-    hm.hmoe_forward(moe.layer, x, ids, gates, bad, offsets, out, moe.ws)
+    hm.hmoe_forward(moe.layer, x, ids, gates, bad, offsets, out, moe.ws, path=path)
     with pytest.raises(hm.HmoeError) as ei:
         hm.hmoe_check_device_status(moe.ws)
     assert ei.value.status == -7

@@ -57,17 +57,24 @@ def test_hybrid_prefill_4096_zipf(hybrid_prefill):
 
 @pytest.mark.parametrize("T", [64, 512])
 def test_mxfp4_kept_tier_full_shape(T):
+    """The automatic path streams at T=64 (2 slots per expert) and takes the grouped kernel at
+    T=512 (16). Both paths run at both sizes: each matches the oracle on sampled rows, and
+    they agree with each other within tolerance on every row."""
     L = synth.make_layer(**synth.HYBRID_256, kept=64, kept_format=synth.FMT_MXFP4, device="cuda")
     moe = U.build(L, T)
     x = synth.gen_x(T, L.H, seed=T, device="cuda")
     logits = synth.gen_logits(T, L.E, seed=T, device="cuda")
     out, (ids, gates, _, _) = U.run(moe, x, logits)
     assert torch.isfinite(out.float()).all()
+    auto_path = hm.PATH_STREAM if T * L.topk <= 8 * L.E else hm.PATH_GROUPED
+    same, _ = U.run(moe, x, logits, path=auto_path)
+    assert torch.equal(out, same)
     tokens = [0, T // 2, T - 1]
-    U.assert_rows_close(_rows(out, tokens), U.oracle_out(L, x, ids, gates, tokens=tokens))
-    # the stream path at the same batch agrees within tolerance
-    s, _ = U.run(moe, x, logits, path=hm.PATH_STREAM)
-    U.assert_rows_close(s.float().cpu().numpy(), out.float().cpu().numpy())
+    ref = U.oracle_out(L, x, ids, gates, tokens=tokens)
+    U.assert_rows_close(_rows(out, tokens), ref)
+    other, _ = U.run(moe, x, logits, path=hm.PATH_GROUPED if auto_path == hm.PATH_STREAM else hm.PATH_STREAM)
+    U.assert_rows_close(_rows(other, tokens), ref)
+    U.assert_rows_close(other.float().cpu().numpy(), out.float().cpu().numpy())
 
 
 @pytest.fixture(scope="module")

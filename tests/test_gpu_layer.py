@@ -59,6 +59,25 @@ def test_stream_path_equals_decode_path_tolerance(tiny):
     U.assert_rows_close(a.float().cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("kept_format", [synth.FMT_NVFP4, synth.FMT_MXFP4])
+def test_odd_k_block_counts(kept_format):
+    """I=192: W2 has 3 k-blocks (the grouped kernel's two-k-block stages end with a phantom one)
+    and W13 has 3 row tiles (the last item holds one). Both paths match the oracle on sampled
+    rows and each other on every row."""
+    L = synth.make_layer(384, 192, 8, 2, kept_ids=[0, 3, 5], kept_format=kept_format, device="cuda")
+    T = 96
+    moe = U.build(L, T)
+    x = synth.gen_x(T, L.H, seed=11, device="cuda")
+    logits = synth.gen_logits(T, L.E, seed=11, device="cuda")
+    g, (ids, gates, _, _) = U.run(moe, x, logits, path=hm.PATH_GROUPED)
+    s, _ = U.run(moe, x, logits, path=hm.PATH_STREAM)
+    tokens = [0, 1, T // 2, T - 1]
+    ref = U.oracle_out(L, x, ids, gates, tokens=tokens)
+    U.assert_rows_close(g.float().cpu().numpy()[tokens], ref)
+    U.assert_rows_close(s.float().cpu().numpy()[tokens], ref)
+    U.assert_rows_close(g.float().cpu().numpy(), s.float().cpu().numpy())
+
+
 def test_top1_single_expert_and_repeat_calls(tiny):
     """top-1 (gate = 1) reduces to one dense expert; repeated calls are bitwise stable."""
     Lh = synth.make_layer(256, 128, 8, 1, kept_ids=[1, 5], device="cuda")

@@ -550,7 +550,7 @@ def run_sweep(args):
             es = np.unique(ids.cpu().numpy().reshape(-1))
             byt = sum(per_w * bpw[fmts[int(e)]] for e in es)
             tfs = 2.0 * L.topk * per_w * M / (ms_ * 1e-3) / 1e12
-            path = "stream" if M * L.topk <= 8 * L.E else "grouped"
+            path = "stream" if hm.hmoe_auto_path(moe.desc, M) == hm.PATH_STREAM else "grouped"
             points.append({"workload": f"{name}, M={M}", "path": path,
                            "us_per_layer": round(ms_ * 1e3, 2), "touched_experts": int(len(es)),
                            "touched_bytes": int(byt), "hbm_gbs": round(byt / (ms_ * 1e-3) / 1e9, 1),

@@ -113,6 +113,16 @@ hmoe_status hmoe_packed_size(const hmoe_layer_desc* desc, const int8_t* bit_map,
  * tokens per call (the scratch is sized from the largest batch). */
 hmoe_status hmoe_workspace_size(const hmoe_layer_desc* desc, int max_tokens, size_t* bytes);
 
+/* The path hmoe_forward takes for T tokens when opts->path is HMOE_PATH_AUTO:
+ * HMOE_PATH_STREAM while T * topk <= 8 * E (at most 8 routed slots per
+ * expert on average; every T <= 8 included), HMOE_PATH_GROUPED above. Host
+ * only: no device work, no GPU needed. The pages give the M <= 8 path
+ * ("quant: nvfp4_nf3_hybrid ...", How it works) but no rule above it; the
+ * factor 8 is this library's measured crossover between its two kernels.
+ * Errors: HMOE_ERR_INVALID_ARG (NULL pointer, T < 0) and the desc checks of
+ * hmoe_workspace_size. */
+hmoe_status hmoe_auto_path(const hmoe_layer_desc* desc, int T, int* path);
+
 /* Zero the workspace once, before its first use, on the stream. Every
  * completed hmoe_forward leaves the workspace's counters at zero again. Zero
  * it once more after a call reports HMOE_ERR_DEVICE_TIMEOUT. */

@@ -65,6 +65,13 @@ def hmoe_workspace_size(desc, max_tokens):
     return b.value
 
 
+def hmoe_auto_path(desc, T):
+    """PATH_STREAM or PATH_GROUPED: the path hmoe_forward takes for T tokens with path=PATH_AUTO."""
+    out = ctypes.c_int()
+    _lib.check(_lib.lib().hmoe_auto_path(ctypes.byref(desc), int(T), ctypes.byref(out)))
+    return out.value
+
+
 def hmoe_workspace_init(ws, stream=None):
     _lib.check(_lib.lib().hmoe_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 

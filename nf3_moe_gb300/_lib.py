@@ -28,6 +28,7 @@ EXPORTS = (
     "hmoe_plan_routes", "hmoe_forward", "hmoe_forward_ex", "hmoe_check_device_status",
     "hmoe_debug_dequant", "hmoe_layer_expert_info", "hmoe_layer_destroy", "hmoe_last_error",
     "hmoe_launch_count", "hmoe_version", "hmoe_forward_static", "hmoe_check_device_status_static",
+    "hmoe_auto_path",
 )
 
 
@@ -76,6 +77,7 @@ def load(path=LIB_PATH):
         "hmoe_forward_static": (i, [vp, vp, i, vp, vp, vp, vp, vp, vp]),
         "hmoe_check_device_status_static": (i, [vp]),
         "hmoe_version": (i, []),
+        "hmoe_auto_path": (i, [P(LayerDesc), i, P(i)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

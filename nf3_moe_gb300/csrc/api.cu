@@ -183,6 +183,18 @@ hmoe_status hmoe_workspace_size(const hmoe_layer_desc* desc, int max_tokens, siz
   return HMOE_OK;
 }
 
+static bool auto_is_grouped(const hmoe_layer_desc& d, int T) {
+  return (long long)T * d.topk > (long long)STREAM_MAX_SLOTS_PER_EXPERT * d.E;
+}
+
+hmoe_status hmoe_auto_path(const hmoe_layer_desc* desc, int T, int* path) {
+  hmoe_status s = check_desc(desc);
+  if (s != HMOE_OK) return s;
+  if (!path || T < 0) return fail(HMOE_ERR_INVALID_ARG, "path NULL or T < 0");
+  *path = auto_is_grouped(*desc, T) ? HMOE_PATH_GROUPED : HMOE_PATH_STREAM;
+  return HMOE_OK;
+}
+
 hmoe_status hmoe_workspace_init(void* ws, size_t ws_bytes, hmoe_stream_t stream) {
   if (!ws) return fail(HMOE_ERR_INVALID_ARG, "workspace is NULL");
   cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream);
@@ -453,9 +465,7 @@ hmoe_status hmoe_forward_ex(const hmoe_layer* L, const void* x, int T, const int
   if (!x || !ids || !gates || !perm || !offsets || !out) return fail(HMOE_ERR_INVALID_ARG, "a buffer is NULL");
   if (!aligned16(x) || !aligned16(out)) return fail(HMOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
   (void)ids;
-  const bool grouped =
-      path == HMOE_PATH_GROUPED ||
-      (path == HMOE_PATH_AUTO && (long long)T * L->d.topk > (long long)STREAM_MAX_SLOTS_PER_EXPERT * L->d.E);
+  const bool grouped = path == HMOE_PATH_GROUPED || (path == HMOE_PATH_AUTO && auto_is_grouped(L->d, T));
   if (grouped && T <= DECODE_MAX_T)
     return fail(HMOE_ERR_INVALID_ARG, "the grouped path needs T > %d (the workspace holds no gather buffer below)",
                 DECODE_MAX_T);

@@ -59,6 +59,24 @@ def test_host_validation_without_gpu(lib):
     assert ei.value.status == -4
 
 
+def test_auto_path_rule():
+    """Streaming while T * topk <= 8 * E, grouped above; every T <= 8 streams."""
+    import nf3_moe_gb300 as hm
+    hyb = hm.LayerDesc(6144, 2048, 256, 8, hm.FMT_NVFP4)
+    uni = hm.LayerDesc(2048, 768, 128, 8, hm.FMT_NVFP4)
+    tiny = hm.LayerDesc(256, 128, 8, 2, hm.FMT_NVFP4)
+    S, G = hm.PATH_STREAM, hm.PATH_GROUPED
+    cases = [(hyb, 0, S), (hyb, 1, S), (hyb, 8, S), (hyb, 64, S), (hyb, 256, S), (hyb, 257, G), (hyb, 4096, G),
+             (uni, 128, S), (uni, 129, G), (tiny, 8, S), (tiny, 32, S), (tiny, 33, G), (tiny, 37, G)]
+    for desc, T, want in cases:
+        assert hm.hmoe_auto_path(desc, T) == want, (desc.E, T)
+    # a layer whose top-k exceeds 8 * E / T for every T > 8 still streams at T <= 8
+    assert hm.hmoe_auto_path(hm.LayerDesc(256, 128, 8, 8, hm.FMT_NVFP4), 8) == S
+    with pytest.raises(hm.HmoeError) as ei:
+        hm.hmoe_auto_path(hyb, -1)
+    assert ei.value.status == -1
+
+
 def test_null_handles_rejected(lib):
     assert lib.hmoe_plan_routes(None, None, 1, None, None, None, None, None, 0, None) == -1
     assert lib.hmoe_forward(None, None, 1, None, None, None, None, None, None, 0, None) == -1

@@ -66,7 +66,8 @@ def test_mxfp4_kept_tier_full_shape(T):
     logits = synth.gen_logits(T, L.E, seed=T, device="cuda")
     out, (ids, gates, _, _) = U.run(moe, x, logits)
     assert torch.isfinite(out.float()).all()
-    auto_path = hm.PATH_STREAM if T * L.topk <= 8 * L.E else hm.PATH_GROUPED
+    auto_path = hm.hmoe_auto_path(moe.desc, T)
+    assert auto_path == (hm.PATH_STREAM if T == 64 else hm.PATH_GROUPED)
     same, _ = U.run(moe, x, logits, path=auto_path)
     assert torch.equal(out, same)
     tokens = [0, T // 2, T - 1]

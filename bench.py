@@ -116,6 +116,21 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ helpers
+def max_over_ranks(t_ms, world, device):
+    """The slowest rank's time, returned on every rank (N > 1 runs one independent
+    replica per rank; the whole job takes as long as its slowest replica)."""
+    if world <= 1:
+        return float(t_ms)
+    tt = torch.tensor([float(t_ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_gbs(bytes_per_rank, world, t_ms):
+    """GB/s over all ranks: every rank moved bytes_per_rank in the (max-over-ranks) time t_ms."""
+    return bytes_per_rank * world / (t_ms * 1e-3) / 1e9
+
+
 def touched(ids_cpu, fmts):
     es = np.unique(np.asarray(ids_cpu).reshape(-1))
     total = sum(BYTES_PER_EXPERT[fmts[e]] for e in es)
@@ -301,14 +316,10 @@ def run_ours(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     clocks = clock.stop()
-    t_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        tt = torch.tensor([t_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_ms = float(tt.item())
+    t_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     hm.hmoe_check_device_status(ws)
     bytes_steps = sum(tb[i % REPLICAS][0] for i in range(K))
-    value = bytes_steps * world / (t_ms * 1e-3) / 1e9
+    value = whole_job_gbs(bytes_steps, world, t_ms)
     # GEMM launch time (W13 + W2, one fused stream-kernel launch) of the last
     # replay of each replica's graph, inside the timed region.
     nlast = min(K, REPLICAS)

@@ -700,13 +700,9 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 cudaError_t launch_grouped_gemm(const GroupedParams& p, const __nv_bfloat16* b_src, int b_rows, int num_sms,
                                 cudaStream_t st) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GT_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  const cudaError_t ea = ensure_smem_attr(grouped_gemm_kernel, GT_SMEM_BYTES, attr_done);
+  if (ea != cudaSuccess) return ea;
   if (b_rows <= 0) return cudaSuccess;
   if ((reinterpret_cast<uintptr_t>(b_src) & 15) != 0 || (p.K % TILE_K) != 0) return cudaErrorInvalidValue;
   auto enc = tensor_map_encoder();

@@ -4,6 +4,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace hmoe {
@@ -95,5 +97,21 @@ cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int* perm, int S, i
 // out[t][c] = bf16(sum_j gates[t*k+j] * y[t*k+j][c])
 cudaError_t launch_finalize(const float* y, const float* gates, int T, int k, int H, __nv_bfloat16* out,
                             cudaStream_t st);
+
+// Raises a kernel's dynamic shared-memory limit once per device: the
+// attribute belongs to the current device, so a process that launches on
+// several GPUs sets it on each. done is the kernel's bit mask of devices
+// already set (ids 0..63; a higher id sets it on every call).
+template <typename Kernel>
+inline cudaError_t ensure_smem_attr(Kernel* kernel, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 }  // namespace hmoe

@@ -436,13 +436,9 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
 int stream_grid(int num_sms) { return 2 * num_sms; }
 
 cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(stream_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SK_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  const cudaError_t ea = ensure_smem_attr(stream_gemm_kernel, SK_SMEM_BYTES, attr_done);
+  if (ea != cudaSuccess) return ea;
   if (p.ph_begin < 0 || p.ph_begin >= p.ph_end || p.ph_end > 2) return cudaErrorInvalidValue;
   if (p.ph_begin == 0 && p.ph_end == 2 && !p.done13) return cudaErrorInvalidValue;
   for (const StreamPhase& P : p.ph)

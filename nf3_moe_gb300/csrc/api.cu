@@ -281,7 +281,7 @@ hmoe_status hmoe_plan_routes(const hmoe_layer* L, const float* logits, int T, in
   if (T < 0) return fail(HMOE_ERR_INVALID_ARG, "T=%d < 0", T);
   if (!offsets || (T > 0 && (!logits || !ids || !gates || !perm)))
     return fail(HMOE_ERR_INVALID_ARG, "a route buffer is NULL");
-  WsLayout w;
+  WsLayout w{};
   hmoe_status s = check_ws(L->d, T, ws, ws_bytes, &w);
   if (s != HMOE_OK) return s;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
@@ -458,7 +458,7 @@ hmoe_status hmoe_forward_ex(const hmoe_layer* L, const void* x, int T, const int
   if (tier_order < 0 || tier_order > 2) return fail(HMOE_ERR_INVALID_ARG, "bad tier_order %d", tier_order);
   if (path < 0 || path > 2) return fail(HMOE_ERR_INVALID_ARG, "bad path %d", path);
   if (o.wait_limit_us < 0) return fail(HMOE_ERR_INVALID_ARG, "wait_limit_us < 0");
-  WsLayout w;
+  WsLayout w{};
   hmoe_status s = check_ws(L->d, T, ws, ws_bytes, &w);
   if (s != HMOE_OK) return s;
   if (T == 0) return HMOE_OK;

@@ -1,6 +1,7 @@
 """Error paths on the GPU. None of them traps, faults or hangs: the kernels skip bad accesses,
 bound every wait, and report through the workspace status word."""
 
+import numpy as np
 import pytest
 import torch
 
@@ -88,3 +89,49 @@ def test_bad_bitmap_and_shape_rejected():
     with pytest.raises(hm.HmoeError) as ei:
         hm.hmoe_workspace_size(hm.LayerDesc(200, 128, 4, 2, 4), 8)
     assert ei.value.status == -2
+
+
+GUARD = 4096      # canary bytes on each side of a caller buffer (keeps 256-byte alignment)
+CANARY = 0xA5
+
+
+def _guarded(nbytes):
+    """A device buffer with CANARY bands of GUARD bytes around it: (whole allocation, inner view)."""
+    full = torch.full((nbytes + 2 * GUARD,), CANARY, dtype=torch.uint8, device="cuda")
+    return full, full[GUARD:GUARD + nbytes]
+
+
+def _bands_intact(full, nbytes):
+    return bool((full[:GUARD] == CANARY).all()) and bool((full[GUARD + nbytes:] == CANARY).all())
+
+
+@pytest.mark.parametrize("T,path", [(8, hm.PATH_STREAM), (64, hm.PATH_STREAM), (64, hm.PATH_GROUPED)])
+def test_no_write_outside_caller_buffers(tiny, T, path):
+    """Routing and forward write nothing outside the workspace, the plan outputs and the layer
+    output: canary bands around each are unchanged, and the result equals the unguarded run."""
+    L, moe = tiny
+    x, logits = _inputs(L, T)
+    ws_bytes = hm.hmoe_workspace_size(moe.desc, T)
+    ws_full, ws = _guarded(ws_bytes)
+    hm.hmoe_workspace_init(ws)
+    bands = {"workspace": (ws_full, ws_bytes)}
+
+    def buffer(name, shape, dtype):
+        nbytes = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+        full, view = _guarded(nbytes)
+        bands[name] = (full, nbytes)
+        return view.view(dtype).view(shape)
+
+    ids = buffer("ids", (T, L.topk), torch.int32)
+    gates = buffer("gates", (T, L.topk), torch.float32)
+    perm = buffer("perm", (T * L.topk,), torch.int32)
+    offsets = buffer("offsets", (L.E + 1,), torch.int32)
+    out = buffer("out", (T, L.H), torch.bfloat16)
+    hm.hmoe_plan_routes(moe.layer, logits, ids, gates, perm, offsets, ws)
+    hm.hmoe_forward(moe.layer, x, ids, gates, perm, offsets, out, ws, path=path)
+    torch.cuda.synchronize()
+    hm.hmoe_check_device_status(ws)
+    for name, (full, nbytes) in bands.items():
+        assert _bands_intact(full, nbytes), name
+    ref, _ = U.run(moe, x, logits, path=path)
+    assert torch.equal(out, ref)

@@ -49,6 +49,10 @@ REPLICAS = 4
 FMT_NF3, FMT_NVFP4 = 3, 4
 BYTES_PER_EXPERT = {4: 21_233_664, 5: 20_054_016, 3: 15_335_424}
 W13_BYTES = {4: 14_155_776, 5: 13_369_344, 3: 10_223_616}
+TIER_NAMES = {0: "one_launch", 1: "kept_first", 2: "nf3_first"}
+# The stream kernel's sources: the traffic figure committed under profiles/ is
+# used only while these are unchanged since the capture.
+STREAM_SOURCES = ("nf3_moe_gb300/csrc/stream.cu", "nf3_moe_gb300/csrc/common.cuh")
 
 
 def peaks():
@@ -62,23 +66,38 @@ def peaks():
 
 
 # ------------------------------------------------------------------ clocks
+def nvsmi_gpu_id(device):
+    """The nvidia-smi selector of the torch device: its UUID ("GPU-..."). nvidia-smi numbers
+    GPUs physically and ignores CUDA_VISIBLE_DEVICES, so a CUDA ordinal could name another
+    user's GPU on a shared machine; the UUID cannot."""
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+    except (AttributeError, RuntimeError):
+        return None
+    if not u:
+        return None
+    return u if u.startswith("GPU-") else "GPU-" + u
+
+
 class ClockSampler:
-    """nvidia-smi clock and throttle-reason samples while the GPU is under load."""
+    """nvidia-smi clock and throttle-reason samples of one GPU (selected by UUID) while it is under load."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index):
-        self.idx = device_index
+    def __init__(self, device):
+        self.gpu = nvsmi_gpu_id(device)
         self.proc = None
         self.lines = []
 
     def start(self):
         try:
+            if self.gpu is None:
+                return
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
-                 "-i", str(self.idx)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-i", self.gpu], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
@@ -90,7 +109,8 @@ class ClockSampler:
 
     def stop(self):
         if not self.proc:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0,
+                    "gpu": self.gpu}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -112,7 +132,7 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "gpu": self.gpu}
 
 
 # ------------------------------------------------------------------ helpers
@@ -159,6 +179,31 @@ def oracle_sample(L_host_experts, H, I, x_row, ids_row, gates_row):
 
 def host_experts(L, ids):
     return {int(e): L.expert_numpy(int(e)) for e in np.unique(ids)}
+
+
+def sources_sha16(paths):
+    import hashlib
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stream_traffic(M):
+    """(DRAM bytes per stream-kernel launch, where the figure comes from). The figure is an
+    ncu capture committed under profiles/, scaled to this workload; it is used only while
+    the kernel's sources are those it was captured on, else (None, reason)."""
+    tpath = os.path.join(ROOT, "profiles", "stream_gemm_traffic.json")
+    try:
+        tj = json.load(open(tpath))
+    except (OSError, ValueError):
+        return None, "no capture committed"
+    if tj.get("M") != M:
+        return None, f"capture is for M={tj.get('M')}"
+    if tj.get("source_sha16") != sources_sha16(STREAM_SOURCES):
+        return None, "stale: the stream kernel changed since the ncu capture"
+    return tj.get("dram_bytes_per_launch"), tj.get("how", "ncu capture, scaled")
 
 
 # ------------------------------------------------------------------ reference arm
@@ -247,12 +292,12 @@ def run_ours(args, rank, world):
             out.append((x, lg, bufs))
         return out
 
-    def step(i, bl, evs=None):
+    def step(i, bl, evs=None, tier_order=hm.TIERS_ONE_LAUNCH):
         r = i % REPLICAS
         x, lg, b = bl[r]
         hm.hmoe_plan_routes(reps[r], lg, b["ids"], b["gates"], b["perm"], b["offsets"], ws)
         hm.hmoe_forward(reps[r], x, b["ids"], b["gates"], b["perm"], b["offsets"], b["out"], ws,
-                        stage_events=evs)
+                        stage_events=evs, tier_order=tier_order)
 
     def batch_bytes(bl):
         res = []
@@ -272,13 +317,13 @@ def run_ours(args, rank, world):
     # as a serving engine replays a decode step. The graph holds exactly
     # the library's kernels; stage events inside it time the GEMM launch
     # (W13 and W2 fused into one stream-kernel launch at M <= 8).
-    def capture(bl_):
+    def capture(bl_, tier_order=hm.TIERS_ONE_LAUNCH):
         graphs, per_step = [], 0
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
             for r in range(REPLICAS):
-                step(r, bl_)                 # warm the launch path outside capture
+                step(r, bl_, tier_order=tier_order)     # warm the launch path outside capture
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
         for r in range(REPLICAS):
@@ -289,7 +334,7 @@ def run_ours(args, rank, world):
             g = torch.cuda.CUDAGraph()
             n0 = hm.hmoe_launch_count()
             with torch.cuda.graph(g):
-                step(r, bl_, evs=evs)
+                step(r, bl_, evs=evs, tier_order=tier_order)
             per_step = hm.hmoe_launch_count() - n0
             graphs.append((g, evs))
         return graphs, per_step
@@ -297,7 +342,7 @@ def run_ours(args, rank, world):
     graphs, launches_per_step = capture(bl)
 
     # warm-up (untimed) and clock soak
-    clock = ClockSampler(torch.cuda.current_device())
+    clock = ClockSampler(dev)
     for i in range(args.warmup):
         graphs[i % REPLICAS][0].replay()
     clock.start()
@@ -385,6 +430,24 @@ def run_ours(args, rank, world):
     e2e_s = time.perf_counter() - t0
     e2e_val = bytes_steps / e2e_s / 1e9
 
+    # tier strategy at decode M=8: one launch per GEMM with per-expert format
+    # dispatch, or one launch per tier (kept first / NF3 first); graph replay
+    tiers = {"decode_m8_us": {}, "prefill_m4096_ms": {}}
+    if world == 1 and not args.skip_tiers:
+        for order in (hm.TIERS_ONE_LAUNCH, hm.TIERS_KEPT_FIRST, hm.TIERS_NF3_FIRST):
+            gs = capture(bl, tier_order=order)[0]
+            for j in range(8):
+                gs[j % REPLICAS][0].replay()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a_.record()
+            for j in range(64):
+                gs[j % REPLICAS][0].replay()
+            b_.record()
+            torch.cuda.synchronize()
+            tiers["decode_m8_us"][TIER_NAMES[order]] = round(a_.elapsed_time(b_) / 64 * 1e3, 2)
+            del gs
+
     # prefill point: M = 4096 with skewed routing
     prefill = None
     if not args.skip_prefill:
@@ -398,31 +461,44 @@ def run_ours(args, rank, world):
                   offsets=torch.empty((E + 1,), dtype=torch.int32, device=dev),
                   out=torch.empty((Mp, H), dtype=torch.bfloat16, device=dev))
 
-        def pstep(r):
+        def pstep(r, order=hm.TIERS_ONE_LAUNCH):
             hm.hmoe_plan_routes(reps[r], lp, bp["ids"], bp["gates"], bp["perm"], bp["offsets"], ws)
             hm.hmoe_forward(reps[r], xp, bp["ids"], bp["gates"], bp["perm"], bp["offsets"], bp["out"], ws,
-                            path=args.prefill_path)
+                            path=args.prefill_path, tier_order=order)
 
-        for r in range(2):
-            pstep(r)
-        torch.cuda.synchronize()
-        n = args.prefill_steps
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for r in range(n):
-            pstep(r % REPLICAS)
-        b.record()
-        torch.cuda.synchronize()
+        def ptime(n, order=hm.TIERS_ONE_LAUNCH):
+            # each forward uses the next weight replica, so no forward finds its weights in L2
+            for r in range(2):
+                pstep(r, order)
+            torch.cuda.synchronize()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record()
+            for r in range(n):
+                pstep(r % REPLICAS, order)
+            b_.record()
+            torch.cuda.synchronize()
+            return a_.elapsed_time(b_) / n
+
+        pclock = ClockSampler(dev)
+        pclock.start()
+        ms = ptime(args.prefill_steps)
+        pclocks = pclock.stop()
         hm.hmoe_check_device_status(ws)
-        ms = a.elapsed_time(b) / n
+        if world == 1 and not args.skip_tiers:
+            for order in (hm.TIERS_ONE_LAUNCH, hm.TIERS_KEPT_FIRST, hm.TIERS_NF3_FIRST):
+                tiers["prefill_m4096_ms"][TIER_NAMES[order]] = round(ptime(3, order), 3)
         flops = 2.0 * k * 3 * H * I * Mp
         tfs = flops / (ms * 1e-3) / 1e12
         cnt = torch.bincount(bp["ids"].reshape(-1).long(), minlength=E).float()
         prefill = {"workload": f"hybrid MoE prefill M={Mp}, Zipf(1.1)-biased router logits "
                                f"(beta={beta:.3f}, hottest expert {float(cnt.max() / cnt.mean()):.1f}x mean)",
                    "ms_per_layer": round(ms, 3), "tokens_per_s": round(Mp / (ms * 1e-3), 1),
-                   "tflops": round(tfs, 2), "frac_bf16_peak": round(tfs / pk["bf16_tflops_sustained"], 4),
-                   "peak_used": "bf16_tflops_sustained (" + pk["source"] + ")",
+                   "tflops": round(tfs, 2), "frac_bf16_peak": round(tfs / pk["bf16_tflops"], 4),
+                   "peak_used": "bf16_tflops, burst (" + pk["source"] + "): the layer is timed alone, "
+                                f"{args.prefill_steps} forwards",
+                   "frac_bf16_sustained_peak": round(tfs / pk["bf16_tflops_sustained"], 4),
+                   "timing": "eager plan + forward, CUDA events; each forward on the next of 4 weight replicas",
+                   "clocks": pclocks,
                    "path": {0: "auto", 1: "stream", 2: "grouped"}[args.prefill_path]}
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
             # The oracle on a bounded sample of the same batch: its first two tokens.
@@ -462,15 +538,12 @@ def run_ours(args, rank, world):
                          f"experts, {byt / 1e6:.0f} MB packed in all), float64 NumPy dequantise-then-matmul, "
                          f"{dt:.1f} s"}
 
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "stream_gemm_traffic.json")
-    if os.path.exists(tpath):
-        try:
-            tj = json.load(open(tpath))
-            if tj.get("M") == M:
-                traffic = tj.get("dram_bytes_per_launch")
-        except (OSError, ValueError):
-            traffic = None
+    traffic, traffic_source = stream_traffic(M)
+    sweep = None
+    if world == 1 and not args.skip_sweep:
+        del graphs
+        torch.cuda.empty_cache()
+        sweep = sweep_points(dev, pk, steps=args.sweep_steps, warmup=3)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -483,7 +556,7 @@ def run_ours(args, rank, world):
                    "l2": f"{REPLICAS} rotating weight replicas and batches; each step touches > L2 (129 MB)",
                    "timing": "CUDA-graph replay of plan + forward per step; CUDA events on the replay stream",
                    "parallelism": "replicas only" if world > 1 else "1 GPU",
-                   "peaks": pk, "per_m": per_m, "prefill": prefill},
+                   "peaks": pk, "per_m": per_m, "prefill": prefill, "tiers": tiers, "sweep": sweep},
         "clocks": clocks,
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(M * H * 2 + M * E * 4), "d2h_bytes_per_step": int(M * H * 2)},
@@ -492,6 +565,7 @@ def run_ours(args, rank, world):
                      "bound": "hbm",
                      "achieved": round(gemm_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(gemm_gbs / pk["hbm_gbs"], 4), "traffic": traffic,
+                     "traffic_source": traffic_source,
                      "algorithmic_bytes_per_launch": int(gemm_bytes), "avg_launch_us": round(gemm_avg * 1e3, 2),
                      "timing": "stage events captured in the step graphs, last replay of each graph in the timed region"},
         "cpu_baseline": cpu,
@@ -526,21 +600,19 @@ def run_profile_case(args):
                                        "touched_packed_bytes": tb}}))
 
 
-def run_sweep(args):
-    """The other configurations of the measurement table, timed one point at a time.
+def sweep_points(dev, pk, steps=10, warmup=3):
+    """The other configurations, one point at a time, timed like the headline.
 
     - the 256-expert shape with the kept tier in MXFP4 (64 MXFP4 + 192 NF3),
       M in {64, 512}, uniform N(0,1) logits;
     - the uniform NVFP4 layer (H=2048, I=768, E=128, top-8, no bit map),
       M in {1, 8, 128, 1024, 8192}.
-    A step is plan + forward on the automatic path. Before every step a
-    512 MB buffer is written, outside the event bracket, so no step finds its
-    weights in L2. Prints one JSON object with one entry per point (median of
-    --steps steps).
+    A step is plan + forward on the automatic path, captured once in a CUDA
+    graph and replayed. Before every replay a 512 MB buffer is written,
+    outside the event bracket, so no step finds its weights in the 129 MB L2.
+    Returns one entry per point (median of ``steps`` replays after ``warmup``).
     """
     import nf3_moe_gb300 as hm
-    dev = torch.device("cuda", torch.cuda.current_device())
-    pk = peaks()
     bpw = {FMT_NVFP4: 0.5625, 5: 0.53125, FMT_NF3: 0.40625}
     cases = [
         ("hybrid MXFP4 kept tier, H=6144 I=2048 E=256 top-8, 64 MXFP4 + 192 NF3",
@@ -560,18 +632,34 @@ def run_sweep(args):
         for M in ms:
             x = synth.gen_x(M, L.H, seed=4000 + M, device=dev)
             lg = synth.gen_logits(M, L.E, seed=4000 + M, device=dev)
+            ids = torch.empty((M, L.topk), dtype=torch.int32, device=dev)
+            gates = torch.empty((M, L.topk), dtype=torch.float32, device=dev)
+            perm = torch.empty((M * L.topk,), dtype=torch.int32, device=dev)
+            off = torch.empty((L.E + 1,), dtype=torch.int32, device=dev)
             out = torch.empty((M, L.H), dtype=torch.bfloat16, device=dev)
-            ids = gates = None
+
+            def fwd():
+                hm.hmoe_plan_routes(moe.layer, lg, ids, gates, perm, off, moe.ws)
+                hm.hmoe_forward(moe.layer, x, ids, gates, perm, off, out, moe.ws)
+
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                fwd()
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fwd()
             ts = []
-            for i in range(args.warmup + args.steps):
+            for i in range(warmup + steps):
                 flush.zero_()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
-                ids, gates, perm, off = moe.plan(lg)
-                hm.hmoe_forward(moe.layer, x, ids, gates, perm, off, out, moe.ws)
+                g.replay()
                 b.record()
                 torch.cuda.synchronize()
-                if i >= args.warmup:
+                if i >= warmup:
                     ts.append(a.elapsed_time(b))
             hm.hmoe_check_device_status(moe.ws)
             ms_ = statistics.median(ts)
@@ -583,12 +671,24 @@ def run_sweep(args):
                            "us_per_layer": round(ms_ * 1e3, 2), "touched_experts": int(len(es)),
                            "touched_bytes": int(byt), "hbm_gbs": round(byt / (ms_ * 1e-3) / 1e9, 1),
                            "frac_hbm": round(byt / (ms_ * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
-                           "tflops": round(tfs, 2), "frac_bf16_peak": round(tfs / pk["bf16_tflops_sustained"], 4)})
+                           "tokens_per_s": round(M / (ms_ * 1e-3), 1),
+                           "tflops": round(tfs, 2), "frac_bf16_peak": round(tfs / pk["bf16_tflops"], 4)})
+            del g
         del moe, L
         torch.cuda.empty_cache()
+    del flush
+    torch.cuda.empty_cache()
+    return points
+
+
+def run_sweep(args):
+    """The sweep of sweep_points() alone, printed as one JSON object."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pk = peaks()
+    points = sweep_points(dev, pk, steps=args.steps, warmup=args.warmup)
     print(json.dumps({"sweep": points, "steps": args.steps, "warmup": args.warmup, "peaks": pk,
-                      "timing": "plan + forward per step, CUDA events, L2 flushed before each step; median"}),
-          flush=True)
+                      "timing": "CUDA-graph replay of plan + forward, CUDA events, L2 flushed before each "
+                                "replay; median"}), flush=True)
 
 
 def main():
@@ -606,7 +706,10 @@ def main():
     ap.add_argument("--soak-s", type=float, default=1.0)
     ap.add_argument("--profile", action="store_true", help="run the small fixed case used for ncu captures")
     ap.add_argument("--experts", type=int, default=64, help="experts in the --profile case")
-    ap.add_argument("--sweep", action="store_true", help="time the MXFP4-kept and uniform NVFP4 configurations")
+    ap.add_argument("--sweep", action="store_true", help="time only the MXFP4-kept and uniform NVFP4 configurations")
+    ap.add_argument("--skip-sweep", action="store_true", help="leave the other configurations out of the line")
+    ap.add_argument("--sweep-steps", type=int, default=10)
+    ap.add_argument("--skip-tiers", action="store_true", help="leave the tier-order timings out of the line")
     args = ap.parse_args()
     if args.profile:
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))

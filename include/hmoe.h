@@ -103,6 +103,10 @@ typedef struct {
 typedef struct hmoe_layer hmoe_layer; /* opaque host handle: tier tables, no device memory */
 
 /* Bytes of the two tier-local packed buffers for this bit map.
+ *   Cites: "quant: nvfp4_nf3_hybrid -- native serving ...", How it works (two
+ *   prepared weight objects per layer, one per tier); "quant: add native
+ *   mixed NVFP4/MXFP4 plus NF3 MoE serving", Summary (compact tier-local
+ *   storage).
  * bit_map: host int8 [E] with 4 or 3 per expert, or NULL for a uniform
  * layer (every expert in kept_format). The two outputs are the sizes of the
  * kept_buf and nf3_buf arguments of hmoe_pack_weights. Either may be 0. */
@@ -110,7 +114,15 @@ hmoe_status hmoe_packed_size(const hmoe_layer_desc* desc, const int8_t* bit_map,
                              size_t* kept_bytes, size_t* nf3_bytes);
 
 /* Workspace bytes for hmoe_plan_routes and hmoe_forward at up to max_tokens
- * tokens per call (the scratch is sized from the largest batch). */
+ * tokens per call.
+ *   Cites: "quant: add native mixed NVFP4/MXFP4 plus NF3 MoE serving",
+ *   Summary (scratch sized from the maximum batched token count).
+ * The workspace holds the status word, the kernels' self-cleaning work
+ * queues, the routing chunk counts, the gathered activation rows (T > 8),
+ * the SwiGLU output h [T*k][I] bf16 and the per-slot W2 output [T*k][H]
+ * fp32. Errors: the desc checks (HMOE_ERR_INVALID_ARG,
+ * HMOE_ERR_UNSUPPORTED_SHAPE); max_tokens < 0 or bytes NULL is
+ * HMOE_ERR_INVALID_ARG. */
 hmoe_status hmoe_workspace_size(const hmoe_layer_desc* desc, int max_tokens, size_t* bytes);
 
 /* The path hmoe_forward takes for T tokens when opts->path is HMOE_PATH_AUTO:
@@ -195,6 +207,15 @@ typedef struct {
 /* The layer: out[t] = sum_j gates[t,j] * W2_e (silu(W1_e x_t) * W3_e x_t) with
  * e = ids[t,j], fp32 accumulation and a bf16 result. Expert weights are
  * dequantised from their tier format as they stream.
+ *   Cites: "quant: nvfp4_nf3_hybrid -- native serving ...", How it works (both
+ *   tiers run off one shared topk_sum; preplanned, CUDA-graph-safe launches;
+ *   an M<=8 decode path); "[Quantization][ModelOpt] W4A16 NVFP4 fused MoE",
+ *   Summary (W4A16: 4-bit weights, bf16 activations, fp32 accumulation).
+ * Errors, all found on the host before anything is enqueued:
+ * HMOE_ERR_INVALID_ARG (NULL layer or buffer, T < 0, x or out not 16-byte
+ * aligned, a bad option, the grouped path forced at T <= 8),
+ * HMOE_ERR_WORKSPACE_TOO_SMALL, and HMOE_ERR_CUDA if a launch fails. Faults
+ * the kernels find are read later with hmoe_check_device_status.
  * x: device bf16 [T][H]. out: device bf16 [T][H], fully overwritten.
  * ids, gates, perm, offsets: exactly as hmoe_plan_routes wrote them for
  * these T tokens.
@@ -226,13 +247,19 @@ hmoe_status hmoe_forward_ex(const hmoe_layer* layer, const void* x, int T, const
  *   stream capture begins.
  * - Size limit: a batch whose scratch would exceed the array returns
  *   HMOE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued. For the
- *   256-expert layer (H=6144, I=2048, top-8) every T <= 8 fits.
+ *   256-expert layer (H=6144, I=2048, top-8) every T <= 51 fits; for the
+ *   128-expert layer (H=2048, I=768, top-8) every T <= 151 fits.
+ * - Checks: every argument check of hmoe_forward runs first; a call that
+ *   returns an error has enqueued nothing.
  * - Sharing: all calls share the one array per device, and it keeps the
- *   last call's contents. Each call first clears, on the stream, the part
- *   that must start at zero. Calls that overlap on the GPU (other streams,
- *   other threads) race on the array. Serialise them.
- * - Arguments and results are as in hmoe_forward. Device faults are read
- *   with hmoe_check_device_status_static. */
+ *   last call's contents. Each call first clears, on the stream, the work
+ *   queues and counters that must start at zero. The device status word is
+ *   not cleared by a call: a fault any earlier call recorded stays until
+ *   hmoe_check_device_status_static reads (and clears) it. Calls that
+ *   overlap on the GPU (other streams, other threads) race on the array.
+ *   Serialise them.
+ * - Arguments and results are as in hmoe_forward with the default options
+ *   (automatic path, one launch per GEMM). */
 #define HMOE_STATIC_SCRATCH_BYTES (16u << 20)
 hmoe_status hmoe_forward_static(const hmoe_layer* layer, const void* x, int T, const int32_t* ids,
                                 const float* gates, const int32_t* perm, const int32_t* offsets, void* out,
@@ -244,16 +271,37 @@ hmoe_status hmoe_check_device_status_static(hmoe_stream_t stream);
 
 /* Synchronise the stream and read the device status word the kernels write
  * into the workspace. Returns HMOE_OK, HMOE_ERR_BAD_ROUTE or
- * HMOE_ERR_DEVICE_TIMEOUT, then clears the word. */
+ * HMOE_ERR_DEVICE_TIMEOUT, then clears the word.
+ *   Cites: "quant: add native mixed NVFP4/MXFP4 plus NF3 MoE serving",
+ *   Summary (the hybrid metadata is validated; here the route geometry the
+ *   kernels read is checked on the device, and bad entries are reported
+ *   instead of trapping).
+ * This is the one call that synchronises; it is not for use inside a stream
+ * capture. HMOE_ERR_CUDA if the copy or the synchronisation fails (for
+ * example after a fault elsewhere in the context). */
 hmoe_status hmoe_check_device_status(void* ws, size_t ws_bytes, hmoe_stream_t stream);
 
-/* Test export. It writes the bf16 operand tile the kernels feed the tensor
- * cores for one expert matrix, in logical row order. which = 13 gives
- * [2I][H]; which = 2 gives [H][I]. dst is device memory. The values are
- * e2m1*e4m3 (NVFP4, without the global scale), e2m1*2^(b-127) (MXFP4), or
- * bf16_rne(cb*s) (NF3). */
+/* Test export of the tensor-core operand. It writes, for one expert matrix
+ * and in logical row order, the bf16 operand tile that the grouped
+ * (tcgen05) kernel writes to shared memory, decoded by the same device
+ * function. which = 13 gives [2I][H]; which = 2 gives [H][I]. dst is device
+ * memory. The values are e2m1*e4m3 (NVFP4, without the global scale),
+ * e2m1*2^(b-127) (MXFP4), or bf16_rne(cb*s) (NF3). The weight-streaming
+ * kernel uses the same values for NVFP4 and MXFP4 but not for NF3: see
+ * hmoe_debug_decode_operand. */
 hmoe_status hmoe_debug_dequant(const hmoe_layer* layer, int expert, int which, void* dst,
                                hmoe_stream_t stream);
+
+/* Test export of the weight-streaming (decode) kernel's operand, decoded by
+ * the same device function that kernel runs. dst: device bf16 [N][K] as in
+ * hmoe_debug_dequant; scales: device fp32 [N][K/64]. The kernel computes each
+ * output row as the sum over 64-wide K groups g of scales[n][g] times the
+ * fp32 sum over the group of dst[n][k] * x[k] (NVFP4 then times its global
+ * scale). NF3: dst is the raw codebook entry cb[code] and scales the group's
+ * bf16 scale; NVFP4 and MXFP4: dst is the tile of hmoe_debug_dequant and
+ * scales are 1. */
+hmoe_status hmoe_debug_decode_operand(const hmoe_layer* layer, int expert, int which, void* dst,
+                                      float* scales, hmoe_stream_t stream);
 
 /* Global scales and tier of one expert, as the handle holds them. */
 hmoe_status hmoe_layer_expert_info(const hmoe_layer* layer, int expert, int* fmt,

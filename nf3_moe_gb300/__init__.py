@@ -24,7 +24,7 @@ from ._lib import (FMT_MXFP4, FMT_NF3, FMT_NVFP4, PATH_AUTO, PATH_GROUPED, PATH_
 __all__ = [
     "LayerDesc", "HmoeError", "hmoe_packed_size", "hmoe_workspace_size", "hmoe_workspace_init",
     "hmoe_pack_weights", "hmoe_plan_routes", "hmoe_forward", "hmoe_check_device_status",
-    "hmoe_debug_dequant", "HybridMoELayer", "library_path",
+    "hmoe_debug_dequant", "hmoe_debug_decode_operand", "HybridMoELayer", "library_path",
 ]
 
 
@@ -143,6 +143,12 @@ def hmoe_check_device_status(ws, stream=None):
 
 def hmoe_debug_dequant(layer, expert, which, dst, stream=None):
     _lib.check(_lib.lib().hmoe_debug_dequant(layer.handle, int(expert), int(which), _ptr(dst), _stream(stream)))
+
+
+def hmoe_debug_decode_operand(layer, expert, which, dst, scales, stream=None):
+    """The weight-streaming kernel's operand (dst bf16 [N, K]) and per-64-group factors (scales fp32 [N, K/64])."""
+    _lib.check(_lib.lib().hmoe_debug_decode_operand(layer.handle, int(expert), int(which), _ptr(dst), _ptr(scales),
+                                                    _stream(stream)))
 
 
 class HybridMoELayer:

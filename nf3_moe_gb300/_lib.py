@@ -28,7 +28,7 @@ EXPORTS = (
     "hmoe_plan_routes", "hmoe_forward", "hmoe_forward_ex", "hmoe_check_device_status",
     "hmoe_debug_dequant", "hmoe_layer_expert_info", "hmoe_layer_destroy", "hmoe_last_error",
     "hmoe_launch_count", "hmoe_version", "hmoe_forward_static", "hmoe_check_device_status_static",
-    "hmoe_auto_path",
+    "hmoe_auto_path", "hmoe_debug_decode_operand",
 )
 
 
@@ -70,6 +70,7 @@ def load(path=LIB_PATH):
         "hmoe_forward_ex": (i, [vp, vp, i, vp, vp, vp, vp, vp, vp, sz, P(ForwardOpts), vp]),
         "hmoe_check_device_status": (i, [vp, sz, vp]),
         "hmoe_debug_dequant": (i, [vp, i, i, vp, vp]),
+        "hmoe_debug_decode_operand": (i, [vp, i, i, vp, vp, vp]),
         "hmoe_layer_expert_info": (i, [vp, i, P(i), P(ctypes.c_float), P(ctypes.c_float)]),
         "hmoe_layer_destroy": (None, [vp]),
         "hmoe_last_error": (ctypes.c_char_p, []),

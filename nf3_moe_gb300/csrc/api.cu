@@ -16,6 +16,8 @@
 #include <new>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/hmoe.h"
 #include "common.cuh"
 #include "internal.h"
@@ -40,6 +42,17 @@ struct hmoe_layer {
 namespace {
 
 thread_local std::string g_err;
+
+// An NVTX range over one library call, so that profilers (ncu --nvtx,
+// Nsight Systems) label the launches it makes. With no tool attached a
+// range costs a few nanoseconds and reads nothing from the environment but
+// the profiler's own injection hook.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 hmoe_status fail(hmoe_status s, const char* fmt, ...) {
   char buf[512];
@@ -204,6 +217,7 @@ hmoe_status hmoe_workspace_init(void* ws, size_t ws_bytes, hmoe_stream_t stream)
 
 hmoe_status hmoe_pack_weights(const hmoe_layer_desc* desc, const int8_t* bit_map, const hmoe_expert_src* src,
                               void* kept_buf, void* nf3_buf, hmoe_stream_t stream, hmoe_layer** out) {
+  const NvtxRange nvtx("hmoe_pack_weights");
   hmoe_status s = check_desc(desc);
   if (s != HMOE_OK) return s;
   if ((s = check_bitmap(desc, bit_map)) != HMOE_OK) return s;
@@ -277,6 +291,7 @@ hmoe_status hmoe_layer_expert_info(const hmoe_layer* L, int expert, int* fmt, fl
 
 hmoe_status hmoe_plan_routes(const hmoe_layer* L, const float* logits, int T, int32_t* ids, float* gates,
                              int32_t* perm, int32_t* offsets, void* ws, size_t ws_bytes, hmoe_stream_t stream) {
+  const NvtxRange nvtx("hmoe_plan_routes");
   if (!L) return fail(HMOE_ERR_INVALID_ARG, "layer is NULL");
   if (T < 0) return fail(HMOE_ERR_INVALID_ARG, "T=%d < 0", T);
   if (!offsets || (T > 0 && (!logits || !ids || !gates || !perm)))
@@ -447,33 +462,56 @@ static hmoe_status run_grouped_path(const hmoe_layer* L, const void* x, int T, c
   return HMOE_OK;
 }
 
-hmoe_status hmoe_forward_ex(const hmoe_layer* L, const void* x, int T, const int32_t* ids, const float* gates,
-                            const int32_t* perm, const int32_t* offsets, void* out, void* ws, size_t ws_bytes,
-                            const hmoe_forward_opts* opts, hmoe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Every host-side check of a forward call except the workspace: run before
+// anything is enqueued, by hmoe_forward_ex and hmoe_forward_static alike.
+// *grouped receives the path the call takes.
+hmoe_status check_forward(const hmoe_layer* L, const void* x, int T, const int32_t* ids, const float* gates,
+                          const int32_t* perm, const int32_t* offsets, const void* out, const hmoe_forward_opts& o,
+                          bool* grouped) {
   if (!L) return fail(HMOE_ERR_INVALID_ARG, "layer is NULL");
   if (T < 0) return fail(HMOE_ERR_INVALID_ARG, "T=%d < 0", T);
-  hmoe_forward_opts o{HMOE_TIERS_ONE_LAUNCH, HMOE_PATH_AUTO, 0, 0, nullptr, 0};
-  if (opts) o = *opts;
-  const int tier_order = o.tier_order, path = o.path;
-  if (tier_order < 0 || tier_order > 2) return fail(HMOE_ERR_INVALID_ARG, "bad tier_order %d", tier_order);
-  if (path < 0 || path > 2) return fail(HMOE_ERR_INVALID_ARG, "bad path %d", path);
+  if (o.tier_order < 0 || o.tier_order > 2) return fail(HMOE_ERR_INVALID_ARG, "bad tier_order %d", o.tier_order);
+  if (o.path < 0 || o.path > 2) return fail(HMOE_ERR_INVALID_ARG, "bad path %d", o.path);
   if (o.wait_limit_us < 0) return fail(HMOE_ERR_INVALID_ARG, "wait_limit_us < 0");
-  WsLayout w{};
-  hmoe_status s = check_ws(L->d, T, ws, ws_bytes, &w);
-  if (s != HMOE_OK) return s;
+  *grouped = o.path == HMOE_PATH_GROUPED || (o.path == HMOE_PATH_AUTO && auto_is_grouped(L->d, T));
   if (T == 0) return HMOE_OK;
   if (!x || !ids || !gates || !perm || !offsets || !out) return fail(HMOE_ERR_INVALID_ARG, "a buffer is NULL");
   if (!aligned16(x) || !aligned16(out)) return fail(HMOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
-  (void)ids;
-  const bool grouped = path == HMOE_PATH_GROUPED || (path == HMOE_PATH_AUTO && auto_is_grouped(L->d, T));
-  if (grouped && T <= DECODE_MAX_T)
+  if (*grouped && T <= DECODE_MAX_T)
     return fail(HMOE_ERR_INVALID_ARG, "the grouped path needs T > %d (the workspace holds no gather buffer below)",
                 DECODE_MAX_T);
-  if (grouped)
-    return run_grouped_path(L, x, T, gates, perm, offsets, out, static_cast<uint8_t*>(ws), w, o,
-                            (cudaStream_t)stream);
-  return run_stream_path(L, x, T, gates, perm, offsets, out, static_cast<uint8_t*>(ws), w, o,
-                         (cudaStream_t)stream);
+  return HMOE_OK;
+}
+
+hmoe_status run_forward(const hmoe_layer* L, const void* x, int T, const float* gates, const int32_t* perm,
+                        const int32_t* offsets, void* out, void* ws, const WsLayout& w, const hmoe_forward_opts& o,
+                        bool grouped, cudaStream_t st) {
+  if (T == 0) return HMOE_OK;
+  if (grouped) return run_grouped_path(L, x, T, gates, perm, offsets, out, static_cast<uint8_t*>(ws), w, o, st);
+  return run_stream_path(L, x, T, gates, perm, offsets, out, static_cast<uint8_t*>(ws), w, o, st);
+}
+
+const hmoe_forward_opts kDefaultOpts{HMOE_TIERS_ONE_LAUNCH, HMOE_PATH_AUTO, 0, 0, nullptr, 0};
+
+}  // namespace
+
+extern "C" {
+
+hmoe_status hmoe_forward_ex(const hmoe_layer* L, const void* x, int T, const int32_t* ids, const float* gates,
+                            const int32_t* perm, const int32_t* offsets, void* out, void* ws, size_t ws_bytes,
+                            const hmoe_forward_opts* opts, hmoe_stream_t stream) {
+  const NvtxRange nvtx("hmoe_forward");
+  const hmoe_forward_opts o = opts ? *opts : kDefaultOpts;
+  bool grouped = false;
+  hmoe_status s = check_forward(L, x, T, ids, gates, perm, offsets, out, o, &grouped);
+  if (s != HMOE_OK) return s;
+  WsLayout w{};
+  if ((s = check_ws(L->d, T, ws, ws_bytes, &w)) != HMOE_OK) return s;
+  return run_forward(L, x, T, gates, perm, offsets, out, ws, w, o, grouped, (cudaStream_t)stream);
 }
 
 hmoe_status hmoe_forward(const hmoe_layer* L, const void* x, int T, const int32_t* ids, const float* gates,
@@ -495,19 +533,33 @@ hmoe_status hmoe_check_device_status(void* ws, size_t ws_bytes, hmoe_stream_t st
   return HMOE_OK;
 }
 
-hmoe_status hmoe_debug_dequant(const hmoe_layer* L, int expert, int which, void* dst, hmoe_stream_t stream) {
-  if (!L || !dst || expert < 0 || expert >= L->d.E || (which != 13 && which != 2))
-    return fail(HMOE_ERR_INVALID_ARG, "bad arguments to hmoe_debug_dequant");
+namespace {
+hmoe_status debug_export(const hmoe_layer* L, int expert, int which, void* dst, float* scales, bool decode_operand,
+                         cudaStream_t st) {
   const bool nf3 = (L->tab.loc[expert] & LOC_NF3) != 0;
   const int fmt = nf3 ? FMT_NF3 : L->d.kept_format;
   const ExpertGeom& g = nf3 ? L->gn : L->gk;
   const uint8_t* base = (nf3 ? L->nf3_buf : L->kept_buf) + (size_t)(L->tab.loc[expert] & 0x7FFF) * g.expert_bytes;
   const int N = which == 13 ? 2 * L->d.I : L->d.H;
   const int K = which == 13 ? L->d.H : L->d.I;
-  cudaError_t e = launch_debug_dequant(fmt, which, base + (which == 2 ? g.w13_bytes : 0), N, K, L->d.I, dst,
-                                       (cudaStream_t)stream);
+  cudaError_t e = launch_debug_dequant(fmt, which, base + (which == 2 ? g.w13_bytes : 0), N, K, L->d.I, dst, scales,
+                                       decode_operand, st);
   if (e != cudaSuccess) return cuda_fail(e, "debug dequant launch");
   return HMOE_OK;
+}
+}  // namespace
+
+hmoe_status hmoe_debug_dequant(const hmoe_layer* L, int expert, int which, void* dst, hmoe_stream_t stream) {
+  if (!L || !dst || expert < 0 || expert >= L->d.E || (which != 13 && which != 2))
+    return fail(HMOE_ERR_INVALID_ARG, "bad arguments to hmoe_debug_dequant");
+  return debug_export(L, expert, which, dst, nullptr, false, (cudaStream_t)stream);
+}
+
+hmoe_status hmoe_debug_decode_operand(const hmoe_layer* L, int expert, int which, void* dst, float* scales,
+                                      hmoe_stream_t stream) {
+  if (!L || !dst || !scales || expert < 0 || expert >= L->d.E || (which != 13 && which != 2))
+    return fail(HMOE_ERR_INVALID_ARG, "bad arguments to hmoe_debug_decode_operand");
+  return debug_export(L, expert, which, dst, scales, true, (cudaStream_t)stream);
 }
 
 }  // extern "C"
@@ -547,21 +599,27 @@ extern "C" {
 
 hmoe_status hmoe_forward_static(const hmoe_layer* L, const void* x, int T, const int32_t* ids, const float* gates,
                                 const int32_t* perm, const int32_t* offsets, void* out, hmoe_stream_t stream) {
-  if (!L) return fail(HMOE_ERR_INVALID_ARG, "layer is NULL");
-  if (T < 0) return fail(HMOE_ERR_INVALID_ARG, "T=%d < 0", T);
+  const NvtxRange nvtx("hmoe_forward_static");
+  // Every argument check runs before anything is enqueued.
+  bool grouped = false;
+  hmoe_status s = check_forward(L, x, T, ids, gates, perm, offsets, out, kDefaultOpts, &grouped);
+  if (s != HMOE_OK) return s;
   const WsLayout w = ws_layout(L->d, T);
   if (w.total > (size_t)HMOE_STATIC_SCRATCH_BYTES)
     return fail(HMOE_ERR_WORKSPACE_TOO_SMALL,
                 "T=%d needs %zu bytes of scratch; the static scratch of hmoe_forward_static holds %u", T, w.total,
                 (unsigned)HMOE_STATIC_SCRATCH_BYTES);
   void* ws = nullptr;
-  hmoe_status s = static_scratch(&ws);
-  if (s != HMOE_OK) return s;
-  // The array keeps the previous call's contents: clear the part that must
-  // start at zero (status word and work queues).
-  cudaError_t e = cudaMemsetAsync(ws, 0, w.chunk_cnt, (cudaStream_t)stream);
+  if ((s = static_scratch(&ws)) != HMOE_OK) return s;
+  if (T == 0) return HMOE_OK;
+  // The array keeps the previous call's contents. The kernels' work queues
+  // and group counters must start at zero: clear them. The status word is
+  // left alone, so a fault an earlier call recorded stays until
+  // hmoe_check_device_status_static reads it.
+  cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + w.queues, 0, w.chunk_cnt - w.queues,
+                                  (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch");
-  return hmoe_forward_ex(L, x, T, ids, gates, perm, offsets, out, ws, HMOE_STATIC_SCRATCH_BYTES, nullptr, stream);
+  return run_forward(L, x, T, gates, perm, offsets, out, ws, w, kDefaultOpts, grouped, (cudaStream_t)stream);
 }
 
 hmoe_status hmoe_check_device_status_static(hmoe_stream_t stream) {

@@ -685,18 +685,20 @@ cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int* perm, int S, i
 }
 
 // ------------------------------------------------------------ host side
-// The driver's tensor-map encoder, looked up once (a function-local static
-// is initialised once even with several host threads).
+// The driver's tensor-map encoder. A successful lookup is cached; a failed
+// one is retried on the next call (the atomic makes the cache safe with
+// several host threads: each may look it up, all store the same pointer).
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
-    cudaDriverEntryPointQueryResult q;
-    void* ptr = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> cached{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 fn = cached.load(std::memory_order_acquire);
+  if (fn) return fn;
+  cudaDriverEntryPointQueryResult q;
+  void* ptr = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !ptr)
     return nullptr;
-  }();
+  fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  cached.store(fn, std::memory_order_release);
   return fn;
 }
 

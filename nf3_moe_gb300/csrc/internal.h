@@ -30,8 +30,10 @@ ExpertGeom expert_geom(int H, int I, int fmt);
 
 cudaError_t launch_pack_matrix(int fmt, int which, const void* codes, const void* scales, int N, int K, int I,
                                uint8_t* dst, cudaStream_t st);
+// Test export of the dequantised operands (pack.cu): the tensor-core tile, or with
+// decode_operand the weight-streaming kernel's operand plus its per-group scales.
 cudaError_t launch_debug_dequant(int fmt, int which, const uint8_t* src, int N, int K, int I, void* dst,
-                                 cudaStream_t st);
+                                 float* scales_out, bool decode_operand, cudaStream_t st);
 
 // ---------------------------------------------------------------- streaming GEMM (any T; the decode path)
 // One matrix of the expert FFN as the streaming kernel sees it.

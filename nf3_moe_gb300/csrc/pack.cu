@@ -163,30 +163,44 @@ cudaError_t launch_pack_matrix(int fmt, int which, const void* codes, const void
 }
 
 // ------------------------------------------------------------ debug export of operand tiles
-template <int FMT>
-__device__ __forceinline__ void debug_tile(const uint8_t* tile, int rg, int lane, uint32_t* r0, uint32_t* r1) {
-  float a, b;
-  dequant_slot<FMT, true>(tile, rg, lane, r0, r1, &a, &b);
-}
-
-__global__ void debug_dequant_kernel(int fmt, int which, const uint8_t* __restrict__ src, int N, int K, int I,
-                                     __nv_bfloat16* __restrict__ dst) {
-  const int KB = K / TILE_K;
-  const int rt = blockIdx.x / KB, kb = blockIdx.x % KB;
-  const int tid = threadIdx.x, rg = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
-  const uint8_t* tile = src + ((size_t)rt * KB + kb) * tile_bytes(fmt);
-  uint32_t r0[8], r1[8];
-  if (fmt == FMT_NVFP4) {
-    debug_tile<FMT_NVFP4>(tile, rg, lane, r0, r1);
-    // The kernels carry NVFP4 tiles times 2^-63; the export is the tile itself.
+// Both exports run dequant_slot, the decoder the GEMM kernels run, with the
+// same shared E4M3 table the kernels build:
+//   tile mode (WITH_NF3_SCALE = true): the bf16 operand tile the tensor-core
+//     grouped kernel writes to shared memory. NVFP4 values are carried times
+//     2^-63 inside the kernels (the factor returns with the global scale), so
+//     the export multiplies 2^63 back, exactly.
+//   decode mode (WITH_NF3_SCALE = false): the operand the weight-streaming
+//     kernel feeds mma.sync. NVFP4 and MXFP4 are the tile values; NF3 values
+//     are the raw codebook entries, and scales_out receives the fp32 factor
+//     the kernel applies to each row's 64-wide group sum (1 for NVFP4/MXFP4).
+template <int FMT, bool WITH_NF3_SCALE>
+__device__ __forceinline__ void debug_slot(const uint8_t* tile, int rg, int lane, const uint32_t* lut, uint32_t* r0,
+                                           uint32_t* r1, float* s0, float* s1) {
+  dequant_slot<FMT, WITH_NF3_SCALE>(tile, rg, lane, r0, r1, s0, s1, lut);
+  if constexpr (FMT == FMT_NVFP4) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       r0[i] = bf16x2_mul(r0[i], BF16X2_2P63);
       r1[i] = bf16x2_mul(r1[i], BF16X2_2P63);
     }
   }
-  else if (fmt == FMT_MXFP4) debug_tile<FMT_MXFP4>(tile, rg, lane, r0, r1);
-  else debug_tile<FMT_NF3>(tile, rg, lane, r0, r1);
+}
+
+template <bool WITH_NF3_SCALE>
+__global__ void debug_dequant_kernel(int fmt, int which, const uint8_t* __restrict__ src, int N, int K, int I,
+                                     __nv_bfloat16* __restrict__ dst, float* __restrict__ scales_out) {
+  __shared__ uint32_t s_e4m3[256];
+  s_e4m3[threadIdx.x] = bf16x2_mul(bf16_bcast(e4m3_to_bf16(threadIdx.x)), BF16X2_2P63);
+  __syncthreads();
+  const int KB = K / TILE_K;
+  const int rt = blockIdx.x / KB, kb = blockIdx.x % KB;
+  const int tid = threadIdx.x, rg = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
+  const uint8_t* tile = src + ((size_t)rt * KB + kb) * tile_bytes(fmt);
+  uint32_t r0[8], r1[8];
+  float s0 = 1.0f, s1 = 1.0f;
+  if (fmt == FMT_NVFP4) debug_slot<FMT_NVFP4, WITH_NF3_SCALE>(tile, rg, lane, s_e4m3, r0, r1, &s0, &s1);
+  else if (fmt == FMT_MXFP4) debug_slot<FMT_MXFP4, WITH_NF3_SCALE>(tile, rg, lane, s_e4m3, r0, r1, &s0, &s1);
+  else debug_slot<FMT_NF3, WITH_NF3_SCALE>(tile, rg, lane, s_e4m3, r0, r1, &s0, &s1);
   const int L0 = logical_row(which, I, rt, rg * 16 + g), L1 = logical_row(which, I, rt, rg * 16 + g + 8);
   const int k0 = kb * TILE_K + 16 * q;
   uint4* d0 = reinterpret_cast<uint4*>(dst + (size_t)L0 * K + k0);
@@ -195,13 +209,22 @@ __global__ void debug_dequant_kernel(int fmt, int which, const uint8_t* __restri
   d0[1] = make_uint4(r0[4], r0[5], r0[6], r0[7]);
   d1[0] = make_uint4(r1[0], r1[1], r1[2], r1[3]);
   d1[1] = make_uint4(r1[4], r1[5], r1[6], r1[7]);
+  if (scales_out && q == 0) {
+    scales_out[(size_t)L0 * KB + kb] = s0;
+    scales_out[(size_t)L1 * KB + kb] = s1;
+  }
 }
 
 cudaError_t launch_debug_dequant(int fmt, int which, const uint8_t* src, int N, int K, int I, void* dst,
-                                 cudaStream_t st) {
+                                 float* scales_out, bool decode_operand, cudaStream_t st) {
   const int tiles = (N / TILE_ROWS) * (K / TILE_K);
   if (tiles == 0) return cudaSuccess;
-  debug_dequant_kernel<<<tiles, 256, 0, st>>>(fmt, which, src, N, K, I, static_cast<__nv_bfloat16*>(dst));
+  if (decode_operand)
+    debug_dequant_kernel<false><<<tiles, 256, 0, st>>>(fmt, which, src, N, K, I, static_cast<__nv_bfloat16*>(dst),
+                                                       scales_out);
+  else
+    debug_dequant_kernel<true><<<tiles, 256, 0, st>>>(fmt, which, src, N, K, I, static_cast<__nv_bfloat16*>(dst),
+                                                      nullptr);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -115,61 +115,24 @@ __device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it,
   }
 }
 
-// One k-block of one thread slot: dequantise (NVFP4/MXFP4 scales from a
-// shared lookup table, NF3 scale applied to the fp32 sum) and 4 MMAs.
+// One k-block of one thread slot: dequantise through dequant_slot<FMT, false>
+// (the decoder hmoe_debug_decode_operand exports; NVFP4/MXFP4 scales applied
+// in bf16 from the shared lookup table, NF3 values raw with the row scales
+// applied to the fp32 sum of the k-block) and 4 MMAs.
 template <int FMT>
 __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xrow, int rg, int lane,
                                           const uint32_t* s_e4m3, float* acc) {
   const uint4 xa = *reinterpret_cast<const uint4*>(xrow);
   const uint4 xb = *reinterpret_cast<const uint4*>(xrow + 16);
   const uint32_t xr[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-  const int slot = rg * 32 + lane;
   uint32_t r0[8], r1[8];
+  float sc0, sc1;
+  dequant_slot<FMT, false>(tile, rg, lane, r0, r1, &sc0, &sc1, s_e4m3);
   if constexpr (FMT == FMT_NVFP4 || FMT == FMT_MXFP4) {
-    const uint4 q = *reinterpret_cast<const uint4*>(tile + slot * 16);
-    uint32_t s0, s1;
-    if constexpr (FMT == FMT_NVFP4) {
-      // Byte loads index a table of bf16 pairs directly: no extract, no broadcast.
-      s0 = s_e4m3[tile[4096 + slot * 2]];
-      s1 = s_e4m3[tile[4096 + slot * 2 + 1]];
-    } else {
-      const int g = lane >> 2, hq = (lane & 3) >> 1;
-      const uint32_t sc = *reinterpret_cast<const uint16_t*>(tile + 4096 + (rg * 16 + g * 2 + hq) * 2);
-      s0 = bf16_bcast(e8m0_to_bf16(sc & 0xFFu));
-      s1 = bf16_bcast(e8m0_to_bf16(sc >> 8));
-    }
-    if constexpr (FMT == FMT_NVFP4) {
-      e2m1s_to_bf16x2(q.x, r0);
-      e2m1s_to_bf16x2(q.y, r0 + 4);
-      e2m1s_to_bf16x2(q.z, r1);
-      e2m1s_to_bf16x2(q.w, r1 + 4);
-    } else {
-      e2m1x8_to_bf16x2(q.x, r0);
-      e2m1x8_to_bf16x2(q.y, r0 + 4);
-      e2m1x8_to_bf16x2(q.z, r1);
-      e2m1x8_to_bf16x2(q.w, r1 + 4);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      r0[i] = bf16x2_mul(r0[i], s0);
-      r1[i] = bf16x2_mul(r1[i], s1);
-    }
 #pragma unroll
     for (int s = 0; s < 4; ++s)
       mma_bf16_16816(acc, r0[2 * s], r1[2 * s], r0[2 * s + 1], r1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
   } else {
-    const uint32_t A = *reinterpret_cast<const uint32_t*>(tile + slot * 4);
-    const uint32_t B = *reinterpret_cast<const uint32_t*>(tile + 1024 + slot * 4);
-    const uint32_t C = *reinterpret_cast<const uint32_t*>(tile + 2048 + slot * 4);
-    const int g = lane >> 2;
-    const float sc0 = bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(tile + 3072 + (rg * 16 + g) * 2));
-    const float sc1 = bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(tile + 3072 + (rg * 16 + g + 8) * 2));
-    uint32_t sel[4];
-    nf3_selectors(A, B, C, sel);
-    nf3x8_to_bf16x2(sel[0], r0);
-    nf3x8_to_bf16x2(sel[1], r0 + 4);
-    nf3x8_to_bf16x2(sel[2], r1);
-    nf3x8_to_bf16x2(sel[3], r1 + 4);
     float d[4];
     mma_bf16_16816_zc(d, r0[0], r1[0], r0[1], r1[1], xr[0], xr[1]);
 #pragma unroll

@@ -6,6 +6,7 @@ import torch
 import nf3_moe_gb300 as hm
 import synth
 from oracle import layer as olayer
+from tests import oracle_pool
 
 # Per token row: max |out - ref| <= REL_TOL * max |ref|, with fp32 accumulation.
 REL_TOL = 2e-2
@@ -40,6 +41,32 @@ def oracle_out(L, x, ids, gates, tokens=None, cols=None):
     xf = x.float().cpu().numpy().astype(np.float64)
     return olayer.moe_forward(xf, ids.cpu().numpy(), gates.cpu().numpy().astype(np.float64), L.expert_numpy,
                               L.H, L.I, tokens=tokens, cols=cols)
+
+
+def oracle_rows(L, x, ids, gates, tokens=None):
+    """oracle_out over all columns, with the per-expert steps spread over host processes
+    (tests/oracle_pool.py): for tests that reach many experts of a full-size layer."""
+    xf = x.float().cpu().numpy().astype(np.float64)
+    return oracle_pool.moe_rows(xf, ids.cpu().numpy(), gates.cpu().numpy().astype(np.float64), L.expert_numpy,
+                                L.H, L.I, tokens=tokens)
+
+
+def cover_tokens(ids, perm, offsets, stride=0):
+    """Tokens that reach every routed expert: for each expert, the token of its first and of
+    its last routed slot (so each expert's first and last, possibly ragged, token tile is
+    checked), plus every stride-th token if stride > 0. Sorted, unique."""
+    ids = ids.cpu().numpy()
+    perm = perm.cpu().numpy()
+    off = offsets.cpu().numpy()
+    k = ids.shape[1]
+    toks = set()
+    for e in range(len(off) - 1):
+        if off[e + 1] > off[e]:
+            toks.add(int(perm[off[e]]) // k)
+            toks.add(int(perm[off[e + 1] - 1]) // k)
+    if stride > 0:
+        toks.update(range(0, ids.shape[0], stride))
+    return sorted(toks)
 
 
 def assert_rows_close(got, ref, tol=REL_TOL):

@@ -1,4 +1,13 @@
-"""The operand tiles the kernels feed the tensor cores are bit-exact with the oracle's dequantised tile."""
+"""The dequantised operands the kernels feed their matrix units are bit-exact with the oracle.
+
+Two exports, each running the decoder its kernel runs (include/hmoe.h):
+- hmoe_debug_dequant: the tensor-core (grouped) kernel's operand tile, equal to
+  oracle.formats.dequant_tile for every format;
+- hmoe_debug_decode_operand: the weight-streaming (decode) kernel's operand and its
+  per-64-group factors. NVFP4 and MXFP4: the same tile, factors 1. NF3: the raw
+  codebook entry of each code (oracle.formats.nf3_codebook indexed by
+  oracle.formats.unpack_nf3) and the group's bf16 scale, exactly.
+"""
 
 import numpy as np
 import pytest
@@ -20,13 +29,27 @@ def _bf16_dev_to_f64(t):
 def _check_expert(moe, L, e):
     ex = L.expert_numpy(e)
     for which, (N, K) in ((13, (2 * L.I, L.H)), (2, (L.H, L.I))):
+        codes, scales, _ = ex["w13" if which == 13 else "w2"]
+        ref = F.dequant_tile(ex["fmt"], codes, scales, K)
         dst = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
         hm.hmoe_debug_dequant(moe.layer, e, which, dst)
         torch.cuda.synchronize()
-        got = _bf16_dev_to_f64(dst)
-        codes, scales, _ = ex["w13" if which == 13 else "w2"]
-        ref = F.dequant_tile(ex["fmt"], codes, scales, K)
-        assert np.array_equal(got, ref), f"expert {e} W{which} fmt {ex['fmt']}"
+        assert np.array_equal(_bf16_dev_to_f64(dst), ref), f"tile: expert {e} W{which} fmt {ex['fmt']}"
+        # the decode kernel's operand
+        vals = torch.full((N, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+        fac = torch.full((N, K // 64), float("nan"), dtype=torch.float32, device="cuda")
+        hm.hmoe_debug_decode_operand(moe.layer, e, which, vals, fac)
+        torch.cuda.synchronize()
+        got_v = _bf16_dev_to_f64(vals)
+        got_f = fac.cpu().numpy().astype(np.float64)
+        if ex["fmt"] == F.FMT_NF3:
+            cb = F.nf3_codebook()
+            assert np.array_equal(got_v, cb[F.unpack_nf3(codes, K)]), f"decode values: expert {e} W{which}"
+            assert np.array_equal(got_f, F.bf16_bits_to_f64(np.asarray(scales, dtype=np.uint16))), \
+                f"decode scales: expert {e} W{which}"
+        else:
+            assert np.array_equal(got_v, ref), f"decode values: expert {e} W{which} fmt {ex['fmt']}"
+            assert np.all(got_f == 1.0)
 
 
 def test_tiny_hybrid_tiles():
@@ -64,6 +87,40 @@ def test_extreme_codes_and_scales():
     moe = U.build(L, 8)
     for e in range(2):
         _check_expert(moe, L, e)
+
+
+def test_mxfp4_extreme_scales_and_subnormals():
+    """MXFP4 with random E8M0 bytes over 0..254 and random codes. Byte 0 is 2^-127, a bf16
+    subnormal, and its products with E2M1 values are bf16 subnormals; they must come out
+    exact. Products beyond the bf16 range are unsupported inputs (the OCP encoder never
+    makes them from finite weights), so codes are clamped where the scale is 2^126 or
+    2^127: magnitude <= 3 (E2M1 <= 3) at byte 253, <= 1.5 at byte 254."""
+    g = torch.Generator(device="cuda").manual_seed(12)
+    H, I, E = 256, 128, 2
+    L = synth.make_layer(H, I, E, 1, kept_ids=[0, 1], kept_format=synth.FMT_MXFP4, device="cuda")
+
+    def rnd(shape, lo, hi):
+        return torch.randint(lo, hi, shape, generator=g, device="cuda", dtype=torch.int32)
+
+    for e in range(E):
+        for key, (N, K) in (("w13", (2 * I, H)), ("w2", (H, I))):
+            sc = rnd((N, K // 32), 0, 255)
+            if e == 1:
+                sc[:, ::2] = rnd((N, K // 64), 0, 4)          # many subnormal scales on expert 1
+            codes = rnd((N, K), 0, 16)
+            mag, sign = codes & 7, codes & 8
+            byte = sc.repeat_interleave(32, dim=1)
+            mag = torch.where(byte == 254, torch.clamp(mag, max=3), mag)
+            mag = torch.where(byte == 253, torch.clamp(mag, max=5), mag)
+            codes = (mag | sign).to(torch.uint8)
+            packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).contiguous()
+            L.experts[e][key] = (packed, sc.to(torch.uint8).contiguous(), 1.0)
+    moe = U.build(L, 8)
+    for e in range(E):
+        _check_expert(moe, L, e)
+    ex = L.expert_numpy(1)
+    tile = F.dequant_tile(F.FMT_MXFP4, ex["w2"][0], ex["w2"][1], I)
+    assert np.any((tile != 0) & (np.abs(tile) < 2.0 ** -126))   # the case really holds subnormals
 
 
 def test_full_size_hybrid_sample_experts():

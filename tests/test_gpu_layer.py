@@ -144,16 +144,14 @@ def hybrid256():
 
 @pytest.mark.parametrize("T", [1, 2, 4, 8])
 def test_full_size_hybrid_decode(hybrid256, T):
-    """256-expert hybrid layer (H=6144, I=2048, top-8; 64 NVFP4 + 192 NF3) at M <= 8.
-    The oracle runs on sampled tokens; every token is checked at M <= 2."""
+    """256-expert hybrid layer (H=6144, I=2048, top-8; 64 NVFP4 + 192 NF3) at M <= 8, in the
+    launch configuration bench.py times. Every token is checked against the oracle (every
+    routed expert of the batch, both tiers)."""
     L, moe = hybrid256
     x = synth.gen_x(T, L.H, seed=100 + T, device="cuda")
     logits = synth.gen_logits(T, L.E, seed=100 + T, device="cuda")
     out, (ids, gates, _, _) = U.run(moe, x, logits)
-    tokens = list(range(T)) if T <= 2 else [0, T - 1]
-    ref = U.oracle_out(L, x, ids, gates, tokens=tokens)
-    U.assert_rows_close(out[tokens].float().cpu().numpy(), ref)
-    # every row: finite, and the tier order does not change a bit
+    U.assert_rows_close(out.float().cpu().numpy(), U.oracle_rows(L, x, ids, gates))
     assert torch.isfinite(out.float()).all()
     out2, _ = U.run(moe, x, logits, tier_order=hm.TIERS_NF3_FIRST)
     assert torch.equal(out, out2)

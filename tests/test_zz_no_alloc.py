@@ -6,10 +6,12 @@ must never reach the allocator or cudaFree's device-wide synchronisation.
 Such callers cannot provide a workspace. hmoe_forward_static runs the same
 layer with its scratch in a fixed device array inside the library.
 
-These tests make two calls in a row, on different batches. Each result must
-agree with the workspace entry point, hmoe_forward, within the per-row
-tolerance the other layer tests use. Batches whose scratch exceeds the
-array are refused before anything runs.
+These tests make two calls in a row, on different batches, and on both
+paths (the weight-streaming kernel at small batches, the tensor-core grouped
+kernel above). Both entry points run the same deterministic kernels, so each
+result must equal the workspace entry point's, hmoe_forward, bit for bit.
+Batches whose scratch exceeds the array, and calls with bad arguments, are
+refused before anything is enqueued.
 """
 
 import ctypes
@@ -49,11 +51,16 @@ def _layer(shape):
     return synth.make_layer(**synth.UNIFORM_128, uniform=True, device="cuda")
 
 
-@pytest.mark.parametrize("shape", ["tiny", "uniform"])
-def test_static_forward_matches_workspace_forward_two_calls(shape):
+# (layer, tokens of the two calls): the tiny layer (E=8, top-2) takes the grouped path at
+# T=64 (128 slots > 8 per expert); the 128-expert layer streams at every T here.
+CASES = [("tiny", (4, 8)), ("tiny", (64, 37)), ("uniform", (4, 8)), ("uniform", (64, 1))]
+
+
+@pytest.mark.parametrize("shape,Ts", CASES)
+def test_static_forward_equals_workspace_forward_two_calls(shape, Ts):
     L = _layer(shape)
-    moe = U.build(L, 8)
-    for call, T in enumerate((4, 8)):
+    moe = U.build(L, max(Ts))
+    for call, T in enumerate(Ts):
         x = synth.gen_x(T, L.H, seed=50 + call, device="cuda")
         logits = synth.gen_logits(T, L.E, seed=50 + call, device="cuda")
         ids, gates, perm, offsets = moe.plan(logits)
@@ -63,7 +70,22 @@ def test_static_forward_matches_workspace_forward_two_calls(shape):
         assert _forward_static(moe, x, ids, gates, perm, offsets, out) == 0, _lib.lib().hmoe_last_error()
         torch.cuda.synchronize()
         assert _lib.lib().hmoe_check_device_status_static(_stream()) == 0, _lib.lib().hmoe_last_error()
-        U.assert_rows_close(out.float().cpu().numpy(), ref.float().cpu().numpy())
+        assert torch.equal(out, ref), f"{shape} T={T}: static and workspace forwards differ"
+
+
+def test_static_forward_refuses_bad_arguments_before_enqueueing():
+    L = _layer("tiny")
+    moe = U.build(L, 8)
+    T = 4
+    x = synth.gen_x(T, L.H, device="cuda")
+    ids, gates, perm, offsets = moe.plan(synth.gen_logits(T, L.E, device="cuda"))
+    out = torch.zeros((T, L.H), dtype=torch.bfloat16, device="cuda")
+    assert _lib.lib().hmoe_forward_static(moe.layer.handle, _ptr(x), T, _ptr(ids), _ptr(gates), _ptr(perm),
+                                          ctypes.c_void_p(0), _ptr(out), _stream()) == -1
+    assert _lib.lib().hmoe_forward_static(moe.layer.handle, ctypes.c_void_p(x.data_ptr() + 2), T, _ptr(ids),
+                                          _ptr(gates), _ptr(perm), _ptr(offsets), _ptr(out), _stream()) == -1
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out) == 0
 
 
 def test_static_forward_refuses_oversized_batch():

@@ -203,6 +203,11 @@ typedef struct {
 } hmoe_forward_opts;
 
 #define HMOE_DEBUG_NO_COPIES 1
+/* Comparison hook: the grouped path runs its CTA-pair tensor-core kernel
+ * (tcgen05.mma.cta_group::2 over two SMs, 256-slot token tiles) instead of
+ * the one-CTA kernel. Same results within the layer tolerance; for
+ * measurements only. */
+#define HMOE_DEBUG_GROUPED_PAIR 2
 
 /* The layer: out[t] = sum_j gates[t,j] * W2_e (silu(W1_e x_t) * W3_e x_t) with
  * e = ids[t,j], fp32 accumulation and a bf16 result. Expert weights are

@@ -19,7 +19,8 @@ import torch
 
 from . import _lib
 from ._lib import (FMT_MXFP4, FMT_NF3, FMT_NVFP4, PATH_AUTO, PATH_GROUPED, PATH_STREAM,  # noqa: F401
-                   TIERS_KEPT_FIRST, TIERS_NF3_FIRST, TIERS_ONE_LAUNCH, HmoeError, LayerDesc)
+                   TIERS_KEPT_FIRST, TIERS_NF3_FIRST, TIERS_ONE_LAUNCH, HmoeError, LayerDesc,
+                   DEBUG_NO_COPIES, DEBUG_GROUPED_PAIR)
 
 __all__ = [
     "LayerDesc", "HmoeError", "hmoe_packed_size", "hmoe_workspace_size", "hmoe_workspace_init",

@@ -21,6 +21,7 @@ FMT_NF3, FMT_NVFP4, FMT_MXFP4 = 3, 4, 5
 TIERS_ONE_LAUNCH, TIERS_KEPT_FIRST, TIERS_NF3_FIRST = 0, 1, 2
 PATH_AUTO, PATH_STREAM, PATH_GROUPED = 0, 1, 2
 DEBUG_NO_COPIES = 1
+DEBUG_GROUPED_PAIR = 2
 
 # Every symbol include/hmoe.h declares.
 EXPORTS = (

@@ -423,6 +423,7 @@ static hmoe_status run_grouped_path(const hmoe_layer* L, const void* x, int T, c
   p.h_out = reinterpret_cast<__nv_bfloat16*>(wsb + w.h);
   p.y_out = reinterpret_cast<float*>(wsb + w.y);
   p.wait_limit_ns = o.wait_limit_us > 0 ? (unsigned long long)o.wait_limit_us * 1000ull : WAIT_LIMIT_NS;
+  p.pair = (o.debug_flags & HMOE_DEBUG_GROUPED_PAIR) ? 1 : 0;
   p.tab = L->tab;
   __nv_bfloat16* xg = reinterpret_cast<__nv_bfloat16*>(wsb + w.xg);
   auto mark = [&](int i) -> cudaError_t {

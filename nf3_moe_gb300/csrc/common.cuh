@@ -300,26 +300,23 @@ __device__ __forceinline__ void nf3_selectors(uint32_t A, uint32_t B, uint32_t C
 // floats for the caller to apply to fp32 sums. Otherwise every format's
 // values come out multiplied by their scale in bf16 (the "tile" values);
 // NVFP4 tile values come out times 2^-63 (see e2m1s_to_bf16x2).
-// e4m3_lut: optional 256-entry table of E4M3 -> bf16 pairs times 2^63 (the
-// value in both halves; shared memory), indexed by the scale bytes directly;
-// NULL converts arithmetically.
+// e4m3_lut: the 256-entry table of E4M3 -> bf16 pairs times 2^63 (the value
+// in both halves; shared memory, built by every kernel that decodes NVFP4
+// with e4m3_lut_entry), indexed by the scale bytes directly.
+__device__ __forceinline__ uint32_t e4m3_lut_entry(uint32_t byte) {
+  return bf16x2_mul(bf16_bcast(e4m3_to_bf16(byte)), BF16X2_2P63);
+}
 template <int FMT, bool WITH_NF3_SCALE>
 __device__ __forceinline__ void dequant_slot(const uint8_t* tile, int rg, int lane, uint32_t* r0, uint32_t* r1,
-                                             float* scale0, float* scale1, const uint32_t* e4m3_lut = nullptr) {
+                                             float* scale0, float* scale1, const uint32_t* e4m3_lut) {
   const int slot = rg * 32 + lane;
   if constexpr (FMT == FMT_NVFP4 || FMT == FMT_MXFP4) {
     const uint4 q = *reinterpret_cast<const uint4*>(tile + slot * 16);
     uint32_t s0, s1;
     if constexpr (FMT == FMT_NVFP4) {
       // Scales carry the factor 2^63 (see e2m1s_to_bf16x2).
-      if (e4m3_lut) {
-        s0 = e4m3_lut[tile[4096 + slot * 2]];
-        s1 = e4m3_lut[tile[4096 + slot * 2 + 1]];
-      } else {
-        const uint32_t sc = *reinterpret_cast<const uint16_t*>(tile + 4096 + slot * 2);
-        s0 = bf16x2_mul(bf16_bcast(e4m3_to_bf16(sc & 0xFFu)), BF16X2_2P63);
-        s1 = bf16x2_mul(bf16_bcast(e4m3_to_bf16(sc >> 8)), BF16X2_2P63);
-      }
+      s0 = e4m3_lut[tile[4096 + slot * 2]];
+      s1 = e4m3_lut[tile[4096 + slot * 2 + 1]];
     } else {
       const int g = lane >> 2, hq = (lane & 3) >> 1;
       const uint32_t sc = *reinterpret_cast<const uint16_t*>(tile + 4096 + (rg * 16 + g * 2 + hq) * 2);

@@ -45,6 +45,7 @@
 // Every mbarrier wait is bounded. On a timeout the CTA records
 // DEV_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
+#include <algorithm>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -86,18 +87,17 @@ static_assert(GT_PSTAGES % GT_DQ_GROUPS == 0, "each dequant group owns its packe
 constexpr int GT_EPI_WARPS = 4;
 constexpr int GT_WARP_PPROD = 0, GT_WARP_MMA = 1, GT_WARP_BPROD = 2, GT_WARP_DQ0 = 3;
 constexpr int GT_WARP_EPI0 = GT_WARP_DQ0 + GT_DQ_WARPS;
-// A second MMA-issuing warp: each issuer drives one row tile's accumulator.
-constexpr int GT_WARP_MMA2 = GT_WARP_EPI0 + GT_EPI_WARPS;
-constexpr int GT_MMA_ISSUERS = GT_R;
-static_assert(GT_MMA_ISSUERS == 2, "issuer r drives row tile r");
-constexpr int GT_THREADS = (GT_WARP_MMA2 + 1) * 32;
-constexpr int GT_TMEM_COLS = 2 * GT_R * GT_N;   // [buffer][row tile] accumulators
+constexpr int GT_THREADS = (GT_WARP_EPI0 + GT_EPI_WARPS) * 32;
+// Accumulator: TMEM lane = token (M = 128), column = weight row of the
+// item's row-tile pair (N = 256), double-buffered.
+constexpr int GT_ACC_COLS = GT_R * 128;
+constexpr int GT_TMEM_COLS = 2 * GT_ACC_COLS;
 // Shared memory map (offsets from the 1024-aligned base).
 constexpr int GT_OFF_A = 0;
 constexpr int GT_OFF_B = GT_OFF_A + GT_OSTAGES * GT_A_BYTES;
 constexpr int GT_OFF_P = GT_OFF_B + GT_OSTAGES * GT_B_BYTES;
 constexpr int GT_OFF_BAR = GT_OFF_P + GT_PSTAGES * GT_P_BYTES;
-constexpr int GT_NBAR = 2 * GT_PSTAGES + 3 * GT_OSTAGES + 4 + GT_MMA_ISSUERS;
+constexpr int GT_NBAR = 2 * GT_PSTAGES + 3 * GT_OSTAGES + 4 + 1;
 constexpr int GT_OFF_MISC = GT_OFF_BAR + ((GT_NBAR * 8 + 16 + 127) / 128) * 128;
 constexpr int GT_SMEM_BYTES = 1024 + GT_OFF_MISC + 2 * (MAX_E + 1) * 4 + 256 * 4;
 static_assert(GT_SMEM_BYTES <= 232448, "shared memory budget");
@@ -115,27 +115,29 @@ __device__ __forceinline__ void tmem_relinquish() {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
+// tcgen05.mma (kind::f16, A and B from shared memory, D in TMEM) and its
+// commit, issued from a converged warp: every lane executes
+// the instruction, and elect.sync predicates it to one lane (the lowest
+// active one, so MMAs and their commits come from the same thread). Measured
+// against issuing from inside an `if (lane == 0)` branch: a 128 x 128 x 16
+// MMA takes 65 instead of 120 cycles of the tensor core's issue slot, the
+// full rate of the tensor core, instead of half of it.
+__device__ __forceinline__ void umma_bf16_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// The same MMA with the accumulate flag known to be set (k-steps after the first).
-__device__ __forceinline__ void umma_bf16_acc(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
+__device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.eq.u32 p, 1, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc)
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
       : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -310,8 +312,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
   uint64_t* oempty = afull + GT_OSTAGES;               // MMAs that read the slot completed
   uint64_t* acc_full = oempty + GT_OSTAGES;            // [2] accumulator ready for the epilogue
   uint64_t* acc_empty = acc_full + 2;                  // [2] epilogue drained it
-  uint64_t* mma_done = acc_empty + 2;                  // [issuer] final drain before TMEM release
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mma_done + GT_MMA_ISSUERS);
+  uint64_t* mma_done = acc_empty + 2;                  // final drain before TMEM release
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* s_flags = reinterpret_cast<volatile int*>(s_tmem + 1);  // [0] abort
   int* s_istart = reinterpret_cast<int*>(smem + GT_OFF_MISC);
   int* s_off = s_istart + MAX_E + 1;
@@ -326,13 +328,13 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     for (int s = 0; s < GT_OSTAGES; ++s) {
       mbar_init(&bfull[s], 1);
       mbar_init(&afull[s], GT_DQ_PER_GROUP);
-      mbar_init(&oempty[s], GT_MMA_ISSUERS);
+      mbar_init(&oempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], GT_MMA_ISSUERS);
+      mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], GT_EPI_WARPS);
     }
-    for (int r = 0; r < GT_MMA_ISSUERS; ++r) mbar_init(&mma_done[r], 1);
+    mbar_init(mma_done, 1);
     fence_mbar_init();
     s_flags[0] = 0;
   }
@@ -341,7 +343,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     tmem_relinquish();
   }
   if (tid >= 96 && tid < 96 + 256)
-    s_e4m3[tid - 96] = bf16x2_mul(bf16_bcast(e4m3_to_bf16((uint32_t)(tid - 96))), BF16X2_2P63);
+    s_e4m3[tid - 96] = e4m3_lut_entry((uint32_t)(tid - 96));
   pdl_wait();  // everything below reads or writes global memory
   pdl_trigger();
   for (int e = tid; e <= p.E; e += blockDim.x) s_off[e] = p.offsets[e];
@@ -468,65 +470,61 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         }
       }
     }
-  } else if (warp == GT_WARP_MMA || warp == GT_WARP_MMA2) {
-    // ------------------------------------------------ MMA issuers
-    // Issuing one tcgen05.mma costs the issuing thread about 100 cycles, so
-    // two threads in different warps (and SM sub-partitions) issue: issuer r
-    // drives row tile r's accumulator. Both wait for the same operand stages
-    // and both commit to the barriers that free them (two arrivals each).
-    const int my_r = warp == GT_WARP_MMA ? 0 : 1;
-    if (lane == 0) {
-      const uint32_t a_lo0 = smem_desc_sw128_lo(smem_u32(smem + GT_OFF_A));
-      const uint32_t b_lo0 = smem_desc_sw128_lo(smem_u32(smem + GT_OFF_B));
-      int os = 0;
-      uint32_t oph = 0;
-      bool aborted = false;
-      int j = 0;
-      for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x, ++j) {
-        const GtItem it = gt_decode(p, s_istart, s_off, i);
-        const int buf = j & 1;
-        if (!mbar_wait(&acc_empty[buf], ((uint32_t)(j >> 1) & 1u) ^ 1u, s_flags, lim)) {
+  } else if (warp == GT_WARP_MMA) {
+    // ------------------------------------------------ MMA issuer
+    // One tcgen05.mma occupies the tensor core for about 125 cycles whatever
+    // its N up to 256 (measured), so the item's token tile is the M side
+    // (M = 128) and its two weight row tiles the N side (N = 256): per
+    // k-block 4 MMAs of 128 x 256 x 16, at the tensor core's full rate,
+    // instead of 8 of 128 x tokens x 16. The whole warp runs the loop and
+    // issues each MMA and commit from converged code (elect.sync).
+    const uint32_t x_lo0 = smem_desc_sw128_lo(smem_u32(smem + GT_OFF_B));  // activation tile: A
+    const uint32_t w_lo0 = smem_desc_sw128_lo(smem_u32(smem + GT_OFF_A));  // weight tiles: B
+    int os = 0;
+    uint32_t oph = 0;
+    bool aborted = false;
+    int j = 0;
+    for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x, ++j) {
+      const GtItem it = gt_decode(p, s_istart, s_off, i);
+      const int buf = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_empty[buf], ((uint32_t)(j >> 1) & 1u) ^ 1u, s_flags, lim))) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16(128, it.nr * 128);
+      const uint32_t d_tmem = tmem_base + (uint32_t)(buf * GT_ACC_COLS);
+      for (int kb = 0; kb < p.KB; ++kb) {
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&afull[os], oph, s_flags, lim) && mbar_wait(&bfull[os], oph, s_flags, lim))) {
           aborted = true;
           break;
         }
         tc_fence_after();
-        const int npad = max(16, (it.n + 15) & ~15);
-        const uint32_t idesc = idesc_bf16(128, npad);
-        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * GT_R * GT_N);
-        for (int kb = 0; kb < p.KB; ++kb) {
-          if (!mbar_wait(&afull[os], oph, s_flags, lim) || !mbar_wait(&bfull[os], oph, s_flags, lim)) {
-            aborted = true;
-            break;
-          }
-          tc_fence_after();
-          // Descriptor low words of this stage's A and B tiles (k-step 0).
-          const uint32_t a_lo = a_lo0 + (uint32_t)os * (GT_A_BYTES >> 4);
-          const uint32_t b_lo = b_lo0 + (uint32_t)os * (GT_B_BYTES >> 4);
-          if (my_r < it.nr) {
-            const uint32_t ar = a_lo + (uint32_t)my_r * (GT_A_TILE >> 4);
-            const uint32_t dr = d_tmem + (uint32_t)(my_r * GT_N);
-            umma_bf16(dr, desc_from_lo(ar), desc_from_lo(b_lo), idesc, kb ? 1u : 0u);
-            umma_bf16_acc(dr, desc_from_lo(ar + 2), desc_from_lo(b_lo + 2), idesc);
-            umma_bf16_acc(dr, desc_from_lo(ar + 4), desc_from_lo(b_lo + 4), idesc);
-            umma_bf16_acc(dr, desc_from_lo(ar + 6), desc_from_lo(b_lo + 6), idesc);
-          }
-          umma_commit(&oempty[os]);
-          if (++os == GT_OSTAGES) {
-            os = 0;
-            oph ^= 1u;
-          }
+        const uint32_t x_lo = x_lo0 + (uint32_t)os * (GT_B_BYTES >> 4);
+        const uint32_t w_lo = w_lo0 + (uint32_t)os * (GT_A_BYTES >> 4);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16_warp(d_tmem, desc_from_lo(x_lo + 2 * ks), desc_from_lo(w_lo + 2 * ks), idesc, (kb | ks) ? 1u : 0u);
+        umma_commit_warp(&oempty[os]);
+        if (++os == GT_OSTAGES) {
+          os = 0;
+          oph ^= 1u;
         }
-        if (!aborted) umma_commit(&acc_full[buf]);
       }
-      if (aborted) {
-        s_flags[0] = 1;
-        set_status(p.status, DEV_TIMEOUT);
-      }
-      // Drain every MMA this thread issued before TMEM can be released.
-      umma_commit(&mma_done[my_r]);
-      volatile int never = 0;
-      mbar_wait(&mma_done[my_r], 0, &never, lim);
+      if (!aborted) umma_commit_warp(&acc_full[buf]);
     }
+    if (aborted && lane == 0) {
+      s_flags[0] = 1;
+      set_status(p.status, DEV_TIMEOUT);
+    }
+    // Drain every MMA issued above before TMEM can be released.
+    umma_commit_warp(mma_done);
+    {
+      volatile int never = 0;
+      mbar_wait(mma_done, 0, &never, lim);
+    }
+    __syncwarp();
   } else if (warp < GT_WARP_EPI0) {
     // ------------------------------------------------ dequantisers: packed tile -> bf16 operand tile
     // Group par expands the k-blocks k with k % GT_DQ_GROUPS == par, every
@@ -559,8 +557,12 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     }
   } else {
     // ------------------------------------------------ epilogue
+    // TMEM lane = token column c of the item (each warp owns 32 lanes), TMEM
+    // column = weight row of the row-tile pair. A thread reads 32 columns at
+    // a time (32x32b.x32): two 16-row groups, i.e. W13 gate rows 0..7 and up
+    // rows 8..15 of 8 channels each, or 32 consecutive W2 output rows.
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;  // tile row = TMEM lane
+    const int c = quarter * 32 + lane;
     const int S = p.T * p.topk;
     int j = 0;
     for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++j) {
@@ -574,68 +576,48 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         break;
       }
       tc_fence_after();
-      // W2: the flat slot of each of the item's token columns (column
-      // 32u + lane in item_slot[u]); -1 past the item or for a bad entry.
-      int item_slot[GT_N / 32];
-#pragma unroll
-      for (int u = 0; u < GT_N / 32; ++u) {
-        item_slot[u] = -1;
-        if (p.which != 13 && 32 * u + lane < it.n) {
-          const int sc = p.perm[it.p0 + 32 * u + lane];
-          if (sc >= 0 && sc < S) item_slot[u] = sc;
-          else set_status(p.status, DEV_BAD_ROUTE);
-        }
+      const bool live = c < it.n;
+      int slot = -1;
+      if (p.which != 13 && live) {
+        const int sc = p.perm[it.p0 + c];
+        if (sc >= 0 && sc < S) slot = sc;
+        else set_status(p.status, DEV_BAD_ROUTE);
       }
-      for (int r = 0; r < it.nr; ++r) {
-        const int rt = it.rt + r;
-        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((buf * GT_R + r) * GT_N);
+      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * GT_ACC_COLS);
+      const int nchunk = it.nr * 4;
+      for (int q = 0; q < nchunk; ++q) {
+        uint32_t v[32];
+        tmem_ld32(tbase + (uint32_t)(32 * q), v);
+        tmem_wait_ld();
+        const int rt = it.rt + (q >> 2);
+        const int r0 = (q & 3) * 32;  // first tile-local row of the chunk
         if (p.which == 13) {
-          // A 16-row group holds 8 gate rows then the 8 up rows of the same
-          // channels, so the 16x256b load gives each thread gate and up of
-          // one channel (row 16j + lane/4) for 8 token columns: SwiGLU in
-          // registers, every lane busy. The quarter holds groups 2q, 2q + 1.
+          if (!live) continue;
           const float gsc = p.tab.g13[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
-          const int g = lane >> 2, qq = lane & 3;
-          for (int h = 0; h < 2; ++h) {
-            const int grp16 = 2 * quarter + h;
-            const int ch = rt * 64 + grp16 * 8 + g;
-            const uint32_t ta = tmem_base + ((uint32_t)(quarter * 32 + 16 * h) << 16) +
-                                (uint32_t)((buf * GT_R + r) * GT_N);
-            for (int c0 = 0; c0 < it.n; c0 += 32) {
-              uint32_t v[16];
-              tmem_ld16x256x4(ta + (uint32_t)c0, v);
-              tmem_wait_ld();
 #pragma unroll
-              for (int rep = 0; rep < 4; ++rep) {
+          for (int g = 0; g < 2; ++g) {
+            // 16-row group (r0 / 16 + g): rows 0..7 gate, 8..15 up, of channels ch .. ch + 7
+            const int ch = rt * 64 + (r0 / 16 + g) * 8;
+            uint32_t hv[4];
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                  const int col = c0 + 8 * rep + 2 * qq + b;
-                  const float gate = __uint_as_float(v[4 * rep + b]) * gsc;
-                  const float up = __uint_as_float(v[4 * rep + 2 + b]) * gsc;
-                  if (col < it.n)
-                    p.h_out[(size_t)(it.p0 + col) * p.I + ch] = __float2bfloat16_rn(silu_fast(gate) * up);
-                }
-              }
+            for (int w = 0; w < 4; ++w) {
+              const float g0 = __uint_as_float(v[16 * g + 2 * w]) * gsc;
+              const float g1 = __uint_as_float(v[16 * g + 2 * w + 1]) * gsc;
+              const float u0 = __uint_as_float(v[16 * g + 8 + 2 * w]) * gsc;
+              const float u1 = __uint_as_float(v[16 * g + 8 + 2 * w + 1]) * gsc;
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(silu_fast(g0) * u0, silu_fast(g1) * u1);
+              hv[w] = *reinterpret_cast<const uint32_t*>(&h2);
             }
+            *reinterpret_cast<uint4*>(p.h_out + (size_t)(it.p0 + c) * p.I + ch) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
           }
         } else {
-          // W2: lanes are output rows, so each column's store is one
-          // coalesced row segment of slot s = perm[p0 + column].
+          if (slot < 0) continue;
           const float gsc = p.tab.g2[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
-          const int orow = rt * 128 + row;
+          float4* dst = reinterpret_cast<float4*>(p.y_out + (size_t)slot * p.H + rt * 128 + r0);
 #pragma unroll
-          for (int u = 0; u < GT_N / 32; ++u) {
-            if (32 * u >= it.n) break;
-            uint32_t v[32];
-            tmem_ld32(taddr + (uint32_t)(32 * u), v);
-            tmem_wait_ld();
-            const int my_s = item_slot[u];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const int sc = __shfl_sync(0xffffffffu, my_s, c);
-              if (sc >= 0) p.y_out[(size_t)sc * p.H + orow] = __uint_as_float(v[c]) * gsc;
-            }
-          }
+          for (int w = 0; w < 8; ++w)
+            dst[w] = make_float4(__uint_as_float(v[4 * w]) * gsc, __uint_as_float(v[4 * w + 1]) * gsc,
+                                 __uint_as_float(v[4 * w + 2]) * gsc, __uint_as_float(v[4 * w + 3]) * gsc);
         }
       }
       tc_fence_before();
@@ -648,6 +630,551 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
   if (warp == GT_WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem_base, GT_TMEM_COLS);
+  }
+}
+
+// ============================================================ the CTA-pair kernel
+// Two CTAs of a cluster (one per SM of a pair) run each work item together
+// with tcgen05.mma.cta_group::2 (M = 256): the leader (cluster rank 0)
+// dequantises row tile 2rp of the item's row pair and the peer row tile
+// 2rp + 1; each CTA loads half of the item's token columns (B) into its own
+// shared memory; one thread in the leader issues the MMAs for both SMs, and
+// each CTA's TMEM receives its own 128 rows x N accumulator. Against the
+// one-CTA kernel this halves, per SM and per k-block, the dequantised rows
+// written to and read from shared memory for the same tensor work, and
+// lets a token tile hold up to 256 slots.
+//
+// Warp roles, in both CTAs:
+//   warp 0       packed-weight producer: 1D bulk copy of its row tile's
+//                packed k-block into a 4-deep ring.
+//   warp 1       TMEM allocation (collective over the pair); in the leader,
+//                the MMA issuer.
+//   warp 2       activation producer: 2D TMA loads (64-row boxes, 128B
+//                swizzle) of its half of the token columns into its own
+//                shared memory, completing on the leader's barrier.
+//   warps 3..18  dequantisers (two groups of 8 taking alternate k-blocks;
+//                warp w of a group expands 16-row group w of the row tile).
+//   warps 19..22 epilogue (tcgen05.ld of the CTA's own accumulator).
+// Hand-offs to the issuer go straight to the leader's barriers: the
+// operand-slot barrier counts the dequant warps of both CTAs and the TMA
+// bytes of both halves, and the accumulator-free barrier counts the
+// epilogue warps of both CTAs. The leader's tcgen05.commit arrives on the
+// same barrier in both CTAs (multicast), which frees the operand slot and
+// hands over accumulators.
+// Every wait is bounded; on a timeout the CTA records DEV_TIMEOUT, tells
+// the other CTA to stop, and both drain before leaving through a final
+// cluster barrier.
+constexpr int G2_N = 256;                 // token tile of an item (both CTAs)
+constexpr int G2_BH = G2_N / 2;           // B rows held by one CTA
+constexpr int G2_BBOX = 64;               // rows per TMA box
+constexpr int G2_A_BYTES = 128 * 128;     // one row tile's bf16 k-block (128 x 64)
+constexpr int G2_B_BYTES = G2_BH * 128;   // bf16 128 x 64
+constexpr int G2_P_TILE = 4608;
+constexpr int G2_PSTAGES = 4;
+constexpr int G2_OSTAGES = 4;
+constexpr int G2_DQ_GROUPS = 2;
+constexpr int G2_DQ_PER_GROUP = 8;        // one warp per 16-row group of the row tile
+constexpr int G2_DQ_WARPS = G2_DQ_GROUPS * G2_DQ_PER_GROUP;
+static_assert(G2_DQ_GROUPS <= 2, "parity-tracked waits need at most two dequant groups");
+static_assert(G2_PSTAGES % G2_DQ_GROUPS == 0 && G2_OSTAGES % G2_DQ_GROUPS == 0,
+              "each dequant group owns its ring slots");
+constexpr int G2_EPI_WARPS = 4;
+constexpr int G2_WARP_PPROD = 0, G2_WARP_MMA = 1, G2_WARP_BPROD = 2, G2_WARP_DQ0 = 3;
+constexpr int G2_WARP_EPI0 = G2_WARP_DQ0 + G2_DQ_WARPS;
+constexpr int G2_THREADS = (G2_WARP_EPI0 + G2_EPI_WARPS) * 32;
+constexpr int G2_TMEM_COLS = 2 * G2_N;    // double-buffered 128 x 256 fp32 accumulators
+constexpr int G2_OFF_A = 0;
+constexpr int G2_OFF_B = G2_OFF_A + G2_OSTAGES * G2_A_BYTES;
+constexpr int G2_OFF_P = G2_OFF_B + G2_OSTAGES * G2_B_BYTES;
+constexpr int G2_OFF_BAR = G2_OFF_P + G2_PSTAGES * G2_P_TILE;
+constexpr int G2_NBAR = 2 * G2_PSTAGES + 3 * G2_OSTAGES + 2 * 2 + 1;
+constexpr int G2_OFF_MISC = G2_OFF_BAR + ((G2_NBAR * 8 + 16 + 127) / 128) * 128;
+constexpr int G2_SMEM_BYTES = 1024 + G2_OFF_MISC + 2 * (MAX_E + 1) * 4 + 256 * 4;
+static_assert(G2_SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(G2_OFF_B % 1024 == 0 && G2_OFF_P % 16 == 0 && G2_B_BYTES % 1024 == 0, "alignment");
+static_assert(G2_TMEM_COLS <= 512, "TMEM columns");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory object in the CTA of the given cluster rank.
+__device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+// Arrive on a barrier in the other CTA of the pair (default release
+// semantics, as for a local arrive). What it publishes is read by the tensor
+// cores through the async proxy, after the usual proxy fence by the writers.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void st_remote_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// try_wait without a suspend-time hint: for the pair's latency-critical
+// hand-offs (barriers completed from the other SM of the pair, and the
+// issuer's waits).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  uint64_t limit_ns) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+__device__ __forceinline__ void tmem_alloc2(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Commit of the pair's MMAs: arrives once on the barrier at this offset in
+// both CTAs of the pair. Both are issued from a converged warp (elect.sync),
+// like umma_bf16_warp.
+__device__ __forceinline__ void umma2_commit_both(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
+          smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void umma2_bf16_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 2D TMA load into this CTA's shared memory whose completion (bytes) is
+// counted on a barrier of the pair given by its shared::cluster address.
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(cluster_bar)
+      : "memory");
+}
+
+struct G2Item {
+  int e, p0, n, rt, valid;  // rt: this CTA's row tile; valid = 0 for the peer of an odd last pair
+};
+
+__device__ __forceinline__ G2Item g2_decode(const GroupedParams& p, const int* s_istart, const int* s_off, int i,
+                                            int rank) {
+  int lo = 0, hi = p.E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_istart[mid] <= i) lo = mid; else hi = mid;
+  }
+  G2Item it;
+  it.e = lo;
+  const int o0 = s_off[lo], ne = s_off[lo + 1] - o0;
+  const int RP = (p.RT + 1) / 2;
+  const int local = i - s_istart[lo];
+  const int rt = (local % RP) * 2 + rank;
+  it.valid = rt < p.RT;
+  it.rt = it.valid ? rt : p.RT - 1;  // a real tile keeps the pipeline uniform; its result is dropped
+  const int nt = local / RP;
+  it.p0 = o0 + nt * G2_N;
+  it.n = min(G2_N, ne - nt * G2_N);
+  return it;
+}
+// MMA width of an item: the token count rounded up to 32 (so each CTA's half
+// is a whole number of 16-row groups).
+__device__ __forceinline__ int g2_width(int n) { return max(32, (n + 31) & ~31); }
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G2_THREADS, 1)
+    grouped_pair_kernel(const __grid_constant__ GroupedParams p, const __grid_constant__ CUtensorMap tmap_b) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G2_OFF_BAR);
+  uint64_t* pfull = bars;                          // packed tile landed (tx)
+  uint64_t* pempty = pfull + G2_PSTAGES;           // dequant warps done reading it
+  uint64_t* bfull = pempty + G2_PSTAGES;           // leader: both B halves landed (tx of both CTAs)
+  uint64_t* afull = bfull + G2_OSTAGES;            // leader: the dequant warps of both CTAs wrote A
+  uint64_t* oempty = afull + G2_OSTAGES;           // the pair's MMAs on the slot completed (leader commit)
+  uint64_t* acc_full = oempty + G2_OSTAGES;        // [2] accumulator complete (leader commit)
+  uint64_t* acc_empty = acc_full + 2;              // [2] leader: the epilogues of both CTAs drained it
+  uint64_t* mma_done = acc_empty + 2;              // final drain (leader commit)
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* s_flags = reinterpret_cast<volatile int*>(s_tmem + 1);  // [0] abort
+  int* s_istart = reinterpret_cast<int*>(smem + G2_OFF_MISC);
+  int* s_off = s_istart + MAX_E + 1;
+  uint32_t* s_e4m3 = reinterpret_cast<uint32_t*>(s_off + MAX_E + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const uint32_t peer_flags = mapa_shared(const_cast<int*>(s_flags), rank ^ 1u);
+  auto abort_pair = [&]() {
+    s_flags[0] = 1;
+    st_remote_u32(peer_flags, 1u);
+    set_status(p.status, DEV_TIMEOUT);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < G2_PSTAGES; ++s) {
+      mbar_init(&pfull[s], 1);
+      mbar_init(&pempty[s], G2_DQ_PER_GROUP);
+    }
+    for (int s = 0; s < G2_OSTAGES; ++s) {
+      mbar_init(&bfull[s], 1);
+      mbar_init(&afull[s], 2 * G2_DQ_PER_GROUP);
+      mbar_init(&oempty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 2 * G2_EPI_WARPS);
+    }
+    mbar_init(mma_done, 1);
+    s_flags[0] = 0;
+    fence_mbar_init();
+  }
+  if (warp == G2_WARP_MMA) {
+    tmem_alloc2(s_tmem, G2_TMEM_COLS);
+    tmem_relinquish2();
+  }
+  if (tid >= 96 && tid < 96 + 256)
+    s_e4m3[tid - 96] = e4m3_lut_entry((uint32_t)(tid - 96));
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated, before any remote access
+  tc_fence_after();
+  pdl_wait();      // everything below reads or writes global memory
+  pdl_trigger();
+  for (int e = tid; e <= p.E; e += blockDim.x) s_off[e] = p.offsets[e];
+  __syncthreads();
+  if (warp == 0) {
+    const int S = p.T * p.topk;
+    bool bad = (s_off[0] != 0) || (s_off[p.E] != S);
+    int run = 0;
+    const int RP = (p.RT + 1) / 2;
+    for (int e0 = 0; e0 < p.E; e0 += 32) {
+      const int e = e0 + lane;
+      int ni = 0;
+      if (e < p.E) {
+        const int ne = s_off[e + 1] - s_off[e];
+        if (ne < 0) bad = true;
+        const bool nf3 = (p.tab.loc[e] & LOC_NF3) != 0;
+        const bool sel = nf3 ? (p.tier_mask & 2) : (p.tier_mask & 1);
+        ni = (sel && ne > 0) ? ((ne + G2_N - 1) / G2_N) * RP : 0;
+      }
+      int incl = ni;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int nb = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += nb;
+      }
+      if (e < p.E) s_istart[e] = run + incl - ni;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      s_istart[p.E] = bad ? 0 : run;
+      if (bad && blockIdx.x == 0) set_status(p.status, DEV_BAD_ROUTE);
+    }
+    if (bad)
+      for (int e = lane; e < p.E; e += 32) s_istart[e] = 0;
+  }
+  __syncthreads();
+  const uint32_t tmem_base = *s_tmem;
+  const int n_items = s_istart[p.E];
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+  const uint64_t lim = p.wait_limit_ns;
+
+  if (warp == G2_WARP_PPROD) {
+    // ------------------------------------------------ packed weight tile of this CTA's row tile
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      int slot = 0, issued = 0;
+      uint32_t ph = 0;
+      bool aborted = false;
+      for (int i = pair; i < n_items && !aborted; i += n_pairs) {
+        const G2Item it = g2_decode(p, s_istart, s_off, i, (int)rank);
+        const int fmt = gt_expert_fmt(p, it.e);
+        const uint32_t tb = (uint32_t)tile_bytes(fmt);
+        const uint8_t* base = (fmt == FMT_NF3 ? p.nf3_buf : p.kept_buf) +
+                              (size_t)(p.tab.loc[it.e] & 0x7FFF) *
+                                  (fmt == FMT_NF3 ? p.nf3_expert_bytes : p.kept_expert_bytes) +
+                              (p.which == 2 ? (fmt == FMT_NF3 ? p.nf3_w2_off : p.kept_w2_off) : 0) +
+                              (size_t)it.rt * p.KB * tb;
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!mbar_wait(&pempty[slot], ph ^ 1u, s_flags, lim)) {
+            aborted = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&pfull[slot], tb);
+          bulk_g2s_stream(smem + G2_OFF_P + slot * G2_P_TILE, base + (size_t)kb * tb, tb, &pfull[slot], pol);
+          ++issued;
+          if (++slot == G2_PSTAGES) {
+            slot = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (aborted) {
+        abort_pair();
+        volatile int never = 0;
+        for (int b = 0; b < G2_PSTAGES && b < issued; ++b) {
+          if (--slot < 0) {
+            slot = G2_PSTAGES - 1;
+            ph ^= 1u;
+          }
+          mbar_wait(&pfull[slot], ph, &never, lim);
+        }
+      }
+    }
+  } else if (warp == G2_WARP_BPROD) {
+    // ------------------------------------------------ this CTA's half of the token columns
+    if (lane == 0) {
+      int slot = 0, issued = 0;
+      uint32_t ph = 0;
+      bool aborted = false;
+      for (int i = pair; i < n_items && !aborted; i += n_pairs) {
+        const G2Item it = g2_decode(p, s_istart, s_off, i, (int)rank);
+        const int half = g2_width(it.n) / 2;
+        const int row0 = it.p0 + (int)rank * half;
+        const int nbox = (half + G2_BBOX - 1) / G2_BBOX;
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!mbar_wait_cluster(&oempty[slot], ph ^ 1u, s_flags, lim)) {
+            aborted = true;
+            break;
+          }
+          // The leader's barrier expects the bytes of both halves; each CTA's
+          // loads land in its own shared memory and complete there.
+          if (leader) mbar_arrive_expect_tx(&bfull[slot], (uint32_t)(2 * nbox * G2_BBOX * 128));
+          const uint32_t bar = mapa_shared(&bfull[slot], 0);
+          for (int b = 0; b < nbox; ++b)
+            tma_load_2d_pair(smem + G2_OFF_B + slot * G2_B_BYTES + b * G2_BBOX * 128, &tmap_b, kb * TILE_K,
+                             row0 + b * G2_BBOX, bar);
+          if (kb + GT_BPREFETCH < p.KB)
+            for (int b = 0; b < nbox; ++b)
+              tma_prefetch_2d(&tmap_b, (kb + GT_BPREFETCH) * TILE_K, row0 + b * G2_BBOX);
+          ++issued;
+          if (++slot == G2_OSTAGES) {
+            slot = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (aborted) {
+        // Loads in flight complete on the leader's barriers; the final
+        // cluster barrier keeps both CTAs (and their shared memory) alive
+        // until the leader has drained its waits.
+        abort_pair();
+        if (leader) {
+          volatile int never = 0;
+          for (int b = 0; b < G2_OSTAGES && b < issued; ++b) {
+            if (--slot < 0) {
+              slot = G2_OSTAGES - 1;
+              ph ^= 1u;
+            }
+            mbar_wait(&bfull[slot], ph, &never, lim);
+          }
+        }
+      }
+    }
+  } else if (warp == G2_WARP_MMA) {
+    if (leader) {
+      // ------------------------------------------------ MMA issuer for the pair
+      // The whole warp runs the loop, so that the MMA operands are computed in
+      // converged code and are warp-uniform; lane 0 issues the MMAs and the
+      // commits (a commit tracks the MMAs of the thread that issues it).
+      int os = 0;
+      uint32_t oph = 0;
+      bool aborted = false;
+      int j = 0;
+      const uint32_t a_lo0 = smem_desc_sw128_lo(smem_u32(smem + G2_OFF_A));
+      const uint32_t b_lo0 = smem_desc_sw128_lo(smem_u32(smem + G2_OFF_B));
+      for (int i = pair; i < n_items && !aborted; i += n_pairs, ++j) {
+        const G2Item it = g2_decode(p, s_istart, s_off, i, 0);
+        const int buf = j & 1;
+        const uint32_t par = ((uint32_t)(j >> 1) & 1u) ^ 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait_cluster(&acc_empty[buf], par, s_flags, lim))) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16(256, g2_width(it.n));
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * G2_N);
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!__all_sync(0xffffffffu, mbar_wait_cluster(&afull[os], oph, s_flags, lim) &&
+                                           mbar_wait_cluster(&bfull[os], oph, s_flags, lim))) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_lo = a_lo0 + (uint32_t)os * (G2_A_BYTES >> 4);
+          const uint32_t b_lo = b_lo0 + (uint32_t)os * (G2_B_BYTES >> 4);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma2_bf16_warp(d_tmem, desc_from_lo(a_lo + 2 * ks), desc_from_lo(b_lo + 2 * ks), idesc,
+                            (kb | ks) ? 1u : 0u);
+          umma2_commit_both(&oempty[os]);
+          if (++os == G2_OSTAGES) {
+            os = 0;
+            oph ^= 1u;
+          }
+        }
+        if (!aborted) umma2_commit_both(&acc_full[buf]);
+      }
+      if (aborted && lane == 0) abort_pair();
+      umma2_commit_both(mma_done);  // completes once every MMA issued above has
+    }
+    // Both CTAs: wait for the leader's final commit, so that no MMA still
+    // reads this CTA's shared memory or writes its TMEM (bounded; the leader
+    // always commits it).
+    if (lane == 0) {
+      volatile int never = 0;
+      if (!mbar_wait_cluster(mma_done, 0, &never, lim)) set_status(p.status, DEV_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp < G2_WARP_EPI0) {
+    // ------------------------------------------------ dequantisers
+    const int dq = warp - G2_WARP_DQ0;
+    const int par = dq / G2_DQ_PER_GROUP, rg = dq % G2_DQ_PER_GROUP;
+    const uint32_t r_afull = mapa_shared(afull, 0);
+    int ps = 0, as = 0;
+    uint32_t pph = 0, aph = 0, gk = 0;
+    bool ok = true;
+    for (int i = pair; i < n_items && ok; i += n_pairs) {
+      const G2Item it = g2_decode(p, s_istart, s_off, i, (int)rank);
+      const int fmt = gt_expert_fmt(p, it.e);
+      for (int kb = 0; kb < p.KB && ok; ++kb, ++gk) {
+        if ((int)(gk % G2_DQ_GROUPS) == par) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&pfull[ps], pph, s_flags, lim)) ||
+              !__all_sync(0xffffffffu, mbar_wait_cluster(&oempty[as], aph ^ 1u, s_flags, lim))) {
+            ok = false;
+            break;
+          }
+          const uint8_t* pt = smem + G2_OFF_P + ps * G2_P_TILE;
+          uint8_t* at = smem + G2_OFF_A + as * G2_A_BYTES;
+          if (fmt == FMT_NVFP4) gt_dequant_slot<FMT_NVFP4>(pt, at, rg, lane, s_e4m3);
+          else if (fmt == FMT_MXFP4) gt_dequant_slot<FMT_MXFP4>(pt, at, rg, lane, s_e4m3);
+          else gt_dequant_slot<FMT_NF3>(pt, at, rg, lane, s_e4m3);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&pempty[ps]);
+            if (leader) mbar_arrive(&afull[as]);
+            else mbar_arrive_remote(r_afull + (uint32_t)(as * 8));
+          }
+        }
+        if (++ps == G2_PSTAGES) {
+          ps = 0;
+          pph ^= 1u;
+        }
+        if (++as == G2_OSTAGES) {
+          as = 0;
+          aph ^= 1u;
+        }
+      }
+    }
+    if (!ok && lane == 0) abort_pair();
+  } else {
+    // ------------------------------------------------ epilogue: this CTA's 128 rows x N accumulator
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int S = p.T * p.topk;
+    const uint32_t r_acc_empty = mapa_shared(acc_empty, 0);
+    int j = 0;
+    for (int i = pair; i < n_items; i += n_pairs, ++j) {
+      const G2Item it = g2_decode(p, s_istart, s_off, i, (int)rank);
+      const int buf = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait_cluster(&acc_full[buf], (uint32_t)(j >> 1) & 1u, s_flags, lim))) {
+        if (lane == 0) abort_pair();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t col0 = (uint32_t)(buf * G2_N);
+      if (it.valid && p.which == 13) {
+        const float gsc = p.tab.g13[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
+        const int g = lane >> 2, qq = lane & 3;
+        for (int h = 0; h < 2; ++h) {
+          const int ch = it.rt * 64 + (2 * quarter + h) * 8 + g;
+          const uint32_t ta = tmem_base + ((uint32_t)(quarter * 32 + 16 * h) << 16) + col0;
+          for (int c0 = 0; c0 < it.n; c0 += 32) {
+            uint32_t v[16];
+            tmem_ld16x256x4(ta + (uint32_t)c0, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int rep = 0; rep < 4; ++rep) {
+#pragma unroll
+              for (int b = 0; b < 2; ++b) {
+                const int col = c0 + 8 * rep + 2 * qq + b;
+                const float gate = __uint_as_float(v[4 * rep + b]) * gsc;
+                const float up = __uint_as_float(v[4 * rep + 2 + b]) * gsc;
+                if (col < it.n) p.h_out[(size_t)(it.p0 + col) * p.I + ch] = __float2bfloat16_rn(silu_fast(gate) * up);
+              }
+            }
+          }
+        }
+      } else if (it.valid) {
+        const float gsc = p.tab.g2[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
+        const int orow = it.rt * 128 + row;
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + col0;
+        for (int c0 = 0; c0 < it.n; c0 += 32) {
+          int my_s = -1;
+          if (c0 + lane < it.n) {
+            const int sc = p.perm[it.p0 + c0 + lane];
+            if (sc >= 0 && sc < S) my_s = sc;
+            else set_status(p.status, DEV_BAD_ROUTE);
+          }
+          uint32_t v[32];
+          tmem_ld32(taddr + (uint32_t)c0, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int sc = __shfl_sync(0xffffffffu, my_s, c);
+            if (sc >= 0) p.y_out[(size_t)sc * p.H + orow] = __uint_as_float(v[c]) * gsc;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&acc_empty[buf]);
+        else mbar_arrive_remote(r_acc_empty + (uint32_t)(buf * 8));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its partner may still touch its shared memory
+  if (warp == G2_WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc2(tmem_base, G2_TMEM_COLS);
   }
 }
 
@@ -702,10 +1229,33 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// Clusters of two that can be resident at once on this device, for the
+// pair kernel: its persistent grid must not exceed them, or the clusters that
+// do not fit would start only after others had finished. Cached per device.
+static int pair_clusters(int num_sms) {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_acquire);
+    if (c > 0) return c;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(num_sms & ~1));
+  cfg.blockDim = dim3(G2_THREADS);
+  cfg.dynamicSmemBytes = G2_SMEM_BYTES;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, grouped_pair_kernel, &cfg) != cudaSuccess || n <= 0) return 0;
+  n = std::min(n, num_sms / 2);
+  if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_release);
+  return n;
+}
+
 cudaError_t launch_grouped_gemm(const GroupedParams& p, const __nv_bfloat16* b_src, int b_rows, int num_sms,
                                 cudaStream_t st) {
-  static std::atomic<unsigned long long> attr_done{0};
-  const cudaError_t ea = ensure_smem_attr(grouped_gemm_kernel, GT_SMEM_BYTES, attr_done);
+  static std::atomic<unsigned long long> attr1{0}, attr2{0};
+  cudaError_t ea = ensure_smem_attr(grouped_gemm_kernel, GT_SMEM_BYTES, attr1);
+  if (ea == cudaSuccess) ea = ensure_smem_attr(grouped_pair_kernel, G2_SMEM_BYTES, attr2);
   if (ea != cudaSuccess) return ea;
   if (b_rows <= 0) return cudaSuccess;
   if ((reinterpret_cast<uintptr_t>(b_src) & 15) != 0 || (p.K % TILE_K) != 0) return cudaErrorInvalidValue;
@@ -714,13 +1264,20 @@ cudaError_t launch_grouped_gemm(const GroupedParams& p, const __nv_bfloat16* b_s
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)b_rows};
   const cuuint64_t strides[1] = {(cuuint64_t)p.K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)TILE_K, (cuuint32_t)GT_N};
+  const cuuint32_t box[2] = {(cuuint32_t)TILE_K, (cuuint32_t)(p.pair ? G2_BBOX : GT_N)};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(b_src), dims, strides, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  cudaError_t e = launch_pdl(grouped_gemm_kernel, dim3(num_sms), dim3(GT_THREADS), GT_SMEM_BYTES, st, p, map);
+  cudaError_t e;
+  if (!p.pair) {
+    e = launch_pdl(grouped_gemm_kernel, dim3(num_sms), dim3(GT_THREADS), GT_SMEM_BYTES, st, p, map);
+  } else {
+    const int pairs = pair_clusters(num_sms);
+    if (pairs <= 0) return cudaErrorNotSupported;
+    e = launch_pdl(grouped_pair_kernel, dim3(2 * pairs), dim3(G2_THREADS), G2_SMEM_BYTES, st, p, map);
+  }
   count_launches(1);
   return e;
 }

@@ -88,6 +88,7 @@ struct GroupedParams {
   float* y_out;
   int* status;
   unsigned long long wait_limit_ns;
+  int pair;            // 1: the CTA-pair kernel; 0: the one-CTA kernel (the default)
   ExpertTable tab;
 };
 cudaError_t launch_grouped_gemm(const GroupedParams& p, const __nv_bfloat16* b_src, int b_rows, int num_sms,

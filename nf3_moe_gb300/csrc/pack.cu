@@ -190,7 +190,7 @@ template <bool WITH_NF3_SCALE>
 __global__ void debug_dequant_kernel(int fmt, int which, const uint8_t* __restrict__ src, int N, int K, int I,
                                      __nv_bfloat16* __restrict__ dst, float* __restrict__ scales_out) {
   __shared__ uint32_t s_e4m3[256];
-  s_e4m3[threadIdx.x] = bf16x2_mul(bf16_bcast(e4m3_to_bf16(threadIdx.x)), BF16X2_2P63);
+  s_e4m3[threadIdx.x] = e4m3_lut_entry(threadIdx.x);
   __syncthreads();
   const int KB = K / TILE_K;
   const int rt = blockIdx.x / KB, kb = blockIdx.x % KB;

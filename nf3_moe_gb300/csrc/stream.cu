@@ -55,7 +55,7 @@ constexpr int SK_HDR_BYTES = 16;                           // {item, stage} writ
 constexpr int SK_STAGE_BYTES = SK_W_BYTES + SK_X_BYTES + SK_HDR_BYTES;
 constexpr int SK_SMEM_DATA = SK_STAGES * SK_STAGE_BYTES;
 constexpr int SK_NBAR = 2 * SK_STAGES;
-constexpr int SK_SMEM_BYTES = SK_SMEM_DATA + SK_NBAR * 8 + (MAX_E + 1) * 4 + 4 * 4 + 256 * 4;
+constexpr int SK_SMEM_BYTES = SK_SMEM_DATA + SK_NBAR * 8 + 2 * (MAX_E + 1) * 4 + 4 * 4 + 256 * 4;
 static_assert(SK_STAGE_BYTES % 16 == 0, "stage alignment");
 
 struct SkItem {
@@ -66,7 +66,7 @@ __device__ __forceinline__ int expert_fmt(const StreamParams& p, int e) {
   return (p.tab.loc[e] & LOC_NF3) ? FMT_NF3 : p.kept_fmt;
 }
 
-__device__ __forceinline__ SkItem decode_item(const StreamParams& p, const int* s_gstart, int i) {
+__device__ __forceinline__ SkItem decode_item(const StreamParams& p, const int* s_gstart, const int* s_off, int i) {
   SkItem it;
   const int n13 = p.ph_begin == 0 ? s_gstart[p.E] * p.ph[0].RT : 0;
   it.ph = i >= n13 ? 1 : 0;
@@ -81,7 +81,7 @@ __device__ __forceinline__ SkItem decode_item(const StreamParams& p, const int* 
   }
   it.e = lo;
   const int c = it.grp - s_gstart[lo];
-  const int o0 = p.offsets[lo], ne = p.offsets[lo + 1] - o0;
+  const int o0 = s_off[lo], ne = s_off[lo + 1] - o0;
   it.p0 = o0 + c * p.group_tokens;
   it.n = min(p.group_tokens, ne - c * p.group_tokens);
   return it;
@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SK_SMEM_DATA);
   uint64_t* empty = full + SK_STAGES;
   int* s_gstart = reinterpret_cast<int*>(empty + SK_STAGES);
-  volatile int* s_flags = s_gstart + MAX_E + 1;  // [0] abort
+  int* s_off = s_gstart + MAX_E + 1;             // the caller's offsets, copied once
+  volatile int* s_flags = s_off + MAX_E + 1;     // [0] abort
   uint32_t* s_e4m3 = reinterpret_cast<uint32_t*>(const_cast<int*>(s_flags) + 4);  // E4M3 -> bf16 pair
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint64_t lim = p.wait_limit_ns;
@@ -181,19 +182,21 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
     fence_mbar_init();
     s_flags[0] = 0;
   }
-  if (tid < 256) s_e4m3[tid] = bf16x2_mul(bf16_bcast(e4m3_to_bf16((uint32_t)tid)), BF16X2_2P63);
+  if (tid < 256) s_e4m3[tid] = e4m3_lut_entry((uint32_t)tid);
   pdl_wait();  // everything below reads or writes global memory
   pdl_trigger();
+  for (int e = tid; e <= p.E; e += blockDim.x) s_off[e] = p.offsets[e];
+  __syncthreads();
   // Group prefix over experts of the selected tiers, from the caller's offsets.
   if (warp == SK_WARP_PRODUCER) {
     const int S = p.T * p.topk;
-    bool bad = (p.offsets[0] != 0) || (p.offsets[p.E] != S);
+    bool bad = (s_off[0] != 0) || (s_off[p.E] != S);
     int run = 0;
     for (int e0 = 0; e0 < p.E; e0 += 32) {
       const int e = e0 + lane;
       int ng = 0;
       if (e < p.E) {
-        const int ne = p.offsets[e + 1] - p.offsets[e];
+        const int ne = s_off[e + 1] - s_off[e];
         if (ne < 0) bad = true;
         const bool nf3 = (p.tab.loc[e] & LOC_NF3) != 0;
         const bool sel = nf3 ? (p.tier_mask & 2) : (p.tier_mask & 1);
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
       while (!aborted) {
         const int i = atomicAdd(p.queue, 1);
         if (i >= n_items) break;
-        const SkItem it = decode_item(p, s_gstart, i);
+        const SkItem it = decode_item(p, s_gstart, s_off, i);
         const StreamPhase& P = p.ph[it.ph];
         const int fmt = expert_fmt(p, it.e);
         const size_t tb = (size_t)tile_bytes(fmt);
@@ -344,7 +347,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
       const int i = hdr[0], st = hdr[1];
       if (i < 0) break;
       if (st == 0) {
-        it = decode_item(p, s_gstart, i);
+        it = decode_item(p, s_gstart, s_off, i);
         fmt = expert_fmt(p, it.e);
         kbs = p.ph[it.ph].kbs;
         nst = p.ph[it.ph].KB / kbs;

@@ -61,20 +61,21 @@ def test_stream_path_equals_decode_path_tolerance(tiny):
 
 @pytest.mark.parametrize("kept_format", [synth.FMT_NVFP4, synth.FMT_MXFP4])
 def test_odd_k_block_counts(kept_format):
-    """I=192: W2 has 3 k-blocks (the grouped kernel's two-k-block stages end with a phantom one)
-    and W13 has 3 row tiles (the last item holds one). Both paths match the oracle on sampled
-    rows and each other on every row."""
+    """I=192: W2 has 3 k-blocks and W13 has 3 row tiles, so the last row pair of the CTA-pair
+    kernel has no row tile for the second CTA (and the one-CTA kernel's last item holds one).
+    Both grouped kernels and the streaming path match the oracle on every row."""
     L = synth.make_layer(384, 192, 8, 2, kept_ids=[0, 3, 5], kept_format=kept_format, device="cuda")
     T = 96
     moe = U.build(L, T)
     x = synth.gen_x(T, L.H, seed=11, device="cuda")
     logits = synth.gen_logits(T, L.E, seed=11, device="cuda")
     g, (ids, gates, _, _) = U.run(moe, x, logits, path=hm.PATH_GROUPED)
+    g1, _ = U.run(moe, x, logits, path=hm.PATH_GROUPED, debug_flags=hm.DEBUG_GROUPED_PAIR)
     s, _ = U.run(moe, x, logits, path=hm.PATH_STREAM)
-    tokens = [0, 1, T // 2, T - 1]
-    ref = U.oracle_out(L, x, ids, gates, tokens=tokens)
-    U.assert_rows_close(g.float().cpu().numpy()[tokens], ref)
-    U.assert_rows_close(s.float().cpu().numpy()[tokens], ref)
+    ref = U.oracle_out(L, x, ids, gates)
+    U.assert_rows_close(g.float().cpu().numpy(), ref)
+    U.assert_rows_close(g1.float().cpu().numpy(), ref)
+    U.assert_rows_close(s.float().cpu().numpy(), ref)
     U.assert_rows_close(g.float().cpu().numpy(), s.float().cpu().numpy())
 
 
@@ -155,6 +156,25 @@ def test_full_size_hybrid_decode(hybrid256, T):
     assert torch.isfinite(out.float()).all()
     out2, _ = U.run(moe, x, logits, tier_order=hm.TIERS_NF3_FIRST)
     assert torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("T", [200, 1200])
+def test_grouped_pair_kernel_matches_single_cta_kernel(tiny, T):
+    """The grouped path's one-CTA kernel (the default) and its CTA-pair kernel
+    (tcgen05.mma.cta_group::2, 256-slot token tiles) agree with the oracle; T=1200 puts about
+    300 slots on each expert, so experts span several token tiles with a ragged last one."""
+    L, _ = tiny
+    moe = U.build(L, T)
+    x = synth.gen_x(T, L.H, seed=T + 1, device="cuda")
+    logits = synth.gen_logits(T, L.E, seed=T + 1, device="cuda")
+    single, (ids, gates, _, _) = U.run(moe, x, logits, path=hm.PATH_GROUPED)
+    pair, _ = U.run(moe, x, logits, path=hm.PATH_GROUPED, debug_flags=hm.DEBUG_GROUPED_PAIR)
+    ref = U.oracle_out(L, x, ids, gates)
+    U.assert_rows_close(single.float().cpu().numpy(), ref)
+    U.assert_rows_close(pair.float().cpu().numpy(), ref)
+    for order in (hm.TIERS_KEPT_FIRST, hm.TIERS_NF3_FIRST):
+        o, _ = U.run(moe, x, logits, path=hm.PATH_GROUPED, tier_order=order)
+        assert torch.equal(o, single)
 
 
 @pytest.mark.parametrize("T", [8, 4200])

@@ -115,6 +115,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe: true if the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete. The wait is bounded:
 // it returns false if *abort becomes non-zero or after limit_ns.
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
@@ -175,6 +188,31 @@ __device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
       "%4;" ::"r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+// From a converged warp: one elected lane registers the expected bytes on the
+// barrier and issues the weight copy (L2 evict-first policy), in one warp
+// instruction sequence without a branch.
+__device__ __forceinline__ void bulk_expect_and_copy_elect(void* dst, const void* src, uint32_t bytes,
+                                                           uint32_t expect_bytes, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%3], %4;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %5;\n\t}" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "r"(expect_bytes), "l"(policy)
+      : "memory");
+}
+// A bulk copy issued by every lane whose predicate is set, in one warp
+// instruction (the lanes' copies are independent requests).
+__device__ __forceinline__ void bulk_g2s_if(bool pred, void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.b32 q, %4, 0;\n\t"
+      "@q cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "r"(pred ? 1u : 0u)
       : "memory");
 }
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {

@@ -60,7 +60,7 @@ constexpr int GT_A_BYTES = GT_R * GT_A_TILE;
 constexpr int GT_B_BYTES = GT_N * 128;    // bf16 B tile GT_N x 64
 constexpr int GT_P_TILE = 4608;           // largest packed tile
 constexpr int GT_P_BYTES = GT_R * GT_P_TILE;
-constexpr int GT_PSTAGES = 4;             // packed weight tiles in flight
+constexpr int GT_PSTAGES = 8;             // packed weight tiles in flight (covers the L2/HBM latency)
 // Operand stages: slot s holds one k-block's dequantised weight tiles (A)
 // and its activation tile (B). One barrier per slot frees both, so each
 // issuer commits once per k-block (measured 3.30 -> 3.21 ms at M=4096
@@ -85,9 +85,23 @@ static_assert(GT_DQ_GROUPS <= 2, "parity-tracked waits need at most two dequant 
 // (measured: a 3-deep packed ring with two groups gave wrong results).
 static_assert(GT_PSTAGES % GT_DQ_GROUPS == 0, "each dequant group owns its packed-ring slots");
 constexpr int GT_EPI_WARPS = 4;
-constexpr int GT_WARP_PPROD = 0, GT_WARP_MMA = 1, GT_WARP_BPROD = 2, GT_WARP_DQ0 = 3;
-constexpr int GT_WARP_EPI0 = GT_WARP_DQ0 + GT_DQ_WARPS;
-constexpr int GT_THREADS = (GT_WARP_EPI0 + GT_EPI_WARPS) * 32;
+// Warp roles by SM sub-partition (a warp runs on sub-partition warp % 4).
+// The MMA issuer's sub-partition (1) holds the light roles (the producers,
+// one epilogue warp) and only one of the 16 ALU-bound dequant warps, so that
+// the issuer gets issue slots at once: with four dequant warps beside it,
+// its bookkeeping between two k-blocks took longer than the tensor core's
+// queued work (measured with per-role timestamps) and left the tensor core
+// idle. The epilogue warps are 12..15, one per sub-partition, because a
+// warp reads the TMEM lanes 32 * (warp % 4) .. + 31.
+constexpr int GT_WARP_MMA = 1, GT_WARP_PPROD = 5, GT_WARP_BPROD = 9, GT_WARP_EPI0 = 12;
+constexpr int GT_WARPS = 24;
+constexpr int GT_THREADS = GT_WARPS * 32;
+// Dequant index of each warp (-1 for the other roles; warp 21 has none).
+// Indices 0..7 (group 0) sit on warps 0, 2, 3, 4, 6, 7, 8, 17 and 8..15
+// (group 1) on warps 10, 11, 16, 18, 19, 20, 22, 23: each group spread over
+// the sub-partitions.
+__device__ __constant__ const int8_t GT_DQ_INDEX[GT_WARPS] = {0,  -1, 1,  2,  3,  -1, 4,  5,  6,  -1, 8,  9,
+                                                              -1, -1, -1, -1, 10, 7,  11, 12, 13, -1, 14, 15};
 // Accumulator: TMEM lane = token (M = 128), column = weight row of the
 // item's row-tile pair (N = 256), double-buffered.
 constexpr int GT_ACC_COLS = GT_R * 128;
@@ -177,6 +191,47 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// The same TMA load from a converged warp: one elected lane registers the
+// tile's bytes on the barrier and issues the load.
+__device__ __forceinline__ void tma_expect_load_2d_elect(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                                         uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%4], %5;\n\t"
+      "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n\t}" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_2d_elect(const CUtensorMap* map, int x, int y) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n\t}" ::"l"(map), "r"(x), "r"(y)
+      : "memory");
+}
+// From a converged warp: an elected lane registers the bytes on the barrier,
+// then every lane whose predicate is set issues its own 1D bulk copy (L2
+// evict-first), all in one warp instruction.
+__device__ __forceinline__ void mbar_expect_tx_elect(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_stream_if(bool pred, void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                   uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.b32 q, %5, 0;\n\t"
+      "@q cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;\n\t}" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy), "r"(pred ? 1u : 0u)
+      : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
                : "memory");
@@ -307,8 +362,10 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GT_OFF_BAR);
   uint64_t* pfull = bars;                              // packed tile landed (tx)
   uint64_t* pempty = pfull + GT_PSTAGES;               // dequant warps done reading it
-  uint64_t* bfull = pempty + GT_PSTAGES;               // activation tile landed (tx)
-  uint64_t* afull = bfull + GT_OSTAGES;                // dequant warps wrote the weight tiles
+  // afull: the operand slot is complete: the group's 8 dequant warps wrote the
+  // weight tiles (8 arrivals) and the activation tile landed (the TMA
+  // producer's arrival and its bytes), so the issuer waits once per k-block.
+  uint64_t* afull = pempty + GT_PSTAGES;
   uint64_t* oempty = afull + GT_OSTAGES;               // MMAs that read the slot completed
   uint64_t* acc_full = oempty + GT_OSTAGES;            // [2] accumulator ready for the epilogue
   uint64_t* acc_empty = acc_full + 2;                  // [2] epilogue drained it
@@ -326,8 +383,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
       mbar_init(&pempty[s], GT_DQ_PER_GROUP);
     }
     for (int s = 0; s < GT_OSTAGES; ++s) {
-      mbar_init(&bfull[s], 1);
-      mbar_init(&afull[s], GT_DQ_PER_GROUP);
+      mbar_init(&afull[s], GT_DQ_PER_GROUP + 1);
       mbar_init(&oempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -389,87 +445,86 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
 
   if (warp == GT_WARP_PPROD) {
     // ------------------------------------------------ packed weight tiles (HBM)
-    if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();
-      int slot = 0, issued = 0;
-      uint32_t ph = 0;
-      bool aborted = false;
-      for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x) {
-        const GtItem it = gt_decode(p, s_istart, s_off, i);
-        const int fmt = gt_expert_fmt(p, it.e);
-        const uint32_t tb = (uint32_t)tile_bytes(fmt);
-        const uint8_t* base = (fmt == FMT_NF3 ? p.nf3_buf : p.kept_buf) +
-                              (size_t)(p.tab.loc[it.e] & 0x7FFF) *
-                                  (fmt == FMT_NF3 ? p.nf3_expert_bytes : p.kept_expert_bytes) +
-                              (p.which == 2 ? (fmt == FMT_NF3 ? p.nf3_w2_off : p.kept_w2_off) : 0) +
-                              (size_t)it.rt * p.KB * tb;
-        const size_t rt_stride = (size_t)p.KB * tb;
-        for (int kb = 0; kb < p.KB; ++kb) {
-          if (!mbar_wait(&pempty[slot], ph ^ 1u, s_flags, lim)) {
-            aborted = true;
-            break;
-          }
-          mbar_arrive_expect_tx(&pfull[slot], tb * (uint32_t)it.nr);
-          for (int r = 0; r < it.nr; ++r)
-            bulk_g2s_stream(smem + GT_OFF_P + slot * GT_P_BYTES + r * GT_P_TILE, base + r * rt_stride + (size_t)kb * tb,
-                            tb, &pfull[slot], pol);
-          ++issued;
-          if (++slot == GT_PSTAGES) {
-            slot = 0;
-            ph ^= 1u;
-          }
+    // Converged warp: lane r < nr copies row tile r, in one warp instruction.
+    const uint64_t pol = l2_policy_evict_first();
+    int slot = 0, issued = 0;
+    uint32_t ph = 0;
+    bool aborted = false;
+    for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x) {
+      const GtItem it = gt_decode(p, s_istart, s_off, i);
+      const int fmt = gt_expert_fmt(p, it.e);
+      const uint32_t tb = (uint32_t)tile_bytes(fmt);
+      const uint8_t* base = (fmt == FMT_NF3 ? p.nf3_buf : p.kept_buf) +
+                            (size_t)(p.tab.loc[it.e] & 0x7FFF) *
+                                (fmt == FMT_NF3 ? p.nf3_expert_bytes : p.kept_expert_bytes) +
+                            (p.which == 2 ? (fmt == FMT_NF3 ? p.nf3_w2_off : p.kept_w2_off) : 0) +
+                            (size_t)it.rt * p.KB * tb;
+      const size_t rt_stride = (size_t)p.KB * tb;
+      const int r = lane < it.nr ? lane : 0;
+      for (int kb = 0; kb < p.KB; ++kb) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&pempty[slot], ph ^ 1u, s_flags, lim))) {
+          aborted = true;
+          break;
         }
-      }
-      if (aborted) {
-        s_flags[0] = 1;
-        set_status(p.status, DEV_TIMEOUT);
-        volatile int never = 0;
-        for (int b = 0; b < GT_PSTAGES && b < issued; ++b) {
-          if (--slot < 0) {
-            slot = GT_PSTAGES - 1;
-            ph ^= 1u;
-          }
-          mbar_wait(&pfull[slot], ph, &never, lim);
+        mbar_expect_tx_elect(&pfull[slot], tb * (uint32_t)it.nr);
+        bulk_g2s_stream_if(lane < it.nr, smem + GT_OFF_P + slot * GT_P_BYTES + r * GT_P_TILE,
+                           base + r * rt_stride + (size_t)kb * tb, tb, &pfull[slot], pol);
+        ++issued;
+        if (++slot == GT_PSTAGES) {
+          slot = 0;
+          ph ^= 1u;
         }
       }
     }
+    if (aborted && lane == 0) {
+      s_flags[0] = 1;
+      set_status(p.status, DEV_TIMEOUT);
+      volatile int never = 0;
+      for (int b = 0; b < GT_PSTAGES && b < issued; ++b) {
+        if (--slot < 0) {
+          slot = GT_PSTAGES - 1;
+          ph ^= 1u;
+        }
+        mbar_wait(&pfull[slot], ph, &never, lim);
+      }
+    }
+    __syncwarp();
   } else if (warp == GT_WARP_BPROD) {
     // ------------------------------------------------ activation tiles (L2), TMA tensor loads
-    if (lane == 0) {
-      int slot = 0, issued = 0;
-      uint32_t ph = 0;
-      bool aborted = false;
-      for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x) {
-        const GtItem it = gt_decode(p, s_istart, s_off, i);
-        for (int kb = 0; kb < p.KB; ++kb) {
-          if (!mbar_wait(&oempty[slot], ph ^ 1u, s_flags, lim)) {
-            aborted = true;
-            break;
-          }
-          mbar_arrive_expect_tx(&bfull[slot], GT_B_BYTES);
-          tma_load_2d(smem + GT_OFF_B + slot * GT_B_BYTES, &tmap_b, kb * TILE_K, it.p0, &bfull[slot]);
-          // Warm L2 with a tile needed a few loads from now (same token tile).
-          if (kb + GT_BPREFETCH < p.KB) tma_prefetch_2d(&tmap_b, (kb + GT_BPREFETCH) * TILE_K, it.p0);
-          ++issued;
-          if (++slot == GT_OSTAGES) {
-            slot = 0;
-            ph ^= 1u;
-          }
+    int slot = 0, issued = 0;
+    uint32_t ph = 0;
+    bool aborted = false;
+    for (int i = blockIdx.x; i < n_items && !aborted; i += gridDim.x) {
+      const GtItem it = gt_decode(p, s_istart, s_off, i);
+      for (int kb = 0; kb < p.KB; ++kb) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&oempty[slot], ph ^ 1u, s_flags, lim))) {
+          aborted = true;
+          break;
         }
-      }
-      if (aborted) {
-        s_flags[0] = 1;
-        set_status(p.status, DEV_TIMEOUT);
-        volatile int never = 0;
-        for (int b = 0; b < GT_OSTAGES && b < issued; ++b) {
-          if (--slot < 0) {
-            slot = GT_OSTAGES - 1;
-            ph ^= 1u;
-          }
-          mbar_wait(&bfull[slot], ph, &never, lim);
+        tma_expect_load_2d_elect(smem + GT_OFF_B + slot * GT_B_BYTES, &tmap_b, kb * TILE_K, it.p0, &afull[slot],
+                                 GT_B_BYTES);
+        // Warm L2 with a tile needed a few loads from now (same token tile).
+        if (kb + GT_BPREFETCH < p.KB) tma_prefetch_2d_elect(&tmap_b, (kb + GT_BPREFETCH) * TILE_K, it.p0);
+        ++issued;
+        if (++slot == GT_OSTAGES) {
+          slot = 0;
+          ph ^= 1u;
         }
       }
     }
+    if (aborted && lane == 0) {
+      s_flags[0] = 1;
+      set_status(p.status, DEV_TIMEOUT);
+      volatile int never = 0;
+      for (int b = 0; b < GT_OSTAGES && b < issued; ++b) {
+        if (--slot < 0) {
+          slot = GT_OSTAGES - 1;
+          ph ^= 1u;
+        }
+        mbar_wait(&afull[slot], ph, &never, lim);
+      }
+    }
+    __syncwarp();
   } else if (warp == GT_WARP_MMA) {
     // ------------------------------------------------ MMA issuer
     // One tcgen05.mma occupies the tensor core for about 125 cycles whatever
@@ -494,23 +549,30 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
       tc_fence_after();
       const uint32_t idesc = idesc_bf16(128, it.nr * 128);
       const uint32_t d_tmem = tmem_base + (uint32_t)(buf * GT_ACC_COLS);
+      // Operand slots are ordered by their barrier and the writers' proxy
+      // fence; the tcgen05 fence after the accumulator hand-off covers TMEM.
+      // The tensor core queues few MMAs, so the issuer must not stall between
+      // k-blocks: the next slot's barrier is probed (non-blocking) between
+      // this k-block's MMAs, while they execute, and only if it was not yet
+      // complete does the issuer block on it after queueing them all.
+      bool ready = false;
       for (int kb = 0; kb < p.KB; ++kb) {
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(&afull[os], oph, s_flags, lim) && mbar_wait(&bfull[os], oph, s_flags, lim))) {
+        if (!ready && !__all_sync(0xffffffffu, mbar_wait(&afull[os], oph, s_flags, lim))) {
           aborted = true;
           break;
         }
-        tc_fence_after();
         const uint32_t x_lo = x_lo0 + (uint32_t)os * (GT_B_BYTES >> 4);
         const uint32_t w_lo = w_lo0 + (uint32_t)os * (GT_A_BYTES >> 4);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16_warp(d_tmem, desc_from_lo(x_lo + 2 * ks), desc_from_lo(w_lo + 2 * ks), idesc, (kb | ks) ? 1u : 0u);
+        umma_bf16_warp(d_tmem, desc_from_lo(x_lo), desc_from_lo(w_lo), idesc, kb ? 1u : 0u);
+        umma_bf16_warp(d_tmem, desc_from_lo(x_lo + 2), desc_from_lo(w_lo + 2), idesc, 1u);
+        const int os_next = os + 1 == GT_OSTAGES ? 0 : os + 1;
+        const uint32_t oph_next = os + 1 == GT_OSTAGES ? oph ^ 1u : oph;
+        ready = kb + 1 < p.KB && __all_sync(0xffffffffu, mbar_test(&afull[os_next], oph_next));
+        umma_bf16_warp(d_tmem, desc_from_lo(x_lo + 4), desc_from_lo(w_lo + 4), idesc, 1u);
+        umma_bf16_warp(d_tmem, desc_from_lo(x_lo + 6), desc_from_lo(w_lo + 6), idesc, 1u);
         umma_commit_warp(&oempty[os]);
-        if (++os == GT_OSTAGES) {
-          os = 0;
-          oph ^= 1u;
-        }
+        os = os_next;
+        oph = oph_next;
       }
       if (!aborted) umma_commit_warp(&acc_full[buf]);
     }
@@ -525,13 +587,13 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
       mbar_wait(mma_done, 0, &never, lim);
     }
     __syncwarp();
-  } else if (warp < GT_WARP_EPI0) {
+  } else if (GT_DQ_INDEX[warp] >= 0) {
     // ------------------------------------------------ dequantisers: packed tile -> bf16 operand tile
     // Group par expands the k-blocks k with k % GT_DQ_GROUPS == par, every
     // row tile; its warps split the 8 row groups. (Eight warps each expanding
     // both row tiles of every k-block was measured slower: 4.18 against 4.03
     // ms at M=4096.)
-    const int dq = warp - GT_WARP_DQ0;
+    const int dq = GT_DQ_INDEX[warp];
     const int par = dq / GT_DQ_PER_GROUP, rg = (dq % GT_DQ_PER_GROUP) * (8 / GT_DQ_PER_GROUP);
     int ps = 0, as = 0;
     uint32_t pph = 0, aph = 0, gk = 0;
@@ -555,7 +617,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
       s_flags[0] = 1;
       set_status(p.status, DEV_TIMEOUT);
     }
-  } else {
+  } else if (warp >= GT_WARP_EPI0 && warp < GT_WARP_EPI0 + GT_EPI_WARPS) {
     // ------------------------------------------------ epilogue
     // TMEM lane = token column c of the item (each warp owns 32 lanes), TMEM
     // column = weight row of the row-tile pair. A thread reads 32 columns at
@@ -1000,7 +1062,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G2_THREADS, 1)
               slot = G2_OSTAGES - 1;
               ph ^= 1u;
             }
-            mbar_wait(&bfull[slot], ph, &never, lim);
+            mbar_wait(&afull[slot], ph, &never, lim);
           }
         }
       }
@@ -1034,7 +1096,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G2_THREADS, 1)
             aborted = true;
             break;
           }
-          tc_fence_after();
           const uint32_t a_lo = a_lo0 + (uint32_t)os * (G2_A_BYTES >> 4);
           const uint32_t b_lo = b_lo0 + (uint32_t)os * (G2_B_BYTES >> 4);
 #pragma unroll

@@ -231,7 +231,10 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
     // ------------------------------------------------ producer: dynamic work queue
     // With the test hook set the producer stays silent, so the consumers'
     // bounded waits run out and report DEV_TIMEOUT.
-    if (lane == 0 && !p.debug_no_copies) {
+    // The whole warp runs the loop (converged), so that each bulk copy issues
+    // as one warp instruction: one elected lane copies the weight tiles and
+    // lane j the activation row of token j, all in the same instruction.
+    if (!p.debug_no_copies) {
       const uint64_t pol = l2_policy_evict_first();
       const int S = p.T * p.topk;
       int slot = 0;
@@ -239,7 +242,9 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
       int issued = 0;
       bool aborted = false;
       while (!aborted) {
-        const int i = atomicAdd(p.queue, 1);
+        int i = 0;
+        if (lane == 0) i = atomicAdd(p.queue, 1);
+        i = __shfl_sync(0xffffffffu, i, 0);
         if (i >= n_items) break;
         const SkItem it = decode_item(p, s_gstart, s_off, i);
         const StreamPhase& P = p.ph[it.ph];
@@ -249,36 +254,43 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
                               (size_t)(p.tab.loc[it.e] & 0x7FFF) *
                                   (fmt == FMT_NF3 ? p.nf3_expert_bytes : p.kept_expert_bytes) +
                               (fmt == FMT_NF3 ? P.nf3_off : P.kept_off);
-        int rows[8];
-        for (int j = 0; j < it.n; ++j) {
+        // Lane j < n: the activation row of the item's token j.
+        int my_row = 0;
+        if (lane < it.n) {
           if (it.ph == 0) {
-            int s = p.perm[it.p0 + j];
+            int s = p.perm[it.p0 + lane];
             if (s < 0 || s >= S) {
               set_status(p.status, DEV_BAD_ROUTE);
               s = 0;
             }
-            rows[j] = s / p.topk;
+            my_row = s / p.topk;
           } else {
-            rows[j] = it.p0 + j;
+            my_row = it.p0 + lane;
           }
         }
         if (fused && it.ph == 1) {
           // The group's h rows come from its W13 items (any CTA): wait until
           // all of them are written, then order the bulk copies after.
-          if (!wait_count_at_least(p.done13 + it.grp, SK_CONSUMER_WARPS * p.ph[0].RT, s_flags, lim)) {
+          bool ok = true;
+          if (lane == 0) ok = wait_count_at_least(p.done13 + it.grp, SK_CONSUMER_WARPS * p.ph[0].RT, s_flags, lim);
+          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
             aborted = true;
-            s_flags[0] = 1;
-            set_status(p.status, DEV_TIMEOUT);
+            if (lane == 0) {
+              s_flags[0] = 1;
+              set_status(p.status, DEV_TIMEOUT);
+            }
             break;
           }
           fence_proxy_async_global();
         }
         const int nst = P.KB / P.kbs;
         for (int st = 0; st < nst; ++st) {
-          if (!mbar_wait(&empty[slot], ph ^ 1u, s_flags, lim)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&empty[slot], ph ^ 1u, s_flags, lim))) {
             aborted = true;
-            s_flags[0] = 1;
-            set_status(p.status, DEV_TIMEOUT);
+            if (lane == 0) {
+              s_flags[0] = 1;
+              set_status(p.status, DEV_TIMEOUT);
+            }
             break;
           }
           const int kbA = st * P.kbs;
@@ -286,14 +298,16 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
           const uint32_t xbytes = (uint32_t)(P.kbs * 128);
           uint8_t* sw = smem + slot * SK_STAGE_BYTES;
           uint8_t* sx = sw + SK_W_BYTES;
-          int* hdr = reinterpret_cast<int*>(sx + SK_X_BYTES);
-          hdr[0] = i;
-          hdr[1] = st;
-          mbar_arrive_expect_tx(&full[slot], wbytes + (uint32_t)it.n * xbytes);
-          bulk_g2s_stream(sw, base + ((size_t)it.rt * P.KB + kbA) * tb, wbytes, &full[slot], pol);
-          for (int j = 0; j < it.n; ++j)
-            bulk_g2s(sx + j * SK_XROW, P.act + (size_t)rows[j] * P.act_stride + (size_t)kbA * 64, xbytes,
-                     &full[slot]);
+          if (lane == 0) {
+            int* hdr = reinterpret_cast<int*>(sx + SK_X_BYTES);
+            hdr[0] = i;
+            hdr[1] = st;
+          }
+          __syncwarp();
+          bulk_expect_and_copy_elect(sw, base + ((size_t)it.rt * P.KB + kbA) * tb, wbytes,
+                                     wbytes + (uint32_t)it.n * xbytes, &full[slot], pol);
+          bulk_g2s_if(lane < it.n, sx + lane * SK_XROW, P.act + (size_t)my_row * P.act_stride + (size_t)kbA * 64,
+                      xbytes, &full[slot]);
           ++issued;
           if (++slot == SK_STAGES) {
             slot = 0;
@@ -301,30 +315,33 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
           }
         }
       }
-      if (!aborted) {
-        // Terminator stage: item -1, no bytes.
-        if (mbar_wait(&empty[slot], ph ^ 1u, s_flags, lim)) {
-          int* hdr = reinterpret_cast<int*>(smem + slot * SK_STAGE_BYTES + SK_W_BYTES + SK_X_BYTES);
-          hdr[0] = -1;
-          mbar_arrive(&full[slot]);
-        } else {
-          aborted = true;
-          s_flags[0] = 1;
-          set_status(p.status, DEV_TIMEOUT);
-        }
-      }
-      if (aborted) {
-        // Drain copies still in flight before the CTA may exit (bounded).
-        volatile int never = 0;
-        for (int b = 0; b < SK_STAGES && b < issued; ++b) {
-          if (--slot < 0) {
-            slot = SK_STAGES - 1;
-            ph ^= 1u;
+      if (lane == 0) {
+        if (!aborted) {
+          // Terminator stage: item -1, no bytes.
+          if (mbar_wait(&empty[slot], ph ^ 1u, s_flags, lim)) {
+            int* hdr = reinterpret_cast<int*>(smem + slot * SK_STAGE_BYTES + SK_W_BYTES + SK_X_BYTES);
+            hdr[0] = -1;
+            mbar_arrive(&full[slot]);
+          } else {
+            aborted = true;
+            s_flags[0] = 1;
+            set_status(p.status, DEV_TIMEOUT);
           }
-          mbar_wait(&full[slot], ph, &never, lim);
         }
-        s_flags[0] = 1;
+        if (aborted) {
+          // Drain copies still in flight before the CTA may exit (bounded).
+          volatile int never = 0;
+          for (int b = 0; b < SK_STAGES && b < issued; ++b) {
+            if (--slot < 0) {
+              slot = SK_STAGES - 1;
+              ph ^= 1u;
+            }
+            mbar_wait(&full[slot], ph, &never, lim);
+          }
+          s_flags[0] = 1;
+        }
       }
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------ consumers

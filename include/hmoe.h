@@ -314,6 +314,59 @@ hmoe_status hmoe_layer_expert_info(const hmoe_layer* layer, int expert, int* fmt
 
 void hmoe_layer_destroy(hmoe_layer* layer);
 
+/* ------------------------------------------------------------ dense Linear W4A16
+ * One weight matrix W [N, K] stored as NVFP4, MXFP4 or NF3 (the logical
+ * layouts at the top of this file), times bf16 activations:
+ *   y[t][n] = sum_k x[t][k] * W[n][k], fp32 accumulation, bf16 result.
+ *   Cites: "[Quantization][ModelOpt] W4A16 NVFP4 fused MoE +
+ *   --override-activation-dtype flag", Summary and Related (the fused-MoE
+ *   W4A16 support follows a dense-Linear W4A16 method: 4-bit weights, 16-bit
+ *   activations, no activation scales).
+ * The same kernels as the MoE layer run it: the matrix is packed like an
+ * expert's W2 (tile layout), and a forward is the W2 phase of the
+ * weight-streaming kernel (T <= 8) or of the tensor-core grouped kernel
+ * (above) over one expert with one slot per token, then the bf16 finalize.
+ * Conventions as for the layer: caller-owned device memory, asynchronous on
+ * the stream, no allocation, argument errors before anything is enqueued,
+ * device faults in the workspace's status word (hmoe_check_device_status).
+ * Zero the workspace once before its first use (hmoe_workspace_init). */
+typedef struct {
+  int N;   /* output features, a multiple of 128 */
+  int K;   /* input features, a multiple of 64 */
+  int fmt; /* HMOE_FMT_NVFP4, HMOE_FMT_MXFP4 or HMOE_FMT_NF3 */
+} hmoe_linear_desc;
+
+typedef struct hmoe_linear hmoe_linear; /* opaque host handle: no device memory */
+
+/* Bytes of the packed matrix (the packed argument of hmoe_linear_pack). */
+hmoe_status hmoe_linear_packed_size(const hmoe_linear_desc* desc, size_t* bytes);
+
+/* Workspace bytes for hmoe_linear_forward at up to max_tokens rows: the
+ * status word, the kernels' work queues, the one-expert route geometry and
+ * the fp32 product [max_tokens][N]. */
+hmoe_status hmoe_linear_workspace_size(const hmoe_linear_desc* desc, int max_tokens, size_t* bytes);
+
+/* Repack W into the tile layout and create the handle. codes, scales: device
+ * tensors in the logical layout of desc->fmt; global_scale: the NVFP4 fp32
+ * global scale (ignored otherwise). packed: device buffer of
+ * hmoe_linear_packed_size bytes, 16-byte aligned, alive while the handle is
+ * used. The sources may be freed once the stream has passed this point. */
+hmoe_status hmoe_linear_pack(const hmoe_linear_desc* desc, const void* codes, const void* scales,
+                             float global_scale, void* packed, hmoe_stream_t stream, hmoe_linear** out);
+
+/* out[t][n] = bf16(sum_k x[t][k] W[n][k]). x: device bf16 [T][K]; out: device
+ * bf16 [T][N], fully overwritten; both 16-byte aligned. T = 0 is valid. */
+hmoe_status hmoe_linear_forward(const hmoe_linear* linear, const void* x, int T, void* out, void* ws,
+                                size_t ws_bytes, hmoe_stream_t stream);
+
+/* With options: path (HMOE_PATH_AUTO chooses the streaming kernel for T <= 8),
+ * wait_limit_us and debug_flags as for hmoe_forward_ex; tier_order and
+ * stage_events are ignored. */
+hmoe_status hmoe_linear_forward_ex(const hmoe_linear* linear, const void* x, int T, void* out, void* ws,
+                                   size_t ws_bytes, const hmoe_forward_opts* opts, hmoe_stream_t stream);
+
+void hmoe_linear_destroy(hmoe_linear* linear);
+
 /* Message for the last failing call on this thread ("" if none). */
 const char* hmoe_last_error(void);
 

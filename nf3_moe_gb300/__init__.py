@@ -19,13 +19,15 @@ import torch
 
 from . import _lib
 from ._lib import (FMT_MXFP4, FMT_NF3, FMT_NVFP4, PATH_AUTO, PATH_GROUPED, PATH_STREAM,  # noqa: F401
-                   TIERS_KEPT_FIRST, TIERS_NF3_FIRST, TIERS_ONE_LAUNCH, HmoeError, LayerDesc,
+                   TIERS_KEPT_FIRST, TIERS_NF3_FIRST, TIERS_ONE_LAUNCH, HmoeError, LayerDesc, LinearDesc,
                    DEBUG_NO_COPIES, DEBUG_GROUPED_PAIR)
 
 __all__ = [
     "LayerDesc", "HmoeError", "hmoe_packed_size", "hmoe_workspace_size", "hmoe_workspace_init",
     "hmoe_pack_weights", "hmoe_plan_routes", "hmoe_forward", "hmoe_check_device_status",
     "hmoe_debug_dequant", "hmoe_debug_decode_operand", "HybridMoELayer", "library_path",
+    "LinearDesc", "hmoe_linear_packed_size", "hmoe_linear_workspace_size", "hmoe_linear_pack", "hmoe_linear_forward",
+    "LinearW4A16",
 ]
 
 
@@ -201,3 +203,63 @@ def hmoe_forward_static(layer, x, ids, gates, perm, offsets, out, stream=None):
 
 def hmoe_check_device_status_static(stream=None):
     _lib.check(_lib.lib().hmoe_check_device_status_static(_stream(stream)))
+
+
+# ------------------------------------------------------------------ dense Linear W4A16
+def hmoe_linear_packed_size(desc):
+    b = ctypes.c_size_t()
+    _lib.check(_lib.lib().hmoe_linear_packed_size(ctypes.byref(desc), ctypes.byref(b)))
+    return b.value
+
+
+def hmoe_linear_workspace_size(desc, max_tokens):
+    b = ctypes.c_size_t()
+    _lib.check(_lib.lib().hmoe_linear_workspace_size(ctypes.byref(desc), int(max_tokens), ctypes.byref(b)))
+    return b.value
+
+
+class Linear:
+    """Owns the C handle of a packed dense W4A16 matrix; keeps the packed buffer alive."""
+
+    def __init__(self, handle, desc, packed):
+        self.handle, self.desc, self.packed = handle, desc, packed
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h and _lib._LIB is not None:
+            _lib._LIB.hmoe_linear_destroy(h)
+
+
+def hmoe_linear_pack(desc, codes, scales, global_scale, packed, stream=None):
+    h = ctypes.c_void_p()
+    _lib.check(_lib.lib().hmoe_linear_pack(ctypes.byref(desc), _ptr(codes), _ptr(scales), float(global_scale),
+                                           _ptr(packed), _stream(stream), ctypes.byref(h)))
+    return Linear(h, desc, packed)
+
+
+def hmoe_linear_forward(linear, x, out, ws, stream=None, path=PATH_AUTO, wait_limit_us=0, debug_flags=0):
+    opts = _lib.ForwardOpts(TIERS_ONE_LAUNCH, int(path), int(wait_limit_us), int(debug_flags), None, 0)
+    _lib.check(_lib.lib().hmoe_linear_forward_ex(linear.handle, _ptr(x), int(x.shape[0]), _ptr(out), _ptr(ws),
+                                                 ws.numel() * ws.element_size(), ctypes.byref(opts), _stream(stream)))
+
+
+class LinearW4A16:
+    """A dense W4A16 Linear with its packed matrix and workspace owned as torch tensors.
+
+    codes, scales: CUDA tensors of one [N, K] matrix in the logical layout of fmt
+    (include/hmoe.h); global_scale: the NVFP4 global scale (ignored otherwise).
+    """
+
+    def __init__(self, N, K, fmt, codes, scales, global_scale=1.0, max_tokens=8, device="cuda"):
+        self.desc = LinearDesc(N, K, fmt)
+        self.packed = torch.empty(hmoe_linear_packed_size(self.desc), dtype=torch.uint8, device=device)
+        self.linear = hmoe_linear_pack(self.desc, codes, scales, global_scale, self.packed)
+        self.ws = torch.empty(hmoe_linear_workspace_size(self.desc, max_tokens), dtype=torch.uint8, device=device)
+        hmoe_workspace_init(self.ws)
+        self.N = N
+
+    def __call__(self, x, out=None, path=PATH_AUTO):
+        if out is None:
+            out = torch.empty((x.shape[0], self.N), dtype=torch.bfloat16, device=x.device)
+        hmoe_linear_forward(self.linear, x, out, self.ws, path=path)
+        return out

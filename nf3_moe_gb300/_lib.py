@@ -29,13 +29,18 @@ EXPORTS = (
     "hmoe_plan_routes", "hmoe_forward", "hmoe_forward_ex", "hmoe_check_device_status",
     "hmoe_debug_dequant", "hmoe_layer_expert_info", "hmoe_layer_destroy", "hmoe_last_error",
     "hmoe_launch_count", "hmoe_version", "hmoe_forward_static", "hmoe_check_device_status_static",
-    "hmoe_auto_path", "hmoe_debug_decode_operand",
+    "hmoe_auto_path", "hmoe_debug_decode_operand", "hmoe_linear_packed_size", "hmoe_linear_workspace_size",
+    "hmoe_linear_pack", "hmoe_linear_forward", "hmoe_linear_forward_ex", "hmoe_linear_destroy",
 )
 
 
 class LayerDesc(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int), ("topk", ctypes.c_int),
                 ("kept_format", ctypes.c_int)]
+
+
+class LinearDesc(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int), ("K", ctypes.c_int), ("fmt", ctypes.c_int)]
 
 
 class ExpertSrc(ctypes.Structure):
@@ -80,6 +85,12 @@ def load(path=LIB_PATH):
         "hmoe_check_device_status_static": (i, [vp]),
         "hmoe_version": (i, []),
         "hmoe_auto_path": (i, [P(LayerDesc), i, P(i)]),
+        "hmoe_linear_packed_size": (i, [P(LinearDesc), P(sz)]),
+        "hmoe_linear_workspace_size": (i, [P(LinearDesc), i, P(sz)]),
+        "hmoe_linear_pack": (i, [P(LinearDesc), vp, vp, ctypes.c_float, vp, vp, P(vp)]),
+        "hmoe_linear_forward": (i, [vp, vp, i, vp, vp, sz, vp]),
+        "hmoe_linear_forward_ex": (i, [vp, vp, i, vp, vp, sz, P(ForwardOpts), vp]),
+        "hmoe_linear_destroy": (None, [vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

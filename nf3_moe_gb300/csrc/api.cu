@@ -631,3 +631,201 @@ hmoe_status hmoe_check_device_status_static(hmoe_stream_t stream) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------ dense Linear W4A16
+// One weight matrix W [N, K] (NVFP4, MXFP4 or NF3) times bf16 activations,
+// run by the layer's own kernels: the matrix is packed like an expert's W2,
+// and a forward is the W2 phase of the streaming kernel (T <= 8) or of the
+// tensor-core grouped kernel (above) over a one-expert route geometry with
+// one slot per token and gate 1, then the finalize to bf16.
+struct hmoe_linear {
+  hmoe_linear_desc d;
+  uint8_t* packed;
+  size_t bytes;
+  ExpertTable tab;
+  int num_sms;
+};
+
+namespace {
+struct LinWs {
+  size_t status, queues, perm, offsets, gates, y, total;
+};
+LinWs lin_layout(const hmoe_linear_desc& d, int T) {
+  LinWs w{};
+  size_t off = 0;
+  w.status = off;
+  off += 256;
+  w.queues = off;
+  off += 256;
+  w.perm = off;
+  off += align256((size_t)T * 4);
+  w.offsets = off;
+  off += 256;
+  w.gates = off;
+  off += align256((size_t)T * 4);
+  w.y = off;
+  off += align256((size_t)T * d.N * 4);
+  w.total = off;
+  return w;
+}
+hmoe_status check_linear_desc(const hmoe_linear_desc* d) {
+  if (!d) return fail(HMOE_ERR_INVALID_ARG, "desc is NULL");
+  if (d->fmt != HMOE_FMT_NVFP4 && d->fmt != HMOE_FMT_MXFP4 && d->fmt != HMOE_FMT_NF3)
+    return fail(HMOE_ERR_INVALID_ARG, "fmt must be NVFP4 (4), MXFP4 (5) or NF3 (3), got %d", d->fmt);
+  if (d->N <= 0 || d->K <= 0) return fail(HMOE_ERR_INVALID_ARG, "N and K must be positive");
+  if (d->N % 128 != 0 || d->K % 64 != 0)
+    return fail(HMOE_ERR_UNSUPPORTED_SHAPE, "N must be a multiple of 128 and K of 64 (N=%d K=%d)", d->N, d->K);
+  return HMOE_OK;
+}
+}  // namespace
+
+extern "C" {
+
+hmoe_status hmoe_linear_packed_size(const hmoe_linear_desc* desc, size_t* bytes) {
+  hmoe_status s = check_linear_desc(desc);
+  if (s != HMOE_OK) return s;
+  if (!bytes) return fail(HMOE_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = (size_t)(desc->N / TILE_ROWS) * (desc->K / TILE_K) * tile_bytes(desc->fmt);
+  return HMOE_OK;
+}
+
+hmoe_status hmoe_linear_workspace_size(const hmoe_linear_desc* desc, int max_tokens, size_t* bytes) {
+  hmoe_status s = check_linear_desc(desc);
+  if (s != HMOE_OK) return s;
+  if (!bytes || max_tokens < 0) return fail(HMOE_ERR_INVALID_ARG, "bytes NULL or max_tokens < 0");
+  *bytes = lin_layout(*desc, max_tokens).total;
+  return HMOE_OK;
+}
+
+hmoe_status hmoe_linear_pack(const hmoe_linear_desc* desc, const void* codes, const void* scales, float global_scale,
+                             void* packed, hmoe_stream_t stream, hmoe_linear** out) {
+  const NvtxRange nvtx("hmoe_linear_pack");
+  hmoe_status s = check_linear_desc(desc);
+  if (s != HMOE_OK) return s;
+  if (!codes || !scales || !packed || !out) return fail(HMOE_ERR_INVALID_ARG, "a pointer is NULL");
+  if (!aligned16(packed)) return fail(HMOE_ERR_INVALID_ARG, "packed buffer must be 16-byte aligned");
+  hmoe_linear* L = new (std::nothrow) hmoe_linear();
+  if (!L) return fail(HMOE_ERR_INVALID_ARG, "out of host memory");
+  L->d = *desc;
+  L->packed = static_cast<uint8_t*>(packed);
+  hmoe_linear_packed_size(desc, &L->bytes);
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ce == cudaSuccess)
+    ce = launch_pack_matrix(desc->fmt, 2, codes, scales, desc->N, desc->K, desc->K, L->packed, (cudaStream_t)stream);
+  if (ce != cudaSuccess) {
+    delete L;
+    return cuda_fail(ce, "linear pack");
+  }
+  L->tab.loc[0] = desc->fmt == HMOE_FMT_NF3 ? LOC_NF3 : 0;
+  L->tab.g13[0] = 1.0f;
+  L->tab.g2[0] = desc->fmt == HMOE_FMT_NVFP4 ? global_scale : 1.0f;
+  *out = L;
+  return HMOE_OK;
+}
+
+void hmoe_linear_destroy(hmoe_linear* L) { delete L; }
+
+hmoe_status hmoe_linear_forward_ex(const hmoe_linear* L, const void* x, int T, void* out, void* ws, size_t ws_bytes,
+                                   const hmoe_forward_opts* opts, hmoe_stream_t stream) {
+  const NvtxRange nvtx("hmoe_linear_forward");
+  if (!L) return fail(HMOE_ERR_INVALID_ARG, "linear is NULL");
+  if (T < 0) return fail(HMOE_ERR_INVALID_ARG, "T=%d < 0", T);
+  const hmoe_forward_opts o = opts ? *opts : kDefaultOpts;
+  if (o.path < 0 || o.path > 2) return fail(HMOE_ERR_INVALID_ARG, "bad path %d", o.path);
+  if (o.wait_limit_us < 0) return fail(HMOE_ERR_INVALID_ARG, "wait_limit_us < 0");
+  if (!ws) return fail(HMOE_ERR_INVALID_ARG, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return fail(HMOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const LinWs w = lin_layout(L->d, T);
+  if (ws_bytes < w.total)
+    return fail(HMOE_ERR_WORKSPACE_TOO_SMALL, "workspace holds %zu bytes, T=%d needs %zu", ws_bytes, T, w.total);
+  if (T == 0) return HMOE_OK;
+  if (!x || !out) return fail(HMOE_ERR_INVALID_ARG, "x or out is NULL");
+  if (!aligned16(x) || !aligned16(out)) return fail(HMOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+  const bool grouped = o.path == HMOE_PATH_GROUPED || (o.path == HMOE_PATH_AUTO && T > DECODE_MAX_T);
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  int* perm = reinterpret_cast<int*>(wsb + w.perm);
+  int* offsets = reinterpret_cast<int*>(wsb + w.offsets);
+  float* gates = reinterpret_cast<float*>(wsb + w.gates);
+  float* y = reinterpret_cast<float*>(wsb + w.y);
+  int* status = reinterpret_cast<int*>(wsb + w.status);
+  const unsigned long long lim =
+      o.wait_limit_us > 0 ? (unsigned long long)o.wait_limit_us * 1000ull : WAIT_LIMIT_NS;
+  const int kept_fmt = L->d.fmt == HMOE_FMT_NF3 ? FMT_NVFP4 : L->d.fmt;  // the unused tier's format
+  cudaError_t e = launch_identity_route(T, perm, offsets, gates, L->num_sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "linear route launch");
+  if (grouped) {
+    GroupedParams p{};
+    p.kept_buf = L->packed;
+    p.nf3_buf = L->packed;
+    p.kept_fmt = kept_fmt;
+    p.which = 2;
+    p.H = L->d.N;
+    p.I = L->d.K;
+    p.E = 1;
+    p.topk = 1;
+    p.T = T;
+    p.K = L->d.K;
+    p.RT = L->d.N / TILE_ROWS;
+    p.KB = L->d.K / TILE_K;
+    p.tier_mask = 3;
+    p.kept_expert_bytes = p.nf3_expert_bytes = L->bytes;
+    p.offsets = offsets;
+    p.perm = perm;
+    p.y_out = y;
+    p.status = status;
+    p.wait_limit_ns = lim;
+    p.pair = (o.debug_flags & HMOE_DEBUG_GROUPED_PAIR) ? 1 : 0;
+    p.tab = L->tab;
+    e = launch_grouped_gemm(p, static_cast<const __nv_bfloat16*>(x), T, L->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "linear grouped GEMM launch");
+  } else {
+    StreamParams p{};
+    p.kept_buf = L->packed;
+    p.nf3_buf = L->packed;
+    p.kept_fmt = kept_fmt;
+    p.H = L->d.N;
+    p.I = L->d.K;
+    p.E = 1;
+    p.topk = 1;
+    p.T = T;
+    p.group_tokens = 8;
+    p.tier_mask = 3;
+    p.kept_expert_bytes = p.nf3_expert_bytes = L->bytes;
+    p.offsets = offsets;
+    p.perm = perm;
+    p.queue = reinterpret_cast<int*>(wsb + w.queues);
+    p.done13 = nullptr;
+    p.y_out = y;
+    p.status = status;
+    p.wait_limit_ns = lim;
+    p.debug_no_copies = (o.debug_flags & HMOE_DEBUG_NO_COPIES) ? 1 : 0;
+    p.tab = L->tab;
+    StreamPhase& P = p.ph[1];
+    P.rows = L->d.N;
+    P.K = L->d.K;
+    P.RT = L->d.N / TILE_ROWS;
+    P.KB = L->d.K / TILE_K;
+    P.kbs = pick_stage(P.KB);
+    P.act = static_cast<const __nv_bfloat16*>(x);
+    P.act_stride = L->d.K;
+    P.kept_off = P.nf3_off = 0;
+    p.ph[0] = P;
+    p.ph_begin = 1;
+    p.ph_end = 2;
+    e = launch_stream_gemm(p, stream_grid(L->num_sms), st);
+    if (e != cudaSuccess) return cuda_fail(e, "linear stream GEMM launch");
+  }
+  e = launch_finalize(y, gates, T, 1, L->d.N, static_cast<__nv_bfloat16*>(out), st);
+  if (e != cudaSuccess) return cuda_fail(e, "linear finalize launch");
+  return HMOE_OK;
+}
+
+hmoe_status hmoe_linear_forward(const hmoe_linear* L, const void* x, int T, void* out, void* ws, size_t ws_bytes,
+                                hmoe_stream_t stream) {
+  return hmoe_linear_forward_ex(L, x, T, out, ws, ws_bytes, nullptr, stream);
+}
+
+}  // extern "C"

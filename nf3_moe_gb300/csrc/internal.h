@@ -18,6 +18,9 @@ int route_chunks(int T);
 cudaError_t launch_route(const float* logits, int T, int E, int k, int* ids, float* gates, int* perm,
                          int* offsets, int* chunk_cnt, int* chunk_base, cudaStream_t st);
 
+// perm[t] = t, offsets = {0, T}, gates[t] = 1 (the dense Linear's route geometry).
+cudaError_t launch_identity_route(int T, int* perm, int* offsets, float* gates, int num_sms, cudaStream_t st);
+
 // ---------------------------------------------------------------- packing
 // Geometry of one expert block inside a tier buffer: W13 tiles then W2 tiles.
 struct ExpertGeom {

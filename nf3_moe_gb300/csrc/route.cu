@@ -283,4 +283,27 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int* ids, flo
   return e;
 }
 
+// The route geometry of a dense Linear: one "expert", one slot per token.
+// perm[t] = t, offsets = {0, T}, gates[t] = 1.
+__global__ void identity_route_kernel(int T, int* perm, int* offsets, float* gates) {
+  pdl_wait();
+  pdl_trigger();
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
+    perm[t] = t;
+    gates[t] = 1.0f;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    offsets[0] = 0;
+    offsets[1] = T;
+  }
+}
+
+cudaError_t launch_identity_route(int T, int* perm, int* offsets, float* gates, int num_sms, cudaStream_t st) {
+  const int blocks = (T + 255) / 256;
+  const int grid = blocks < 1 ? 1 : (blocks < num_sms ? blocks : num_sms);
+  cudaError_t e = launch_pdl(identity_route_kernel, dim3(grid), dim3(256), 0, st, T, perm, offsets, gates);
+  count_launches(1);
+  return e;
+}
+
 }  // namespace hmoe

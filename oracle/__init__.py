@@ -25,9 +25,10 @@ Modules:
              layouts.
   route   -- top-k routing, renormalised gates, stable permutation, offsets.
   layer   -- the SwiGLU expert layer: dequantise, then matmul, gate, sum.
+  linear  -- the dense-Linear W4A16 product: dequantise, then matmul.
 
 Every function here is pinned by ``tests/test_oracle_*.py`` against library
 routines, closed forms, golden fixtures or brute force.
 """
 
-from . import formats, route, layer  # noqa: F401
+from . import formats, route, layer, linear  # noqa: F401

@@ -87,3 +87,14 @@ def test_null_handles_rejected(lib):
     assert lib.hmoe_pack_weights(ctypes.byref(desc), None, None, None, None, None, ctypes.byref(h)) == -1
     assert b"NULL" in lib.hmoe_last_error()
     lib.hmoe_layer_destroy(None)
+
+
+def test_linear_desc_checks_on_host(lib):
+    import nf3_moe_gb300 as hm
+    assert hm.hmoe_linear_packed_size(hm.LinearDesc(256, 384, hm.FMT_NF3)) == 2 * 6 * 3328
+    assert hm.hmoe_linear_packed_size(hm.LinearDesc(128, 64, hm.FMT_NVFP4)) == 4608
+    for bad, status in (((100, 64, 4), -2), ((128, 32, 4), -2), ((128, 64, 7), -1), ((0, 64, 3), -1)):
+        with pytest.raises(hm.HmoeError) as ei:
+            hm.hmoe_linear_packed_size(hm.LinearDesc(*bad))
+        assert ei.value.status == status
+    assert hm.hmoe_linear_workspace_size(hm.LinearDesc(256, 384, hm.FMT_NVFP4), 0) == 768

@@ -7,9 +7,9 @@
  * bit map:
  *   4 = the kept tier, NVFP4 (or MXFP4 when kept_format says so),
  *   3 = the NF3 tier, 3-bit NormalFloat.
- * Activations are bf16 throughout. Both tiers run off one shared route
- * geometry (top-k ids, gates, token permutation, expert offsets) and sum
- * into one output.
+ * Activations are 16-bit throughout, bf16 or fp16 as the layer descriptor
+ * says (act_dtype). Both tiers run off one shared route geometry (top-k ids,
+ * gates, token permutation, expert offsets) and sum into one output.
  *   Cites: "quant: nvfp4_nf3_hybrid -- native serving for mixed NVFP4+NF3 MoE
  *   checkpoints", How it works (two prepared weight sets per layer, one
  *   shared route geometry and topk_sum, CUDA-graph-safe launches, an M<=8
@@ -18,7 +18,7 @@
  *   selects MXFP4; scratch sized from the maximum batched token count; no
  *   environment variables). "[Quantization][ModelOpt] W4A16 NVFP4 fused
  *   MoE", Summary (W4A16: 4-bit weights, 16-bit activations, no activation
- *   scales).
+ *   scales) and item 2 (the activation type may be bfloat16 or float16).
  *
  * Conventions
  *   - Every pointer argument named *_dev or documented "device" is device
@@ -79,6 +79,19 @@ typedef enum {
 
 typedef enum { HMOE_FMT_NF3 = 3, HMOE_FMT_NVFP4 = 4, HMOE_FMT_MXFP4 = 5 } hmoe_fmt;
 
+/* Activation type: x, the SwiGLU output h, the result, and the tensor-core
+ * operands (the weights are dequantised to this type). Accumulation is fp32
+ * either way.
+ *   Cites: "[Quantization][ModelOpt] W4A16 NVFP4 fused MoE +
+ *   --override-activation-dtype flag", Summary item 2 (bfloat16 or float16
+ *   activations for the W4A16 path).
+ * fp16 ranges (the weights are exact in fp16 only inside them; outside, a
+ * value rounds to 0 or to infinity and the result is undefined): MXFP4
+ * scale bytes b in 104..140 (2^-23 .. 2^13); NF3 scales in the fp16 normal
+ * range 2^-14 .. 65504. Every NVFP4 value is exact in fp16. Activations
+ * must fit fp16 like any fp16 model's. */
+typedef enum { HMOE_ACT_BF16 = 0, HMOE_ACT_F16 = 1 } hmoe_act_dtype;
+
 /* One MoE layer's shape. kept_format is HMOE_FMT_NVFP4 or HMOE_FMT_MXFP4. */
 typedef struct {
   int H;           /* hidden size, a multiple of 128 */
@@ -86,6 +99,7 @@ typedef struct {
   int E;           /* experts, 1..512 */
   int topk;        /* experts per token, 1..min(E, 32) */
   int kept_format; /* hmoe_fmt of the kept (bit 4) tier */
+  int act_dtype;   /* hmoe_act_dtype; 0 (a zeroed struct) is bf16 */
 } hmoe_layer_desc;
 
 /* One expert's logical checkpoint tensors (device pointers, layout above).
@@ -119,7 +133,7 @@ hmoe_status hmoe_packed_size(const hmoe_layer_desc* desc, const int8_t* bit_map,
  *   Summary (scratch sized from the maximum batched token count).
  * The workspace holds the status word, the kernels' self-cleaning work
  * queues, the routing chunk counts, the gathered activation rows (T > 8),
- * the SwiGLU output h [T*k][I] bf16 and the per-slot W2 output [T*k][H]
+ * the SwiGLU output h [T*k][I] (16-bit) and the per-slot W2 output [T*k][H]
  * fp32. Errors: the desc checks (HMOE_ERR_INVALID_ARG,
  * HMOE_ERR_UNSUPPORTED_SHAPE); max_tokens < 0 or bytes NULL is
  * HMOE_ERR_INVALID_ARG. */
@@ -142,7 +156,8 @@ hmoe_status hmoe_workspace_init(void* ws_dev, size_t ws_bytes, hmoe_stream_t str
 
 /* Demultiplex the experts into tier-local packed buffers per the bit map. Each
  * tier's experts are stored contiguously in ascending expert id, in this
- * library's tile layout. It then creates the layer handle.
+ * library's tile layout, which depends on act_dtype (NVFP4 codes are stored
+ * for the decoder of that type). It then creates the layer handle.
  *   Cites: "quant: add native mixed NVFP4/MXFP4 plus NF3 MoE serving",
  *   Summary (demultiplex the expert weights into compact tier-local storage;
  *   the metadata is validated).
@@ -206,22 +221,25 @@ typedef struct {
 /* Comparison hook: the grouped path runs its CTA-pair tensor-core kernel
  * (tcgen05.mma.cta_group::2 over two SMs, 256-slot token tiles) instead of
  * the one-CTA kernel. Same results within the layer tolerance; for
- * measurements only. */
+ * measurements only; bf16 layers only. */
 #define HMOE_DEBUG_GROUPED_PAIR 2
 
 /* The layer: out[t] = sum_j gates[t,j] * W2_e (silu(W1_e x_t) * W3_e x_t) with
- * e = ids[t,j], fp32 accumulation and a bf16 result. Expert weights are
- * dequantised from their tier format as they stream.
+ * e = ids[t,j], fp32 accumulation and a result of the activation type
+ * (h is rounded to that type too). Expert weights are dequantised from their
+ * tier format to the activation type as they stream.
  *   Cites: "quant: nvfp4_nf3_hybrid -- native serving ...", How it works (both
  *   tiers run off one shared topk_sum; preplanned, CUDA-graph-safe launches;
  *   an M<=8 decode path); "[Quantization][ModelOpt] W4A16 NVFP4 fused MoE",
  *   Summary (W4A16: 4-bit weights, bf16 activations, fp32 accumulation).
  * Errors, all found on the host before anything is enqueued:
  * HMOE_ERR_INVALID_ARG (NULL layer or buffer, T < 0, x or out not 16-byte
- * aligned, a bad option, the grouped path forced at T <= 8),
+ * aligned, a bad option, the grouped path forced at T <= 8,
+ * HMOE_DEBUG_GROUPED_PAIR with fp16 activations),
  * HMOE_ERR_WORKSPACE_TOO_SMALL, and HMOE_ERR_CUDA if a launch fails. Faults
  * the kernels find are read later with hmoe_check_device_status.
- * x: device bf16 [T][H]. out: device bf16 [T][H], fully overwritten.
+ * x: device [T][H] of the activation type. out: device [T][H] of the same
+ * type, fully overwritten.
  * ids, gates, perm, offsets: exactly as hmoe_plan_routes wrote them for
  * these T tokens.
  * The result does not depend on tier_order or on the order of the tokens:
@@ -287,23 +305,25 @@ hmoe_status hmoe_check_device_status_static(hmoe_stream_t stream);
 hmoe_status hmoe_check_device_status(void* ws, size_t ws_bytes, hmoe_stream_t stream);
 
 /* Test export of the tensor-core operand. It writes, for one expert matrix
- * and in logical row order, the bf16 operand tile that the grouped
- * (tcgen05) kernel writes to shared memory, decoded by the same device
- * function. which = 13 gives [2I][H]; which = 2 gives [H][I]. dst is device
- * memory. The values are e2m1*e4m3 (NVFP4, without the global scale),
- * e2m1*2^(b-127) (MXFP4), or bf16_rne(cb*s) (NF3). The weight-streaming
+ * and in logical row order, the operand tile (of the activation type) that
+ * the grouped (tcgen05) kernel writes to shared memory, decoded by the same
+ * device function. which = 13 gives [2I][H]; which = 2 gives [H][I]. dst is
+ * device memory. The values are e2m1*e4m3 (NVFP4, without the global scale),
+ * e2m1*2^(b-127) (MXFP4), or rne(cb*s) (NF3; in fp16 with s first converted
+ * to fp16), exact or rounded once to the activation type. The weight-streaming
  * kernel uses the same values for NVFP4 and MXFP4 but not for NF3: see
  * hmoe_debug_decode_operand. */
 hmoe_status hmoe_debug_dequant(const hmoe_layer* layer, int expert, int which, void* dst,
                                hmoe_stream_t stream);
 
 /* Test export of the weight-streaming (decode) kernel's operand, decoded by
- * the same device function that kernel runs. dst: device bf16 [N][K] as in
+ * the same device function that kernel runs. dst: device [N][K] of the
+ * activation type, as in
  * hmoe_debug_dequant; scales: device fp32 [N][K/64]. The kernel computes each
  * output row as the sum over 64-wide K groups g of scales[n][g] times the
  * fp32 sum over the group of dst[n][k] * x[k] (NVFP4 then times its global
  * scale). NF3: dst is the raw codebook entry cb[code] and scales the group's
- * bf16 scale; NVFP4 and MXFP4: dst is the tile of hmoe_debug_dequant and
+ * bf16 scale as fp32; NVFP4 and MXFP4: dst is the tile of hmoe_debug_dequant and
  * scales are 1. */
 hmoe_status hmoe_debug_decode_operand(const hmoe_layer* layer, int expert, int which, void* dst,
                                       float* scales, hmoe_stream_t stream);
@@ -316,8 +336,9 @@ void hmoe_layer_destroy(hmoe_layer* layer);
 
 /* ------------------------------------------------------------ dense Linear W4A16
  * One weight matrix W [N, K] stored as NVFP4, MXFP4 or NF3 (the logical
- * layouts at the top of this file), times bf16 activations:
- *   y[t][n] = sum_k x[t][k] * W[n][k], fp32 accumulation, bf16 result.
+ * layouts at the top of this file), times bf16 or fp16 activations:
+ *   y[t][n] = sum_k x[t][k] * W[n][k], fp32 accumulation, a result of the
+ *   activation type.
  *   Cites: "[Quantization][ModelOpt] W4A16 NVFP4 fused MoE +
  *   --override-activation-dtype flag", Summary and Related (the fused-MoE
  *   W4A16 support follows a dense-Linear W4A16 method: 4-bit weights, 16-bit
@@ -325,7 +346,7 @@ void hmoe_layer_destroy(hmoe_layer* layer);
  * The same kernels as the MoE layer run it: the matrix is packed like an
  * expert's W2 (tile layout), and a forward is the W2 phase of the
  * weight-streaming kernel (T <= 8) or of the tensor-core grouped kernel
- * (above) over one expert with one slot per token, then the bf16 finalize.
+ * (above) over one expert with one slot per token, then the finalize.
  * Conventions as for the layer: caller-owned device memory, asynchronous on
  * the stream, no allocation, argument errors before anything is enqueued,
  * device faults in the workspace's status word (hmoe_check_device_status).
@@ -333,7 +354,8 @@ void hmoe_layer_destroy(hmoe_layer* layer);
 typedef struct {
   int N;   /* output features, a multiple of 128 */
   int K;   /* input features, a multiple of 64 */
-  int fmt; /* HMOE_FMT_NVFP4, HMOE_FMT_MXFP4 or HMOE_FMT_NF3 */
+  int fmt;       /* HMOE_FMT_NVFP4, HMOE_FMT_MXFP4 or HMOE_FMT_NF3 */
+  int act_dtype; /* hmoe_act_dtype (fp16 ranges as for the layer); 0 is bf16 */
 } hmoe_linear_desc;
 
 typedef struct hmoe_linear hmoe_linear; /* opaque host handle: no device memory */
@@ -354,14 +376,16 @@ hmoe_status hmoe_linear_workspace_size(const hmoe_linear_desc* desc, int max_tok
 hmoe_status hmoe_linear_pack(const hmoe_linear_desc* desc, const void* codes, const void* scales,
                              float global_scale, void* packed, hmoe_stream_t stream, hmoe_linear** out);
 
-/* out[t][n] = bf16(sum_k x[t][k] W[n][k]). x: device bf16 [T][K]; out: device
- * bf16 [T][N], fully overwritten; both 16-byte aligned. T = 0 is valid. */
+/* out[t][n] = act(sum_k x[t][k] W[n][k]). x: device [T][K] and out: device
+ * [T][N], both of the activation type (act), out fully overwritten; both
+ * 16-byte aligned. T = 0 is valid. */
 hmoe_status hmoe_linear_forward(const hmoe_linear* linear, const void* x, int T, void* out, void* ws,
                                 size_t ws_bytes, hmoe_stream_t stream);
 
 /* With options: path (HMOE_PATH_AUTO chooses the streaming kernel for T <= 8),
- * wait_limit_us and debug_flags as for hmoe_forward_ex; tier_order and
- * stage_events are ignored. */
+ * wait_limit_us and debug_flags as for hmoe_forward_ex (HMOE_DEBUG_GROUPED_PAIR
+ * with fp16 is HMOE_ERR_INVALID_ARG); tier_order and stage_events are
+ * ignored. */
 hmoe_status hmoe_linear_forward_ex(const hmoe_linear* linear, const void* x, int T, void* out, void* ws,
                                    size_t ws_bytes, const hmoe_forward_opts* opts, hmoe_stream_t stream);
 

@@ -20,14 +20,14 @@ import torch
 from . import _lib
 from ._lib import (FMT_MXFP4, FMT_NF3, FMT_NVFP4, PATH_AUTO, PATH_GROUPED, PATH_STREAM,  # noqa: F401
                    TIERS_KEPT_FIRST, TIERS_NF3_FIRST, TIERS_ONE_LAUNCH, HmoeError, LayerDesc, LinearDesc,
-                   DEBUG_NO_COPIES, DEBUG_GROUPED_PAIR)
+                   DEBUG_NO_COPIES, DEBUG_GROUPED_PAIR, ACT_BF16, ACT_F16)
 
 __all__ = [
     "LayerDesc", "HmoeError", "hmoe_packed_size", "hmoe_workspace_size", "hmoe_workspace_init",
     "hmoe_pack_weights", "hmoe_plan_routes", "hmoe_forward", "hmoe_check_device_status",
     "hmoe_debug_dequant", "hmoe_debug_decode_operand", "HybridMoELayer", "library_path",
     "LinearDesc", "hmoe_linear_packed_size", "hmoe_linear_workspace_size", "hmoe_linear_pack", "hmoe_linear_forward",
-    "LinearW4A16",
+    "LinearW4A16", "ACT_BF16", "ACT_F16", "act_torch_dtype",
 ]
 
 
@@ -44,8 +44,13 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _desc(H, I, E, topk, kept_format=FMT_NVFP4):
-    return LayerDesc(H, I, E, topk, kept_format)
+def _desc(H, I, E, topk, kept_format=FMT_NVFP4, act_dtype=ACT_BF16):
+    return LayerDesc(H, I, E, topk, kept_format, act_dtype)
+
+
+def act_torch_dtype(act_dtype):
+    """The torch dtype of x, h and out for an ACT_* value."""
+    return {ACT_BF16: torch.bfloat16, ACT_F16: torch.float16}[int(act_dtype)]
 
 
 def _bitmap_arg(bit_map):
@@ -149,7 +154,8 @@ def hmoe_debug_dequant(layer, expert, which, dst, stream=None):
 
 
 def hmoe_debug_decode_operand(layer, expert, which, dst, scales, stream=None):
-    """The weight-streaming kernel's operand (dst bf16 [N, K]) and per-64-group factors (scales fp32 [N, K/64])."""
+    """The weight-streaming kernel's operand (dst [N, K] of the activation type) and per-64-group
+    factors (scales fp32 [N, K/64])."""
     _lib.check(_lib.lib().hmoe_debug_decode_operand(layer.handle, int(expert), int(which), _ptr(dst), _ptr(scales),
                                                     _stream(stream)))
 
@@ -157,13 +163,15 @@ def hmoe_debug_decode_operand(layer, expert, which, dst, scales, stream=None):
 class HybridMoELayer:
     """One hybrid MoE layer with its packed tier buffers and workspace owned as torch tensors.
 
-    desc_args: H, I, E, topk, kept_format. bit_map: per-expert 4/3 list, or
-    None for uniform. experts: as in hmoe_pack_weights. max_tokens sizes the
-    workspace.
+    desc_args: H, I, E, topk, kept_format, act_dtype. bit_map: per-expert 4/3
+    list, or None for uniform. experts: as in hmoe_pack_weights. max_tokens
+    sizes the workspace.
     """
 
-    def __init__(self, H, I, E, topk, bit_map, experts, kept_format=FMT_NVFP4, max_tokens=8, device="cuda"):
-        self.desc = _desc(H, I, E, topk, kept_format)
+    def __init__(self, H, I, E, topk, bit_map, experts, kept_format=FMT_NVFP4, max_tokens=8, device="cuda",
+                 act_dtype=ACT_BF16):
+        self.desc = _desc(H, I, E, topk, kept_format, act_dtype)
+        self.dtype = act_torch_dtype(act_dtype)
         kb, nb = hmoe_packed_size(self.desc, bit_map)
         self.kept_buf = torch.empty(max(kb, 16), dtype=torch.uint8, device=device) if kb else None
         self.nf3_buf = torch.empty(max(nb, 16), dtype=torch.uint8, device=device) if nb else None
@@ -188,7 +196,7 @@ class HybridMoELayer:
     def __call__(self, x, logits, tier_order=TIERS_ONE_LAUNCH, path=PATH_AUTO, out=None):
         ids, gates, perm, offsets = self.plan(logits)
         if out is None:
-            out = torch.empty((x.shape[0], self.H), dtype=torch.bfloat16, device=x.device)
+            out = torch.empty((x.shape[0], self.H), dtype=self.dtype, device=x.device)
         hmoe_forward(self.layer, x, ids, gates, perm, offsets, out, self.ws, tier_order=tier_order, path=path)
         return out
 
@@ -250,8 +258,9 @@ class LinearW4A16:
     (include/hmoe.h); global_scale: the NVFP4 global scale (ignored otherwise).
     """
 
-    def __init__(self, N, K, fmt, codes, scales, global_scale=1.0, max_tokens=8, device="cuda"):
-        self.desc = LinearDesc(N, K, fmt)
+    def __init__(self, N, K, fmt, codes, scales, global_scale=1.0, max_tokens=8, device="cuda", act_dtype=ACT_BF16):
+        self.desc = LinearDesc(N, K, fmt, act_dtype)
+        self.dtype = act_torch_dtype(act_dtype)
         self.packed = torch.empty(hmoe_linear_packed_size(self.desc), dtype=torch.uint8, device=device)
         self.linear = hmoe_linear_pack(self.desc, codes, scales, global_scale, self.packed)
         self.ws = torch.empty(hmoe_linear_workspace_size(self.desc, max_tokens), dtype=torch.uint8, device=device)
@@ -260,6 +269,6 @@ class LinearW4A16:
 
     def __call__(self, x, out=None, path=PATH_AUTO):
         if out is None:
-            out = torch.empty((x.shape[0], self.N), dtype=torch.bfloat16, device=x.device)
+            out = torch.empty((x.shape[0], self.N), dtype=self.dtype, device=x.device)
         hmoe_linear_forward(self.linear, x, out, self.ws, path=path)
         return out

@@ -18,6 +18,7 @@ STATUS_NAMES = {
     -6: "HMOE_ERR_DEVICE_TIMEOUT", -7: "HMOE_ERR_BAD_ROUTE",
 }
 FMT_NF3, FMT_NVFP4, FMT_MXFP4 = 3, 4, 5
+ACT_BF16, ACT_F16 = 0, 1
 TIERS_ONE_LAUNCH, TIERS_KEPT_FIRST, TIERS_NF3_FIRST = 0, 1, 2
 PATH_AUTO, PATH_STREAM, PATH_GROUPED = 0, 1, 2
 DEBUG_NO_COPIES = 1
@@ -36,11 +37,11 @@ EXPORTS = (
 
 class LayerDesc(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int), ("topk", ctypes.c_int),
-                ("kept_format", ctypes.c_int)]
+                ("kept_format", ctypes.c_int), ("act_dtype", ctypes.c_int)]
 
 
 class LinearDesc(ctypes.Structure):
-    _fields_ = [("N", ctypes.c_int), ("K", ctypes.c_int), ("fmt", ctypes.c_int)]
+    _fields_ = [("N", ctypes.c_int), ("K", ctypes.c_int), ("fmt", ctypes.c_int), ("act_dtype", ctypes.c_int)]
 
 
 class ExpertSrc(ctypes.Structure):

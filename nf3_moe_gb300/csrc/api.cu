@@ -81,6 +81,8 @@ hmoe_status check_desc(const hmoe_layer_desc* d) {
   if (d->E > MAX_E) return fail(HMOE_ERR_UNSUPPORTED_SHAPE, "E=%d exceeds %d", d->E, MAX_E);
   if (d->topk > MAX_TOPK || d->topk > d->E)
     return fail(HMOE_ERR_UNSUPPORTED_SHAPE, "topk=%d must be <= min(E, %d)", d->topk, MAX_TOPK);
+  if (d->act_dtype != HMOE_ACT_BF16 && d->act_dtype != HMOE_ACT_F16)
+    return fail(HMOE_ERR_INVALID_ARG, "act_dtype must be HMOE_ACT_BF16 (0) or HMOE_ACT_F16 (1), got %d", d->act_dtype);
   return HMOE_OK;
 }
 
@@ -263,11 +265,12 @@ hmoe_status hmoe_pack_weights(const hmoe_layer_desc* desc, const int8_t* bit_map
     L->tab.g13[e] = fmt == FMT_NVFP4 ? src[e].w13_global : 1.0f;
     L->tab.g2[e] = fmt == FMT_NVFP4 ? src[e].w2_global : 1.0f;
     const ExpertGeom& g = kept ? L->gk : L->gn;
+    const bool nibbles = desc->act_dtype == HMOE_ACT_F16;
     ce = launch_pack_matrix(fmt, 13, src[e].w13_codes, src[e].w13_scales, 2 * desc->I, desc->H, desc->I, dst,
-                            (cudaStream_t)stream);
+                            nibbles, (cudaStream_t)stream);
     if (ce == cudaSuccess)
       ce = launch_pack_matrix(fmt, 2, src[e].w2_codes, src[e].w2_scales, desc->H, desc->I, desc->I,
-                              dst + g.w13_bytes, (cudaStream_t)stream);
+                              dst + g.w13_bytes, nibbles, (cudaStream_t)stream);
     if (ce != cudaSuccess) {
       delete L;
       return cuda_fail(ce, "pack kernel launch");
@@ -327,6 +330,7 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
   p.kept_buf = L->kept_buf;
   p.nf3_buf = L->nf3_buf;
   p.kept_fmt = d.kept_format;
+  p.act_type = d.act_dtype;
   p.H = d.H;
   p.I = d.I;
   p.E = d.E;
@@ -339,7 +343,7 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
   p.perm = perm;
   p.status = reinterpret_cast<int*>(wsb + w.status);
   p.done13 = reinterpret_cast<int*>(wsb + w.done13);
-  p.h_out = reinterpret_cast<__nv_bfloat16*>(wsb + w.h);
+  p.h_out = reinterpret_cast<uint16_t*>(wsb + w.h);
   p.y_out = reinterpret_cast<float*>(wsb + w.y);
   p.tab = L->tab;
   p.wait_limit_ns = o.wait_limit_us > 0 ? (unsigned long long)o.wait_limit_us * 1000ull : WAIT_LIMIT_NS;
@@ -366,7 +370,7 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
     P.RT = P.rows / TILE_ROWS;
     P.KB = P.K / TILE_K;
     P.kbs = pick_stage(P.KB);
-    P.act = f == 0 ? static_cast<const __nv_bfloat16*>(x) : p.h_out;
+    P.act = f == 0 ? static_cast<const uint16_t*>(x) : p.h_out;
     P.act_stride = f == 0 ? d.H : d.I;
     P.kept_off = f == 0 ? 0 : L->gk.w13_bytes;
     P.nf3_off = f == 0 ? 0 : L->gn.w13_bytes;
@@ -393,7 +397,7 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
     if (e == cudaSuccess && fused) e = mark(2);
     if (e != cudaSuccess) return cuda_fail(e, "stage event record");
   }
-  cudaError_t e = launch_finalize(p.y_out, gates, T, d.topk, d.H, static_cast<__nv_bfloat16*>(out), st);
+  cudaError_t e = launch_finalize(p.y_out, gates, T, d.topk, d.H, static_cast<uint16_t*>(out), d.act_dtype, st);
   if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
   if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "stage event record");
   return HMOE_OK;
@@ -408,6 +412,7 @@ static hmoe_status run_grouped_path(const hmoe_layer* L, const void* x, int T, c
   p.kept_buf = L->kept_buf;
   p.nf3_buf = L->nf3_buf;
   p.kept_fmt = d.kept_format;
+  p.act_type = d.act_dtype;
   p.H = d.H;
   p.I = d.I;
   p.E = d.E;
@@ -420,12 +425,12 @@ static hmoe_status run_grouped_path(const hmoe_layer* L, const void* x, int T, c
   p.offsets = offsets;
   p.perm = perm;
   p.status = reinterpret_cast<int*>(wsb + w.status);
-  p.h_out = reinterpret_cast<__nv_bfloat16*>(wsb + w.h);
+  p.h_out = reinterpret_cast<uint16_t*>(wsb + w.h);
   p.y_out = reinterpret_cast<float*>(wsb + w.y);
   p.wait_limit_ns = o.wait_limit_us > 0 ? (unsigned long long)o.wait_limit_us * 1000ull : WAIT_LIMIT_NS;
   p.pair = (o.debug_flags & HMOE_DEBUG_GROUPED_PAIR) ? 1 : 0;
   p.tab = L->tab;
-  __nv_bfloat16* xg = reinterpret_cast<__nv_bfloat16*>(wsb + w.xg);
+  uint16_t* xg = reinterpret_cast<uint16_t*>(wsb + w.xg);
   auto mark = [&](int i) -> cudaError_t {
     if (o.stage_events && i < o.n_stage_events && o.stage_events[i])
       return record_stage_event((cudaEvent_t)o.stage_events[i], st);
@@ -439,7 +444,7 @@ static hmoe_status run_grouped_path(const hmoe_layer* L, const void* x, int T, c
     masks[0] = 2;
     masks[1] = 1;
   }
-  cudaError_t e = launch_gather_rows(static_cast<const __nv_bfloat16*>(x), perm, S, d.topk, T, d.H, xg, p.status,
+  cudaError_t e = launch_gather_rows(static_cast<const uint16_t*>(x), perm, S, d.topk, T, d.H, xg, p.status,
                                      L->num_sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "gather launch");
   if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "stage event record");
@@ -448,7 +453,7 @@ static hmoe_status run_grouped_path(const hmoe_layer* L, const void* x, int T, c
     p.K = which == 13 ? d.H : d.I;
     p.RT = (which == 13 ? 2 * d.I : d.H) / TILE_ROWS;
     p.KB = p.K / TILE_K;
-    const __nv_bfloat16* b = which == 13 ? xg : p.h_out;
+    const uint16_t* b = which == 13 ? xg : p.h_out;
     for (int m : masks) {
       if (!m) continue;
       p.tier_mask = m;
@@ -457,7 +462,7 @@ static hmoe_status run_grouped_path(const hmoe_layer* L, const void* x, int T, c
     }
     if ((e = mark(which == 13 ? 1 : 2)) != cudaSuccess) return cuda_fail(e, "stage event record");
   }
-  e = launch_finalize(p.y_out, gates, T, d.topk, d.H, static_cast<__nv_bfloat16*>(out), st);
+  e = launch_finalize(p.y_out, gates, T, d.topk, d.H, static_cast<uint16_t*>(out), d.act_dtype, st);
   if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
   if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "stage event record");
   return HMOE_OK;
@@ -485,6 +490,8 @@ hmoe_status check_forward(const hmoe_layer* L, const void* x, int T, const int32
   if (*grouped && T <= DECODE_MAX_T)
     return fail(HMOE_ERR_INVALID_ARG, "the grouped path needs T > %d (the workspace holds no gather buffer below)",
                 DECODE_MAX_T);
+  if ((o.debug_flags & HMOE_DEBUG_GROUPED_PAIR) && L->d.act_dtype != HMOE_ACT_BF16)
+    return fail(HMOE_ERR_INVALID_ARG, "the CTA-pair grouped kernel takes bf16 activations only");
   return HMOE_OK;
 }
 
@@ -544,7 +551,7 @@ hmoe_status debug_export(const hmoe_layer* L, int expert, int which, void* dst, 
   const int N = which == 13 ? 2 * L->d.I : L->d.H;
   const int K = which == 13 ? L->d.H : L->d.I;
   cudaError_t e = launch_debug_dequant(fmt, which, base + (which == 2 ? g.w13_bytes : 0), N, K, L->d.I, dst, scales,
-                                       decode_operand, st);
+                                       decode_operand, L->d.act_dtype, st);
   if (e != cudaSuccess) return cuda_fail(e, "debug dequant launch");
   return HMOE_OK;
 }
@@ -633,11 +640,12 @@ hmoe_status hmoe_check_device_status_static(hmoe_stream_t stream) {
 }  // extern "C"
 
 // ------------------------------------------------------------ dense Linear W4A16
-// One weight matrix W [N, K] (NVFP4, MXFP4 or NF3) times bf16 activations,
-// run by the layer's own kernels: the matrix is packed like an expert's W2,
-// and a forward is the W2 phase of the streaming kernel (T <= 8) or of the
-// tensor-core grouped kernel (above) over a one-expert route geometry with
-// one slot per token and gate 1, then the finalize to bf16.
+// One weight matrix W [N, K] (NVFP4, MXFP4 or NF3) times bf16 or fp16
+// activations, run by the layer's own kernels: the matrix is packed like an
+// expert's W2, and a forward is the W2 phase of the streaming kernel
+// (T <= 8) or of the tensor-core grouped kernel (above) over a one-expert
+// route geometry with one slot per token and gate 1, then the finalize to
+// the activation type.
 struct hmoe_linear {
   hmoe_linear_desc d;
   uint8_t* packed;
@@ -675,6 +683,8 @@ hmoe_status check_linear_desc(const hmoe_linear_desc* d) {
   if (d->N <= 0 || d->K <= 0) return fail(HMOE_ERR_INVALID_ARG, "N and K must be positive");
   if (d->N % 128 != 0 || d->K % 64 != 0)
     return fail(HMOE_ERR_UNSUPPORTED_SHAPE, "N must be a multiple of 128 and K of 64 (N=%d K=%d)", d->N, d->K);
+  if (d->act_dtype != HMOE_ACT_BF16 && d->act_dtype != HMOE_ACT_F16)
+    return fail(HMOE_ERR_INVALID_ARG, "act_dtype must be HMOE_ACT_BF16 (0) or HMOE_ACT_F16 (1), got %d", d->act_dtype);
   return HMOE_OK;
 }
 }  // namespace
@@ -713,7 +723,8 @@ hmoe_status hmoe_linear_pack(const hmoe_linear_desc* desc, const void* codes, co
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (ce == cudaSuccess)
-    ce = launch_pack_matrix(desc->fmt, 2, codes, scales, desc->N, desc->K, desc->K, L->packed, (cudaStream_t)stream);
+    ce = launch_pack_matrix(desc->fmt, 2, codes, scales, desc->N, desc->K, desc->K, L->packed,
+                            desc->act_dtype == HMOE_ACT_F16, (cudaStream_t)stream);
   if (ce != cudaSuccess) {
     delete L;
     return cuda_fail(ce, "linear pack");
@@ -735,6 +746,8 @@ hmoe_status hmoe_linear_forward_ex(const hmoe_linear* L, const void* x, int T, v
   const hmoe_forward_opts o = opts ? *opts : kDefaultOpts;
   if (o.path < 0 || o.path > 2) return fail(HMOE_ERR_INVALID_ARG, "bad path %d", o.path);
   if (o.wait_limit_us < 0) return fail(HMOE_ERR_INVALID_ARG, "wait_limit_us < 0");
+  if ((o.debug_flags & HMOE_DEBUG_GROUPED_PAIR) && L->d.act_dtype != HMOE_ACT_BF16)
+    return fail(HMOE_ERR_INVALID_ARG, "the CTA-pair grouped kernel takes bf16 activations only");
   if (!ws) return fail(HMOE_ERR_INVALID_ARG, "workspace is NULL");
   if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return fail(HMOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   const LinWs w = lin_layout(L->d, T);
@@ -761,6 +774,7 @@ hmoe_status hmoe_linear_forward_ex(const hmoe_linear* L, const void* x, int T, v
     p.kept_buf = L->packed;
     p.nf3_buf = L->packed;
     p.kept_fmt = kept_fmt;
+    p.act_type = L->d.act_dtype;
     p.which = 2;
     p.H = L->d.N;
     p.I = L->d.K;
@@ -779,13 +793,14 @@ hmoe_status hmoe_linear_forward_ex(const hmoe_linear* L, const void* x, int T, v
     p.wait_limit_ns = lim;
     p.pair = (o.debug_flags & HMOE_DEBUG_GROUPED_PAIR) ? 1 : 0;
     p.tab = L->tab;
-    e = launch_grouped_gemm(p, static_cast<const __nv_bfloat16*>(x), T, L->num_sms, st);
+    e = launch_grouped_gemm(p, static_cast<const uint16_t*>(x), T, L->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "linear grouped GEMM launch");
   } else {
     StreamParams p{};
     p.kept_buf = L->packed;
     p.nf3_buf = L->packed;
     p.kept_fmt = kept_fmt;
+    p.act_type = L->d.act_dtype;
     p.H = L->d.N;
     p.I = L->d.K;
     p.E = 1;
@@ -809,7 +824,7 @@ hmoe_status hmoe_linear_forward_ex(const hmoe_linear* L, const void* x, int T, v
     P.RT = L->d.N / TILE_ROWS;
     P.KB = L->d.K / TILE_K;
     P.kbs = pick_stage(P.KB);
-    P.act = static_cast<const __nv_bfloat16*>(x);
+    P.act = static_cast<const uint16_t*>(x);
     P.act_stride = L->d.K;
     P.kept_off = P.nf3_off = 0;
     p.ph[0] = P;
@@ -818,7 +833,7 @@ hmoe_status hmoe_linear_forward_ex(const hmoe_linear* L, const void* x, int T, v
     e = launch_stream_gemm(p, stream_grid(L->num_sms), st);
     if (e != cudaSuccess) return cuda_fail(e, "linear stream GEMM launch");
   }
-  e = launch_finalize(y, gates, T, 1, L->d.N, static_cast<__nv_bfloat16*>(out), st);
+  e = launch_finalize(y, gates, T, 1, L->d.N, static_cast<uint16_t*>(out), L->d.act_dtype, st);
   if (e != cudaSuccess) return cuda_fail(e, "linear finalize launch");
   return HMOE_OK;
 }

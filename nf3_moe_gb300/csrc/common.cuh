@@ -33,6 +33,7 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace hmoe {
@@ -67,6 +68,17 @@ constexpr uint32_t NF3_HI0 = 0x00BEBFBFu, NF3_HI1 = 0x3F3F3E3Eu;
 // E2M1 magnitudes {0,.5,1,1.5,2,3,4,6} as bf16: low bytes and high bytes.
 constexpr uint32_t E2M1_LO0 = 0xC0800000u, E2M1_LO1 = 0xC0804000u;
 constexpr uint32_t E2M1_HI0 = 0x3F3F3F00u, E2M1_HI1 = 0x40404040u;
+
+// Activation (operand) types: the MMA operands, h and the output are bf16 or
+// fp16; the weights are decoded to the same type.
+constexpr int ACT_BF16 = 0, ACT_F16 = 1;
+// The same tables for fp16 operands. The E2M1 magnitudes in fp16 have zero
+// low bytes ({0000, 3800, 3C00, 3E00, 4000, 4200, 4400, 4600}), so one table
+// of high bytes serves; the NF3 entries in fp16 are the bf16 values exactly
+// ({BC00, B848, B3E8, 0000, 31E0, 3620, 38F8, 3C00}).
+constexpr uint32_t E2M1F_HI0 = 0x3E3C3800u, E2M1F_HI1 = 0x46444240u;
+constexpr uint32_t NF3F_LO0 = 0x00E84800u, NF3F_LO1 = 0x00F820E0u;
+constexpr uint32_t NF3F_HI0 = 0x00B3B8BCu, NF3F_HI1 = 0x3C383631u;
 
 // ---------------------------------------------------------------- generic helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -278,6 +290,40 @@ __device__ __forceinline__ uint16_t e8m0_to_bf16(uint32_t byte) {
 }
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+template <int ACT>
+__device__ __forceinline__ uint32_t mul_x2(uint32_t a, uint32_t b) {
+  if constexpr (ACT == ACT_F16) return f16x2_mul(a, b);
+  else return bf16x2_mul(a, b);
+}
+// fp32 -> fp16 bits, round to nearest even (exact for the values used here).
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float f) { return __half_as_ushort(__float2half_rn(f)); }
+// E4M3 byte -> fp16 bits (exact: every E4M3 value is an fp16 value).
+__device__ __forceinline__ uint16_t e4m3_to_f16(uint32_t byte) {
+  return f32_to_f16_bits(bf16_bits_to_float(e4m3_to_bf16(byte)));
+}
+// E8M0 byte -> fp16 bits of 2^(b-127). Exact for b in 103..142 (fp16
+// subnormals included); outside that range the scale is unsupported for fp16
+// operands (rounds to 0 or to infinity).
+__device__ __forceinline__ uint16_t e8m0_to_f16(uint32_t byte) {
+  if (byte == 0 || byte == 255) return byte ? 0x7E00 : 0;
+  return f32_to_f16_bits(__uint_as_float(byte << 23));
+}
+// Output conversions of the fp32 results.
+template <int ACT>
+__device__ __forceinline__ uint16_t f32_to_act(float f) {
+  if constexpr (ACT == ACT_F16) return __half_as_ushort(__float2half_rn(f));
+  else return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+template <int ACT>
+__device__ __forceinline__ uint32_t f32x2_to_act(float a, float b) {
+  return (uint32_t)f32_to_act<ACT>(a) | ((uint32_t)f32_to_act<ACT>(b) << 16);
+}
+
 // ---------------------------------------------------------------- code word decoders
 // 8 E2M1 codes (word layout in the header comment) -> 4 bf16x2 (codes 0,1 | 2,3 | 4,5 | 6,7).
 __device__ __forceinline__ void e2m1x8_to_bf16x2(uint32_t w, uint32_t* p) {
@@ -321,6 +367,32 @@ __device__ __forceinline__ void nf3x8_to_bf16x2(uint32_t sel, uint32_t* p) {
   p[3] = __byte_perm(lo, hi, 0x7362);
 }
 
+// 8 E2M1 codes (the nibble word layout of e2m1x8_to_bf16x2) -> 4 fp16x2.
+// The fp16 values have zero low bytes: one lookup of high bytes, the sign
+// OR-ed in, and two byte permutations that interleave zero low bytes.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t* p) {
+  const uint32_t m = w & 0x77777777u;
+  const uint32_t hi = __byte_perm(E2M1F_HI0, E2M1F_HI1, m) | (w & 0x80808080u);
+  p[0] = __byte_perm(hi, 0u, 0x1404);
+  p[1] = __byte_perm(hi, 0u, 0x3424);
+  const uint32_t hi2 = __byte_perm(E2M1F_HI0, E2M1F_HI1, m >> 16) | ((w << 4) & 0x80808080u);
+  p[2] = __byte_perm(hi2, 0u, 0x1404);
+  p[3] = __byte_perm(hi2, 0u, 0x3424);
+}
+
+// 8 NF3 codes held as selector nibbles -> 4 fp16x2 (table values, unscaled).
+__device__ __forceinline__ void nf3x8_to_f16x2(uint32_t sel, uint32_t* p) {
+  uint32_t lo = __byte_perm(NF3F_LO0, NF3F_LO1, sel);
+  uint32_t hi = __byte_perm(NF3F_HI0, NF3F_HI1, sel);
+  p[0] = __byte_perm(lo, hi, 0x5140);
+  p[1] = __byte_perm(lo, hi, 0x7362);
+  sel >>= 16;
+  lo = __byte_perm(NF3F_LO0, NF3F_LO1, sel);
+  hi = __byte_perm(NF3F_HI0, NF3F_HI1, sel);
+  p[2] = __byte_perm(lo, hi, 0x5140);
+  p[3] = __byte_perm(lo, hi, 0x7362);
+}
+
 // NF3 words A, B, C of one thread slot -> selector words for R0 codes 0..7,
 // R0 8..15, R1 0..7 and R1 8..15.
 __device__ __forceinline__ void nf3_selectors(uint32_t A, uint32_t B, uint32_t C, uint32_t* s) {
@@ -332,19 +404,27 @@ __device__ __forceinline__ void nf3_selectors(uint32_t A, uint32_t B, uint32_t C
 }
 
 // Load one thread slot's packed data from a tile in shared memory and
-// produce its dequantised bf16x2 operands: r0[8] for row R0 (k pairs in
-// order) and r1[8] for row R1. With with_nf3_scale == false the NF3 values
-// are raw codebook entries, and scale0/scale1 return the two row scales as
-// floats for the caller to apply to fp32 sums. Otherwise every format's
-// values come out multiplied by their scale in bf16 (the "tile" values);
-// NVFP4 tile values come out times 2^-63 (see e2m1s_to_bf16x2).
-// e4m3_lut: the 256-entry table of E4M3 -> bf16 pairs times 2^63 (the value
-// in both halves; shared memory, built by every kernel that decodes NVFP4
-// with e4m3_lut_entry), indexed by the scale bytes directly.
+// produce its dequantised operand pairs (bf16x2 or fp16x2 by ACT): r0[8] for
+// row R0 (k pairs in order) and r1[8] for row R1. With with_nf3_scale ==
+// false the NF3 values are raw codebook entries, and scale0/scale1 return the
+// two row scales as floats for the caller to apply to fp32 sums. Otherwise
+// every format's values come out multiplied by their scale (the "tile"
+// values; NF3 rounded once to the operand type). NVFP4 tile values in bf16
+// come out times 2^-63 (see e2m1s_to_bf16x2; nvfp4_unscale<ACT> returns the
+// factor), in fp16 exactly.
+// e4m3_lut: the 256-entry table of E4M3 scale pairs of the operand type,
+// built by every kernel that decodes NVFP4 with e4m3_lut_entry<ACT>, indexed
+// by the scale bytes directly (shared memory).
+template <int ACT>
 __device__ __forceinline__ uint32_t e4m3_lut_entry(uint32_t byte) {
-  return bf16x2_mul(bf16_bcast(e4m3_to_bf16(byte)), BF16X2_2P63);
+  if constexpr (ACT == ACT_F16) return bf16_bcast(e4m3_to_f16(byte));
+  else return bf16x2_mul(bf16_bcast(e4m3_to_bf16(byte)), BF16X2_2P63);
 }
-template <int FMT, bool WITH_NF3_SCALE>
+template <int ACT>
+__host__ __device__ constexpr float nvfp4_unscale() {
+  return ACT == ACT_F16 ? 1.0f : NVFP4_UNSCALE;
+}
+template <int FMT, bool WITH_NF3_SCALE, int ACT = ACT_BF16>
 __device__ __forceinline__ void dequant_slot(const uint8_t* tile, int rg, int lane, uint32_t* r0, uint32_t* r1,
                                              float* scale0, float* scale1, const uint32_t* e4m3_lut) {
   const int slot = rg * 32 + lane;
@@ -352,16 +432,26 @@ __device__ __forceinline__ void dequant_slot(const uint8_t* tile, int rg, int la
     const uint4 q = *reinterpret_cast<const uint4*>(tile + slot * 16);
     uint32_t s0, s1;
     if constexpr (FMT == FMT_NVFP4) {
-      // Scales carry the factor 2^63 (see e2m1s_to_bf16x2).
       s0 = e4m3_lut[tile[4096 + slot * 2]];
       s1 = e4m3_lut[tile[4096 + slot * 2 + 1]];
     } else {
       const int g = lane >> 2, hq = (lane & 3) >> 1;
       const uint32_t sc = *reinterpret_cast<const uint16_t*>(tile + 4096 + (rg * 16 + g * 2 + hq) * 2);
-      s0 = bf16_bcast(e8m0_to_bf16(sc & 0xFFu));
-      s1 = bf16_bcast(e8m0_to_bf16(sc >> 8));
+      if constexpr (ACT == ACT_F16) {
+        s0 = bf16_bcast(e8m0_to_f16(sc & 0xFFu));
+        s1 = bf16_bcast(e8m0_to_f16(sc >> 8));
+      } else {
+        s0 = bf16_bcast(e8m0_to_bf16(sc & 0xFFu));
+        s1 = bf16_bcast(e8m0_to_bf16(sc >> 8));
+      }
     }
-    if constexpr (FMT == FMT_NVFP4) {
+    if constexpr (ACT == ACT_F16) {
+      // fp16 layers store NVFP4 codes in the nibble layout of MXFP4.
+      e2m1x8_to_f16x2(q.x, r0);
+      e2m1x8_to_f16x2(q.y, r0 + 4);
+      e2m1x8_to_f16x2(q.z, r1);
+      e2m1x8_to_f16x2(q.w, r1 + 4);
+    } else if constexpr (FMT == FMT_NVFP4) {
       e2m1s_to_bf16x2(q.x, r0);
       e2m1s_to_bf16x2(q.y, r0 + 4);
       e2m1s_to_bf16x2(q.z, r1);
@@ -374,8 +464,8 @@ __device__ __forceinline__ void dequant_slot(const uint8_t* tile, int rg, int la
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      r0[i] = bf16x2_mul(r0[i], s0);
-      r1[i] = bf16x2_mul(r1[i], s1);
+      r0[i] = mul_x2<ACT>(r0[i], s0);
+      r1[i] = mul_x2<ACT>(r1[i], s1);
     }
     *scale0 = 1.0f;
     *scale1 = 1.0f;
@@ -388,16 +478,31 @@ __device__ __forceinline__ void dequant_slot(const uint8_t* tile, int rg, int la
     const uint32_t sb1 = *reinterpret_cast<const uint16_t*>(tile + 3072 + (rg * 16 + g + 8) * 2);
     uint32_t s[4];
     nf3_selectors(A, B, C, s);
-    nf3x8_to_bf16x2(s[0], r0);
-    nf3x8_to_bf16x2(s[1], r0 + 4);
-    nf3x8_to_bf16x2(s[2], r1);
-    nf3x8_to_bf16x2(s[3], r1 + 4);
+    if constexpr (ACT == ACT_F16) {
+      nf3x8_to_f16x2(s[0], r0);
+      nf3x8_to_f16x2(s[1], r0 + 4);
+      nf3x8_to_f16x2(s[2], r1);
+      nf3x8_to_f16x2(s[3], r1 + 4);
+    } else {
+      nf3x8_to_bf16x2(s[0], r0);
+      nf3x8_to_bf16x2(s[1], r0 + 4);
+      nf3x8_to_bf16x2(s[2], r1);
+      nf3x8_to_bf16x2(s[3], r1 + 4);
+    }
     if constexpr (WITH_NF3_SCALE) {
-      const uint32_t S0 = bf16_bcast((uint16_t)sb0), S1 = bf16_bcast((uint16_t)sb1);
+      uint32_t S0, S1;
+      if constexpr (ACT == ACT_F16) {
+        // the bf16 scale as fp16 (exact for scales in the fp16 normal range)
+        S0 = bf16_bcast(f32_to_f16_bits(bf16_bits_to_float(sb0)));
+        S1 = bf16_bcast(f32_to_f16_bits(bf16_bits_to_float(sb1)));
+      } else {
+        S0 = bf16_bcast((uint16_t)sb0);
+        S1 = bf16_bcast((uint16_t)sb1);
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        r0[i] = bf16x2_mul(r0[i], S0);
-        r1[i] = bf16x2_mul(r1[i], S1);
+        r0[i] = mul_x2<ACT>(r0[i], S0);
+        r1[i] = mul_x2<ACT>(r1[i], S1);
       }
       *scale0 = 1.0f;
       *scale1 = 1.0f;
@@ -409,23 +514,39 @@ __device__ __forceinline__ void dequant_slot(const uint8_t* tile, int rg, int la
 }
 
 // ---------------------------------------------------------------- mma.sync (decode path)
-__device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+template <int ACT = ACT_BF16>
+__device__ __forceinline__ void mma_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                          uint32_t b1) {
+  if constexpr (ACT == ACT_F16)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // The same MMA with a zero accumulator input (d = a * b).
-__device__ __forceinline__ void mma_bf16_16816_zc(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                                  uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%10,%10,%10,%10};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+template <int ACT = ACT_BF16>
+__device__ __forceinline__ void mma_16816_zc(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+  if constexpr (ACT == ACT_F16)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }

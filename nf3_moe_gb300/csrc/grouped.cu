@@ -8,39 +8,45 @@
 //
 // One persistent CTA per SM takes work items (expert e, token tile nt of up
 // to 128 permuted slots, a pair of weight row tiles rt, rt+1 of 128 rows
-// each), with row-tile pairs fastest. Both row tiles of an item multiply
-// the same activation tile, so each activation tile is read from L2 once per
-// 256 weight rows; the CTAs running together also share it through L2. An
-// expert's token tiles follow each other, so its weight tiles are re-read
-// from L2 rather than HBM.
+// each), with row-tile pairs fastest. The tokens sit on the MMA's M side
+// (A = the activation tile, 128 x 64 per k-block) and the two dequantised
+// weight row tiles on its N side (B, 256 x 64), so one MMA covers both row
+// tiles and each activation tile is read from L2 once per 256 weight rows;
+// the CTAs running together also share it through L2. An expert's token
+// tiles follow each other, so its weight tiles are re-read from L2 rather
+// than HBM.
 //
-// Warp roles (24 warps):
-//   warp 0       packed-weight producer. 1D bulk copies of each k-block's
-//                two packed tiles (64 K each) into a 4-deep ring.
-//   warp 2       activation producer. A 2D TMA tensor load (128 rows x 64
-//                bf16, 128B swizzle) into the k-block's operand slot (a
-//                3-deep ring whose slots also hold the dequantised weight
-//                tiles), plus an L2 prefetch of the tile needed 8 k-blocks
-//                later.
-//   warps 1, 23  MMA issuers (warp 1 also allocates 512 TMEM columns).
-//                Issuing a tcgen05.mma costs the issuing thread about 100
-//                cycles, so each row tile has its own issuing lane: per
-//                k-block it issues 4 tcgen05.mma.kind::f16 (M=128, N = token
-//                count rounded up to 16, K=16) into its row tile's fp32
-//                accumulator, double-buffered in TMEM. Both issuers'
-//                tcgen05.commits free the operand slot (one commit each per
-//                k-block).
-//   warps 3..18  dequantisers, in two groups of 8 that take alternate
+// Operand type: bf16 or fp16 (template parameter ACT). Activations, the
+// dequantised weights, h and the output are all of that type; tcgen05.mma
+// kind::f16 takes A and B of the same type, so the instruction descriptor
+// names it for both.
+//
+// Warp roles (24 warps; the role of warp w is chosen by its SM
+// sub-partition w % 4, see GT_WARP_*):
+//   warp 5       packed-weight producer. 1D bulk copies of each k-block's
+//                two packed tiles (64 K each) into an 8-deep ring.
+//   warp 9       activation producer. A 2D TMA tensor load (128 rows x 64,
+//                128B swizzle) into the k-block's operand slot (a 3-deep
+//                ring whose slots also hold the dequantised weight tiles),
+//                completing on the slot's barrier, plus an L2 prefetch of
+//                the tile needed 8 k-blocks later.
+//   warp 1       MMA issuer (also allocates 512 TMEM columns). Per k-block:
+//                one wait on the operand slot, 4 tcgen05.mma.kind::f16
+//                (M = 128 tokens, N = 256 weight rows, K = 16) into a
+//                double-buffered fp32 accumulator, one tcgen05.commit that
+//                frees the slot.
+//   16 warps     dequantisers, in two groups of 8 that take alternate
 //                k-blocks. Per k-block each warp expands its 16-row group of
 //                both row tiles: each thread turns one tile slot (2 rows x
-//                16 K) of each into bf16 (E2M1 x E4M3, E2M1 x 2^e, or
-//                bf16_rne(NF3 codebook x scale)) in the canonical K-major
-//                SWIZZLE_128B operand layout, then fences the async proxy.
-//   warps 19..22 epilogue. tcgen05.ld of the accumulators (each warp owns 32
-//                TMEM lanes, i.e. 32 weight rows of each row tile).
-//                W13: rows come in gate/up pairs 8 lanes apart, and one
-//                16x256b load gives a thread both, so
-//                h = bf16(silu(g13*gate) * (g13*up)) needs no shuffle.
+//                16 K) of each into the operand type (E2M1 x E4M3,
+//                E2M1 x 2^e, or the rounded product NF3 codebook x scale)
+//                in the canonical K-major SWIZZLE_128B layout, then fences
+//                the async proxy.
+//   warps 12..15 epilogue. tcgen05.ld of the accumulator: TMEM lane = token,
+//                column = weight row, so one thread holds one token's rows.
+//                W13: gate and up rows of a 16-row group sit 8 columns
+//                apart, so h = silu(g13*gate) * (g13*up) needs no shuffle
+//                and 8 channels go out in one 16-byte store.
 //                W2: y[s][row] = g2 * acc for the flat slot s = perm[p].
 // Every mbarrier wait is bounded. On a timeout the CTA records
 // DEV_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
@@ -55,9 +61,9 @@ namespace hmoe {
 
 constexpr int GT_N = 128;                 // token tile
 constexpr int GT_R = 2;                   // weight row tiles per item (they share the activation tile)
-constexpr int GT_A_TILE = 128 * 128;      // bf16 A tile 128 x 64
+constexpr int GT_A_TILE = 128 * 128;      // one dequantised weight row tile, 128 x 64 2-byte values
 constexpr int GT_A_BYTES = GT_R * GT_A_TILE;
-constexpr int GT_B_BYTES = GT_N * 128;    // bf16 B tile GT_N x 64
+constexpr int GT_B_BYTES = GT_N * 128;    // activation tile GT_N x 64 2-byte values
 constexpr int GT_P_TILE = 4608;           // largest packed tile
 constexpr int GT_P_BYTES = GT_R * GT_P_TILE;
 constexpr int GT_PSTAGES = 8;             // packed weight tiles in flight (covers the L2/HBM latency)
@@ -136,7 +142,7 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 // against issuing from inside an `if (lane == 0)` branch: a 128 x 128 x 16
 // MMA takes 65 instead of 120 cycles of the tensor core's issue slot, the
 // full rate of the tensor core, instead of half of it.
-__device__ __forceinline__ void umma_bf16_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+__device__ __forceinline__ void umma_kf16_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                                uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p, e;\n\t"
@@ -256,9 +262,12 @@ __device__ __forceinline__ uint64_t desc_from_lo(uint32_t lo) {
   return ((uint64_t)SW128_DESC_HI << 32) | (uint64_t)lo;
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
-__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor, kind::f16: D fp32, A and B of the same type (bf16,
+// type code 1, or fp16, code 0), both K-major.
+template <int ACT = ACT_BF16>
+__device__ __forceinline__ uint32_t idesc_kf16(int M, int N) {
+  constexpr uint32_t ab = ACT == ACT_F16 ? 0u : 1u;
+  return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 struct GtItem {
@@ -294,12 +303,12 @@ __device__ __forceinline__ GtItem gt_decode(const GroupedParams& p, const int* s
 // Writes one thread slot's dequantised rows (2 rows x 16 K) into the
 // canonical K-major SWIZZLE_128B tile: row r of atom (r / 8) at (r % 8) * 128,
 // 16-byte chunk c stored at chunk position c ^ (r % 8).
-template <int FMT>
+template <int FMT, int ACT = ACT_BF16>
 __device__ __forceinline__ void gt_dequant_slot(const uint8_t* ptile, uint8_t* atile, int rg, int lane,
                                                 const uint32_t* e4m3_lut) {
   uint32_t r0[8], r1[8];
   float s0, s1;
-  dequant_slot<FMT, true>(ptile, rg, lane, r0, r1, &s0, &s1, e4m3_lut);
+  dequant_slot<FMT, true, ACT>(ptile, rg, lane, r0, r1, &s0, &s1, e4m3_lut);
   const int g = lane >> 2, q = lane & 3;
   uint8_t* a0 = atile + (2 * rg) * 1024 + g * 128;
   uint8_t* a1 = atile + (2 * rg + 1) * 1024 + g * 128;
@@ -317,7 +326,7 @@ __device__ __forceinline__ void gt_dequant_slot(const uint8_t* ptile, uint8_t* a
 // row groups rg, rg + 1, ... of every row tile of its k-blocks: the waits,
 // fence and arrivals are paid once per several slots while all the warps
 // stay busy. Returns false if a bounded wait gave up.
-template <int FMT>
+template <int FMT, int ACT>
 __device__ __forceinline__ bool gt_dequant_item(int KB, int nr, int par, const uint8_t* p_base, uint8_t* a_base,
                                                 uint64_t* pfull, uint64_t* pempty, uint64_t* afull,
                                                 uint64_t* oempty, const uint32_t* s_e4m3, int rg, int lane,
@@ -332,8 +341,8 @@ __device__ __forceinline__ bool gt_dequant_item(int KB, int nr, int par, const u
       uint8_t* at = a_base + as * GT_A_BYTES;
 #pragma unroll
       for (int h = 0; h < 8 / GT_DQ_PER_GROUP; ++h) {
-        gt_dequant_slot<FMT>(pt, at, rg + h, lane, s_e4m3);
-        if (nr > 1) gt_dequant_slot<FMT>(pt + GT_P_TILE, at + GT_A_TILE, rg + h, lane, s_e4m3);
+        gt_dequant_slot<FMT, ACT>(pt, at, rg + h, lane, s_e4m3);
+        if (nr > 1) gt_dequant_slot<FMT, ACT>(pt + GT_P_TILE, at + GT_A_TILE, rg + h, lane, s_e4m3);
       }
       fence_async_smem();
       __syncwarp();
@@ -354,6 +363,7 @@ __device__ __forceinline__ bool gt_dequant_item(int KB, int nr, int par, const u
   return true;
 }
 
+template <int ACT>
 __global__ void __launch_bounds__(GT_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ GroupedParams p, const __grid_constant__ CUtensorMap tmap_b) {
   extern __shared__ uint8_t smem_raw[];
@@ -374,7 +384,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
   volatile int* s_flags = reinterpret_cast<volatile int*>(s_tmem + 1);  // [0] abort
   int* s_istart = reinterpret_cast<int*>(smem + GT_OFF_MISC);
   int* s_off = s_istart + MAX_E + 1;
-  uint32_t* s_e4m3 = reinterpret_cast<uint32_t*>(s_off + MAX_E + 1);  // E4M3 -> bf16 pair
+  uint32_t* s_e4m3 = reinterpret_cast<uint32_t*>(s_off + MAX_E + 1);  // E4M3 -> operand-type pair
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -399,7 +409,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     tmem_relinquish();
   }
   if (tid >= 96 && tid < 96 + 256)
-    s_e4m3[tid - 96] = e4m3_lut_entry((uint32_t)(tid - 96));
+    s_e4m3[tid - 96] = e4m3_lut_entry<ACT>((uint32_t)(tid - 96));
   pdl_wait();  // everything below reads or writes global memory
   pdl_trigger();
   for (int e = tid; e <= p.E; e += blockDim.x) s_off[e] = p.offsets[e];
@@ -547,7 +557,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, it.nr * 128);
+      const uint32_t idesc = idesc_kf16<ACT>(128, it.nr * 128);
       const uint32_t d_tmem = tmem_base + (uint32_t)(buf * GT_ACC_COLS);
       // Operand slots are ordered by their barrier and the writers' proxy
       // fence; the tcgen05 fence after the accumulator hand-off covers TMEM.
@@ -563,13 +573,13 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         }
         const uint32_t x_lo = x_lo0 + (uint32_t)os * (GT_B_BYTES >> 4);
         const uint32_t w_lo = w_lo0 + (uint32_t)os * (GT_A_BYTES >> 4);
-        umma_bf16_warp(d_tmem, desc_from_lo(x_lo), desc_from_lo(w_lo), idesc, kb ? 1u : 0u);
-        umma_bf16_warp(d_tmem, desc_from_lo(x_lo + 2), desc_from_lo(w_lo + 2), idesc, 1u);
+        umma_kf16_warp(d_tmem, desc_from_lo(x_lo), desc_from_lo(w_lo), idesc, kb ? 1u : 0u);
+        umma_kf16_warp(d_tmem, desc_from_lo(x_lo + 2), desc_from_lo(w_lo + 2), idesc, 1u);
         const int os_next = os + 1 == GT_OSTAGES ? 0 : os + 1;
         const uint32_t oph_next = os + 1 == GT_OSTAGES ? oph ^ 1u : oph;
         ready = kb + 1 < p.KB && __all_sync(0xffffffffu, mbar_test(&afull[os_next], oph_next));
-        umma_bf16_warp(d_tmem, desc_from_lo(x_lo + 4), desc_from_lo(w_lo + 4), idesc, 1u);
-        umma_bf16_warp(d_tmem, desc_from_lo(x_lo + 6), desc_from_lo(w_lo + 6), idesc, 1u);
+        umma_kf16_warp(d_tmem, desc_from_lo(x_lo + 4), desc_from_lo(w_lo + 4), idesc, 1u);
+        umma_kf16_warp(d_tmem, desc_from_lo(x_lo + 6), desc_from_lo(w_lo + 6), idesc, 1u);
         umma_commit_warp(&oempty[os]);
         os = os_next;
         oph = oph_next;
@@ -588,7 +598,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     }
     __syncwarp();
   } else if (GT_DQ_INDEX[warp] >= 0) {
-    // ------------------------------------------------ dequantisers: packed tile -> bf16 operand tile
+    // ------------------------------------------------ dequantisers: packed tile -> operand tile
     // Group par expands the k-blocks k with k % GT_DQ_GROUPS == par, every
     // row tile; its warps split the 8 row groups. (Eight warps each expanding
     // both row tiles of every k-block was measured slower: 4.18 against 4.03
@@ -604,13 +614,13 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
       const GtItem it = gt_decode(p, s_istart, s_off, i);
       const int fmt = gt_expert_fmt(p, it.e);
       if (fmt == FMT_NVFP4)
-        ok = gt_dequant_item<FMT_NVFP4>(p.KB, it.nr, par, p_base, a_base, pfull, pempty, afull, oempty, s_e4m3, rg,
+        ok = gt_dequant_item<FMT_NVFP4, ACT>(p.KB, it.nr, par, p_base, a_base, pfull, pempty, afull, oempty, s_e4m3, rg,
                                         lane, s_flags, lim, gk, ps, pph, as, aph);
       else if (fmt == FMT_MXFP4)
-        ok = gt_dequant_item<FMT_MXFP4>(p.KB, it.nr, par, p_base, a_base, pfull, pempty, afull, oempty, s_e4m3, rg,
+        ok = gt_dequant_item<FMT_MXFP4, ACT>(p.KB, it.nr, par, p_base, a_base, pfull, pempty, afull, oempty, s_e4m3, rg,
                                         lane, s_flags, lim, gk, ps, pph, as, aph);
       else
-        ok = gt_dequant_item<FMT_NF3>(p.KB, it.nr, par, p_base, a_base, pfull, pempty, afull, oempty, s_e4m3, rg,
+        ok = gt_dequant_item<FMT_NF3, ACT>(p.KB, it.nr, par, p_base, a_base, pfull, pempty, afull, oempty, s_e4m3, rg,
                                       lane, s_flags, lim, gk, ps, pph, as, aph);
     }
     if (!ok && lane == 0) {
@@ -655,7 +665,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         const int r0 = (q & 3) * 32;  // first tile-local row of the chunk
         if (p.which == 13) {
           if (!live) continue;
-          const float gsc = p.tab.g13[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
+          const float gsc = p.tab.g13[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f);
 #pragma unroll
           for (int g = 0; g < 2; ++g) {
             // 16-row group (r0 / 16 + g): rows 0..7 gate, 8..15 up, of channels ch .. ch + 7
@@ -667,14 +677,13 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
               const float g1 = __uint_as_float(v[16 * g + 2 * w + 1]) * gsc;
               const float u0 = __uint_as_float(v[16 * g + 8 + 2 * w]) * gsc;
               const float u1 = __uint_as_float(v[16 * g + 8 + 2 * w + 1]) * gsc;
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(silu_fast(g0) * u0, silu_fast(g1) * u1);
-              hv[w] = *reinterpret_cast<const uint32_t*>(&h2);
+              hv[w] = f32x2_to_act<ACT>(silu_fast(g0) * u0, silu_fast(g1) * u1);
             }
             *reinterpret_cast<uint4*>(p.h_out + (size_t)(it.p0 + c) * p.I + ch) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
           }
         } else {
           if (slot < 0) continue;
-          const float gsc = p.tab.g2[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
+          const float gsc = p.tab.g2[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f);
           float4* dst = reinterpret_cast<float4*>(p.y_out + (size_t)slot * p.H + rt * 128 + r0);
 #pragma unroll
           for (int w = 0; w < 8; ++w)
@@ -817,7 +826,7 @@ __device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
 }
 // Commit of the pair's MMAs: arrives once on the barrier at this offset in
 // both CTAs of the pair. Both are issued from a converged warp (elect.sync),
-// like umma_bf16_warp.
+// like umma_kf16_warp.
 __device__ __forceinline__ void umma2_commit_both(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
@@ -827,7 +836,7 @@ __device__ __forceinline__ void umma2_commit_both(uint64_t* bar) {
       "h"((uint16_t)3)
       : "memory");
 }
-__device__ __forceinline__ void umma2_bf16_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+__device__ __forceinline__ void umma2_kf16_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                                 uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p, e;\n\t"
@@ -929,7 +938,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G2_THREADS, 1)
     tmem_relinquish2();
   }
   if (tid >= 96 && tid < 96 + 256)
-    s_e4m3[tid - 96] = e4m3_lut_entry((uint32_t)(tid - 96));
+    s_e4m3[tid - 96] = e4m3_lut_entry<ACT_BF16>((uint32_t)(tid - 96));
   tc_fence_before();
   cluster_sync();  // barriers of both CTAs initialised, TMEM allocated, before any remote access
   tc_fence_after();
@@ -1088,7 +1097,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G2_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t idesc = idesc_bf16(256, g2_width(it.n));
+        const uint32_t idesc = idesc_kf16<ACT_BF16>(256, g2_width(it.n));
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * G2_N);
         for (int kb = 0; kb < p.KB; ++kb) {
           if (!__all_sync(0xffffffffu, mbar_wait_cluster(&afull[os], oph, s_flags, lim) &&
@@ -1100,7 +1109,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G2_THREADS, 1)
           const uint32_t b_lo = b_lo0 + (uint32_t)os * (G2_B_BYTES >> 4);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            umma2_bf16_warp(d_tmem, desc_from_lo(a_lo + 2 * ks), desc_from_lo(b_lo + 2 * ks), idesc,
+            umma2_kf16_warp(d_tmem, desc_from_lo(a_lo + 2 * ks), desc_from_lo(b_lo + 2 * ks), idesc,
                             (kb | ks) ? 1u : 0u);
           umma2_commit_both(&oempty[os]);
           if (++os == G2_OSTAGES) {
@@ -1196,7 +1205,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G2_THREADS, 1)
                 const int col = c0 + 8 * rep + 2 * qq + b;
                 const float gate = __uint_as_float(v[4 * rep + b]) * gsc;
                 const float up = __uint_as_float(v[4 * rep + 2 + b]) * gsc;
-                if (col < it.n) p.h_out[(size_t)(it.p0 + col) * p.I + ch] = __float2bfloat16_rn(silu_fast(gate) * up);
+                if (col < it.n) p.h_out[(size_t)(it.p0 + col) * p.I + ch] = f32_to_act<ACT_BF16>(silu_fast(gate) * up);
               }
             }
           }
@@ -1240,8 +1249,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G2_THREADS, 1)
 }
 
 // ------------------------------------------------------------ gather of activation rows
-__global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict__ perm, int S, int k,
-                                   int T, int H, __nv_bfloat16* __restrict__ xg, int* status) {
+__global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int* __restrict__ perm, int S, int k,
+                                   int T, int H, uint16_t* __restrict__ xg, int* status) {
   pdl_wait();
   pdl_trigger();
   const int vec = H / 8;  // 16-byte vectors per row
@@ -1261,8 +1270,8 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x, const in
   (void)T;
 }
 
-cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int* perm, int S, int k, int T, int H,
-                               __nv_bfloat16* xg, int* status, int num_sms, cudaStream_t st) {
+cudaError_t launch_gather_rows(const uint16_t* x, const int* perm, int S, int k, int T, int H, uint16_t* xg,
+                               int* status, int num_sms, cudaStream_t st) {
   if (S == 0) return cudaSuccess;
   const long long n = (long long)S * (H / 8);
   const long long blocks = (n + 255) / 256;
@@ -1312,12 +1321,16 @@ static int pair_clusters(int num_sms) {
   return n;
 }
 
-cudaError_t launch_grouped_gemm(const GroupedParams& p, const __nv_bfloat16* b_src, int b_rows, int num_sms,
+cudaError_t launch_grouped_gemm(const GroupedParams& p, const uint16_t* b_src, int b_rows, int num_sms,
                                 cudaStream_t st) {
-  static std::atomic<unsigned long long> attr1{0}, attr2{0};
-  cudaError_t ea = ensure_smem_attr(grouped_gemm_kernel, GT_SMEM_BYTES, attr1);
+  static std::atomic<unsigned long long> attr1{0}, attr1h{0}, attr2{0};
+  cudaError_t ea = ensure_smem_attr(grouped_gemm_kernel<ACT_BF16>, GT_SMEM_BYTES, attr1);
+  if (ea == cudaSuccess) ea = ensure_smem_attr(grouped_gemm_kernel<ACT_F16>, GT_SMEM_BYTES, attr1h);
   if (ea == cudaSuccess) ea = ensure_smem_attr(grouped_pair_kernel, G2_SMEM_BYTES, attr2);
   if (ea != cudaSuccess) return ea;
+  // The CTA-pair kernel takes bf16 operands only.
+  if ((p.act_type != ACT_BF16 && p.act_type != ACT_F16) || (p.pair && p.act_type != ACT_BF16))
+    return cudaErrorInvalidValue;
   if (b_rows <= 0) return cudaSuccess;
   if ((reinterpret_cast<uintptr_t>(b_src) & 15) != 0 || (p.K % TILE_K) != 0) return cudaErrorInvalidValue;
   auto enc = tensor_map_encoder();
@@ -1327,13 +1340,16 @@ cudaError_t launch_grouped_gemm(const GroupedParams& p, const __nv_bfloat16* b_s
   const cuuint64_t strides[1] = {(cuuint64_t)p.K * 2};
   const cuuint32_t box[2] = {(cuuint32_t)TILE_K, (cuuint32_t)(p.pair ? G2_BBOX : GT_N)};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(b_src), dims, strides, box,
+  CUresult r = enc(&map, p.act_type == ACT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<uint16_t*>(b_src), dims, strides, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   cudaError_t e;
   if (!p.pair) {
-    e = launch_pdl(grouped_gemm_kernel, dim3(num_sms), dim3(GT_THREADS), GT_SMEM_BYTES, st, p, map);
+    e = p.act_type == ACT_F16
+            ? launch_pdl(grouped_gemm_kernel<ACT_F16>, dim3(num_sms), dim3(GT_THREADS), GT_SMEM_BYTES, st, p, map)
+            : launch_pdl(grouped_gemm_kernel<ACT_BF16>, dim3(num_sms), dim3(GT_THREADS), GT_SMEM_BYTES, st, p, map);
   } else {
     const int pairs = pair_clusters(num_sms);
     if (pairs <= 0) return cudaErrorNotSupported;

@@ -31,12 +31,14 @@ struct ExpertGeom {
 };
 ExpertGeom expert_geom(int H, int I, int fmt);
 
+// nvfp4_nibbles: store NVFP4 codes in the nibble layout of MXFP4 (fp16 operand layers) instead of
+// the shift-and-mask layout (bf16 operand layers).
 cudaError_t launch_pack_matrix(int fmt, int which, const void* codes, const void* scales, int N, int K, int I,
-                               uint8_t* dst, cudaStream_t st);
+                               uint8_t* dst, bool nvfp4_nibbles, cudaStream_t st);
 // Test export of the dequantised operands (pack.cu): the tensor-core tile, or with
 // decode_operand the weight-streaming kernel's operand plus its per-group scales.
 cudaError_t launch_debug_dequant(int fmt, int which, const uint8_t* src, int N, int K, int I, void* dst,
-                                 float* scales_out, bool decode_operand, cudaStream_t st);
+                                 float* scales_out, bool decode_operand, int act_type, cudaStream_t st);
 
 // ---------------------------------------------------------------- streaming GEMM (any T; the decode path)
 // One matrix of the expert FFN as the streaming kernel sees it.
@@ -44,7 +46,7 @@ struct StreamPhase {
   int rows, K;               // rows = 2I (W13) or H (W2); K = H or I
   int RT, KB;                // row tiles, k-blocks
   int kbs;                   // k-blocks per pipeline stage
-  const __nv_bfloat16* act;  // W13: x [T][H] by token; W2: h [S][I] by permuted position
+  const uint16_t* act;       // W13: x [T][H] by token; W2: h [S][I] by permuted position (operand type)
   int act_stride;
   size_t kept_off, nf3_off;  // byte offset of this matrix inside an expert's block
 };
@@ -53,6 +55,7 @@ struct StreamParams {
   const uint8_t* kept_buf;
   const uint8_t* nf3_buf;
   int kept_fmt;
+  int act_type;          // ACT_BF16 or ACT_F16: operand, h and output type
   int H, I, E, topk, T;
   StreamPhase ph[2];     // [0] W13 (output h), [1] W2 (output y)
   int ph_begin, ph_end;  // phases this launch runs: [0,2) both (W2 items wait on done13), [0,1) or [1,2)
@@ -63,7 +66,7 @@ struct StreamParams {
   const int* perm;
   int* queue;                // [2] work-queue head and finished-CTA count, self-cleaning
   int* done13;               // [token groups] finished W13 warp-items per group, self-cleaning ([0,2) only)
-  __nv_bfloat16* h_out;      // W13 output: [S][I] bf16, row = permuted position p
+  uint16_t* h_out;           // W13 output: [S][I] in the operand type (bf16 or fp16 bits), row = permuted position p
   float* y_out;              // W2 output:  [S][H] fp32, row = flat slot s
   int* status;
   unsigned long long wait_limit_ns;  // bound on every wait
@@ -79,6 +82,7 @@ struct GroupedParams {
   const uint8_t* kept_buf;
   const uint8_t* nf3_buf;
   int kept_fmt;
+  int act_type;        // ACT_BF16 or ACT_F16
   int which;           // 13: B = gathered x, output h;  2: B = h, output y
   int H, I, E, topk, T;
   int K, RT, KB;
@@ -87,21 +91,21 @@ struct GroupedParams {
   size_t kept_w2_off, nf3_w2_off;
   const int* offsets;
   const int* perm;
-  __nv_bfloat16* h_out;
+  uint16_t* h_out;     // [S][I] in the operand type
   float* y_out;
   int* status;
   unsigned long long wait_limit_ns;
   int pair;            // 1: the CTA-pair kernel; 0: the one-CTA kernel (the default)
   ExpertTable tab;
 };
-cudaError_t launch_grouped_gemm(const GroupedParams& p, const __nv_bfloat16* b_src, int b_rows, int num_sms,
+cudaError_t launch_grouped_gemm(const GroupedParams& p, const uint16_t* b_src, int b_rows, int num_sms,
                                 cudaStream_t st);
-// xg[p] = x[perm[p] / k] for the S permuted slots.
-cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int* perm, int S, int k, int T, int H,
-                               __nv_bfloat16* xg, int* status, int num_sms, cudaStream_t st);
+// xg[p] = x[perm[p] / k] for the S permuted slots (2-byte elements of either operand type).
+cudaError_t launch_gather_rows(const uint16_t* x, const int* perm, int S, int k, int T, int H, uint16_t* xg,
+                               int* status, int num_sms, cudaStream_t st);
 
-// out[t][c] = bf16(sum_j gates[t*k+j] * y[t*k+j][c])
-cudaError_t launch_finalize(const float* y, const float* gates, int T, int k, int H, __nv_bfloat16* out,
+// out[t][c] = act(sum_j gates[t*k+j] * y[t*k+j][c]), act = bf16 or fp16 by act_type
+cudaError_t launch_finalize(const float* y, const float* gates, int T, int k, int H, uint16_t* out, int act_type,
                             cudaStream_t st);
 
 // Raises a kernel's dynamic shared-memory limit once per device: the

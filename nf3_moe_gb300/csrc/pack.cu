@@ -78,7 +78,7 @@ __device__ __forceinline__ uint32_t e2m1_word(const uint32_t* d) {
 
 __global__ void pack_matrix_kernel(int fmt, int which, const uint8_t* __restrict__ codes,
                                    const uint8_t* __restrict__ scales, int N, int K, int I,
-                                   uint8_t* __restrict__ dst) {
+                                   uint8_t* __restrict__ dst, bool nvfp4_nibbles) {
   const int KB = K / TILE_K;
   const int rt = blockIdx.x / KB, kb = blockIdx.x % KB;
   const int tid = threadIdx.x, rg = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
@@ -99,7 +99,7 @@ __global__ void pack_matrix_kernel(int fmt, int which, const uint8_t* __restrict
       c1[2 * m + 1] = s1[m] >> 4;
     }
     uint4 v;
-    if (fmt == FMT_NVFP4) {
+    if (fmt == FMT_NVFP4 && !nvfp4_nibbles) {
       v.x = e2m1s_word(c0);
       v.y = e2m1s_word(c0 + 8);
       v.z = e2m1s_word(c1);
@@ -153,11 +153,11 @@ __global__ void pack_matrix_kernel(int fmt, int which, const uint8_t* __restrict
 }
 
 cudaError_t launch_pack_matrix(int fmt, int which, const void* codes, const void* scales, int N, int K, int I,
-                               uint8_t* dst, cudaStream_t st) {
+                               uint8_t* dst, bool nvfp4_nibbles, cudaStream_t st) {
   const int tiles = (N / TILE_ROWS) * (K / TILE_K);
   if (tiles == 0) return cudaSuccess;
   pack_matrix_kernel<<<tiles, 256, 0, st>>>(fmt, which, static_cast<const uint8_t*>(codes),
-                                            static_cast<const uint8_t*>(scales), N, K, I, dst);
+                                            static_cast<const uint8_t*>(scales), N, K, I, dst, nvfp4_nibbles);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -165,19 +165,19 @@ cudaError_t launch_pack_matrix(int fmt, int which, const void* codes, const void
 // ------------------------------------------------------------ debug export of operand tiles
 // Both exports run dequant_slot, the decoder the GEMM kernels run, with the
 // same shared E4M3 table the kernels build:
-//   tile mode (WITH_NF3_SCALE = true): the bf16 operand tile the tensor-core
-//     grouped kernel writes to shared memory. NVFP4 values are carried times
-//     2^-63 inside the kernels (the factor returns with the global scale), so
-//     the export multiplies 2^63 back, exactly.
+//   tile mode (WITH_NF3_SCALE = true): the operand tile (bf16 or fp16) the
+//     tensor-core grouped kernel writes to shared memory. NVFP4 values in
+//     bf16 are carried times 2^-63 inside the kernels (the factor returns
+//     with the global scale), so the export multiplies 2^63 back, exactly.
 //   decode mode (WITH_NF3_SCALE = false): the operand the weight-streaming
 //     kernel feeds mma.sync. NVFP4 and MXFP4 are the tile values; NF3 values
 //     are the raw codebook entries, and scales_out receives the fp32 factor
 //     the kernel applies to each row's 64-wide group sum (1 for NVFP4/MXFP4).
-template <int FMT, bool WITH_NF3_SCALE>
+template <int FMT, bool WITH_NF3_SCALE, int ACT>
 __device__ __forceinline__ void debug_slot(const uint8_t* tile, int rg, int lane, const uint32_t* lut, uint32_t* r0,
                                            uint32_t* r1, float* s0, float* s1) {
-  dequant_slot<FMT, WITH_NF3_SCALE>(tile, rg, lane, r0, r1, s0, s1, lut);
-  if constexpr (FMT == FMT_NVFP4) {
+  dequant_slot<FMT, WITH_NF3_SCALE, ACT>(tile, rg, lane, r0, r1, s0, s1, lut);
+  if constexpr (FMT == FMT_NVFP4 && ACT == ACT_BF16) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       r0[i] = bf16x2_mul(r0[i], BF16X2_2P63);
@@ -186,11 +186,11 @@ __device__ __forceinline__ void debug_slot(const uint8_t* tile, int rg, int lane
   }
 }
 
-template <bool WITH_NF3_SCALE>
+template <bool WITH_NF3_SCALE, int ACT>
 __global__ void debug_dequant_kernel(int fmt, int which, const uint8_t* __restrict__ src, int N, int K, int I,
-                                     __nv_bfloat16* __restrict__ dst, float* __restrict__ scales_out) {
+                                     uint16_t* __restrict__ dst, float* __restrict__ scales_out) {
   __shared__ uint32_t s_e4m3[256];
-  s_e4m3[threadIdx.x] = e4m3_lut_entry(threadIdx.x);
+  s_e4m3[threadIdx.x] = e4m3_lut_entry<ACT>(threadIdx.x);
   __syncthreads();
   const int KB = K / TILE_K;
   const int rt = blockIdx.x / KB, kb = blockIdx.x % KB;
@@ -198,9 +198,9 @@ __global__ void debug_dequant_kernel(int fmt, int which, const uint8_t* __restri
   const uint8_t* tile = src + ((size_t)rt * KB + kb) * tile_bytes(fmt);
   uint32_t r0[8], r1[8];
   float s0 = 1.0f, s1 = 1.0f;
-  if (fmt == FMT_NVFP4) debug_slot<FMT_NVFP4, WITH_NF3_SCALE>(tile, rg, lane, s_e4m3, r0, r1, &s0, &s1);
-  else if (fmt == FMT_MXFP4) debug_slot<FMT_MXFP4, WITH_NF3_SCALE>(tile, rg, lane, s_e4m3, r0, r1, &s0, &s1);
-  else debug_slot<FMT_NF3, WITH_NF3_SCALE>(tile, rg, lane, s_e4m3, r0, r1, &s0, &s1);
+  if (fmt == FMT_NVFP4) debug_slot<FMT_NVFP4, WITH_NF3_SCALE, ACT>(tile, rg, lane, s_e4m3, r0, r1, &s0, &s1);
+  else if (fmt == FMT_MXFP4) debug_slot<FMT_MXFP4, WITH_NF3_SCALE, ACT>(tile, rg, lane, s_e4m3, r0, r1, &s0, &s1);
+  else debug_slot<FMT_NF3, WITH_NF3_SCALE, ACT>(tile, rg, lane, s_e4m3, r0, r1, &s0, &s1);
   const int L0 = logical_row(which, I, rt, rg * 16 + g), L1 = logical_row(which, I, rt, rg * 16 + g + 8);
   const int k0 = kb * TILE_K + 16 * q;
   uint4* d0 = reinterpret_cast<uint4*>(dst + (size_t)L0 * K + k0);
@@ -216,15 +216,18 @@ __global__ void debug_dequant_kernel(int fmt, int which, const uint8_t* __restri
 }
 
 cudaError_t launch_debug_dequant(int fmt, int which, const uint8_t* src, int N, int K, int I, void* dst,
-                                 float* scales_out, bool decode_operand, cudaStream_t st) {
+                                 float* scales_out, bool decode_operand, int act_type, cudaStream_t st) {
   const int tiles = (N / TILE_ROWS) * (K / TILE_K);
   if (tiles == 0) return cudaSuccess;
-  if (decode_operand)
-    debug_dequant_kernel<false><<<tiles, 256, 0, st>>>(fmt, which, src, N, K, I, static_cast<__nv_bfloat16*>(dst),
-                                                       scales_out);
-  else
-    debug_dequant_kernel<true><<<tiles, 256, 0, st>>>(fmt, which, src, N, K, I, static_cast<__nv_bfloat16*>(dst),
-                                                      nullptr);
+  uint16_t* d = static_cast<uint16_t*>(dst);
+  const bool f16 = act_type == ACT_F16;
+  if (decode_operand) {
+    if (f16) debug_dequant_kernel<false, ACT_F16><<<tiles, 256, 0, st>>>(fmt, which, src, N, K, I, d, scales_out);
+    else debug_dequant_kernel<false, ACT_BF16><<<tiles, 256, 0, st>>>(fmt, which, src, N, K, I, d, scales_out);
+  } else {
+    if (f16) debug_dequant_kernel<true, ACT_F16><<<tiles, 256, 0, st>>>(fmt, which, src, N, K, I, d, nullptr);
+    else debug_dequant_kernel<true, ACT_BF16><<<tiles, 256, 0, st>>>(fmt, which, src, N, K, I, d, nullptr);
+  }
   count_launches(1);
   return cudaGetLastError();
 }

@@ -88,6 +88,7 @@ __device__ __forceinline__ SkItem decode_item(const StreamParams& p, const int* 
 }
 
 // Output of one thread's 2 rows x 2 tokens (v[0],v[1]: row R0; v[2],v[3]: row R1).
+template <int ACT>
 __device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it, int rg, int g, int q,
                                         const float* v) {
   const int S = p.T * p.topk;
@@ -97,12 +98,12 @@ __device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it,
     if (c >= it.n) continue;
     const int pp = it.p0 + c;
     if (it.ph == 0) {
-      const float gsc = p.tab.g13[it.e] * (expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
+      const float gsc = p.tab.g13[it.e] * (expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f);
       const int ch = it.rt * 64 + rg * 8 + g;
       const float gate = v[h] * gsc, up = v[2 + h] * gsc;
-      p.h_out[(size_t)pp * p.I + ch] = __float2bfloat16_rn(silu_f(gate) * up);
+      p.h_out[(size_t)pp * p.I + ch] = f32_to_act<ACT>(silu_f(gate) * up);
     } else {
-      const float gsc = p.tab.g2[it.e] * (expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
+      const float gsc = p.tab.g2[it.e] * (expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f);
       const int s = p.perm[pp];
       if (s < 0 || s >= S) {
         set_status(p.status, DEV_BAD_ROUTE);
@@ -119,7 +120,7 @@ __device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it,
 // (the decoder hmoe_debug_decode_operand exports; NVFP4/MXFP4 scales applied
 // in bf16 from the shared lookup table, NF3 values raw with the row scales
 // applied to the fp32 sum of the k-block) and 4 MMAs.
-template <int FMT>
+template <int FMT, int ACT>
 __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xrow, int rg, int lane,
                                           const uint32_t* s_e4m3, float* acc) {
   const uint4 xa = *reinterpret_cast<const uint4*>(xrow);
@@ -127,17 +128,17 @@ __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xr
   const uint32_t xr[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
   uint32_t r0[8], r1[8];
   float sc0, sc1;
-  dequant_slot<FMT, false>(tile, rg, lane, r0, r1, &sc0, &sc1, s_e4m3);
+  dequant_slot<FMT, false, ACT>(tile, rg, lane, r0, r1, &sc0, &sc1, s_e4m3);
   if constexpr (FMT == FMT_NVFP4 || FMT == FMT_MXFP4) {
 #pragma unroll
     for (int s = 0; s < 4; ++s)
-      mma_bf16_16816(acc, r0[2 * s], r1[2 * s], r0[2 * s + 1], r1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
+      mma_16816<ACT>(acc, r0[2 * s], r1[2 * s], r0[2 * s + 1], r1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
   } else {
     float d[4];
-    mma_bf16_16816_zc(d, r0[0], r1[0], r0[1], r1[1], xr[0], xr[1]);
+    mma_16816_zc<ACT>(d, r0[0], r1[0], r0[1], r1[1], xr[0], xr[1]);
 #pragma unroll
     for (int s = 1; s < 4; ++s)
-      mma_bf16_16816(d, r0[2 * s], r1[2 * s], r0[2 * s + 1], r1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
+      mma_16816<ACT>(d, r0[2 * s], r1[2 * s], r0[2 * s + 1], r1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
     acc[0] = fmaf(sc0, d[0], acc[0]);
     acc[1] = fmaf(sc0, d[1], acc[1]);
     acc[2] = fmaf(sc1, d[2], acc[2]);
@@ -146,23 +147,24 @@ __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xr
 }
 
 // All k-blocks of one stage, two accumulator sets to break the MMA chain.
-template <int FMT>
+template <int FMT, int ACT>
 __device__ __forceinline__ void sk_stage(const uint8_t* sw, const uint8_t* sx, int kbs, int rg, int lane,
                                          const uint32_t* s_e4m3, float* accA, float* accB) {
   constexpr int TB = tile_bytes(FMT);
   if (kbs == 8) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) sk_kblock<FMT>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, (j & 1) ? accB : accA);
+    for (int j = 0; j < 8; ++j) sk_kblock<FMT, ACT>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, (j & 1) ? accB : accA);
   } else if (kbs == 4) {
-    sk_kblock<FMT>(sw, sx, rg, lane, s_e4m3, accA);
-    sk_kblock<FMT>(sw + TB, sx + 128, rg, lane, s_e4m3, accB);
-    sk_kblock<FMT>(sw + 2 * TB, sx + 256, rg, lane, s_e4m3, accA);
-    sk_kblock<FMT>(sw + 3 * TB, sx + 384, rg, lane, s_e4m3, accB);
+    sk_kblock<FMT, ACT>(sw, sx, rg, lane, s_e4m3, accA);
+    sk_kblock<FMT, ACT>(sw + TB, sx + 128, rg, lane, s_e4m3, accB);
+    sk_kblock<FMT, ACT>(sw + 2 * TB, sx + 256, rg, lane, s_e4m3, accA);
+    sk_kblock<FMT, ACT>(sw + 3 * TB, sx + 384, rg, lane, s_e4m3, accB);
   } else {
-    for (int j = 0; j < kbs; ++j) sk_kblock<FMT>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, (j & 1) ? accB : accA);
+    for (int j = 0; j < kbs; ++j) sk_kblock<FMT, ACT>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, (j & 1) ? accB : accA);
   }
 }
 
+template <int ACT>
 __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid_constant__ StreamParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SK_SMEM_DATA);
@@ -182,7 +184,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
     fence_mbar_init();
     s_flags[0] = 0;
   }
-  if (tid < 256) s_e4m3[tid] = e4m3_lut_entry((uint32_t)tid);
+  if (tid < 256) s_e4m3[tid] = e4m3_lut_entry<ACT>((uint32_t)tid);
   pdl_wait();  // everything below reads or writes global memory
   pdl_trigger();
   for (int e = tid; e <= p.E; e += blockDim.x) s_off[e] = p.offsets[e];
@@ -372,9 +374,9 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
         for (int r = 0; r < 4; ++r) accA[r] = accB[r] = 0.f;
       }
       const uint8_t* sx = sw + SK_W_BYTES + g * SK_XROW + q * 32;
-      if (fmt == FMT_NVFP4) sk_stage<FMT_NVFP4>(sw, sx, kbs, rg, lane, s_e4m3, accA, accB);
-      else if (fmt == FMT_MXFP4) sk_stage<FMT_MXFP4>(sw, sx, kbs, rg, lane, s_e4m3, accA, accB);
-      else sk_stage<FMT_NF3>(sw, sx, kbs, rg, lane, s_e4m3, accA, accB);
+      if (fmt == FMT_NVFP4) sk_stage<FMT_NVFP4, ACT>(sw, sx, kbs, rg, lane, s_e4m3, accA, accB);
+      else if (fmt == FMT_MXFP4) sk_stage<FMT_MXFP4, ACT>(sw, sx, kbs, rg, lane, s_e4m3, accA, accB);
+      else sk_stage<FMT_NF3, ACT>(sw, sx, kbs, rg, lane, s_e4m3, accA, accB);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
       if (++slot == SK_STAGES) {
@@ -386,7 +388,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
       float acc[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) acc[r] = accA[r] + accB[r];
-      sk_emit(p, it, rg, g, q, acc);
+      sk_emit<ACT>(p, it, rg, g, q, acc);
       if (fused && it.ph == 0) {
         // Publish this warp's h rows to the W2 producers, whose bulk copies
         // (async proxy) may run on any SM: every lane fences its own stores
@@ -419,22 +421,27 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
 int stream_grid(int num_sms) { return 2 * num_sms; }
 
 cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st) {
-  static std::atomic<unsigned long long> attr_done{0};
-  const cudaError_t ea = ensure_smem_attr(stream_gemm_kernel, SK_SMEM_BYTES, attr_done);
+  static std::atomic<unsigned long long> attr_bf16{0}, attr_f16{0};
+  cudaError_t ea = ensure_smem_attr(stream_gemm_kernel<ACT_BF16>, SK_SMEM_BYTES, attr_bf16);
+  if (ea == cudaSuccess) ea = ensure_smem_attr(stream_gemm_kernel<ACT_F16>, SK_SMEM_BYTES, attr_f16);
   if (ea != cudaSuccess) return ea;
+  if (p.act_type != ACT_BF16 && p.act_type != ACT_F16) return cudaErrorInvalidValue;
   if (p.ph_begin < 0 || p.ph_begin >= p.ph_end || p.ph_end > 2) return cudaErrorInvalidValue;
   if (p.ph_begin == 0 && p.ph_end == 2 && !p.done13) return cudaErrorInvalidValue;
   for (const StreamPhase& P : p.ph)
     if (P.kbs < 1 || P.kbs > SK_MAX_KBS || P.KB % P.kbs != 0) return cudaErrorInvalidValue;
   if (p.group_tokens < 1 || p.group_tokens > 8) return cudaErrorInvalidValue;
-  cudaError_t e = launch_pdl(stream_gemm_kernel, dim3(grid), dim3(SK_THREADS), SK_SMEM_BYTES, st, p);
+  cudaError_t e = p.act_type == ACT_F16
+                      ? launch_pdl(stream_gemm_kernel<ACT_F16>, dim3(grid), dim3(SK_THREADS), SK_SMEM_BYTES, st, p)
+                      : launch_pdl(stream_gemm_kernel<ACT_BF16>, dim3(grid), dim3(SK_THREADS), SK_SMEM_BYTES, st, p);
   count_launches(1);
   return e;
 }
 
 // ------------------------------------------------------------ finalize
+template <int ACT>
 __global__ void finalize_kernel(const float* __restrict__ y, const float* __restrict__ gates, int T, int k, int H,
-                                __nv_bfloat16* __restrict__ out) {
+                                uint16_t* __restrict__ out) {
   pdl_wait();
   pdl_trigger();
   const int half = H / 2;
@@ -448,18 +455,20 @@ __global__ void finalize_kernel(const float* __restrict__ y, const float* __rest
       a = fmaf(gt, v.x, a);
       b = fmaf(gt, v.y, b);
     }
-    *reinterpret_cast<__nv_bfloat162*>(out + (size_t)t * H + c) = __floats2bfloat162_rn(a, b);
+    *reinterpret_cast<uint32_t*>(out + (size_t)t * H + c) = f32x2_to_act<ACT>(a, b);
   }
 }
 
-cudaError_t launch_finalize(const float* y, const float* gates, int T, int k, int H, __nv_bfloat16* out,
+cudaError_t launch_finalize(const float* y, const float* gates, int T, int k, int H, uint16_t* out, int act_type,
                             cudaStream_t st) {
   const long long n = (long long)T * (H / 2);
   if (n == 0) return cudaSuccess;
   const int threads = 256;
   const long long blocks = (n + threads - 1) / threads;
-  cudaError_t e = launch_pdl(finalize_kernel, dim3((unsigned)(blocks < 4096 ? blocks : 4096)), dim3(threads), 0, st, y,
-                             gates, T, k, H, out);
+  const dim3 grid((unsigned)(blocks < 4096 ? blocks : 4096));
+  cudaError_t e = act_type == ACT_F16
+                      ? launch_pdl(finalize_kernel<ACT_F16>, grid, dim3(threads), 0, st, y, gates, T, k, H, out)
+                      : launch_pdl(finalize_kernel<ACT_BF16>, grid, dim3(threads), 0, st, y, gates, T, k, H, out);
   count_launches(1);
   return e;
 }

@@ -21,7 +21,7 @@ the repository's design notes. Each module header states its own.
 
 Modules:
   formats -- element and scale decoders (E2M1, E4M3, E8M0, NF3 codebook,
-             bf16 rounding) and dequantisation of the logical checkpoint
+             bf16 and fp16 rounding) and dequantisation of the logical checkpoint
              layouts.
   route   -- top-k routing, renormalised gates, stable permutation, offsets.
   layer   -- the SwiGLU expert layer: dequantise, then matmul, gate, sum.

@@ -30,10 +30,18 @@ Logical checkpoint layouts (the input to the packer and the oracle):
   Scales are bf16 [N, K/64], stored as uint16 bit patterns.
   w = bf16_rne(cb[code] * scale).
 
-The "dequantised tile" is the bf16 operand a kernel feeds to its matrix unit:
-  NVFP4: e2m1*e4m3. This is exact in bf16; g is applied to the fp32 sum.
-  MXFP4: e2m1*2**(b-127). Exact.
-  NF3:   bf16_rne(cb*s).
+The "dequantised tile" is the 16-bit operand a kernel feeds to its matrix
+unit, in the layer's activation type ([P3] "Summary", item 2: the W4A16
+activations are bfloat16 or float16, and the weights are dequantised to the
+activation type). With rne the rounding to that type:
+  NVFP4: e2m1*e4m3. This is exact in bf16 and in fp16; g is applied to the
+         fp32 sum.
+  MXFP4: e2m1*2**(b-127). Exact in bf16; in fp16 exact for b in 104..140
+         and rounded (to 0 or infinity) outside.
+  NF3:   rne(cb*s). For bf16 layers this is the logical weight above; for
+         fp16 layers the same product rounded once to fp16 (the pages give
+         no fp16 NF3 rule: this is the plainest reading of "dequantised to
+         the activation type").
 """
 
 import numpy as np
@@ -103,6 +111,34 @@ def bf16_rne(x):
     return r.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
+def f16_rne(x):
+    """Round float64 values to IEEE binary16 (fp16), round-to-nearest-even, as float64.
+
+    binary16 has 11 significant bits, a minimum normal exponent of -14 and
+    subnormals spaced 2**-24 apart, so a value of binary exponent e is
+    rounded to a multiple of 2**(max(e, -14) - 10), ties to the even
+    multiple. Results above the largest finite value 65504 after rounding
+    become infinity (with the sign). NaN is not supported.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, e2 = np.frexp(a)                  # a = m * 2**e2, m in [0.5, 1): binary exponent e2 - 1
+    e = np.where(a > 0, e2 - 1, -14)
+    q = np.exp2(np.maximum(e, -14) - 10.0)
+    r = np.rint(a / q) * q               # np.rint rounds half to even; a / q is exact
+    r = np.where(r > 65504.0, np.inf, r)
+    return np.copysign(r, x)
+
+
+def act_rne(x, act):
+    """Round to the activation type: act is "bf16" or "f16"."""
+    if act == "bf16":
+        return bf16_rne(x)
+    if act == "f16":
+        return f16_rne(x)
+    raise ValueError(f"unknown activation type {act!r}")
+
+
 # ---------------------------------------------------------------- NF3 codebook
 def normalfloat_levels(bits):
     """NormalFloat code values from Dettmers et al., "QLoRA" (2023), Sec. 3.
@@ -152,31 +188,35 @@ def unpack_nf3(codes, K):
 
 
 # ---------------------------------------------------------------- dequantisation
-def dequant_tile(fmt, codes, scales, K):
-    """The dequantised tile: [N, K] float64. Every entry is a bf16 value.
+def dequant_tile(fmt, codes, scales, K, act="bf16"):
+    """The dequantised tile: [N, K] float64. Every entry is a value of the activation type.
 
     NVFP4: e2m1 * e4m3 (global scale excluded). MXFP4: e2m1 * 2**(b-127).
-    NF3: bf16_rne(cb * s).
+    NF3: rne(cb * s). act: "bf16" or "f16". The NVFP4 and MXFP4 products
+    are exact in bf16, so only fp16 rounds them (an identity inside the fp16
+    ranges stated in the module docstring).
     """
     if fmt == FMT_NVFP4:
         v = e2m1_value(unpack_nibbles(codes, K))
         s = e4m3_value(np.asarray(scales, dtype=np.uint8))
-        return v * np.repeat(s, NVFP4_GROUP, axis=1)
+        t = v * np.repeat(s, NVFP4_GROUP, axis=1)
+        return t if act == "bf16" else act_rne(t, act)
     if fmt == FMT_MXFP4:
         v = e2m1_value(unpack_nibbles(codes, K))
         s = e8m0_value(np.asarray(scales, dtype=np.uint8))
-        return v * np.repeat(s, MXFP4_GROUP, axis=1)
+        t = v * np.repeat(s, MXFP4_GROUP, axis=1)
+        return t if act == "bf16" else act_rne(t, act)
     if fmt == FMT_NF3:
         cb = nf3_codebook()
         v = cb[unpack_nf3(codes, K)]
         s = bf16_bits_to_f64(np.asarray(scales, dtype=np.uint16))
-        return bf16_rne(v * np.repeat(s, NF3_GROUP, axis=1))
+        return act_rne(v * np.repeat(s, NF3_GROUP, axis=1), act)
     raise ValueError(f"unknown format {fmt}")
 
 
-def dequant(fmt, codes, scales, g, K):
+def dequant(fmt, codes, scales, g, K, act="bf16"):
     """Full dequantised weights [N, K] float64. This is the tile times g for NVFP4."""
-    t = dequant_tile(fmt, codes, scales, K)
+    t = dequant_tile(fmt, codes, scales, K, act)
     if fmt == FMT_NVFP4:
         return t * float(g)
     return t

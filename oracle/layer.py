@@ -21,7 +21,9 @@ the comparison: the reference value is the float64 sum.
 Experts are supplied through ``get_expert(e)``. It returns a dict with keys
 ``fmt``, ``w13`` and ``w2``. Each of ``w13`` and ``w2`` is a tuple
 (codes, scales, g) in the logical layout of ``oracle.formats``. This lets a
-caller stream experts one at a time at full size.
+caller stream experts one at a time at full size. An optional key ``act``
+("bf16", the default, or "f16") names the layer's activation type, to which
+the weights are dequantised ([P3] "Summary", item 2).
 """
 
 import numpy as np
@@ -38,8 +40,9 @@ def expert_weights(ex, H, I):
     fmt = ex["fmt"]
     c13, s13, g13 = ex["w13"]
     c2, s2, g2 = ex["w2"]
-    w13 = formats.dequant(fmt, c13, s13, g13, H)
-    w2 = formats.dequant(fmt, c2, s2, g2, I)
+    act = ex.get("act", "bf16")
+    w13 = formats.dequant(fmt, c13, s13, g13, H, act)
+    w2 = formats.dequant(fmt, c2, s2, g2, I, act)
     assert w13.shape == (2 * I, H) and w2.shape == (H, I)
     return w13, w2
 

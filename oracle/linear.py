@@ -11,7 +11,9 @@ plainest reading for one weight matrix W [N, K] in a logical layout of
     y[t, n] = sum_k x[t, k] * W[n, k]        (float64)
 
 with W the full dequantised weights (``formats.dequant``: the NVFP4 global
-scale included). The bf16 rounding of the result is left to the comparison.
+scale included), dequantised to the activation type act ("bf16" or "f16",
+[P3] "Summary", item 2). The rounding of the result to that type is left to
+the comparison.
 """
 
 import numpy as np
@@ -19,7 +21,7 @@ import numpy as np
 from . import formats
 
 
-def linear_forward(x, fmt, codes, scales, g, K):
+def linear_forward(x, fmt, codes, scales, g, K, act="bf16"):
     """float64 [T, N]: x [T, K] times the dequantised weights [N, K] transposed."""
-    w = formats.dequant(fmt, codes, scales, g, K)
+    w = formats.dequant(fmt, codes, scales, g, K, act)
     return np.asarray(x, dtype=np.float64) @ w.T

@@ -10,7 +10,8 @@ Each op is IEEE-exact or a correctly rounded division, so a given device
 always produces the same bytes.
 
 The recipe is that of the workloads in the design notes:
-  * x ~ N(0, 1), rounded to bf16; router logits ~ N(0, 1) in fp32.
+  * x ~ N(0, 1), rounded to bf16 (fp16 for fp16 layers); router logits
+    ~ N(0, 1) in fp32.
   * Master weights ~ N(0, 0.02) in fp32, seeded per (seed, layer, expert,
     matrix). Any one expert can be regenerated alone.
   * NVFP4 quantiser. g = amax / (6 * 448), or 1 if amax = 0. Each 16-group
@@ -49,9 +50,10 @@ def _gen(seed_tuple, device):
     return g
 
 
-def gen_x(T, H, seed=0, device="cpu", stream_id=0):
+def gen_x(T, H, seed=0, device="cpu", stream_id=0, dtype=torch.bfloat16):
+    """Activations ~ N(0, 1), rounded to dtype (bf16, or fp16 for fp16 layers)."""
     g = _gen((seed, 101, stream_id, T, H), device)
-    return torch.randn((T, H), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    return torch.randn((T, H), generator=g, device=device, dtype=torch.float32).to(dtype)
 
 
 def gen_logits(T, E, seed=0, device="cpu", stream_id=0):
@@ -168,8 +170,9 @@ def quantise(fmt, w):
 class Layer:
     """One synthetic layer: per-expert formats plus logical packed tensors."""
 
-    def __init__(self, H, I, E, topk, bit_map, kept_format, experts):
+    def __init__(self, H, I, E, topk, bit_map, kept_format, experts, act="bf16"):
         self.H, self.I, self.E, self.topk = H, I, E, topk
+        self.act = act                    # activation type: "bf16" or "f16"
         self.bit_map = bit_map            # numpy int8 [E] (4 kept / 3 NF3) or None (uniform)
         self.kept_format = kept_format
         self.experts = experts            # list of dicts: fmt, w13=(c,s,g), w2=(c,s,g)
@@ -190,7 +193,11 @@ class Layer:
         c13, s13, g13 = ex["w13"]
         c2, s2, g2 = ex["w2"]
         return {"fmt": ex["fmt"], "w13": (host(c13), host(s13), g13),
-                "w2": (host(c2), host(s2), g2)}
+                "w2": (host(c2), host(s2), g2), "act": self.act}
+
+    @property
+    def x_dtype(self):
+        return torch.float16 if self.act == "f16" else torch.bfloat16
 
 
 def _expert_norm(e, H, I, seed, layer, device):
@@ -200,9 +207,11 @@ def _expert_norm(e, H, I, seed, layer, device):
 
 
 def make_layer(H, I, E, topk, *, kept=None, kept_ids=None, kept_format=FMT_NVFP4,
-               uniform=False, seed=0, layer=0, device="cpu"):
+               uniform=False, seed=0, layer=0, device="cpu", act="bf16"):
     """Build a synthetic layer.
 
+    act: the activation type the layer is served with ("bf16" or "f16"); the
+    quantised weights do not depend on it.
     uniform=True: no bit map, every expert in ``kept_format``.
     kept_ids: explicit list of kept experts.
     kept=n: the n experts with the largest Frobenius norm of [W13; W2], ties
@@ -227,7 +236,7 @@ def make_layer(H, I, E, topk, *, kept=None, kept_ids=None, kept_format=FMT_NVFP4
         q2 = quantise(fmt, w2)
         del w2
         experts.append({"fmt": fmt, "w13": q13, "w2": q2})
-    return Layer(H, I, E, topk, bit_map, kept_format, experts)
+    return Layer(H, I, E, topk, bit_map, kept_format, experts, act)
 
 
 # ---------------------------------------------------------------- skewed router bias

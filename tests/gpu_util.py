@@ -22,15 +22,25 @@ def device_experts(L):
     return out
 
 
+def act_dtype(L):
+    """The library's activation-type code for a synthetic layer."""
+    return hm.ACT_F16 if getattr(L, "act", "bf16") == "f16" else hm.ACT_BF16
+
+
 def build(L, max_tokens):
     bm = None if L.bit_map is None else [int(b) for b in L.bit_map]
     return hm.HybridMoELayer(L.H, L.I, L.E, L.topk, bm, device_experts(L), kept_format=L.kept_format,
-                             max_tokens=max_tokens)
+                             max_tokens=max_tokens, act_dtype=act_dtype(L))
+
+
+def dev_to_f64(t):
+    """A bf16 or fp16 device tensor as float64 numpy values (exact)."""
+    return t.cpu().float().numpy().astype(np.float64)
 
 
 def run(moe, x, logits, **kw):
     ids, gates, perm, offsets = moe.plan(logits)
-    out = torch.empty((x.shape[0], moe.H), dtype=torch.bfloat16, device=x.device)
+    out = torch.empty((x.shape[0], moe.H), dtype=moe.dtype, device=x.device)
     hm.hmoe_forward(moe.layer, x, ids, gates, perm, offsets, out, moe.ws, **kw)
     torch.cuda.synchronize()
     hm.hmoe_check_device_status(moe.ws)

@@ -48,9 +48,14 @@ def test_host_validation_without_gpu(lib):
     assert hm.hmoe_packed_size(hm.LayerDesc(2048, 768, 128, 8, 4), None) == (128 * 2_654_208, 0)
     sizes = [hm.hmoe_workspace_size(d, t) for t in (0, 1, 8, 9, 4096)]
     assert sizes == sorted(sizes)
+    # fp16 layers: same packed sizes and workspace (2-byte activations either way)
+    d16 = hm.LayerDesc(6144, 2048, 256, 8, hm.FMT_NVFP4, hm.ACT_F16)
+    assert hm.hmoe_packed_size(d16, [4] * 64 + [3] * 192) == (kept, nf3)
+    assert [hm.hmoe_workspace_size(d16, t) for t in (0, 1, 8, 9, 4096)] == sizes
     for bad, status in [(hm.LayerDesc(6144, 2048, 256, 8, 7), -1), (hm.LayerDesc(6100, 2048, 256, 8, 4), -2),
                         (hm.LayerDesc(6144, 2000, 256, 8, 4), -2), (hm.LayerDesc(6144, 2048, 600, 8, 4), -2),
-                        (hm.LayerDesc(6144, 2048, 4, 8, 4), -2), (hm.LayerDesc(0, 2048, 4, 2, 4), -1)]:
+                        (hm.LayerDesc(6144, 2048, 4, 8, 4), -2), (hm.LayerDesc(0, 2048, 4, 2, 4), -1),
+                        (hm.LayerDesc(6144, 2048, 256, 8, 4, 2), -1), (hm.LayerDesc(6144, 2048, 256, 8, 4, -1), -1)]:
         with pytest.raises(hm.HmoeError) as ei:
             hm.hmoe_workspace_size(bad, 8)
         assert ei.value.status == status
@@ -93,7 +98,9 @@ def test_linear_desc_checks_on_host(lib):
     import nf3_moe_gb300 as hm
     assert hm.hmoe_linear_packed_size(hm.LinearDesc(256, 384, hm.FMT_NF3)) == 2 * 6 * 3328
     assert hm.hmoe_linear_packed_size(hm.LinearDesc(128, 64, hm.FMT_NVFP4)) == 4608
-    for bad, status in (((100, 64, 4), -2), ((128, 32, 4), -2), ((128, 64, 7), -1), ((0, 64, 3), -1)):
+    assert hm.hmoe_linear_packed_size(hm.LinearDesc(128, 64, hm.FMT_NVFP4, hm.ACT_F16)) == 4608
+    for bad, status in (((100, 64, 4), -2), ((128, 32, 4), -2), ((128, 64, 7), -1), ((0, 64, 3), -1),
+                        ((128, 64, 4, 3), -1)):
         with pytest.raises(hm.HmoeError) as ei:
             hm.hmoe_linear_packed_size(hm.LinearDesc(*bad))
         assert ei.value.status == status

@@ -7,6 +7,8 @@ Two exports, each running the decoder its kernel runs (include/hmoe.h):
   per-64-group factors. NVFP4 and MXFP4: the same tile, factors 1. NF3: the raw
   codebook entry of each code (oracle.formats.nf3_codebook indexed by
   oracle.formats.unpack_nf3) and the group's bf16 scale, exactly.
+Both activation types: the operands are bf16 or fp16 values of the layer's type
+(oracle.formats.dequant_tile with act).
 """
 
 import numpy as np
@@ -21,26 +23,22 @@ from tests import gpu_util as U
 pytestmark = pytest.mark.gpu
 
 
-def _bf16_dev_to_f64(t):
-    bits = t.view(torch.int16).cpu().numpy().view(np.uint16)
-    return F.bf16_bits_to_f64(bits)
-
-
 def _check_expert(moe, L, e):
     ex = L.expert_numpy(e)
+    act = ex["act"]
     for which, (N, K) in ((13, (2 * L.I, L.H)), (2, (L.H, L.I))):
         codes, scales, _ = ex["w13" if which == 13 else "w2"]
-        ref = F.dequant_tile(ex["fmt"], codes, scales, K)
-        dst = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+        ref = F.dequant_tile(ex["fmt"], codes, scales, K, act)
+        dst = torch.empty((N, K), dtype=moe.dtype, device="cuda")
         hm.hmoe_debug_dequant(moe.layer, e, which, dst)
         torch.cuda.synchronize()
-        assert np.array_equal(_bf16_dev_to_f64(dst), ref), f"tile: expert {e} W{which} fmt {ex['fmt']}"
+        assert np.array_equal(U.dev_to_f64(dst), ref), f"tile: expert {e} W{which} fmt {ex['fmt']} {act}"
         # the decode kernel's operand
-        vals = torch.full((N, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+        vals = torch.full((N, K), float("nan"), dtype=moe.dtype, device="cuda")
         fac = torch.full((N, K // 64), float("nan"), dtype=torch.float32, device="cuda")
         hm.hmoe_debug_decode_operand(moe.layer, e, which, vals, fac)
         torch.cuda.synchronize()
-        got_v = _bf16_dev_to_f64(vals)
+        got_v = U.dev_to_f64(vals)
         got_f = fac.cpu().numpy().astype(np.float64)
         if ex["fmt"] == F.FMT_NF3:
             cb = F.nf3_codebook()
@@ -128,3 +126,45 @@ def test_full_size_hybrid_sample_experts():
     moe = U.build(L, 8)
     for e in (0, 1, 255):
         _check_expert(moe, L, e)
+
+
+# ------------------------------------------------------------------ fp16 activations
+@pytest.mark.parametrize("kept_format", [synth.FMT_NVFP4, synth.FMT_MXFP4])
+def test_f16_tiles(kept_format):
+    L = synth.make_layer(256, 128, 6, 2, kept_ids=[0, 2, 4], kept_format=kept_format, device="cuda", act="f16")
+    moe = U.build(L, 8)
+    assert moe.dtype == torch.float16
+    for e in range(6):
+        _check_expert(moe, L, e)
+
+
+def test_f16_extreme_codes_and_scales():
+    """fp16 operands over every code byte and the whole supported scale ranges: every finite
+    E4M3 scale (NVFP4 products are all exact in fp16), E8M0 bytes 104..140 (MXFP4), and NF3
+    scales over the fp16 normal range, where the tile is the product rounded once."""
+    g = torch.Generator(device="cuda").manual_seed(13)
+    H, I = 256, 128
+
+    def rnd(shape, lo, hi):
+        return torch.randint(lo, hi, shape, generator=g, device="cuda", dtype=torch.int32).to(torch.uint8)
+
+    L = synth.make_layer(H, I, 3, 1, kept_ids=[0], device="cuda", act="f16")
+    c13, _, g13 = L.experts[0]["w13"]
+    s13 = rnd((2 * I, H // 16), 0, 0xFF)
+    s13[(s13 & 0x7F) == 0x7F] = 0x7E
+    L.experts[0]["w13"] = (rnd(c13.shape, 0, 256), s13, g13)
+    c13n, _, _ = L.experts[1]["w13"]
+    sc = (torch.rand((2 * I, H // 64), generator=g, device="cuda") * 28 - 14).exp2().to(torch.bfloat16)
+    L.experts[1]["w13"] = (rnd(c13n.shape, 0, 256), sc.view(torch.int16), 1.0)
+    moe = U.build(L, 8)
+    for e in range(2):
+        _check_expert(moe, L, e)
+
+    Lm = synth.make_layer(H, I, 2, 1, kept_ids=[0, 1], kept_format=synth.FMT_MXFP4, device="cuda", act="f16")
+    for e in range(2):
+        for key, (N, K) in (("w13", (2 * I, H)), ("w2", (H, I))):
+            c, _, _ = Lm.experts[e][key]
+            Lm.experts[e][key] = (rnd(c.shape, 0, 256), rnd((N, K // 32), 104, 141), 1.0)
+    moe = U.build(Lm, 8)
+    for e in range(2):
+        _check_expert(moe, Lm, e)

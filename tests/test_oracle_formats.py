@@ -1,4 +1,4 @@
-"""Pins for oracle.formats: element decoders, codebook, bf16 rounding, unpacking, dequant.
+"""Pins for oracle.formats: element decoders, codebook, bf16 and fp16 rounding, unpacking, dequant.
 
 Each check ties the oracle to something outside itself: a library conversion
 (torch float8 / bfloat16), a golden fixture with its citation, an independent
@@ -63,6 +63,98 @@ def test_bf16_rne_matches_torch():
 def test_bf16_rne_rejects_non_fp32_inputs():
     with pytest.raises(ValueError):
         F.bf16_rne(np.array([1.0 + 2.0 ** -40]))
+
+
+def _f16_grid(fine=False):
+    """Every finite fp16 value, its neighbours' midpoints (exact ties), and points just off them:
+    one fp32 ulp off (fp32-exact inputs), or with fine=True a few float64 ulps off."""
+    bits = np.arange(0, 0x7C00, dtype=np.uint16)          # +0 .. largest finite
+    v = bits.view(np.float16).astype(np.float64)
+    mid = 0.5 * (v[:-1] + v[1:])                           # exact in fp32 (12 significant bits)
+    off = np.spacing(mid) * 4 if fine else np.spacing(mid.astype(np.float32)).astype(np.float64)
+    pts = np.concatenate([v, mid, mid + off, mid - off, [65519.0, 65520.0, 65536.0, 1e6, 2.0 ** -25,
+                                                         3 * 2.0 ** -26, 2.0 ** -26]])
+    return np.concatenate([pts, -pts])
+
+
+def test_f16_rne_matches_numpy_and_torch():
+    # torch rounds float64 to fp16 through fp32, so it is a reference only on
+    # fp32-exact inputs; numpy rounds float64 directly.
+    x = _f16_grid()
+    assert np.array_equal(x.astype(np.float32).astype(np.float64), x)
+    got = F.f16_rne(x)
+    ref_t = torch.from_numpy(x).to(torch.float16).double().numpy()
+    assert np.array_equal(got, ref_t)
+    assert np.array_equal(np.signbit(got), np.signbit(ref_t))
+    with np.errstate(over="ignore"):
+        assert np.array_equal(got, x.astype(np.float16).astype(np.float64))
+        xf = _f16_grid(fine=True)
+        assert np.array_equal(F.f16_rne(xf), xf.astype(np.float16).astype(np.float64))
+
+
+def test_f16_rne_closed_form_cases():
+    # Ties go to the even significand; the largest finite value is 65504;
+    # 65520 (the midpoint to 2**16) rounds to infinity; 2**-25 (half the
+    # smallest subnormal) rounds to 0, 3 * 2**-26 to 2**-24.
+    cases = {1.0 + 2.0 ** -11: 1.0, 1.0 + 3 * 2.0 ** -11: 1.0 + 2.0 ** -9, 65519.0: 65504.0,
+             65520.0: np.inf, 2.0 ** -25: 0.0, 3 * 2.0 ** -26: 2.0 ** -24, 2.0 ** -14: 2.0 ** -14,
+             -2.5 * 2.0 ** -24: -2.0 * 2.0 ** -24}
+    for x, want in cases.items():
+        assert F.f16_rne(np.array([x]))[0] == want, x
+
+
+def test_act_rne_dispatch():
+    x = np.array([1.0 + 2.0 ** -9])                       # exact in fp16, not in bf16
+    assert F.act_rne(x, "f16")[0] == x[0]
+    assert F.act_rne(x, "bf16")[0] == 1.0
+    with pytest.raises(ValueError):
+        F.act_rne(x, "fp8")
+
+
+def test_f16_tiles_nvfp4_mxfp4_are_the_exact_products():
+    # Inside the fp16 ranges every NVFP4 and MXFP4 tile value is exact in fp16,
+    # so the fp16 tile equals the (exact) bf16 tile.
+    rng = np.random.default_rng(11)
+    N, K = 8, 128
+    codes = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    e4m3 = rng.integers(0, 0x7F, size=(N, K // 16)).astype(np.uint8)      # every finite positive E4M3
+    e4m3[0, :] = np.arange(K // 16) + 0x76                                  # up to 448 = 0x7E
+    e4m3[0, -1] = 0x01                                                      # the smallest subnormal
+    a = F.dequant_tile(F.FMT_NVFP4, codes, e4m3, K, "f16")
+    assert np.array_equal(a, F.dequant_tile(F.FMT_NVFP4, codes, e4m3, K))
+    e8 = rng.integers(104, 141, size=(N, K // 32)).astype(np.uint8)
+    e8[0] = [104, 140, 127, 120]
+    b = F.dequant_tile(F.FMT_MXFP4, codes, e8, K, "f16")
+    assert np.array_equal(b, F.dequant_tile(F.FMT_MXFP4, codes, e8, K))
+    assert np.isfinite(b).all()
+    # Just outside: b = 141 with code 6 (0x7) overflows fp16, b = 102 with code 0.5 underflows to 0.
+    c1 = np.full((1, 16), 0x77, dtype=np.uint8)
+    hi = F.dequant_tile(F.FMT_MXFP4, c1, np.full((1, 1), 141, np.uint8), 32, "f16")
+    assert np.isinf(hi).all()
+    c2 = np.full((1, 16), 0x11, dtype=np.uint8)
+    lo = F.dequant_tile(F.FMT_MXFP4, c2, np.full((1, 1), 102, np.uint8), 32, "f16")
+    assert np.all(lo == 0.0)
+
+
+def test_f16_nf3_tile_rounds_the_product_once():
+    cb = F.nf3_codebook()
+    idx = np.tile(np.arange(8), 16).reshape(1, 128)
+    codes = synth.pack_nf3_bits(torch.from_numpy(idx)).numpy()
+    # scale 1 and powers of two: the codebook itself, scaled exactly (every
+    # entry has at most 8 significant bits, so fits fp16's 11)
+    for sc in (1.0, 2.0 ** -6, 2.0 ** 5):
+        sbits = np.full((1, 2), torch.tensor(sc, dtype=torch.bfloat16).view(torch.int16).item(), np.int64)
+        t = F.dequant_tile(F.FMT_NF3, codes, sbits.astype(np.uint16), 128, "f16")
+        assert np.array_equal(t[0], cb[idx[0]] * sc)
+    # a general scale: within half an fp16 ulp of the exact product, and the
+    # nearest fp16 value (checked against numpy's conversion)
+    sb = 0x3D4B                                            # bf16 0.0495...
+    s = F.bf16_bits_to_f64(np.array([sb]))[0]
+    t = F.dequant_tile(F.FMT_NF3, codes, np.full((1, 2), sb, np.uint16), 128, "f16")[0]
+    exact = cb[idx[0]] * s
+    assert np.array_equal(t, exact.astype(np.float16).astype(np.float64))
+    assert np.all(np.abs(t - exact) <= np.abs(exact) * 2.0 ** -11)
+    assert not np.array_equal(t, F.bf16_rne(exact))      # fp16 keeps bits bf16 drops
 
 
 def test_normalfloat_construction_reproduces_published_nf4():

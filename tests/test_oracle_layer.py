@@ -100,3 +100,24 @@ def test_gate_linearity_and_subsets():
     sub = layer.moe_forward(x, ids, g, L.expert_numpy, H, I, tokens=[1, 3], cols=[5, 9, 250])
     want = full[[1, 3]][:, [5, 9, 250]]
     assert np.max(np.abs(sub - want)) <= 1e-13 * np.max(np.abs(want))
+
+
+def test_f16_layer_differs_from_bf16_only_in_nf3_rounding():
+    """The activation type enters the layer only through the NF3 tile rounding (fp16 keeps
+    more bits of cb * s; NVFP4 and MXFP4 tiles are exact in both): with the same x, an
+    all-kept layer gives identical results, and a hybrid one differs by at most one bf16
+    rounding of each NF3 weight."""
+    T = 6
+    xs = synth.gen_x(T, 256, seed=4, dtype=torch.float16).float().numpy().astype(np.float64)
+    logits = synth.gen_logits(T, 8, seed=4).numpy()
+    ids, g, _, _ = route.plan(logits, 2)
+    for kept in ([0, 1, 2, 3, 4, 5, 6, 7], [0, 1, 2, 3]):
+        Lb = synth.make_layer(256, 128, 8, 2, kept_ids=kept, kept_format=synth.FMT_MXFP4)
+        Lf = synth.make_layer(256, 128, 8, 2, kept_ids=kept, kept_format=synth.FMT_MXFP4, act="f16")
+        ob = layer.moe_forward(xs, ids, g, Lb.expert_numpy, 256, 128)
+        of = layer.moe_forward(xs, ids, g, Lf.expert_numpy, 256, 128)
+        if len(kept) == 8:
+            assert np.array_equal(ob, of)
+        else:
+            assert not np.array_equal(ob, of)
+            assert np.abs(ob - of).max() <= 2.0 ** -8 * np.abs(ob).max()

@@ -2,7 +2,9 @@
 
 * scalar loops that decode every code by hand from the format definitions
   (E2M1 and E4M3 bit fields, E8M0 exponents, the NF3 bitstream and codebook)
-  and sum x * w in Python floats, for all three formats;
+  and sum x * w in Python floats, for all three formats and both activation
+  types (the NF3 product rounded by torch's fp32 -> bf16 / fp16 conversion,
+  a single rounding since the product is exact in fp32);
 * the SwiGLU layer with one expert and top-1 gate 1, whose W2 step is the same
   product: with W13 chosen so that h = silu(gate) * up is known, the layer's
   output equals linear_forward(h, W2).
@@ -11,6 +13,7 @@
 import math
 
 import numpy as np
+import pytest
 import torch
 
 import synth
@@ -25,7 +28,7 @@ def _e4m3(b):
     return -v if s else v
 
 
-def _w_scalar(fmt, codes, scales, g, n, k):
+def _w_scalar(fmt, codes, scales, g, n, k, act="bf16"):
     if fmt in (F.FMT_NVFP4, F.FMT_MXFP4):
         byte = int(codes[n, k // 2])
         c = byte & 15 if k % 2 == 0 else byte >> 4
@@ -40,22 +43,25 @@ def _w_scalar(fmt, codes, scales, g, n, k):
                                                                   "3F1F", "3F80")], dtype=torch.int32)
           .mul(65536).view(torch.float32)]
     s = float(torch.tensor([int(scales[n, k // 64])], dtype=torch.int32).mul(65536).view(torch.float32)[0])
-    return float(torch.tensor(cb[c] * s, dtype=torch.float32).to(torch.bfloat16).float())
+    dt = torch.bfloat16 if act == "bf16" else torch.float16
+    return float(torch.tensor(cb[c] * s, dtype=torch.float32).to(dt).float())
 
 
-def test_linear_matches_scalar_loops_all_formats():
+@pytest.mark.parametrize("act", ["bf16", "f16"])
+def test_linear_matches_scalar_loops_all_formats(act):
     N, K, T = 4, 128, 3
-    x = synth.gen_x(T, K, seed=9).float().numpy().astype(np.float64)
+    xdt = torch.bfloat16 if act == "bf16" else torch.float16
+    x = synth.gen_x(T, K, seed=9, dtype=xdt).float().numpy().astype(np.float64)
     for fmt in (F.FMT_NVFP4, F.FMT_MXFP4, F.FMT_NF3):
         w = synth.gen_master(0, 2, N, K, seed=5)
         codes, scales, g = synth.quantise(fmt, w)
         c, s = codes.numpy(), scales.numpy()
         if fmt == F.FMT_NF3:
             s = s.view(np.uint16)
-        ref = linear.linear_forward(x, fmt, c, s, g, K)
+        ref = linear.linear_forward(x, fmt, c, s, g, K, act)
         for t in range(T):
             for n in range(N):
-                acc = sum(float(x[t, k]) * _w_scalar(fmt, c, s, g, n, k) for k in range(K))
+                acc = sum(float(x[t, k]) * _w_scalar(fmt, c, s, g, n, k, act) for k in range(K))
                 assert math.isclose(acc, ref[t, n], rel_tol=1e-12, abs_tol=1e-15), (fmt, t, n)
 
 

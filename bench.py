@@ -577,26 +577,27 @@ def run_profile_case(args):
     """A small, fixed case for ncu captures. It prints nothing timed.
 
     The layer has the 256-expert shape with fewer experts (--experts;
-    H=6144, I=2048, top-8, a quarter kept NVFP4). It runs --steps forwards
-    at M = --m tokens: the stream kernel for M <= 8, the tcgen05 grouped
-    kernel above that.
+    H=6144, I=2048, top-8, --kept experts kept NVFP4, a quarter by default).
+    It runs --steps forwards at M = --m tokens in tier order --tier-order:
+    the stream kernel for M <= 8, the tcgen05 grouped kernel above that.
     """
     import nf3_moe_gb300 as hm
     dev = torch.device("cuda", torch.cuda.current_device())
     E, M = args.experts, args.m
-    L = synth.make_layer(SHAPE["H"], SHAPE["I"], E, SHAPE["topk"], kept=max(1, E // 4), device=dev)
+    L = synth.make_layer(SHAPE["H"], SHAPE["I"], E, SHAPE["topk"], kept=args.kept or max(1, E // 4), device=dev)
     moe = hm.HybridMoELayer(L.H, L.I, E, L.topk, [int(b) for b in L.bit_map], expert_tuples(L), max_tokens=M)
     x = synth.gen_x(M, L.H, device=dev)
     lg = synth.gen_logits(M, E, device=dev)
     ids, gates, perm, off = moe.plan(lg)
     out = torch.empty((M, L.H), dtype=torch.bfloat16, device=dev)
     for _ in range(args.steps):
-        hm.hmoe_forward(moe.layer, x, ids, gates, perm, off, out, moe.ws)
+        hm.hmoe_forward(moe.layer, x, ids, gates, perm, off, out, moe.ws, tier_order=args.tier_order)
     torch.cuda.synchronize()
     hm.hmoe_check_device_status(moe.ws)
     fmts = [moe.layer.expert_info(e)[0] for e in range(E)]
     tb, _, ne = touched(ids.cpu().numpy(), fmts)
-    print(json.dumps({"profile_case": {"experts": E, "m": M, "steps": args.steps, "touched_experts": ne,
+    print(json.dumps({"profile_case": {"experts": E, "m": M, "steps": args.steps, "tier_order": args.tier_order,
+                                       "touched_experts": ne,
                                        "touched_packed_bytes": tb}}))
 
 
@@ -606,7 +607,9 @@ def sweep_points(dev, pk, steps=10, warmup=3):
     - the 256-expert shape with the kept tier in MXFP4 (64 MXFP4 + 192 NF3),
       M in {64, 512}, uniform N(0,1) logits;
     - the uniform NVFP4 layer (H=2048, I=768, E=128, top-8, no bit map),
-      M in {1, 8, 128, 1024, 8192}.
+      M in {1, 8, 128, 1024, 8192};
+    - the headline 256-expert hybrid layer (64 NVFP4 + 192 NF3) with fp16
+      activations, M in {8, 4096}.
     A step is plan + forward on the automatic path, captured once in a CUDA
     graph and replayed. Before every replay a 512 MB buffer is written,
     outside the event bracket, so no step finds its weights in the 129 MB L2.
@@ -619,6 +622,8 @@ def sweep_points(dev, pk, steps=10, warmup=3):
          dict(**SHAPE, kept=KEPT, kept_format=synth.FMT_MXFP4), (64, 512)),
         ("uniform NVFP4, H=2048 I=768 E=128 top-8", dict(**synth.UNIFORM_128, uniform=True),
          (1, 8, 128, 1024, 8192)),
+        ("hybrid NVFP4 + NF3 with fp16 activations, H=6144 I=2048 E=256 top-8, 64 NVFP4 + 192 NF3",
+         dict(**SHAPE, kept=KEPT, act="f16"), (8, 4096)),
     ]
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     points = []
@@ -626,17 +631,17 @@ def sweep_points(dev, pk, steps=10, warmup=3):
         L = synth.make_layer(device=dev, **kw)
         bm = None if L.bit_map is None else [int(b) for b in L.bit_map]
         moe = hm.HybridMoELayer(L.H, L.I, L.E, L.topk, bm, expert_tuples(L), kept_format=L.kept_format,
-                                max_tokens=max(ms))
+                                max_tokens=max(ms), act_dtype=hm.ACT_F16 if L.act == "f16" else hm.ACT_BF16)
         fmts = [moe.layer.expert_info(e)[0] for e in range(L.E)]
         per_w = 3 * L.H * L.I
         for M in ms:
-            x = synth.gen_x(M, L.H, seed=4000 + M, device=dev)
+            x = synth.gen_x(M, L.H, seed=4000 + M, device=dev, dtype=L.x_dtype)
             lg = synth.gen_logits(M, L.E, seed=4000 + M, device=dev)
             ids = torch.empty((M, L.topk), dtype=torch.int32, device=dev)
             gates = torch.empty((M, L.topk), dtype=torch.float32, device=dev)
             perm = torch.empty((M * L.topk,), dtype=torch.int32, device=dev)
             off = torch.empty((L.E + 1,), dtype=torch.int32, device=dev)
-            out = torch.empty((M, L.H), dtype=torch.bfloat16, device=dev)
+            out = torch.empty((M, L.H), dtype=moe.dtype, device=dev)
 
             def fwd():
                 hm.hmoe_plan_routes(moe.layer, lg, ids, gates, perm, off, moe.ws)
@@ -667,7 +672,7 @@ def sweep_points(dev, pk, steps=10, warmup=3):
             byt = sum(per_w * bpw[fmts[int(e)]] for e in es)
             tfs = 2.0 * L.topk * per_w * M / (ms_ * 1e-3) / 1e12
             path = "stream" if hm.hmoe_auto_path(moe.desc, M) == hm.PATH_STREAM else "grouped"
-            points.append({"workload": f"{name}, M={M}", "path": path,
+            points.append({"workload": f"{name}, M={M}", "path": path, "act": L.act,
                            "us_per_layer": round(ms_ * 1e3, 2), "touched_experts": int(len(es)),
                            "touched_bytes": int(byt), "hbm_gbs": round(byt / (ms_ * 1e-3) / 1e9, 1),
                            "frac_hbm": round(byt / (ms_ * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
@@ -706,6 +711,9 @@ def main():
     ap.add_argument("--soak-s", type=float, default=1.0)
     ap.add_argument("--profile", action="store_true", help="run the small fixed case used for ncu captures")
     ap.add_argument("--experts", type=int, default=64, help="experts in the --profile case")
+    ap.add_argument("--tier-order", type=int, default=0, choices=(0, 1, 2),
+                    help="tier_order of the --profile case's forwards (0 one launch, 1 kept first, 2 NF3 first)")
+    ap.add_argument("--kept", type=int, default=0, help="kept experts in the --profile case (0: a quarter)")
     ap.add_argument("--sweep", action="store_true", help="time only the MXFP4-kept and uniform NVFP4 configurations")
     ap.add_argument("--skip-sweep", action="store_true", help="leave the other configurations out of the line")
     ap.add_argument("--sweep-steps", type=int, default=10)

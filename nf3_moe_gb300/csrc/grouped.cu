@@ -210,6 +210,17 @@ __device__ __forceinline__ void tma_expect_load_2d_elect(void* dst, const CUtens
       "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "r"(bytes)
       : "memory");
 }
+// The same load without the expect_tx arrival (a second box on a barrier
+// whose bytes an earlier tma_expect_load_2d_elect already registered).
+__device__ __forceinline__ void tma_load_2d_elect(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n\t}" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_2d_elect(const CUtensorMap* map, int x, int y) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
@@ -270,9 +281,33 @@ __device__ __forceinline__ uint32_t idesc_kf16(int M, int N) {
   return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// A work item: nt token tiles of 128 permuted slots from p0 (n slots in all)
+// times nr weight row tiles from rt. Two shapes, both 512 cycles of tensor
+// work per k-block and 256 accumulator columns:
+//   nt = 1, nr = 1 or 2: one token tile (A, M = 128) times the row-tile pair
+//     (B, N = 256): 4 MMAs of 128 x 256 x 16 per k-block;
+//   nt = 2, nr = 1: two token tiles (two A operands) times one row tile (B,
+//     N = 128): 8 MMAs of 128 x 128 x 16, into accumulator columns 0..127
+//     (tile 0) and 128..255 (tile 1).
+// An expert with more than 128 routed slots takes the second shape for each
+// full 256-slot pair of token tiles (and for a remainder above 128), so each
+// weight row tile is dequantised once per 256 slots instead of once per 128
+// (measured 3.33 -> 3.22 ms at M=4096 with Zipf routing, where the 256
+// experts need 379 token tiles); a remainder of at most 128 slots takes the
+// first shape. (An N = 128 MMA issues in about 77 cycles against 64 of
+// tensor work, so the second shape is bound by its issuing thread.)
 struct GtItem {
-  int e, p0, n, rt, nr;  // row tiles rt .. rt + nr - 1 (nr = 1 or 2)
+  int e, p0, n, rt, nr, nt;
 };
+
+__host__ __device__ __forceinline__ int gt_items_of(int ne, int RT) {
+  if (ne <= 0) return 0;
+  const int RP = (RT + GT_R - 1) / GT_R;
+  const int full = ne / (2 * GT_N), r = ne % (2 * GT_N);
+  const int n2 = full + (r > GT_N ? 1 : 0);
+  const int n1 = (r > 0 && r <= GT_N) ? 1 : 0;
+  return n2 * RT + n1 * RP;
+}
 
 __device__ __forceinline__ int gt_expert_fmt(const GroupedParams& p, int e) {
   return (p.tab.loc[e] & LOC_NF3) ? FMT_NF3 : p.kept_fmt;
@@ -287,16 +322,27 @@ __device__ __forceinline__ GtItem gt_decode(const GroupedParams& p, const int* s
   GtItem it;
   it.e = lo;
   const int o0 = s_off[lo], ne = s_off[lo + 1] - o0;
-  // Row-tile pairs fastest: the CTAs that run together share one activation
-  // tile through L2, and an expert's token tiles follow each other, so its
-  // weight tiles are re-read from L2 rather than HBM.
-  const int RP = (p.RT + GT_R - 1) / GT_R;
+  // Row tiles (or row-tile pairs) fastest: the CTAs that run together share
+  // one activation tile through L2, and an expert's token tiles follow each
+  // other, so its weight tiles are re-read from L2 rather than HBM.
   const int local = i - s_istart[lo];
-  it.rt = (local % RP) * GT_R;
-  it.nr = min(GT_R, p.RT - it.rt);
-  const int nt = local / RP;
-  it.p0 = o0 + nt * GT_N;
-  it.n = min(GT_N, ne - nt * GT_N);
+  const int full = ne / (2 * GT_N), r = ne % (2 * GT_N);
+  const int n2 = full + (r > GT_N ? 1 : 0);
+  if (local < n2 * p.RT) {
+    const int tp = local / p.RT;
+    it.rt = local % p.RT;
+    it.nr = 1;
+    it.nt = 2;
+    it.p0 = o0 + tp * 2 * GT_N;
+    it.n = min(2 * GT_N, ne - tp * 2 * GT_N);
+  } else {
+    const int l1 = local - n2 * p.RT;
+    it.rt = l1 * GT_R;
+    it.nr = min(GT_R, p.RT - it.rt);
+    it.nt = 1;
+    it.p0 = o0 + n2 * 2 * GT_N;
+    it.n = ne - n2 * 2 * GT_N;
+  }
   return it;
 }
 
@@ -427,7 +473,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         if (ne < 0) bad = true;
         const bool nf3 = (p.tab.loc[e] & LOC_NF3) != 0;
         const bool sel = nf3 ? (p.tier_mask & 2) : (p.tier_mask & 1);
-        ni = (sel && ne > 0) ? ((ne + GT_N - 1) / GT_N) * ((p.RT + GT_R - 1) / GT_R) : 0;
+        ni = sel ? gt_items_of(ne, p.RT) : 0;
       }
       int incl = ni;
 #pragma unroll
@@ -511,10 +557,19 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
           aborted = true;
           break;
         }
+        // Token tile 0 goes to the slot's activation tile; with two token
+        // tiles, tile 1 goes to the second weight-tile half, unused by
+        // one-row-tile items.
         tma_expect_load_2d_elect(smem + GT_OFF_B + slot * GT_B_BYTES, &tmap_b, kb * TILE_K, it.p0, &afull[slot],
-                                 GT_B_BYTES);
-        // Warm L2 with a tile needed a few loads from now (same token tile).
-        if (kb + GT_BPREFETCH < p.KB) tma_prefetch_2d_elect(&tmap_b, (kb + GT_BPREFETCH) * TILE_K, it.p0);
+                                 (uint32_t)(it.nt * GT_B_BYTES));
+        if (it.nt == 2)
+          tma_load_2d_elect(smem + GT_OFF_A + slot * GT_A_BYTES + GT_A_TILE, &tmap_b, kb * TILE_K, it.p0 + GT_N,
+                            &afull[slot]);
+        // Warm L2 with the tiles needed a few loads from now (same token tiles).
+        if (kb + GT_BPREFETCH < p.KB) {
+          tma_prefetch_2d_elect(&tmap_b, (kb + GT_BPREFETCH) * TILE_K, it.p0);
+          if (it.nt == 2) tma_prefetch_2d_elect(&tmap_b, (kb + GT_BPREFETCH) * TILE_K, it.p0 + GT_N);
+        }
         ++issued;
         if (++slot == GT_OSTAGES) {
           slot = 0;
@@ -557,7 +612,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t idesc = idesc_kf16<ACT>(128, it.nr * 128);
+      const uint32_t idesc = idesc_kf16<ACT>(128, it.nt == 2 ? 128 : it.nr * 128);
       const uint32_t d_tmem = tmem_base + (uint32_t)(buf * GT_ACC_COLS);
       // Operand slots are ordered by their barrier and the writers' proxy
       // fence; the tcgen05 fence after the accumulator hand-off covers TMEM.
@@ -573,13 +628,27 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         }
         const uint32_t x_lo = x_lo0 + (uint32_t)os * (GT_B_BYTES >> 4);
         const uint32_t w_lo = w_lo0 + (uint32_t)os * (GT_A_BYTES >> 4);
-        umma_kf16_warp(d_tmem, desc_from_lo(x_lo), desc_from_lo(w_lo), idesc, kb ? 1u : 0u);
-        umma_kf16_warp(d_tmem, desc_from_lo(x_lo + 2), desc_from_lo(w_lo + 2), idesc, 1u);
         const int os_next = os + 1 == GT_OSTAGES ? 0 : os + 1;
         const uint32_t oph_next = os + 1 == GT_OSTAGES ? oph ^ 1u : oph;
-        ready = kb + 1 < p.KB && __all_sync(0xffffffffu, mbar_test(&afull[os_next], oph_next));
-        umma_kf16_warp(d_tmem, desc_from_lo(x_lo + 4), desc_from_lo(w_lo + 4), idesc, 1u);
-        umma_kf16_warp(d_tmem, desc_from_lo(x_lo + 6), desc_from_lo(w_lo + 6), idesc, 1u);
+        if (it.nt == 2) {
+          // token tile 1's activations sit in the second weight-tile half
+          const uint32_t x1_lo = w_lo + (GT_A_TILE >> 4);
+          umma_kf16_warp(d_tmem, desc_from_lo(x_lo), desc_from_lo(w_lo), idesc, kb ? 1u : 0u);
+          umma_kf16_warp(d_tmem, desc_from_lo(x_lo + 2), desc_from_lo(w_lo + 2), idesc, 1u);
+          umma_kf16_warp(d_tmem, desc_from_lo(x_lo + 4), desc_from_lo(w_lo + 4), idesc, 1u);
+          umma_kf16_warp(d_tmem, desc_from_lo(x_lo + 6), desc_from_lo(w_lo + 6), idesc, 1u);
+          ready = kb + 1 < p.KB && __all_sync(0xffffffffu, mbar_test(&afull[os_next], oph_next));
+          umma_kf16_warp(d_tmem + 128, desc_from_lo(x1_lo), desc_from_lo(w_lo), idesc, kb ? 1u : 0u);
+          umma_kf16_warp(d_tmem + 128, desc_from_lo(x1_lo + 2), desc_from_lo(w_lo + 2), idesc, 1u);
+          umma_kf16_warp(d_tmem + 128, desc_from_lo(x1_lo + 4), desc_from_lo(w_lo + 4), idesc, 1u);
+          umma_kf16_warp(d_tmem + 128, desc_from_lo(x1_lo + 6), desc_from_lo(w_lo + 6), idesc, 1u);
+        } else {
+          umma_kf16_warp(d_tmem, desc_from_lo(x_lo), desc_from_lo(w_lo), idesc, kb ? 1u : 0u);
+          umma_kf16_warp(d_tmem, desc_from_lo(x_lo + 2), desc_from_lo(w_lo + 2), idesc, 1u);
+          ready = kb + 1 < p.KB && __all_sync(0xffffffffu, mbar_test(&afull[os_next], oph_next));
+          umma_kf16_warp(d_tmem, desc_from_lo(x_lo + 4), desc_from_lo(w_lo + 4), idesc, 1u);
+          umma_kf16_warp(d_tmem, desc_from_lo(x_lo + 6), desc_from_lo(w_lo + 6), idesc, 1u);
+        }
         umma_commit_warp(&oempty[os]);
         os = os_next;
         oph = oph_next;
@@ -648,23 +717,33 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const bool live = c < it.n;
-      int slot = -1;
-      if (p.which != 13 && live) {
-        const int sc = p.perm[it.p0 + c];
-        if (sc >= 0 && sc < S) slot = sc;
-        else set_status(p.status, DEV_BAD_ROUTE);
+      // Thread c holds token c of each token tile: slot c (tile 0) and, for
+      // two-tile items, slot 128 + c (tile 1, accumulator columns 128..255).
+      int slot0 = -1, slot1 = -1;
+      if (p.which != 13) {
+        if (c < it.n) {
+          const int sc = p.perm[it.p0 + c];
+          if (sc >= 0 && sc < S) slot0 = sc;
+          else set_status(p.status, DEV_BAD_ROUTE);
+        }
+        if (it.nt == 2 && GT_N + c < it.n) {
+          const int sc = p.perm[it.p0 + GT_N + c];
+          if (sc >= 0 && sc < S) slot1 = sc;
+          else set_status(p.status, DEV_BAD_ROUTE);
+        }
       }
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * GT_ACC_COLS);
-      const int nchunk = it.nr * 4;
+      const int nchunk = it.nt == 2 ? 8 : it.nr * 4;
       for (int q = 0; q < nchunk; ++q) {
         uint32_t v[32];
         tmem_ld32(tbase + (uint32_t)(32 * q), v);
         tmem_wait_ld();
-        const int rt = it.rt + (q >> 2);
+        const int tt = it.nt == 2 ? (q >> 2) : 0;             // token tile of the chunk
+        const int rt = it.nt == 2 ? it.rt : it.rt + (q >> 2);  // row tile of the chunk
         const int r0 = (q & 3) * 32;  // first tile-local row of the chunk
+        const int tok = tt * GT_N + c;
         if (p.which == 13) {
-          if (!live) continue;
+          if (tok >= it.n) continue;
           const float gsc = p.tab.g13[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f);
 #pragma unroll
           for (int g = 0; g < 2; ++g) {
@@ -679,9 +758,10 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
               const float u1 = __uint_as_float(v[16 * g + 8 + 2 * w + 1]) * gsc;
               hv[w] = f32x2_to_act<ACT>(silu_fast(g0) * u0, silu_fast(g1) * u1);
             }
-            *reinterpret_cast<uint4*>(p.h_out + (size_t)(it.p0 + c) * p.I + ch) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            *reinterpret_cast<uint4*>(p.h_out + (size_t)(it.p0 + tok) * p.I + ch) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
           }
         } else {
+          const int slot = tt ? slot1 : slot0;
           if (slot < 0) continue;
           const float gsc = p.tab.g2[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f);
           float4* dst = reinterpret_cast<float4*>(p.y_out + (size_t)slot * p.H + rt * 128 + r0);

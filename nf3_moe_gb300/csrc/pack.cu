@@ -164,7 +164,7 @@ cudaError_t launch_pack_matrix(int fmt, int which, const void* codes, const void
 
 // ------------------------------------------------------------ debug export of operand tiles
 // Both exports run dequant_slot, the decoder the GEMM kernels run, with the
-// same shared E4M3 table the kernels build:
+// same shared tables the kernels build (E4M3; NF3 pairs in decode mode):
 //   tile mode (WITH_NF3_SCALE = true): the operand tile (bf16 or fp16) the
 //     tensor-core grouped kernel writes to shared memory. NVFP4 values in
 //     bf16 are carried times 2^-63 inside the kernels (the factor returns
@@ -174,9 +174,11 @@ cudaError_t launch_pack_matrix(int fmt, int which, const void* codes, const void
 //     are the raw codebook entries, and scales_out receives the fp32 factor
 //     the kernel applies to each row's 64-wide group sum (1 for NVFP4/MXFP4).
 template <int FMT, bool WITH_NF3_SCALE, int ACT>
-__device__ __forceinline__ void debug_slot(const uint8_t* tile, int rg, int lane, const uint32_t* lut, uint32_t* r0,
-                                           uint32_t* r1, float* s0, float* s1) {
-  dequant_slot<FMT, WITH_NF3_SCALE, ACT>(tile, rg, lane, r0, r1, s0, s1, lut);
+__device__ __forceinline__ void debug_slot(const uint8_t* tile, int rg, int lane, const uint32_t* lut,
+                                           uint32_t nf3_lut, uint32_t* r0, uint32_t* r1, float* s0, float* s1) {
+  // The tensor-core kernel (tile mode) decodes NF3 with byte permutes, the
+  // weight-streaming kernel (decode mode) with the shared pair table.
+  dequant_slot<FMT, WITH_NF3_SCALE, ACT, !WITH_NF3_SCALE>(tile, rg, lane, r0, r1, s0, s1, lut, nf3_lut);
   if constexpr (FMT == FMT_NVFP4 && ACT == ACT_BF16) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -190,17 +192,20 @@ template <bool WITH_NF3_SCALE, int ACT>
 __global__ void debug_dequant_kernel(int fmt, int which, const uint8_t* __restrict__ src, int N, int K, int I,
                                      uint16_t* __restrict__ dst, float* __restrict__ scales_out) {
   __shared__ uint32_t s_e4m3[256];
+  __shared__ uint32_t s_nf3[NF3_LUT_WORDS];
   s_e4m3[threadIdx.x] = e4m3_lut_entry<ACT>(threadIdx.x);
+  nf3_lut_fill<ACT>(s_nf3, threadIdx.x, blockDim.x);
   __syncthreads();
+  const uint32_t nf3_lut = smem_u32(s_nf3) + 4u * (threadIdx.x & 31);
   const int KB = K / TILE_K;
   const int rt = blockIdx.x / KB, kb = blockIdx.x % KB;
   const int tid = threadIdx.x, rg = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
   const uint8_t* tile = src + ((size_t)rt * KB + kb) * tile_bytes(fmt);
   uint32_t r0[8], r1[8];
   float s0 = 1.0f, s1 = 1.0f;
-  if (fmt == FMT_NVFP4) debug_slot<FMT_NVFP4, WITH_NF3_SCALE, ACT>(tile, rg, lane, s_e4m3, r0, r1, &s0, &s1);
-  else if (fmt == FMT_MXFP4) debug_slot<FMT_MXFP4, WITH_NF3_SCALE, ACT>(tile, rg, lane, s_e4m3, r0, r1, &s0, &s1);
-  else debug_slot<FMT_NF3, WITH_NF3_SCALE, ACT>(tile, rg, lane, s_e4m3, r0, r1, &s0, &s1);
+  if (fmt == FMT_NVFP4) debug_slot<FMT_NVFP4, WITH_NF3_SCALE, ACT>(tile, rg, lane, s_e4m3, nf3_lut, r0, r1, &s0, &s1);
+  else if (fmt == FMT_MXFP4) debug_slot<FMT_MXFP4, WITH_NF3_SCALE, ACT>(tile, rg, lane, s_e4m3, nf3_lut, r0, r1, &s0, &s1);
+  else debug_slot<FMT_NF3, WITH_NF3_SCALE, ACT>(tile, rg, lane, s_e4m3, nf3_lut, r0, r1, &s0, &s1);
   const int L0 = logical_row(which, I, rt, rg * 16 + g), L1 = logical_row(which, I, rt, rg * 16 + g + 8);
   const int k0 = kb * TILE_K + 16 * q;
   uint4* d0 = reinterpret_cast<uint4*>(dst + (size_t)L0 * K + k0);

@@ -55,7 +55,8 @@ constexpr int SK_HDR_BYTES = 16;                           // {item, stage} writ
 constexpr int SK_STAGE_BYTES = SK_W_BYTES + SK_X_BYTES + SK_HDR_BYTES;
 constexpr int SK_SMEM_DATA = SK_STAGES * SK_STAGE_BYTES;
 constexpr int SK_NBAR = 2 * SK_STAGES;
-constexpr int SK_SMEM_BYTES = SK_SMEM_DATA + SK_NBAR * 8 + 2 * (MAX_E + 1) * 4 + 4 * 4 + 256 * 4;
+constexpr int SK_SMEM_BYTES = SK_SMEM_DATA + SK_NBAR * 8 + 2 * (MAX_E + 1) * 4 + 4 * 4 + 256 * 4 + NF3_LUT_BYTES;
+static_assert(2 * (SK_SMEM_BYTES + 1024) <= 233472, "two CTAs per SM");
 static_assert(SK_STAGE_BYTES % 16 == 0, "stage alignment");
 
 struct SkItem {
@@ -122,13 +123,13 @@ __device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it,
 // applied to the fp32 sum of the k-block) and 4 MMAs.
 template <int FMT, int ACT>
 __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xrow, int rg, int lane,
-                                          const uint32_t* s_e4m3, float* acc) {
+                                          const uint32_t* s_e4m3, uint32_t nf3_lut, float* acc) {
   const uint4 xa = *reinterpret_cast<const uint4*>(xrow);
   const uint4 xb = *reinterpret_cast<const uint4*>(xrow + 16);
   const uint32_t xr[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
   uint32_t r0[8], r1[8];
   float sc0, sc1;
-  dequant_slot<FMT, false, ACT>(tile, rg, lane, r0, r1, &sc0, &sc1, s_e4m3);
+  dequant_slot<FMT, false, ACT, true>(tile, rg, lane, r0, r1, &sc0, &sc1, s_e4m3, nf3_lut);
   if constexpr (FMT == FMT_NVFP4 || FMT == FMT_MXFP4) {
 #pragma unroll
     for (int s = 0; s < 4; ++s)
@@ -149,18 +150,18 @@ __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xr
 // All k-blocks of one stage, two accumulator sets to break the MMA chain.
 template <int FMT, int ACT>
 __device__ __forceinline__ void sk_stage(const uint8_t* sw, const uint8_t* sx, int kbs, int rg, int lane,
-                                         const uint32_t* s_e4m3, float* accA, float* accB) {
+                                         const uint32_t* s_e4m3, uint32_t nf3_lut, float* accA, float* accB) {
   constexpr int TB = tile_bytes(FMT);
   if (kbs == 8) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) sk_kblock<FMT, ACT>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, (j & 1) ? accB : accA);
+    for (int j = 0; j < 8; ++j) sk_kblock<FMT, ACT>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, nf3_lut, (j & 1) ? accB : accA);
   } else if (kbs == 4) {
-    sk_kblock<FMT, ACT>(sw, sx, rg, lane, s_e4m3, accA);
-    sk_kblock<FMT, ACT>(sw + TB, sx + 128, rg, lane, s_e4m3, accB);
-    sk_kblock<FMT, ACT>(sw + 2 * TB, sx + 256, rg, lane, s_e4m3, accA);
-    sk_kblock<FMT, ACT>(sw + 3 * TB, sx + 384, rg, lane, s_e4m3, accB);
+    sk_kblock<FMT, ACT>(sw, sx, rg, lane, s_e4m3, nf3_lut, accA);
+    sk_kblock<FMT, ACT>(sw + TB, sx + 128, rg, lane, s_e4m3, nf3_lut, accB);
+    sk_kblock<FMT, ACT>(sw + 2 * TB, sx + 256, rg, lane, s_e4m3, nf3_lut, accA);
+    sk_kblock<FMT, ACT>(sw + 3 * TB, sx + 384, rg, lane, s_e4m3, nf3_lut, accB);
   } else {
-    for (int j = 0; j < kbs; ++j) sk_kblock<FMT, ACT>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, (j & 1) ? accB : accA);
+    for (int j = 0; j < kbs; ++j) sk_kblock<FMT, ACT>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, nf3_lut, (j & 1) ? accB : accA);
   }
 }
 
@@ -172,7 +173,8 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
   int* s_gstart = reinterpret_cast<int*>(empty + SK_STAGES);
   int* s_off = s_gstart + MAX_E + 1;             // the caller's offsets, copied once
   volatile int* s_flags = s_off + MAX_E + 1;     // [0] abort
-  uint32_t* s_e4m3 = reinterpret_cast<uint32_t*>(const_cast<int*>(s_flags) + 4);  // E4M3 -> bf16 pair
+  uint32_t* s_e4m3 = reinterpret_cast<uint32_t*>(const_cast<int*>(s_flags) + 4);  // E4M3 -> operand-type pair
+  uint32_t* s_nf3 = s_e4m3 + 256;                                                // NF3 pair table
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint64_t lim = p.wait_limit_ns;
 
@@ -185,6 +187,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
     s_flags[0] = 0;
   }
   if (tid < 256) s_e4m3[tid] = e4m3_lut_entry<ACT>((uint32_t)tid);
+  nf3_lut_fill<ACT>(s_nf3, tid, blockDim.x);
   pdl_wait();  // everything below reads or writes global memory
   pdl_trigger();
   for (int e = tid; e <= p.E; e += blockDim.x) s_off[e] = p.offsets[e];
@@ -348,6 +351,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
   } else {
     // ------------------------------------------------ consumers
     const int rg = warp, g = lane >> 2, q = lane & 3;
+    const uint32_t nf3_lut = smem_u32(s_nf3) + 4u * (uint32_t)lane;
     int slot = 0;
     uint32_t ph = 0;
     SkItem it{};
@@ -374,9 +378,9 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
         for (int r = 0; r < 4; ++r) accA[r] = accB[r] = 0.f;
       }
       const uint8_t* sx = sw + SK_W_BYTES + g * SK_XROW + q * 32;
-      if (fmt == FMT_NVFP4) sk_stage<FMT_NVFP4, ACT>(sw, sx, kbs, rg, lane, s_e4m3, accA, accB);
-      else if (fmt == FMT_MXFP4) sk_stage<FMT_MXFP4, ACT>(sw, sx, kbs, rg, lane, s_e4m3, accA, accB);
-      else sk_stage<FMT_NF3, ACT>(sw, sx, kbs, rg, lane, s_e4m3, accA, accB);
+      if (fmt == FMT_NVFP4) sk_stage<FMT_NVFP4, ACT>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, accA, accB);
+      else if (fmt == FMT_MXFP4) sk_stage<FMT_MXFP4, ACT>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, accA, accB);
+      else sk_stage<FMT_NF3, ACT>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, accA, accB);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
       if (++slot == SK_STAGES) {

@@ -35,8 +35,10 @@
  *     range, inconsistent offsets, a bounded wait that timed out) do not
  *     trap. Kernels skip the bad access and record a code in the workspace.
  *     hmoe_check_device_status reads that code.
- *   - No C++ exceptions cross this boundary, and no environment variable is
- *     read.
+ *   - No C++ exceptions cross this boundary, and no environment variable
+ *     configures the library. (Each entry point opens an NVTX range named
+ *     after it, for profiler timelines; NVTX looks up its profiler-injection
+ *     hook once, and without a profiler the ranges do nothing.)
  *   - Layout of the logical checkpoint tensors (the input to
  *     hmoe_pack_weights), for one matrix [N rows, K] of one expert:
  *       NVFP4: codes uint8 [N][K/2]. Element 2i is the low nibble, element

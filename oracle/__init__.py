@@ -26,9 +26,10 @@ Modules:
   route   -- top-k routing, renormalised gates, stable permutation, offsets.
   layer   -- the SwiGLU expert layer: dequantise, then matmul, gate, sum.
   linear  -- the dense-Linear W4A16 product: dequantise, then matmul.
+  actquant -- NVFP4 activation quantisation (the W4A4 layer's x and h).
 
 Every function here is pinned by ``tests/test_oracle_*.py`` against library
 routines, closed forms, golden fixtures or brute force.
 """
 
-from . import formats, route, layer, linear  # noqa: F401
+from . import formats, route, layer, linear, actquant  # noqa: F401

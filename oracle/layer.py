@@ -24,11 +24,17 @@ Experts are supplied through ``get_expert(e)``. It returns a dict with keys
 caller stream experts one at a time at full size. An optional key ``act``
 ("bf16", the default, or "f16") names the layer's activation type, to which
 the weights are dequantised ([P3] "Summary", item 2).
+
+W4A4 ([P3] "Summary": the W4A4 NVFP4 scheme, activations quantised to NVFP4
+as they arrive): an optional key ``act_quant`` = (g13, g2) holds the static
+global scales of the two activations. Then x is replaced by
+actquant.fake_quant(x, g13) before W13, and h, rounded to the activation type
+(it is an activation of the layer), by actquant.fake_quant(h, g2) before W2.
 """
 
 import numpy as np
 
-from . import formats
+from . import actquant, formats
 
 
 def silu(z):
@@ -47,10 +53,22 @@ def expert_weights(ex, H, I):
     return w13, w2
 
 
-def expert_ffn(w13, w2, xf, I, out_rows=None):
-    """SwiGLU FFN of one expert on a batch of rows xf [n, H] -> [n, H] (or [n, len(out_rows)])."""
+def round_act(h, act):
+    """h rounded to the activation type (through fp32, as the kernels form h in fp32)."""
+    h32 = np.asarray(h, dtype=np.float64).astype(np.float32).astype(np.float64)
+    return formats.bf16_rne(h32) if act == "bf16" else formats.f16_rne(h32)
+
+
+def expert_ffn(w13, w2, xf, I, out_rows=None, act_quant=None, act="bf16"):
+    """SwiGLU FFN of one expert on a batch of rows xf [n, H] -> [n, H] (or [n, len(out_rows)]).
+
+    act_quant = (g13, g2): the W4A4 activation quantisation (module docstring)."""
+    if act_quant is not None:
+        xf = actquant.fake_quant(xf, act_quant[0])
     gu = xf @ w13.T                       # [n, 2I]
     h = silu(gu[:, :I]) * gu[:, I:]       # [n, I]
+    if act_quant is not None:
+        h = actquant.fake_quant(round_act(h, act), act_quant[1])
     w2r = w2 if out_rows is None else w2[out_rows]
     return h @ w2r.T
 
@@ -76,8 +94,10 @@ def moe_forward(x, ids, gates, get_expert, H, I, tokens=None, cols=None):
     sub_ids = ids[tokens]
     for e in np.unique(sub_ids):
         tl, jj = np.nonzero(sub_ids == e)
-        w13, w2 = expert_weights(get_expert(int(e)), H, I)
-        y[tl, jj] = expert_ffn(w13, w2, x[tokens[tl]], I, out_rows=cols)
+        ex = get_expert(int(e))
+        w13, w2 = expert_weights(ex, H, I)
+        y[tl, jj] = expert_ffn(w13, w2, x[tokens[tl]], I, out_rows=cols, act_quant=ex.get("act_quant"),
+                               act=ex.get("act", "bf16"))
     out = np.zeros((len(tokens), ncol), dtype=np.float64)
     for j in range(k):
         out += gates[tokens, j][:, None] * y[:, j]

@@ -170,9 +170,10 @@ def quantise(fmt, w):
 class Layer:
     """One synthetic layer: per-expert formats plus logical packed tensors."""
 
-    def __init__(self, H, I, E, topk, bit_map, kept_format, experts, act="bf16"):
+    def __init__(self, H, I, E, topk, bit_map, kept_format, experts, act="bf16", act_quant=None):
         self.H, self.I, self.E, self.topk = H, I, E, topk
         self.act = act                    # activation type: "bf16" or "f16"
+        self.act_quant = act_quant        # None, or (g13, g2): W4A4 activation global scales
         self.bit_map = bit_map            # numpy int8 [E] (4 kept / 3 NF3) or None (uniform)
         self.kept_format = kept_format
         self.experts = experts            # list of dicts: fmt, w13=(c,s,g), w2=(c,s,g)
@@ -192,8 +193,11 @@ class Layer:
             return t.cpu().numpy()
         c13, s13, g13 = ex["w13"]
         c2, s2, g2 = ex["w2"]
-        return {"fmt": ex["fmt"], "w13": (host(c13), host(s13), g13),
-                "w2": (host(c2), host(s2), g2), "act": self.act}
+        d = {"fmt": ex["fmt"], "w13": (host(c13), host(s13), g13), "w2": (host(c2), host(s2), g2),
+             "act": self.act}
+        if self.act_quant is not None:
+            d["act_quant"] = tuple(float(v) for v in self.act_quant)
+        return d
 
     @property
     def x_dtype(self):

@@ -34,7 +34,7 @@ _BLAS_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
 def _expert_rows(job):
     ex, H, I, xs = job
     w13, w2 = olayer.expert_weights(ex, H, I)
-    return olayer.expert_ffn(w13, w2, xs, I)
+    return olayer.expert_ffn(w13, w2, xs, I, act_quant=ex.get("act_quant"), act=ex.get("act", "bf16"))
 
 
 def host_workers(n_jobs, cap=16):

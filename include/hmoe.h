@@ -94,6 +94,19 @@ typedef enum { HMOE_FMT_NF3 = 3, HMOE_FMT_NVFP4 = 4, HMOE_FMT_MXFP4 = 5 } hmoe_f
  * must fit fp16 like any fp16 model's. */
 typedef enum { HMOE_ACT_BF16 = 0, HMOE_ACT_F16 = 1 } hmoe_act_dtype;
 
+/* Activation quantisation: none (W4A16) or NVFP4 (W4A4).
+ *   Cites: "[Quantization][ModelOpt] W4A16 NVFP4 fused MoE + ...", Summary
+ *   (the W4A4 NVFP4 scheme: static NVFP4 weights, activations quantised to
+ *   NVFP4 as they arrive).
+ * With HMOE_ACT_QUANT_NVFP4 the forward quantises x before W13 and h (after
+ * rounding to the activation type) before W2, each in blocks of 16 along the
+ * row with the rule of hmoe_quantize_act_nvfp4 and the layer's static global
+ * scale of that activation (act_global13, act_global2). The products are
+ * computed exactly: e2m1 * e4m3 values are exact in bf16 and fp16, so the
+ * same tensor-core and streaming kernels run on them, and the global scales
+ * are applied to the fp32 sums. */
+typedef enum { HMOE_ACT_QUANT_NONE = 0, HMOE_ACT_QUANT_NVFP4 = 1 } hmoe_act_quant;
+
 /* One MoE layer's shape. kept_format is HMOE_FMT_NVFP4 or HMOE_FMT_MXFP4. */
 typedef struct {
   int H;           /* hidden size, a multiple of 128 */
@@ -102,6 +115,9 @@ typedef struct {
   int topk;        /* experts per token, 1..min(E, 32) */
   int kept_format; /* hmoe_fmt of the kept (bit 4) tier */
   int act_dtype;   /* hmoe_act_dtype; 0 (a zeroed struct) is bf16 */
+  int act_quant;   /* hmoe_act_quant; 0 (a zeroed struct) is W4A16 */
+  float act_global13; /* W4A4: static global scale of x (the W13 input), finite and > 0 */
+  float act_global2;  /* W4A4: static global scale of h (the W2 input), finite and > 0 */
 } hmoe_layer_desc;
 
 /* One expert's logical checkpoint tensors (device pointers, layout above).
@@ -134,7 +150,8 @@ hmoe_status hmoe_packed_size(const hmoe_layer_desc* desc, const int8_t* bit_map,
  *   Cites: "quant: add native mixed NVFP4/MXFP4 plus NF3 MoE serving",
  *   Summary (scratch sized from the maximum batched token count).
  * The workspace holds the status word, the kernels' self-cleaning work
- * queues, the routing chunk counts, the gathered activation rows (T > 8),
+ * queues, the routing chunk counts, the quantised input (W4A4 only), the
+ * gathered activation rows (T > 8),
  * the SwiGLU output h [T*k][I] (16-bit) and the per-slot W2 output [T*k][H]
  * fp32. Errors: the desc checks (HMOE_ERR_INVALID_ARG,
  * HMOE_ERR_UNSUPPORTED_SHAPE); max_tokens < 0 or bytes NULL is
@@ -325,7 +342,9 @@ hmoe_status hmoe_debug_dequant(const hmoe_layer* layer, int expert, int which, v
  * output row as the sum over 64-wide K groups g of scales[n][g] times the
  * fp32 sum over the group of dst[n][k] * x[k] (NVFP4 then times its global
  * scale). NF3: dst is the raw codebook entry cb[code] and scales the group's
- * bf16 scale as fp32; NVFP4 and MXFP4: dst is the tile of hmoe_debug_dequant and
+ * bf16 scale as fp32 (for W4A4 layers, whose h the streaming kernel must form
+ * from the same weights as the tensor-core kernel: the tile of
+ * hmoe_debug_dequant and scales 1); NVFP4 and MXFP4: dst is the tile of hmoe_debug_dequant and
  * scales are 1. */
 hmoe_status hmoe_debug_decode_operand(const hmoe_layer* layer, int expert, int which, void* dst,
                                       float* scales, hmoe_stream_t stream);
@@ -392,6 +411,23 @@ hmoe_status hmoe_linear_forward_ex(const hmoe_linear* linear, const void* x, int
                                    size_t ws_bytes, const hmoe_forward_opts* opts, hmoe_stream_t stream);
 
 void hmoe_linear_destroy(hmoe_linear* linear);
+
+/* NVFP4 activation quantisation, the rule the W4A4 forward applies:
+ *   for each block of 16 consecutive values of a row, in fp32 arithmetic
+ *   (each operation correctly rounded),
+ *     s = E4M3_rne(min(amax / (6 g), 448)),  d = e4m3(s) * g,
+ *     q_i = E2M1_rne_sat(a_i / d) (0 where d = 0; ties to the even mantissa
+ *     bit, saturating at 6; a value that rounds to 0 gives code 0).
+ *   Cites: "[Quantization][ModelOpt] W4A16 NVFP4 fused MoE + ...", Summary.
+ * x: device [rows][K] of act_dtype, 16-byte aligned; K a multiple of 16.
+ * codes: device uint8 [rows][K/2] (element 2i in the low nibble), 8-byte
+ * aligned; scales: device uint8 [rows][K/16] E4M3 bytes. The logical NVFP4
+ * layout of this header, so the output can be dequantised like weights with
+ * global scale g. global_scale: finite and > 0. rows = 0 is valid.
+ * Errors: HMOE_ERR_INVALID_ARG (NULL or misaligned pointer, rows < 0, K not a
+ * positive multiple of 16, bad act_dtype or scale), HMOE_ERR_CUDA. */
+hmoe_status hmoe_quantize_act_nvfp4(const void* x, int rows, int K, int act_dtype, float global_scale,
+                                    void* codes, void* scales, hmoe_stream_t stream);
 
 /* Message for the last failing call on this thread ("" if none). */
 const char* hmoe_last_error(void);

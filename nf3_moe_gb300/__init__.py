@@ -20,14 +20,15 @@ import torch
 from . import _lib
 from ._lib import (FMT_MXFP4, FMT_NF3, FMT_NVFP4, PATH_AUTO, PATH_GROUPED, PATH_STREAM,  # noqa: F401
                    TIERS_KEPT_FIRST, TIERS_NF3_FIRST, TIERS_ONE_LAUNCH, HmoeError, LayerDesc, LinearDesc,
-                   DEBUG_NO_COPIES, DEBUG_GROUPED_PAIR, ACT_BF16, ACT_F16)
+                   DEBUG_NO_COPIES, DEBUG_GROUPED_PAIR, ACT_BF16, ACT_F16, ACT_QUANT_NONE, ACT_QUANT_NVFP4)
 
 __all__ = [
     "LayerDesc", "HmoeError", "hmoe_packed_size", "hmoe_workspace_size", "hmoe_workspace_init",
     "hmoe_pack_weights", "hmoe_plan_routes", "hmoe_forward", "hmoe_check_device_status",
     "hmoe_debug_dequant", "hmoe_debug_decode_operand", "HybridMoELayer", "library_path",
     "LinearDesc", "hmoe_linear_packed_size", "hmoe_linear_workspace_size", "hmoe_linear_pack", "hmoe_linear_forward",
-    "LinearW4A16", "ACT_BF16", "ACT_F16", "act_torch_dtype",
+    "LinearW4A16", "ACT_BF16", "ACT_F16", "act_torch_dtype", "ACT_QUANT_NONE", "ACT_QUANT_NVFP4",
+    "hmoe_quantize_act_nvfp4",
 ]
 
 
@@ -44,8 +45,12 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _desc(H, I, E, topk, kept_format=FMT_NVFP4, act_dtype=ACT_BF16):
-    return LayerDesc(H, I, E, topk, kept_format, act_dtype)
+def _desc(H, I, E, topk, kept_format=FMT_NVFP4, act_dtype=ACT_BF16, act_globals=None):
+    """act_globals: None (W4A16), or (g13, g2): W4A4 with those static activation global scales."""
+    if act_globals is None:
+        return LayerDesc(H, I, E, topk, kept_format, act_dtype, ACT_QUANT_NONE, 0.0, 0.0)
+    return LayerDesc(H, I, E, topk, kept_format, act_dtype, ACT_QUANT_NVFP4, float(act_globals[0]),
+                     float(act_globals[1]))
 
 
 def act_torch_dtype(act_dtype):
@@ -163,14 +168,15 @@ def hmoe_debug_decode_operand(layer, expert, which, dst, scales, stream=None):
 class HybridMoELayer:
     """One hybrid MoE layer with its packed tier buffers and workspace owned as torch tensors.
 
-    desc_args: H, I, E, topk, kept_format, act_dtype. bit_map: per-expert 4/3
-    list, or None for uniform. experts: as in hmoe_pack_weights. max_tokens
-    sizes the workspace.
+    desc_args: H, I, E, topk, kept_format, act_dtype, act_globals (None for
+    W4A16, (g13, g2) for W4A4). bit_map: per-expert 4/3 list, or None for
+    uniform. experts: as in hmoe_pack_weights. max_tokens sizes the
+    workspace.
     """
 
     def __init__(self, H, I, E, topk, bit_map, experts, kept_format=FMT_NVFP4, max_tokens=8, device="cuda",
-                 act_dtype=ACT_BF16):
-        self.desc = _desc(H, I, E, topk, kept_format, act_dtype)
+                 act_dtype=ACT_BF16, act_globals=None):
+        self.desc = _desc(H, I, E, topk, kept_format, act_dtype, act_globals)
         self.dtype = act_torch_dtype(act_dtype)
         kb, nb = hmoe_packed_size(self.desc, bit_map)
         self.kept_buf = torch.empty(max(kb, 16), dtype=torch.uint8, device=device) if kb else None
@@ -272,3 +278,12 @@ class LinearW4A16:
             out = torch.empty((x.shape[0], self.N), dtype=self.dtype, device=x.device)
         hmoe_linear_forward(self.linear, x, out, self.ws, path=path)
         return out
+
+
+def hmoe_quantize_act_nvfp4(x, global_scale, codes, scales, stream=None):
+    """NVFP4 activation quantisation of x [rows, K] (bf16 or fp16): codes uint8 [rows, K/2],
+    scales uint8 [rows, K/16] (include/hmoe.h)."""
+    act = ACT_F16 if x.dtype == torch.float16 else ACT_BF16
+    _lib.check(_lib.lib().hmoe_quantize_act_nvfp4(_ptr(x), int(x.shape[0]), int(x.shape[1]), act,
+                                                  ctypes.c_float(global_scale), _ptr(codes), _ptr(scales),
+                                                  _stream(stream)))

@@ -19,6 +19,7 @@ STATUS_NAMES = {
 }
 FMT_NF3, FMT_NVFP4, FMT_MXFP4 = 3, 4, 5
 ACT_BF16, ACT_F16 = 0, 1
+ACT_QUANT_NONE, ACT_QUANT_NVFP4 = 0, 1
 TIERS_ONE_LAUNCH, TIERS_KEPT_FIRST, TIERS_NF3_FIRST = 0, 1, 2
 PATH_AUTO, PATH_STREAM, PATH_GROUPED = 0, 1, 2
 DEBUG_NO_COPIES = 1
@@ -32,12 +33,14 @@ EXPORTS = (
     "hmoe_launch_count", "hmoe_version", "hmoe_forward_static", "hmoe_check_device_status_static",
     "hmoe_auto_path", "hmoe_debug_decode_operand", "hmoe_linear_packed_size", "hmoe_linear_workspace_size",
     "hmoe_linear_pack", "hmoe_linear_forward", "hmoe_linear_forward_ex", "hmoe_linear_destroy",
+    "hmoe_quantize_act_nvfp4",
 )
 
 
 class LayerDesc(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int), ("topk", ctypes.c_int),
-                ("kept_format", ctypes.c_int), ("act_dtype", ctypes.c_int)]
+                ("kept_format", ctypes.c_int), ("act_dtype", ctypes.c_int), ("act_quant", ctypes.c_int),
+                ("act_global13", ctypes.c_float), ("act_global2", ctypes.c_float)]
 
 
 class LinearDesc(ctypes.Structure):
@@ -92,6 +95,7 @@ def load(path=LIB_PATH):
         "hmoe_linear_forward": (i, [vp, vp, i, vp, vp, sz, vp]),
         "hmoe_linear_forward_ex": (i, [vp, vp, i, vp, vp, sz, P(ForwardOpts), vp]),
         "hmoe_linear_destroy": (None, [vp]),
+        "hmoe_quantize_act_nvfp4": (i, [vp, i, i, i, ctypes.c_float, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libhmoe.so")
-SOURCES = ["api.cu", "route.cu", "pack.cu", "stream.cu", "grouped.cu"]
+SOURCES = ["api.cu", "route.cu", "pack.cu", "stream.cu", "grouped.cu", "actquant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -83,6 +83,13 @@ hmoe_status check_desc(const hmoe_layer_desc* d) {
     return fail(HMOE_ERR_UNSUPPORTED_SHAPE, "topk=%d must be <= min(E, %d)", d->topk, MAX_TOPK);
   if (d->act_dtype != HMOE_ACT_BF16 && d->act_dtype != HMOE_ACT_F16)
     return fail(HMOE_ERR_INVALID_ARG, "act_dtype must be HMOE_ACT_BF16 (0) or HMOE_ACT_F16 (1), got %d", d->act_dtype);
+  if (d->act_quant != HMOE_ACT_QUANT_NONE && d->act_quant != HMOE_ACT_QUANT_NVFP4)
+    return fail(HMOE_ERR_INVALID_ARG, "act_quant must be HMOE_ACT_QUANT_NONE (0) or HMOE_ACT_QUANT_NVFP4 (1), got %d",
+                d->act_quant);
+  if (d->act_quant == HMOE_ACT_QUANT_NVFP4 &&
+      !(d->act_global13 > 0.0f && d->act_global13 < 3.0e38f && d->act_global2 > 0.0f && d->act_global2 < 3.0e38f))
+    return fail(HMOE_ERR_INVALID_ARG, "W4A4 needs finite positive activation global scales (got %g, %g)",
+                (double)d->act_global13, (double)d->act_global2);
   return HMOE_OK;
 }
 
@@ -116,7 +123,7 @@ constexpr int STREAM_MAX_SLOTS_PER_EXPERT = 8;
 constexpr int STREAM_FUSED_MAX_GROUPS = 1024;
 
 struct WsLayout {
-  size_t status, queues, done13, chunk_cnt, chunk_base, xg, h, y, total;
+  size_t status, queues, done13, chunk_cnt, chunk_base, xq, xg, h, y, total;
 };
 
 // Fixed prefix (status word, work queues) first, so that it stays at the
@@ -137,6 +144,8 @@ WsLayout ws_layout(const hmoe_layer_desc& d, int T) {
   w.chunk_base = off;
   off += align256(nch * d.E * 4);
   const size_t S = (size_t)T * d.topk;
+  w.xq = off;                           // W4A4: the quantised layer input [T][H]
+  off += align256(d.act_quant ? (size_t)T * d.H * 2 : 0);
   w.xg = off;
   off += align256(T > DECODE_MAX_T ? S * d.H * 2 : 0);
   w.h = off;
@@ -331,6 +340,10 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
   p.nf3_buf = L->nf3_buf;
   p.kept_fmt = d.kept_format;
   p.act_type = d.act_dtype;
+  const bool w4a4 = d.act_quant == HMOE_ACT_QUANT_NVFP4;
+  p.act_scale13 = w4a4 ? d.act_global13 : 1.0f;
+  p.act_scale2 = w4a4 ? d.act_global2 : 1.0f;
+  p.nf3_tile = w4a4 ? 1 : 0;
   p.H = d.H;
   p.I = d.I;
   p.E = d.E;
@@ -363,6 +376,16 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
     return cudaSuccess;
   };
   if (mark(0) != cudaSuccess) return cuda_fail(cudaGetLastError(), "stage event record");
+  // W4A4: the layer input quantised to NVFP4 operand values (the global
+  // scale goes to the W13 epilogue).
+  const void* xin = x;
+  if (w4a4) {
+    uint16_t* xq = reinterpret_cast<uint16_t*>(wsb + w.xq);
+    cudaError_t e = launch_act_quant(static_cast<const uint16_t*>(x), (long long)T * d.H, d.act_global13, d.act_dtype,
+                                     xq, nullptr, nullptr, L->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "activation quantisation launch");
+    xin = xq;
+  }
   for (int f = 0; f < 2; ++f) {
     StreamPhase& P = p.ph[f];
     P.rows = f == 0 ? 2 * d.I : d.H;
@@ -370,7 +393,7 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
     P.RT = P.rows / TILE_ROWS;
     P.KB = P.K / TILE_K;
     P.kbs = pick_stage(P.KB);
-    P.act = f == 0 ? static_cast<const uint16_t*>(x) : p.h_out;
+    P.act = f == 0 ? static_cast<const uint16_t*>(xin) : p.h_out;
     P.act_stride = f == 0 ? d.H : d.I;
     P.kept_off = f == 0 ? 0 : L->gk.w13_bytes;
     P.nf3_off = f == 0 ? 0 : L->gn.w13_bytes;
@@ -378,7 +401,8 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
   // Upper bound on the token groups of one launch: every slot of an expert
   // goes to one group of up to 8, so G <= min(S, ceil(S / 8) + E).
   const long long g_bound = std::min<long long>(S, (S + 7) / 8 + d.E);
-  const bool fused = g_bound <= STREAM_FUSED_MAX_GROUPS;
+  // W4A4 quantises h between the two GEMMs, so they run as two launches.
+  const bool fused = g_bound <= STREAM_FUSED_MAX_GROUPS && !w4a4;
   // Fused: W13 and W2 run in one launch per tier selection, and the events
   // that follow W13 and W2 are both recorded after it.
   const int ranges[2][2] = {{0, fused ? 2 : 1}, {1, 2}};
@@ -392,6 +416,11 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
       p.queue = reinterpret_cast<int*>(wsb + w.queues) + 2 * (2 * r + li);
       cudaError_t e = launch_stream_gemm(p, grid, st);
       if (e != cudaSuccess) return cuda_fail(e, "stream GEMM launch");
+    }
+    if (r == 0 && w4a4) {
+      cudaError_t eq = launch_act_quant(p.h_out, (long long)S * d.I, d.act_global2, d.act_dtype, p.h_out, nullptr,
+                                        nullptr, L->num_sms, st);
+      if (eq != cudaSuccess) return cuda_fail(eq, "activation quantisation launch");
     }
     cudaError_t e = mark(fused || r == 0 ? 1 : 2);
     if (e == cudaSuccess && fused) e = mark(2);
@@ -413,6 +442,7 @@ static hmoe_status run_grouped_path(const hmoe_layer* L, const void* x, int T, c
   p.nf3_buf = L->nf3_buf;
   p.kept_fmt = d.kept_format;
   p.act_type = d.act_dtype;
+  const bool w4a4 = d.act_quant == HMOE_ACT_QUANT_NVFP4;
   p.H = d.H;
   p.I = d.I;
   p.E = d.E;
@@ -444,8 +474,17 @@ static hmoe_status run_grouped_path(const hmoe_layer* L, const void* x, int T, c
     masks[0] = 2;
     masks[1] = 1;
   }
-  cudaError_t e = launch_gather_rows(static_cast<const uint16_t*>(x), perm, S, d.topk, T, d.H, xg, p.status,
-                                     L->num_sms, st);
+  // W4A4: the layer input quantised to NVFP4 operand values first (the
+  // global scale goes to the W13 epilogue).
+  const uint16_t* xin = static_cast<const uint16_t*>(x);
+  cudaError_t e = cudaSuccess;
+  if (w4a4) {
+    uint16_t* xq = reinterpret_cast<uint16_t*>(wsb + w.xq);
+    e = launch_act_quant(xin, (long long)T * d.H, d.act_global13, d.act_dtype, xq, nullptr, nullptr, L->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "activation quantisation launch");
+    xin = xq;
+  }
+  e = launch_gather_rows(xin, perm, S, d.topk, T, d.H, xg, p.status, L->num_sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "gather launch");
   if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "stage event record");
   for (int which : {13, 2}) {
@@ -454,6 +493,12 @@ static hmoe_status run_grouped_path(const hmoe_layer* L, const void* x, int T, c
     p.RT = (which == 13 ? 2 * d.I : d.H) / TILE_ROWS;
     p.KB = p.K / TILE_K;
     const uint16_t* b = which == 13 ? xg : p.h_out;
+    p.act_scale = !w4a4 ? 1.0f : (which == 13 ? d.act_global13 : d.act_global2);
+    if (which == 2 && w4a4) {
+      e = launch_act_quant(p.h_out, (long long)S * d.I, d.act_global2, d.act_dtype, p.h_out, nullptr, nullptr,
+                           L->num_sms, st);
+      if (e != cudaSuccess) return cuda_fail(e, "activation quantisation launch");
+    }
     for (int m : masks) {
       if (!m) continue;
       p.tier_mask = m;
@@ -551,7 +596,7 @@ hmoe_status debug_export(const hmoe_layer* L, int expert, int which, void* dst, 
   const int N = which == 13 ? 2 * L->d.I : L->d.H;
   const int K = which == 13 ? L->d.H : L->d.I;
   cudaError_t e = launch_debug_dequant(fmt, which, base + (which == 2 ? g.w13_bytes : 0), N, K, L->d.I, dst, scales,
-                                       decode_operand, L->d.act_dtype, st);
+                                       decode_operand, L->d.act_dtype, L->d.act_quant == HMOE_ACT_QUANT_NVFP4, st);
   if (e != cudaSuccess) return cuda_fail(e, "debug dequant launch");
   return HMOE_OK;
 }
@@ -775,6 +820,7 @@ hmoe_status hmoe_linear_forward_ex(const hmoe_linear* L, const void* x, int T, v
     p.nf3_buf = L->packed;
     p.kept_fmt = kept_fmt;
     p.act_type = L->d.act_dtype;
+    p.act_scale = 1.0f;
     p.which = 2;
     p.H = L->d.N;
     p.I = L->d.K;
@@ -801,6 +847,7 @@ hmoe_status hmoe_linear_forward_ex(const hmoe_linear* L, const void* x, int T, v
     p.nf3_buf = L->packed;
     p.kept_fmt = kept_fmt;
     p.act_type = L->d.act_dtype;
+    p.act_scale13 = p.act_scale2 = 1.0f;
     p.H = L->d.N;
     p.I = L->d.K;
     p.E = 1;
@@ -841,6 +888,29 @@ hmoe_status hmoe_linear_forward_ex(const hmoe_linear* L, const void* x, int T, v
 hmoe_status hmoe_linear_forward(const hmoe_linear* L, const void* x, int T, void* out, void* ws, size_t ws_bytes,
                                 hmoe_stream_t stream) {
   return hmoe_linear_forward_ex(L, x, T, out, ws, ws_bytes, nullptr, stream);
+}
+
+hmoe_status hmoe_quantize_act_nvfp4(const void* x, int rows, int K, int act_dtype, float global_scale, void* codes,
+                                    void* scales, hmoe_stream_t stream) {
+  const NvtxRange nvtx("hmoe_quantize_act_nvfp4");
+  if (rows < 0) return fail(HMOE_ERR_INVALID_ARG, "rows=%d < 0", rows);
+  if (K <= 0 || K % 16 != 0) return fail(HMOE_ERR_INVALID_ARG, "K=%d must be a positive multiple of 16", K);
+  if (act_dtype != HMOE_ACT_BF16 && act_dtype != HMOE_ACT_F16)
+    return fail(HMOE_ERR_INVALID_ARG, "act_dtype must be HMOE_ACT_BF16 (0) or HMOE_ACT_F16 (1), got %d", act_dtype);
+  if (!(global_scale > 0.0f && global_scale < 3.0e38f))
+    return fail(HMOE_ERR_INVALID_ARG, "global_scale must be finite and > 0 (got %g)", (double)global_scale);
+  if (rows == 0) return HMOE_OK;
+  if (!x || !codes || !scales) return fail(HMOE_ERR_INVALID_ARG, "a pointer is NULL");
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(codes) & 7) != 0)
+    return fail(HMOE_ERR_INVALID_ARG, "x must be 16-byte and codes 8-byte aligned");
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = launch_act_quant(static_cast<const uint16_t*>(x), (long long)rows * K, global_scale, act_dtype, nullptr,
+                         static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales), sms, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "activation quantisation launch");
+  return HMOE_OK;
 }
 
 }  // extern "C"

@@ -744,7 +744,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         const int tok = tt * GT_N + c;
         if (p.which == 13) {
           if (tok >= it.n) continue;
-          const float gsc = p.tab.g13[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f);
+          const float gsc =
+              p.tab.g13[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f) * p.act_scale;
 #pragma unroll
           for (int g = 0; g < 2; ++g) {
             // 16-row group (r0 / 16 + g): rows 0..7 gate, 8..15 up, of channels ch .. ch + 7
@@ -763,7 +764,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         } else {
           const int slot = tt ? slot1 : slot0;
           if (slot < 0) continue;
-          const float gsc = p.tab.g2[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f);
+          const float gsc =
+              p.tab.g2[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f) * p.act_scale;
           float4* dst = reinterpret_cast<float4*>(p.y_out + (size_t)slot * p.H + rt * 128 + r0);
 #pragma unroll
           for (int w = 0; w < 8; ++w)
@@ -1269,7 +1271,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G2_THREADS, 1)
       tc_fence_after();
       const uint32_t col0 = (uint32_t)(buf * G2_N);
       if (it.valid && p.which == 13) {
-        const float gsc = p.tab.g13[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
+        const float gsc = p.tab.g13[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f) * p.act_scale;
         const int g = lane >> 2, qq = lane & 3;
         for (int h = 0; h < 2; ++h) {
           const int ch = it.rt * 64 + (2 * quarter + h) * 8 + g;
@@ -1291,7 +1293,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G2_THREADS, 1)
           }
         }
       } else if (it.valid) {
-        const float gsc = p.tab.g2[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f);
+        const float gsc = p.tab.g2[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? NVFP4_UNSCALE : 1.0f) * p.act_scale;
         const int orow = it.rt * 128 + row;
         const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + col0;
         for (int c0 = 0; c0 < it.n; c0 += 32) {

@@ -38,7 +38,8 @@ cudaError_t launch_pack_matrix(int fmt, int which, const void* codes, const void
 // Test export of the dequantised operands (pack.cu): the tensor-core tile, or with
 // decode_operand the weight-streaming kernel's operand plus its per-group scales.
 cudaError_t launch_debug_dequant(int fmt, int which, const uint8_t* src, int N, int K, int I, void* dst,
-                                 float* scales_out, bool decode_operand, int act_type, cudaStream_t st);
+                                 float* scales_out, bool decode_operand, int act_type, bool nf3_tile,
+                                 cudaStream_t st);
 
 // ---------------------------------------------------------------- streaming GEMM (any T; the decode path)
 // One matrix of the expert FFN as the streaming kernel sees it.
@@ -56,6 +57,9 @@ struct StreamParams {
   const uint8_t* nf3_buf;
   int kept_fmt;
   int act_type;          // ACT_BF16 or ACT_F16: operand, h and output type
+  float act_scale13;     // the W13 input's activation global scale (W4A4), else 1
+  float act_scale2;      // the W2 input's activation global scale (W4A4), else 1
+  int nf3_tile;          // 1: NF3 decoded to the tile values rne(cb * s) (W4A4 layers); 0: raw codes, scale on sums
   int H, I, E, topk, T;
   StreamPhase ph[2];     // [0] W13 (output h), [1] W2 (output y)
   int ph_begin, ph_end;  // phases this launch runs: [0,2) both (W2 items wait on done13), [0,1) or [1,2)
@@ -83,6 +87,7 @@ struct GroupedParams {
   const uint8_t* nf3_buf;
   int kept_fmt;
   int act_type;        // ACT_BF16 or ACT_F16
+  float act_scale;     // this GEMM's input activation global scale (W4A4), else 1
   int which;           // 13: B = gathered x, output h;  2: B = h, output y
   int H, I, E, topk, T;
   int K, RT, KB;
@@ -103,6 +108,13 @@ cudaError_t launch_grouped_gemm(const GroupedParams& p, const uint16_t* b_src, i
 // xg[p] = x[perm[p] / k] for the S permuted slots (2-byte elements of either operand type).
 cudaError_t launch_gather_rows(const uint16_t* x, const int* perm, int S, int k, int T, int H, uint16_t* xg,
                                int* status, int num_sms, cudaStream_t st);
+
+// NVFP4 activation quantisation of n_values (a multiple of 16, rows of a
+// multiple of 16 laid end to end) with global scale g (actquant.cu). With
+// out set: the operand values e2m1 * e4m3 in the activation type (out may be
+// x); else the codes (8 bytes per 16 values) and E4M3 scale bytes.
+cudaError_t launch_act_quant(const uint16_t* x, long long n_values, float g, int act_type, uint16_t* out,
+                             uint8_t* codes, uint8_t* scales, int num_sms, cudaStream_t st);
 
 // out[t][c] = act(sum_j gates[t*k+j] * y[t*k+j][c]), act = bf16 or fp16 by act_type
 cudaError_t launch_finalize(const float* y, const float* gates, int T, int k, int H, uint16_t* out, int act_type,

@@ -99,12 +99,14 @@ __device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it,
     if (c >= it.n) continue;
     const int pp = it.p0 + c;
     if (it.ph == 0) {
-      const float gsc = p.tab.g13[it.e] * (expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f);
+      const float gsc =
+          p.tab.g13[it.e] * (expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f) * p.act_scale13;
       const int ch = it.rt * 64 + rg * 8 + g;
       const float gate = v[h] * gsc, up = v[2 + h] * gsc;
       p.h_out[(size_t)pp * p.I + ch] = f32_to_act<ACT>(silu_f(gate) * up);
     } else {
-      const float gsc = p.tab.g2[it.e] * (expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f);
+      const float gsc =
+          p.tab.g2[it.e] * (expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f) * p.act_scale2;
       const int s = p.perm[pp];
       if (s < 0 || s >= S) {
         set_status(p.status, DEV_BAD_ROUTE);
@@ -117,11 +119,14 @@ __device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it,
   }
 }
 
-// One k-block of one thread slot: dequantise through dequant_slot<FMT, false>
-// (the decoder hmoe_debug_decode_operand exports; NVFP4/MXFP4 scales applied
-// in bf16 from the shared lookup table, NF3 values raw with the row scales
-// applied to the fp32 sum of the k-block) and 4 MMAs.
-template <int FMT, int ACT>
+// One k-block of one thread slot: dequantise through dequant_slot (the
+// decoder hmoe_debug_decode_operand exports; NVFP4/MXFP4 scales applied in
+// the operand type from the shared lookup table, NF3 values raw with the row
+// scales applied to the fp32 sum of the k-block) and 4 MMAs. With TILE (W4A4
+// layers) NF3 is decoded to the tile values rne(cb * s) instead, the weights
+// the definition and the tensor-core kernel use: W4A4 quantises h, so h must
+// come from the same weights on both paths.
+template <int FMT, int ACT, bool TILE>
 __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xrow, int rg, int lane,
                                           const uint32_t* s_e4m3, uint32_t nf3_lut, float* acc) {
   const uint4 xa = *reinterpret_cast<const uint4*>(xrow);
@@ -129,8 +134,8 @@ __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xr
   const uint32_t xr[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
   uint32_t r0[8], r1[8];
   float sc0, sc1;
-  dequant_slot<FMT, false, ACT, true>(tile, rg, lane, r0, r1, &sc0, &sc1, s_e4m3, nf3_lut);
-  if constexpr (FMT == FMT_NVFP4 || FMT == FMT_MXFP4) {
+  dequant_slot<FMT, TILE, ACT, true>(tile, rg, lane, r0, r1, &sc0, &sc1, s_e4m3, nf3_lut);
+  if constexpr (FMT == FMT_NVFP4 || FMT == FMT_MXFP4 || TILE) {
 #pragma unroll
     for (int s = 0; s < 4; ++s)
       mma_16816<ACT>(acc, r0[2 * s], r1[2 * s], r0[2 * s + 1], r1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
@@ -148,24 +153,24 @@ __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xr
 }
 
 // All k-blocks of one stage, two accumulator sets to break the MMA chain.
-template <int FMT, int ACT>
+template <int FMT, int ACT, bool TILE>
 __device__ __forceinline__ void sk_stage(const uint8_t* sw, const uint8_t* sx, int kbs, int rg, int lane,
                                          const uint32_t* s_e4m3, uint32_t nf3_lut, float* accA, float* accB) {
   constexpr int TB = tile_bytes(FMT);
   if (kbs == 8) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) sk_kblock<FMT, ACT>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, nf3_lut, (j & 1) ? accB : accA);
+    for (int j = 0; j < 8; ++j) sk_kblock<FMT, ACT, TILE>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, nf3_lut, (j & 1) ? accB : accA);
   } else if (kbs == 4) {
-    sk_kblock<FMT, ACT>(sw, sx, rg, lane, s_e4m3, nf3_lut, accA);
-    sk_kblock<FMT, ACT>(sw + TB, sx + 128, rg, lane, s_e4m3, nf3_lut, accB);
-    sk_kblock<FMT, ACT>(sw + 2 * TB, sx + 256, rg, lane, s_e4m3, nf3_lut, accA);
-    sk_kblock<FMT, ACT>(sw + 3 * TB, sx + 384, rg, lane, s_e4m3, nf3_lut, accB);
+    sk_kblock<FMT, ACT, TILE>(sw, sx, rg, lane, s_e4m3, nf3_lut, accA);
+    sk_kblock<FMT, ACT, TILE>(sw + TB, sx + 128, rg, lane, s_e4m3, nf3_lut, accB);
+    sk_kblock<FMT, ACT, TILE>(sw + 2 * TB, sx + 256, rg, lane, s_e4m3, nf3_lut, accA);
+    sk_kblock<FMT, ACT, TILE>(sw + 3 * TB, sx + 384, rg, lane, s_e4m3, nf3_lut, accB);
   } else {
-    for (int j = 0; j < kbs; ++j) sk_kblock<FMT, ACT>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, nf3_lut, (j & 1) ? accB : accA);
+    for (int j = 0; j < kbs; ++j) sk_kblock<FMT, ACT, TILE>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, nf3_lut, (j & 1) ? accB : accA);
   }
 }
 
-template <int ACT>
+template <int ACT, bool TILE>
 __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid_constant__ StreamParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SK_SMEM_DATA);
@@ -378,9 +383,9 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
         for (int r = 0; r < 4; ++r) accA[r] = accB[r] = 0.f;
       }
       const uint8_t* sx = sw + SK_W_BYTES + g * SK_XROW + q * 32;
-      if (fmt == FMT_NVFP4) sk_stage<FMT_NVFP4, ACT>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, accA, accB);
-      else if (fmt == FMT_MXFP4) sk_stage<FMT_MXFP4, ACT>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, accA, accB);
-      else sk_stage<FMT_NF3, ACT>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, accA, accB);
+      if (fmt == FMT_NVFP4) sk_stage<FMT_NVFP4, ACT, TILE>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, accA, accB);
+      else if (fmt == FMT_MXFP4) sk_stage<FMT_MXFP4, ACT, TILE>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, accA, accB);
+      else sk_stage<FMT_NF3, ACT, TILE>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, accA, accB);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
       if (++slot == SK_STAGES) {
@@ -425,9 +430,11 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
 int stream_grid(int num_sms) { return 2 * num_sms; }
 
 cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st) {
-  static std::atomic<unsigned long long> attr_bf16{0}, attr_f16{0};
-  cudaError_t ea = ensure_smem_attr(stream_gemm_kernel<ACT_BF16>, SK_SMEM_BYTES, attr_bf16);
-  if (ea == cudaSuccess) ea = ensure_smem_attr(stream_gemm_kernel<ACT_F16>, SK_SMEM_BYTES, attr_f16);
+  static std::atomic<unsigned long long> attr[4] = {};
+  cudaError_t ea = ensure_smem_attr(stream_gemm_kernel<ACT_BF16, false>, SK_SMEM_BYTES, attr[0]);
+  if (ea == cudaSuccess) ea = ensure_smem_attr(stream_gemm_kernel<ACT_F16, false>, SK_SMEM_BYTES, attr[1]);
+  if (ea == cudaSuccess) ea = ensure_smem_attr(stream_gemm_kernel<ACT_BF16, true>, SK_SMEM_BYTES, attr[2]);
+  if (ea == cudaSuccess) ea = ensure_smem_attr(stream_gemm_kernel<ACT_F16, true>, SK_SMEM_BYTES, attr[3]);
   if (ea != cudaSuccess) return ea;
   if (p.act_type != ACT_BF16 && p.act_type != ACT_F16) return cudaErrorInvalidValue;
   if (p.ph_begin < 0 || p.ph_begin >= p.ph_end || p.ph_end > 2) return cudaErrorInvalidValue;
@@ -435,9 +442,9 @@ cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st)
   for (const StreamPhase& P : p.ph)
     if (P.kbs < 1 || P.kbs > SK_MAX_KBS || P.KB % P.kbs != 0) return cudaErrorInvalidValue;
   if (p.group_tokens < 1 || p.group_tokens > 8) return cudaErrorInvalidValue;
-  cudaError_t e = p.act_type == ACT_F16
-                      ? launch_pdl(stream_gemm_kernel<ACT_F16>, dim3(grid), dim3(SK_THREADS), SK_SMEM_BYTES, st, p)
-                      : launch_pdl(stream_gemm_kernel<ACT_BF16>, dim3(grid), dim3(SK_THREADS), SK_SMEM_BYTES, st, p);
+  auto kern = p.act_type == ACT_F16 ? (p.nf3_tile ? stream_gemm_kernel<ACT_F16, true> : stream_gemm_kernel<ACT_F16, false>)
+                                    : (p.nf3_tile ? stream_gemm_kernel<ACT_BF16, true> : stream_gemm_kernel<ACT_BF16, false>);
+  cudaError_t e = launch_pdl(kern, dim3(grid), dim3(SK_THREADS), SK_SMEM_BYTES, st, p);
   count_launches(1);
   return e;
 }

@@ -105,3 +105,23 @@ def test_linear_desc_checks_on_host(lib):
             hm.hmoe_linear_packed_size(hm.LinearDesc(*bad))
         assert ei.value.status == status
     assert hm.hmoe_linear_workspace_size(hm.LinearDesc(256, 384, hm.FMT_NVFP4), 0) == 768
+
+
+def test_w4a4_desc_and_quantizer_checks_on_host(lib):
+    import nf3_moe_gb300 as hm
+    base = hm.LayerDesc(6144, 2048, 256, 8, hm.FMT_NVFP4)
+    w4 = hm.LayerDesc(6144, 2048, 256, 8, hm.FMT_NVFP4, hm.ACT_BF16, hm.ACT_QUANT_NVFP4, 1e-3, 2e-3)
+    # the W4A4 workspace holds the quantised input [T][H] on top
+    assert hm.hmoe_workspace_size(w4, 64) - hm.hmoe_workspace_size(base, 64) == 64 * 6144 * 2
+    for bad in (hm.LayerDesc(6144, 2048, 256, 8, 4, 0, 2, 1e-3, 1e-3), hm.LayerDesc(6144, 2048, 256, 8, 4, 0, 1, 0.0, 1e-3),
+                hm.LayerDesc(6144, 2048, 256, 8, 4, 0, 1, 1e-3, float("inf"))):
+        with pytest.raises(hm.HmoeError) as ei:
+            hm.hmoe_workspace_size(bad, 8)
+        assert ei.value.status == -1
+    q = lib.hmoe_quantize_act_nvfp4
+    assert q(None, 0, 256, 0, ctypes.c_float(1e-3), None, None, None) == 0    # rows = 0: nothing to do
+    assert q(None, -1, 256, 0, ctypes.c_float(1e-3), None, None, None) == -1
+    assert q(None, 1, 250, 0, ctypes.c_float(1e-3), None, None, None) == -1
+    assert q(None, 1, 256, 7, ctypes.c_float(1e-3), None, None, None) == -1
+    assert q(None, 1, 256, 0, ctypes.c_float(-1.0), None, None, None) == -1
+    assert q(None, 1, 256, 0, ctypes.c_float(1e-3), None, None, None) == -1  # NULL buffers

@@ -609,7 +609,9 @@ def sweep_points(dev, pk, steps=10, warmup=3):
     - the uniform NVFP4 layer (H=2048, I=768, E=128, top-8, no bit map),
       M in {1, 8, 128, 1024, 8192};
     - the headline 256-expert hybrid layer (64 NVFP4 + 192 NF3) with fp16
-      activations, M in {8, 4096}.
+      activations, M in {8, 4096};
+    - the same layer as W4A4 (activations quantised to NVFP4, static global
+      scales 5 / 2688 for x and 24 / 2688 for h), M in {8, 4096}.
     A step is plan + forward on the automatic path, captured once in a CUDA
     graph and replayed. Before every replay a 512 MB buffer is written,
     outside the event bracket, so no step finds its weights in the 129 MB L2.
@@ -624,14 +626,19 @@ def sweep_points(dev, pk, steps=10, warmup=3):
          (1, 8, 128, 1024, 8192)),
         ("hybrid NVFP4 + NF3 with fp16 activations, H=6144 I=2048 E=256 top-8, 64 NVFP4 + 192 NF3",
          dict(**SHAPE, kept=KEPT, act="f16"), (8, 4096)),
+        ("hybrid NVFP4 + NF3, W4A4 (NVFP4 activations), H=6144 I=2048 E=256 top-8, 64 NVFP4 + 192 NF3",
+         dict(**SHAPE, kept=KEPT), (8, 4096)),
     ]
+    w4a4_globals = (5.0 / (6 * 448), 24.0 / (6 * 448))
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     points = []
     for name, kw, ms in cases:
         L = synth.make_layer(device=dev, **kw)
         bm = None if L.bit_map is None else [int(b) for b in L.bit_map]
+        w4a4 = "W4A4" in name
         moe = hm.HybridMoELayer(L.H, L.I, L.E, L.topk, bm, expert_tuples(L), kept_format=L.kept_format,
-                                max_tokens=max(ms), act_dtype=hm.ACT_F16 if L.act == "f16" else hm.ACT_BF16)
+                                max_tokens=max(ms), act_dtype=hm.ACT_F16 if L.act == "f16" else hm.ACT_BF16,
+                                act_globals=w4a4_globals if w4a4 else None)
         fmts = [moe.layer.expert_info(e)[0] for e in range(L.E)]
         per_w = 3 * L.H * L.I
         for M in ms:
@@ -673,6 +680,7 @@ def sweep_points(dev, pk, steps=10, warmup=3):
             tfs = 2.0 * L.topk * per_w * M / (ms_ * 1e-3) / 1e12
             path = "stream" if hm.hmoe_auto_path(moe.desc, M) == hm.PATH_STREAM else "grouped"
             points.append({"workload": f"{name}, M={M}", "path": path, "act": L.act,
+                           "act_quant": "nvfp4" if w4a4 else None,
                            "us_per_layer": round(ms_ * 1e3, 2), "touched_experts": int(len(es)),
                            "touched_bytes": int(byt), "hbm_gbs": round(byt / (ms_ * 1e-3) / 1e9, 1),
                            "frac_hbm": round(byt / (ms_ * 1e-3) / 1e9 / pk["hbm_gbs"], 4),

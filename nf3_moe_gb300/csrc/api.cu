@@ -102,7 +102,7 @@ hmoe_status check_bitmap(const hmoe_layer_desc* d, const int8_t* bit_map) {
 }
 
 int pick_stage(int kbi) {
-  for (int s = 8; s > 1; s >>= 1)
+  for (int s = STREAM_MAX_KBS; s > 1; s >>= 1)
     if (kbi % s == 0) return s;
   return 1;
 }

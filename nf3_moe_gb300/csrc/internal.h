@@ -42,6 +42,8 @@ cudaError_t launch_debug_dequant(int fmt, int which, const uint8_t* src, int N, 
                                  cudaStream_t st);
 
 // ---------------------------------------------------------------- streaming GEMM (any T; the decode path)
+// Largest number of k-blocks per pipeline stage of the streaming kernel.
+constexpr int STREAM_MAX_KBS = 8;
 // One matrix of the expert FFN as the streaming kernel sees it.
 struct StreamPhase {
   int rows, K;               // rows = 2I (W13) or H (W2); K = H or I

@@ -47,7 +47,11 @@ constexpr int SK_CONSUMER_WARPS = 8;
 constexpr int SK_WARP_PRODUCER = SK_CONSUMER_WARPS;       // warp 8
 constexpr int SK_THREADS = (SK_CONSUMER_WARPS + 1) * 32;
 constexpr int SK_STAGES = 2;
-constexpr int SK_MAX_KBS = 8;
+constexpr int SK_MAX_KBS = STREAM_MAX_KBS;
+// Two CTAs per SM: three (4 k-blocks per stage, 72 registers) measured
+// slower, 252.3 against 249.5 us per M=8 launch, and 88.8 against 74.8 us at
+// M=1.
+constexpr int SK_CTAS_PER_SM = 2;
 constexpr int SK_XROW = SK_MAX_KBS * 128 + 16;            // padded token row, bytes
 constexpr int SK_W_BYTES = SK_MAX_KBS * 4608;
 constexpr int SK_X_BYTES = 8 * SK_XROW;
@@ -56,7 +60,7 @@ constexpr int SK_STAGE_BYTES = SK_W_BYTES + SK_X_BYTES + SK_HDR_BYTES;
 constexpr int SK_SMEM_DATA = SK_STAGES * SK_STAGE_BYTES;
 constexpr int SK_NBAR = 2 * SK_STAGES;
 constexpr int SK_SMEM_BYTES = SK_SMEM_DATA + SK_NBAR * 8 + 2 * (MAX_E + 1) * 4 + 4 * 4 + 256 * 4 + NF3_LUT_BYTES;
-static_assert(2 * (SK_SMEM_BYTES + 1024) <= 233472, "two CTAs per SM");
+static_assert(SK_CTAS_PER_SM * (SK_SMEM_BYTES + 1024) <= 233472, "CTAs per SM");
 static_assert(SK_STAGE_BYTES % 16 == 0, "stage alignment");
 
 struct SkItem {
@@ -152,6 +156,49 @@ __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xr
   }
 }
 
+// Two consecutive k-blocks of one thread slot: both slots decoded before
+// either k-block's MMAs, so the warp has two independent decode chains to
+// interleave (k-block j into accA, j + 1 into accB).
+template <int FMT, int ACT, bool TILE>
+__device__ __forceinline__ void sk_kblock2(const uint8_t* tile, const uint8_t* xrow, int rg, int lane,
+                                           const uint32_t* s_e4m3, uint32_t nf3_lut, float* accA, float* accB) {
+  constexpr int TB = tile_bytes(FMT);
+  uint32_t a0[8], a1[8], b0[8], b1[8];
+  float sa0, sa1, sb0, sb1;
+  dequant_slot<FMT, TILE, ACT, true>(tile, rg, lane, a0, a1, &sa0, &sa1, s_e4m3, nf3_lut);
+  dequant_slot<FMT, TILE, ACT, true>(tile + TB, rg, lane, b0, b1, &sb0, &sb1, s_e4m3, nf3_lut);
+  const uint4 xa = *reinterpret_cast<const uint4*>(xrow);
+  const uint4 xb = *reinterpret_cast<const uint4*>(xrow + 16);
+  const uint4 ya = *reinterpret_cast<const uint4*>(xrow + 128);
+  const uint4 yb = *reinterpret_cast<const uint4*>(xrow + 144);
+  const uint32_t xr[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+  const uint32_t yr[8] = {ya.x, ya.y, ya.z, ya.w, yb.x, yb.y, yb.z, yb.w};
+  if constexpr (FMT == FMT_NVFP4 || FMT == FMT_MXFP4 || TILE) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      mma_16816<ACT>(accA, a0[2 * s], a1[2 * s], a0[2 * s + 1], a1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
+      mma_16816<ACT>(accB, b0[2 * s], b1[2 * s], b0[2 * s + 1], b1[2 * s + 1], yr[2 * s], yr[2 * s + 1]);
+    }
+  } else {
+    float d[4], e[4];
+    mma_16816_zc<ACT>(d, a0[0], a1[0], a0[1], a1[1], xr[0], xr[1]);
+    mma_16816_zc<ACT>(e, b0[0], b1[0], b0[1], b1[1], yr[0], yr[1]);
+#pragma unroll
+    for (int s = 1; s < 4; ++s) {
+      mma_16816<ACT>(d, a0[2 * s], a1[2 * s], a0[2 * s + 1], a1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
+      mma_16816<ACT>(e, b0[2 * s], b1[2 * s], b0[2 * s + 1], b1[2 * s + 1], yr[2 * s], yr[2 * s + 1]);
+    }
+    accA[0] = fmaf(sa0, d[0], accA[0]);
+    accA[1] = fmaf(sa0, d[1], accA[1]);
+    accA[2] = fmaf(sa1, d[2], accA[2]);
+    accA[3] = fmaf(sa1, d[3], accA[3]);
+    accB[0] = fmaf(sb0, e[0], accB[0]);
+    accB[1] = fmaf(sb0, e[1], accB[1]);
+    accB[2] = fmaf(sb1, e[2], accB[2]);
+    accB[3] = fmaf(sb1, e[3], accB[3]);
+  }
+}
+
 // All k-blocks of one stage, two accumulator sets to break the MMA chain.
 template <int FMT, int ACT, bool TILE>
 __device__ __forceinline__ void sk_stage(const uint8_t* sw, const uint8_t* sx, int kbs, int rg, int lane,
@@ -159,19 +206,18 @@ __device__ __forceinline__ void sk_stage(const uint8_t* sw, const uint8_t* sx, i
   constexpr int TB = tile_bytes(FMT);
   if (kbs == 8) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) sk_kblock<FMT, ACT, TILE>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, nf3_lut, (j & 1) ? accB : accA);
+    for (int j = 0; j < 8; j += 2)
+      sk_kblock2<FMT, ACT, TILE>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, nf3_lut, accA, accB);
   } else if (kbs == 4) {
-    sk_kblock<FMT, ACT, TILE>(sw, sx, rg, lane, s_e4m3, nf3_lut, accA);
-    sk_kblock<FMT, ACT, TILE>(sw + TB, sx + 128, rg, lane, s_e4m3, nf3_lut, accB);
-    sk_kblock<FMT, ACT, TILE>(sw + 2 * TB, sx + 256, rg, lane, s_e4m3, nf3_lut, accA);
-    sk_kblock<FMT, ACT, TILE>(sw + 3 * TB, sx + 384, rg, lane, s_e4m3, nf3_lut, accB);
+    sk_kblock2<FMT, ACT, TILE>(sw, sx, rg, lane, s_e4m3, nf3_lut, accA, accB);
+    sk_kblock2<FMT, ACT, TILE>(sw + 2 * TB, sx + 256, rg, lane, s_e4m3, nf3_lut, accA, accB);
   } else {
     for (int j = 0; j < kbs; ++j) sk_kblock<FMT, ACT, TILE>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, nf3_lut, (j & 1) ? accB : accA);
   }
 }
 
 template <int ACT, bool TILE>
-__global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid_constant__ StreamParams p) {
+__global__ void __launch_bounds__(SK_THREADS, SK_CTAS_PER_SM) stream_gemm_kernel(const __grid_constant__ StreamParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SK_SMEM_DATA);
   uint64_t* empty = full + SK_STAGES;
@@ -427,7 +473,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) stream_gemm_kernel(const __grid
   }
 }
 
-int stream_grid(int num_sms) { return 2 * num_sms; }
+int stream_grid(int num_sms) { return SK_CTAS_PER_SM * num_sms; }
 
 cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st) {
   static std::atomic<unsigned long long> attr[4] = {};

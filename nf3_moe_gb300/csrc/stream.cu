@@ -20,18 +20,27 @@
 // instead of two. (Past the counter array's capacity the host runs the two
 // phases as two launches of the same kernel.)
 //
-// One producer lane streams each item's packed tiles and the group's
+// The producer warp streams each item's packed tiles and the group's
 // activation rows into a 2-stage shared-memory ring of up to 8 k-blocks per
-// stage with 1D bulk copies (TMA engine). Eight k-blocks per stage instead of
-// four halve the per-stage waits and bookkeeping of the consumers; measured
-// 308 -> 284 us at M=8. It writes the item number into each stage header, and a
-// terminator stage ends the consumers' loop. Eight consumer warps, one per
-// 16-row group, dequantise in registers (prmt byte-table lookups; E4M3
-// scales from a shared table of bf16 pairs; bf16x2 scale multiply) and
-// issue m16n8k16 bf16 MMAs with the tokens as the N=8 side. Accumulation is
-// fp32, with two accumulator sets per thread. The epilogue writes straight
-// from registers:
-//   W13: h[p][c] = bf16(silu(g13 * gate) * (g13 * up)), SwiGLU fused.
+// stage with 1D bulk copies (TMA engine), one warp instruction per stage: an
+// elected lane copies the weight tiles and lane j the activation row of
+// token j. Eight k-blocks per stage instead of four halve the per-stage waits
+// and bookkeeping of the consumers; measured 308 -> 284 us at M=8. It writes
+// the item number into each stage header, and a terminator stage ends the
+// consumers' loop. Eight consumer warps, one per 16-row group, dequantise in
+// registers and issue m16n8k16 MMAs (bf16 or fp16 operands, template ACT)
+// with the tokens as the N=8 side, two k-blocks' slots decoded before their
+// MMAs:
+//   NVFP4: shift-and-mask decode (bf16) or nibble-table decode (fp16), the
+//     E4M3 scales from a shared table of operand-type pairs, one x2 multiply;
+//   MXFP4: nibble-table decode, E8M0 scale multiply;
+//   NF3: code pairs looked up in a bank-replicated shared table of operand
+//     pairs, raw codebook values with the group scale applied to the fp32
+//     partial sums; for W4A4 layers (template TILE) the tile values
+//     rne(cb * s), the weights the definition and the tensor-core kernel use.
+// Accumulation is fp32, with two accumulator sets per thread. The epilogue
+// writes straight from registers:
+//   W13: h[p][c] = act(silu(g13 * gate) * (g13 * up)), SwiGLU fused.
 //   W2:  y[s][r] = g2 * sum, fp32, indexed by the flat slot s.
 // The finalize kernel then applies the gates and sums each token's k slots
 // in slot order, so every output element is summed in a fixed order.

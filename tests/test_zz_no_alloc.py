@@ -8,7 +8,7 @@ layer with its scratch in a fixed device array inside the library.
 
 These tests make two calls in a row, on different batches, and on both
 paths (the weight-streaming kernel at small batches, the tensor-core grouped
-kernel above). Both entry points run the same deterministic kernels, so each
+kernel above), for bf16, fp16 and W4A4 layers. Both entry points run the same deterministic kernels, so each
 result must equal the workspace entry point's, hmoe_forward, bit for bit.
 Batches whose scratch exceeds the array, and calls with bad arguments, are
 refused before anything is enqueued.
@@ -48,24 +48,39 @@ def _forward_ws(moe, x, ids, gates, perm, offsets, out):
 def _layer(shape):
     if shape == "tiny":
         return synth.tiny_layer(device="cuda")
+    if shape == "tiny-f16":
+        return synth.make_layer(**synth.TINY, kept_ids=[0, 1, 2, 3], device="cuda", act="f16")
+    if shape == "tiny-w4a4":
+        L = synth.tiny_layer(device="cuda")
+        L.act_quant = (5.0 / (6 * 448), 0.6 / (6 * 448))
+        return L
     return synth.make_layer(**synth.UNIFORM_128, uniform=True, device="cuda")
+
+
+def _build(L, max_tokens):
+    if getattr(L, "act_quant", None) is None:
+        return U.build(L, max_tokens)
+    import nf3_moe_gb300 as hm
+    return hm.HybridMoELayer(L.H, L.I, L.E, L.topk, [int(b) for b in L.bit_map], U.device_experts(L),
+                             max_tokens=max_tokens, act_globals=L.act_quant)
 
 
 # (layer, tokens of the two calls): the tiny layer (E=8, top-2) takes the grouped path at
 # T=64 (128 slots > 8 per expert); the 128-expert layer streams at every T here.
-CASES = [("tiny", (4, 8)), ("tiny", (64, 37)), ("uniform", (4, 8)), ("uniform", (64, 1))]
+CASES = [("tiny", (4, 8)), ("tiny", (64, 37)), ("uniform", (4, 8)), ("uniform", (64, 1)),
+         ("tiny-f16", (8, 64)), ("tiny-w4a4", (8, 64))]
 
 
 @pytest.mark.parametrize("shape,Ts", CASES)
 def test_static_forward_equals_workspace_forward_two_calls(shape, Ts):
     L = _layer(shape)
-    moe = U.build(L, max(Ts))
+    moe = _build(L, max(Ts))
     for call, T in enumerate(Ts):
-        x = synth.gen_x(T, L.H, seed=50 + call, device="cuda")
+        x = synth.gen_x(T, L.H, seed=50 + call, device="cuda", dtype=L.x_dtype)
         logits = synth.gen_logits(T, L.E, seed=50 + call, device="cuda")
         ids, gates, perm, offsets = moe.plan(logits)
-        ref = torch.empty((T, L.H), dtype=torch.bfloat16, device="cuda")
-        out = torch.full((T, L.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+        ref = torch.empty((T, L.H), dtype=L.x_dtype, device="cuda")
+        out = torch.full((T, L.H), float("nan"), dtype=L.x_dtype, device="cuda")
         assert _forward_ws(moe, x, ids, gates, perm, offsets, ref) == 0, _lib.lib().hmoe_last_error()
         assert _forward_static(moe, x, ids, gates, perm, offsets, out) == 0, _lib.lib().hmoe_last_error()
         torch.cuda.synchronize()

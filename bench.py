@@ -314,10 +314,14 @@ def run_ours(args, rank, world):
     hm.hmoe_check_device_status(ws)
 
     # Each replica's step (plan + forward) is captured once into a CUDA graph,
-    # as a serving engine replays a decode step. The graph holds exactly
-    # the library's kernels; stage events inside it time the GEMM launch
-    # (W13 and W2 fused into one stream-kernel launch at M <= 8).
-    def capture(bl_, tier_order=hm.TIERS_ONE_LAUNCH):
+    # as a serving engine replays a decode step; the graph holds exactly the
+    # library's kernels. A second graph per replica adds two stage events
+    # around the GEMM launch (W13 and W2 fused into one stream-kernel launch
+    # at M <= 8). Event nodes split a graph and cost about 11 us per replay
+    # at M=8 (they also stop the launch from overlapping the routing kernel
+    # through programmatic dependent launch), so only the last replay of each
+    # replica inside the timed region uses the event graph.
+    def capture(bl_, tier_order=hm.TIERS_ONE_LAUNCH, events=False):
         graphs, per_step = [], 0
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
@@ -327,10 +331,12 @@ def run_ours(args, rank, world):
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
         for r in range(REPLICAS):
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-            for e in evs:
-                e.record()
-            torch.cuda.synchronize()
+            evs = None
+            if events:
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                for e in evs:
+                    e.record()
+                torch.cuda.synchronize()
             g = torch.cuda.CUDAGraph()
             n0 = hm.hmoe_launch_count()
             with torch.cuda.graph(g):
@@ -340,11 +346,15 @@ def run_ours(args, rank, world):
         return graphs, per_step
 
     graphs, launches_per_step = capture(bl)
+    graphs_ev, launches_per_step_ev = capture(bl, events=True)
+    assert launches_per_step_ev == launches_per_step
 
     # warm-up (untimed) and clock soak
     clock = ClockSampler(dev)
     for i in range(args.warmup):
         graphs[i % REPLICAS][0].replay()
+    for r in range(REPLICAS):
+        graphs_ev[r][0].replay()
     clock.start()
     t_soak = time.perf_counter()
     i = 0
@@ -355,15 +365,17 @@ def run_ours(args, rank, world):
             torch.cuda.synchronize()
     torch.cuda.synchronize()
 
-    # timed region: exactly K steps, barrier + synchronize on both sides
+    # timed region: exactly K steps, barrier + synchronize on both sides; the
+    # last min(K, REPLICAS) steps replay the event graphs
     K = args.steps
+    nlast = min(K, REPLICAS)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record()
     for i in range(K):
-        graphs[i % REPLICAS][0].replay()
+        (graphs_ev if i >= K - nlast else graphs)[i % REPLICAS][0].replay()
     ev1.record()
     torch.cuda.synchronize()
     launches = launches_per_step * K
@@ -374,12 +386,12 @@ def run_ours(args, rank, world):
     hm.hmoe_check_device_status(ws)
     bytes_steps = sum(tb[i % REPLICAS][0] for i in range(K))
     value = whole_job_gbs(bytes_steps, world, t_ms)
-    # GEMM launch time (W13 + W2, one fused stream-kernel launch) of the last
-    # replay of each replica's graph, inside the timed region.
-    nlast = min(K, REPLICAS)
-    gemm_ms = [graphs[r][1][0].elapsed_time(graphs[r][1][1]) for r in range(nlast)]
+    # GEMM launch time (W13 + W2, one fused stream-kernel launch) of the
+    # event-graph replays at the end of the timed region.
+    ev_reps = [i % REPLICAS for i in range(K - nlast, K)]
+    gemm_ms = [graphs_ev[r][1][0].elapsed_time(graphs_ev[r][1][1]) for r in ev_reps]
     gemm_avg = sum(gemm_ms) / nlast
-    gemm_bytes = sum(tb[r][0] for r in range(nlast)) / nlast
+    gemm_bytes = sum(tb[r][0] for r in ev_reps) / nlast
     gemm_gbs = gemm_bytes / (gemm_avg * 1e-3) / 1e9
 
     # per-M table (extra)
@@ -541,7 +553,7 @@ def run_ours(args, rank, world):
     traffic, traffic_source = stream_traffic(M)
     sweep = None
     if world == 1 and not args.skip_sweep:
-        del graphs
+        del graphs, graphs_ev
         torch.cuda.empty_cache()
         sweep = sweep_points(dev, pk, steps=args.sweep_steps, warmup=3)
 
@@ -554,7 +566,8 @@ def run_ours(args, rank, world):
                    "frac_hbm": round(value / world / pk["hbm_gbs"], 4),
                    "bytes_per_step": int(bytes_steps / K),
                    "l2": f"{REPLICAS} rotating weight replicas and batches; each step touches > L2 (129 MB)",
-                   "timing": "CUDA-graph replay of plan + forward per step; CUDA events on the replay stream",
+                   "timing": "CUDA-graph replay of plan + forward per step; CUDA events on the replay stream; "
+                             "the last replay of each replica carries the stage events of the roofline timing",
                    "parallelism": "replicas only" if world > 1 else "1 GPU",
                    "peaks": pk, "per_m": per_m, "prefill": prefill, "tiers": tiers, "sweep": sweep},
         "clocks": clocks,
@@ -567,7 +580,8 @@ def run_ours(args, rank, world):
                      "frac": round(gemm_gbs / pk["hbm_gbs"], 4), "traffic": traffic,
                      "traffic_source": traffic_source,
                      "algorithmic_bytes_per_launch": int(gemm_bytes), "avg_launch_us": round(gemm_avg * 1e3, 2),
-                     "timing": "stage events captured in the step graphs, last replay of each graph in the timed region"},
+                     "timing": "stage events around the launch in a second graph per replica, replayed as the last "
+                               "step of each replica inside the timed region"},
         "cpu_baseline": cpu,
     }
     return line if rank == 0 else None

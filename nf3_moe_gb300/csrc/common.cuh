@@ -25,7 +25,8 @@
 //     (each [256 slots][4 B]). A's nibbles 0..7 hold R0 codes 0..7, B's hold
 //     R0 codes 8..15, C's hold R1 codes 0..7, each in bits 0..2. Bit 3 of
 //     nibble j in A, B and C holds bits 0, 1 and 2 of R1 code 8+j. Then bf16
-//     scales [128 rows][2 B] at 3072.
+//     scales at 3072: [8 rg][8 g][R0, R1][2 B], the two rows of a slot side
+//     by side.
 //   W13 rows are interleaved per 16-row group: group rows 0..7 are the gate
 //   rows of 8 consecutive channels and rows 8..15 the up rows of the same
 //   channels. So R0 and R1 of a thread slot are the gate and up rows of one
@@ -432,6 +433,15 @@ __device__ __forceinline__ void nf3x8_lut(uint32_t sel, uint32_t lut, uint32_t* 
   p[3] = lds_u32(lut + __byte_perm(sel, 0u, 0x4443) * 128u);
 }
 
+// The weight-streaming kernel's NF3 decode mix: selector words per slot
+// taken through the pair table (of 4), the rest decoded with byte-table
+// permutes. The table costs shared-memory bandwidth (one 128-byte wavefront
+// per warp and code pair), the permutes ALU issue (about 2.25 operations
+// per pair); with 16 consumer warps per SM sharing both, a mix keeps either
+// from saturating. Measured per M=8 launch (table words of 4): 4: 249.0 us,
+// 3 and 2 alternating: 242.6, 2: 242.1, 2 and 1: 245.4, 1: 249.3, 0: 257.4.
+constexpr int NF3_MIX_LUT = 2;
+
 // NF3 words A, B, C of one thread slot -> selector words for R0 codes 0..7,
 // R0 8..15, R1 0..7 and R1 8..15.
 __device__ __forceinline__ void nf3_selectors(uint32_t A, uint32_t B, uint32_t C, uint32_t* s) {
@@ -463,9 +473,11 @@ template <int ACT>
 __host__ __device__ constexpr float nvfp4_unscale() {
   return ACT == ACT_F16 ? 1.0f : NVFP4_UNSCALE;
 }
-// With NF3_LUT the NF3 codes are looked up in the shared pair table whose
-// lane address is nf3_lut (see nf3x8_lut); the values are the same.
-template <int FMT, bool WITH_NF3_SCALE, int ACT = ACT_BF16, bool NF3_LUT = false>
+// NF3_LUT (0..4): how many of the slot's four NF3 selector words are looked
+// up in the shared pair table whose lane address is nf3_lut (see
+// nf3x8_lut); the others are decoded with byte-table permutes. The values
+// are the same either way.
+template <int FMT, bool WITH_NF3_SCALE, int ACT = ACT_BF16, int NF3_LUT = 0>
 __device__ __forceinline__ void dequant_slot(const uint8_t* tile, int rg, int lane, uint32_t* r0, uint32_t* r1,
                                              float* scale0, float* scale1, const uint32_t* e4m3_lut,
                                              uint32_t nf3_lut = 0) {
@@ -516,25 +528,17 @@ __device__ __forceinline__ void dequant_slot(const uint8_t* tile, int rg, int la
     const uint32_t B = *reinterpret_cast<const uint32_t*>(tile + 1024 + slot * 4);
     const uint32_t C = *reinterpret_cast<const uint32_t*>(tile + 2048 + slot * 4);
     const int g = lane >> 2;
-    const uint32_t sb0 = *reinterpret_cast<const uint16_t*>(tile + 3072 + (rg * 16 + g) * 2);
-    const uint32_t sb1 = *reinterpret_cast<const uint16_t*>(tile + 3072 + (rg * 16 + g + 8) * 2);
+    const uint32_t sbb = *reinterpret_cast<const uint32_t*>(tile + 3072 + (rg * 8 + g) * 4);
+    const uint32_t sb0 = sbb & 0xFFFFu, sb1 = sbb >> 16;
     uint32_t s[4];
     nf3_selectors(A, B, C, s);
-    if constexpr (NF3_LUT) {
-      nf3x8_lut(s[0], nf3_lut, r0);
-      nf3x8_lut(s[1], nf3_lut, r0 + 4);
-      nf3x8_lut(s[2], nf3_lut, r1);
-      nf3x8_lut(s[3], nf3_lut, r1 + 4);
-    } else if constexpr (ACT == ACT_F16) {
-      nf3x8_to_f16x2(s[0], r0);
-      nf3x8_to_f16x2(s[1], r0 + 4);
-      nf3x8_to_f16x2(s[2], r1);
-      nf3x8_to_f16x2(s[3], r1 + 4);
-    } else {
-      nf3x8_to_bf16x2(s[0], r0);
-      nf3x8_to_bf16x2(s[1], r0 + 4);
-      nf3x8_to_bf16x2(s[2], r1);
-      nf3x8_to_bf16x2(s[3], r1 + 4);
+    static_assert(NF3_LUT >= 0 && NF3_LUT <= 4, "selector words through the table");
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t* p = (w < 2 ? r0 : r1) + 4 * (w & 1);  // s[0], s[1]: R0 codes 0..15; s[2], s[3]: R1
+      if (w < NF3_LUT) nf3x8_lut(s[w], nf3_lut, p);
+      else if constexpr (ACT == ACT_F16) nf3x8_to_f16x2(s[w], p);
+      else nf3x8_to_bf16x2(s[w], p);
     }
     if constexpr (WITH_NF3_SCALE) {
       uint32_t S0, S1;

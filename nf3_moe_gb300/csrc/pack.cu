@@ -146,8 +146,9 @@ __global__ void pack_matrix_kernel(int fmt, int which, const uint8_t* __restrict
     *reinterpret_cast<uint32_t*>(tile + 2048 + slot * 4) = C;
     if (q == 0) {
       const uint16_t* sc = reinterpret_cast<const uint16_t*>(scales);
-      *reinterpret_cast<uint16_t*>(tile + 3072 + R0 * 2) = sc[(size_t)L0 * (K / 64) + kb];
-      *reinterpret_cast<uint16_t*>(tile + 3072 + R1 * 2) = sc[(size_t)L1 * (K / 64) + kb];
+      // the scales of R0 and R1 side by side: one 32-bit load per slot
+      *reinterpret_cast<uint32_t*>(tile + 3072 + (rg * 8 + g) * 4) =
+          (uint32_t)sc[(size_t)L0 * (K / 64) + kb] | ((uint32_t)sc[(size_t)L1 * (K / 64) + kb] << 16);
     }
   }
 }
@@ -173,12 +174,10 @@ cudaError_t launch_pack_matrix(int fmt, int which, const void* codes, const void
 //     kernel feeds mma.sync. NVFP4 and MXFP4 are the tile values; NF3 values
 //     are the raw codebook entries, and scales_out receives the fp32 factor
 //     the kernel applies to each row's 64-wide group sum (1 for NVFP4/MXFP4).
-template <int FMT, bool WITH_NF3_SCALE, bool NF3_LUT, int ACT>
+template <int FMT, bool WITH_NF3_SCALE, int NLUT, int ACT>
 __device__ __forceinline__ void debug_slot(const uint8_t* tile, int rg, int lane, const uint32_t* lut,
                                            uint32_t nf3_lut, uint32_t* r0, uint32_t* r1, float* s0, float* s1) {
-  // The tensor-core kernel decodes NF3 with byte permutes, the
-  // weight-streaming kernel with the shared pair table.
-  dequant_slot<FMT, WITH_NF3_SCALE, ACT, NF3_LUT>(tile, rg, lane, r0, r1, s0, s1, lut, nf3_lut);
+  dequant_slot<FMT, WITH_NF3_SCALE, ACT, NLUT>(tile, rg, lane, r0, r1, s0, s1, lut, nf3_lut);
   if constexpr (FMT == FMT_NVFP4 && ACT == ACT_BF16) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -188,7 +187,7 @@ __device__ __forceinline__ void debug_slot(const uint8_t* tile, int rg, int lane
   }
 }
 
-template <bool WITH_NF3_SCALE, bool NF3_LUT, int ACT>
+template <bool WITH_NF3_SCALE, bool DECODE, int ACT>
 __global__ void debug_dequant_kernel(int fmt, int which, const uint8_t* __restrict__ src, int N, int K, int I,
                                      uint16_t* __restrict__ dst, float* __restrict__ scales_out) {
   __shared__ uint32_t s_e4m3[256];
@@ -203,11 +202,14 @@ __global__ void debug_dequant_kernel(int fmt, int which, const uint8_t* __restri
   const uint8_t* tile = src + ((size_t)rt * KB + kb) * tile_bytes(fmt);
   uint32_t r0[8], r1[8];
   float s0 = 1.0f, s1 = 1.0f;
+  // The tensor-core kernel decodes NF3 with byte permutes only; the
+  // weight-streaming kernel mixes the pair table and byte permutes.
+  constexpr int NLUT = DECODE ? NF3_MIX_LUT : 0;
   if (fmt == FMT_NVFP4)
-    debug_slot<FMT_NVFP4, WITH_NF3_SCALE, NF3_LUT, ACT>(tile, rg, lane, s_e4m3, nf3_lut, r0, r1, &s0, &s1);
+    debug_slot<FMT_NVFP4, WITH_NF3_SCALE, NLUT, ACT>(tile, rg, lane, s_e4m3, nf3_lut, r0, r1, &s0, &s1);
   else if (fmt == FMT_MXFP4)
-    debug_slot<FMT_MXFP4, WITH_NF3_SCALE, NF3_LUT, ACT>(tile, rg, lane, s_e4m3, nf3_lut, r0, r1, &s0, &s1);
-  else debug_slot<FMT_NF3, WITH_NF3_SCALE, NF3_LUT, ACT>(tile, rg, lane, s_e4m3, nf3_lut, r0, r1, &s0, &s1);
+    debug_slot<FMT_MXFP4, WITH_NF3_SCALE, NLUT, ACT>(tile, rg, lane, s_e4m3, nf3_lut, r0, r1, &s0, &s1);
+  else debug_slot<FMT_NF3, WITH_NF3_SCALE, NLUT, ACT>(tile, rg, lane, s_e4m3, nf3_lut, r0, r1, &s0, &s1);
   const int L0 = logical_row(which, I, rt, rg * 16 + g), L1 = logical_row(which, I, rt, rg * 16 + g + 8);
   const int k0 = kb * TILE_K + 16 * q;
   uint4* d0 = reinterpret_cast<uint4*>(dst + (size_t)L0 * K + k0);
@@ -229,8 +231,9 @@ cudaError_t launch_debug_dequant(int fmt, int which, const uint8_t* src, int N, 
   if (tiles == 0) return cudaSuccess;
   uint16_t* d = static_cast<uint16_t*>(dst);
   const bool f16 = act_type == ACT_F16;
-  // decode mode: the streaming kernel's decoder (pair table; NF3 tile values
-  // for W4A4 layers); tile mode: the tensor-core kernel's.
+  // decode mode: the streaming kernel's decoder (pair table and byte
+  // permutes; NF3 tile values for W4A4 layers); tile mode: the tensor-core
+  // kernel's.
   if (decode_operand && nf3_tile) {
     if (f16) debug_dequant_kernel<true, true, ACT_F16><<<tiles, 256, 0, st>>>(fmt, which, src, N, K, I, d, scales_out);
     else debug_dequant_kernel<true, true, ACT_BF16><<<tiles, 256, 0, st>>>(fmt, which, src, N, K, I, d, scales_out);

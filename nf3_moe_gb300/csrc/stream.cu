@@ -34,10 +34,14 @@
 //   NVFP4: shift-and-mask decode (bf16) or nibble-table decode (fp16), the
 //     E4M3 scales from a shared table of operand-type pairs, one x2 multiply;
 //   MXFP4: nibble-table decode, E8M0 scale multiply;
-//   NF3: code pairs looked up in a bank-replicated shared table of operand
-//     pairs, raw codebook values with the group scale applied to the fp32
-//     partial sums; for W4A4 layers (template TILE) the tile values
-//     rne(cb * s), the weights the definition and the tensor-core kernel use.
+//   NF3: half of the code pairs looked up in a bank-replicated shared
+//     table of operand pairs, the other half decoded with byte-table
+//     permutes (the table is bound by shared-memory bandwidth, the permutes
+//     by ALU issue; counters put the kernel's shared-memory wavefronts at
+//     74% of peak with the table alone), raw codebook values with the group
+//     scale applied to the fp32 partial sums; for W4A4 layers (template
+//     TILE) the tile values rne(cb * s), the weights the definition and the
+//     tensor-core kernel use.
 // Accumulation is fp32, with two accumulator sets per thread. The epilogue
 // writes straight from registers:
 //   W13: h[p][c] = act(silu(g13 * gate) * (g13 * up)), SwiGLU fused.
@@ -147,7 +151,7 @@ __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xr
   const uint32_t xr[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
   uint32_t r0[8], r1[8];
   float sc0, sc1;
-  dequant_slot<FMT, TILE, ACT, true>(tile, rg, lane, r0, r1, &sc0, &sc1, s_e4m3, nf3_lut);
+  dequant_slot<FMT, TILE, ACT, NF3_MIX_LUT>(tile, rg, lane, r0, r1, &sc0, &sc1, s_e4m3, nf3_lut);
   if constexpr (FMT == FMT_NVFP4 || FMT == FMT_MXFP4 || TILE) {
 #pragma unroll
     for (int s = 0; s < 4; ++s)
@@ -174,8 +178,8 @@ __device__ __forceinline__ void sk_kblock2(const uint8_t* tile, const uint8_t* x
   constexpr int TB = tile_bytes(FMT);
   uint32_t a0[8], a1[8], b0[8], b1[8];
   float sa0, sa1, sb0, sb1;
-  dequant_slot<FMT, TILE, ACT, true>(tile, rg, lane, a0, a1, &sa0, &sa1, s_e4m3, nf3_lut);
-  dequant_slot<FMT, TILE, ACT, true>(tile + TB, rg, lane, b0, b1, &sb0, &sb1, s_e4m3, nf3_lut);
+  dequant_slot<FMT, TILE, ACT, NF3_MIX_LUT>(tile, rg, lane, a0, a1, &sa0, &sa1, s_e4m3, nf3_lut);
+  dequant_slot<FMT, TILE, ACT, NF3_MIX_LUT>(tile + TB, rg, lane, b0, b1, &sb0, &sb1, s_e4m3, nf3_lut);
   const uint4 xa = *reinterpret_cast<const uint4*>(xrow);
   const uint4 xb = *reinterpret_cast<const uint4*>(xrow + 16);
   const uint4 ya = *reinterpret_cast<const uint4*>(xrow + 128);

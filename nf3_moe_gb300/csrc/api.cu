@@ -101,8 +101,9 @@ hmoe_status check_bitmap(const hmoe_layer_desc* d, const int8_t* bit_map) {
   return HMOE_OK;
 }
 
-int pick_stage(int kbi) {
-  for (int s = STREAM_MAX_KBS; s > 1; s >>= 1)
+// The largest power of two up to max_kbs that divides the k-block count.
+int pick_stage(int kbi, int max_kbs = STREAM_MAX_KBS) {
+  for (int s = max_kbs; s > 1; s >>= 1)
     if (kbi % s == 0) return s;
   return 1;
 }
@@ -393,10 +394,15 @@ static hmoe_status run_stream_path(const hmoe_layer* L, const void* x, int T, co
     P.RT = P.rows / TILE_ROWS;
     P.KB = P.K / TILE_K;
     P.kbs = pick_stage(P.KB);
+    P.kbs1 = pick_stage(P.KB, 2 * STREAM_MAX_KBS);
     P.act = f == 0 ? static_cast<const uint16_t*>(xin) : p.h_out;
     P.act_stride = f == 0 ? d.H : d.I;
     P.kept_off = f == 0 ? 0 : L->gk.w13_bytes;
     P.nf3_off = f == 0 ? 0 : L->gn.w13_bytes;
+  }
+  {
+    const long long groups = std::min<long long>(S, d.E);
+    p.pair_items = groups * ((p.ph[0].RT + 1) / 2) >= (long long)STREAM_PAIR_MIN_ITEMS_PER_CTA * grid ? 1 : 0;
   }
   // Upper bound on the token groups of one launch: every slot of an expert
   // goes to one group of up to 8, so G <= min(S, ceil(S / 8) + E).
@@ -871,12 +877,17 @@ hmoe_status hmoe_linear_forward_ex(const hmoe_linear* L, const void* x, int T, v
     P.RT = L->d.N / TILE_ROWS;
     P.KB = L->d.K / TILE_K;
     P.kbs = pick_stage(P.KB);
+    P.kbs1 = pick_stage(P.KB, 2 * STREAM_MAX_KBS);
     P.act = static_cast<const uint16_t*>(x);
     P.act_stride = L->d.K;
     P.kept_off = P.nf3_off = 0;
     p.ph[0] = P;
     p.ph_begin = 1;
     p.ph_end = 2;
+    p.pair_items = (long long)std::min(T, 1) * ((P.RT + 1) / 2) >=
+                           (long long)STREAM_PAIR_MIN_ITEMS_PER_CTA * stream_grid(L->num_sms)
+                       ? 1
+                       : 0;
     e = launch_stream_gemm(p, stream_grid(L->num_sms), st);
     if (e != cudaSuccess) return cuda_fail(e, "linear stream GEMM launch");
   }

@@ -217,6 +217,23 @@ __device__ __forceinline__ void bulk_expect_and_copy_elect(void* dst, const void
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "r"(expect_bytes), "l"(policy)
       : "memory");
 }
+// Same with two weight ranges of the same size (the second only if second
+// is set) under one expected byte count.
+__device__ __forceinline__ void bulk_expect_and_copy2_elect(void* dst0, const void* src0, void* dst1, const void* src1,
+                                                            uint32_t bytes, bool second, uint32_t expect_bytes,
+                                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred e, t;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.and.b32 t, %7, 0, e;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%3], %4;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %5;\n\t"
+      "@t cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%6], [%8], %2, [%3], %5;\n\t}" ::"r"(
+          smem_u32(dst0)),
+      "l"(src0), "r"(bytes), "r"(smem_u32(bar)), "r"(expect_bytes), "l"(policy), "r"(smem_u32(dst1)),
+      "r"(second ? 1u : 0u), "l"(src1)
+      : "memory");
+}
 // A bulk copy issued by every lane whose predicate is set, in one warp
 // instruction (the lanes' copies are independent requests).
 __device__ __forceinline__ void bulk_g2s_if(bool pred, void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -438,9 +455,13 @@ __device__ __forceinline__ void nf3x8_lut(uint32_t sel, uint32_t lut, uint32_t* 
 // permutes. The table costs shared-memory bandwidth (one 128-byte wavefront
 // per warp and code pair), the permutes ALU issue (about 2.25 operations
 // per pair); with 16 consumer warps per SM sharing both, a mix keeps either
-// from saturating. Measured per M=8 launch (table words of 4): 4: 249.0 us,
-// 3 and 2 alternating: 242.6, 2: 242.1, 2 and 1: 245.4, 1: 249.3, 0: 257.4.
-constexpr int NF3_MIX_LUT = 2;
+// from saturating. Measured per M=8 launch with single-tile items (table
+// words of 4): 4: 249.0 us, 3 and 2 alternating: 242.6, 2: 242.1, 2 and 1:
+// 245.4, 1: 249.3, 0: 257.4; with items of two row tiles, which load the
+// activations once for both and leave more shared-memory bandwidth to the
+// table: 4: 231.8, 3: 229.2 to 231.3, 2: 237.4, 1: 243.6. At M=2 (single-tile
+// items) 3 words took 83.8 us, 2 words 90.0.
+constexpr int NF3_MIX_LUT = 3;
 
 // NF3 words A, B, C of one thread slot -> selector words for R0 codes 0..7,
 // R0 8..15, R1 0..7 and R1 8..15.

@@ -42,13 +42,22 @@ cudaError_t launch_debug_dequant(int fmt, int which, const uint8_t* src, int N, 
                                  cudaStream_t st);
 
 // ---------------------------------------------------------------- streaming GEMM (any T; the decode path)
-// Largest number of k-blocks per pipeline stage of the streaming kernel.
-constexpr int STREAM_MAX_KBS = 8;
+// Largest number of k-blocks per row tile in a pipeline stage of the
+// streaming kernel (a stage holds two row tiles).
+constexpr int STREAM_MAX_KBS = 4;
+// The streaming kernel's work items are pairs of row tiles (one activation
+// load serves both) when the batch can make at least this many W13 pair
+// items per CTA, counting min(T * topk, E) token groups; else single row
+// tiles, so that small batches keep more SMs busy. The choice depends only
+// on the batch size and the layer, so every tier order of a forward makes
+// the same choice and sums in the same order.
+constexpr int STREAM_PAIR_MIN_ITEMS_PER_CTA = 2;
 // One matrix of the expert FFN as the streaming kernel sees it.
 struct StreamPhase {
   int rows, K;               // rows = 2I (W13) or H (W2); K = H or I
   int RT, KB;                // row tiles, k-blocks
-  int kbs;                   // k-blocks per pipeline stage
+  int kbs;                   // k-blocks per row tile and pipeline stage, items of two row tiles
+  int kbs1;                  // k-blocks per pipeline stage, items of one row tile (up to 2 STREAM_MAX_KBS)
   const uint16_t* act;       // W13: x [T][H] by token; W2: h [S][I] by permuted position (operand type)
   int act_stride;
   size_t kept_off, nf3_off;  // byte offset of this matrix inside an expert's block
@@ -66,6 +75,7 @@ struct StreamParams {
   StreamPhase ph[2];     // [0] W13 (output h), [1] W2 (output y)
   int ph_begin, ph_end;  // phases this launch runs: [0,2) both (W2 items wait on done13), [0,1) or [1,2)
   int group_tokens;      // tokens per token group (<= 8)
+  int pair_items;        // 1: work items are pairs of row tiles; 0: single row tiles
   int tier_mask;         // bit 0: kept experts, bit 1: NF3 experts
   size_t kept_expert_bytes, nf3_expert_bytes;
   const int* offsets;

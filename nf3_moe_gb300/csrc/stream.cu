@@ -7,42 +7,50 @@
 // weights are streamed from HBM once per group of up to 8 of its tokens.
 //
 // One launch runs both matrices of the expert FFN. Work items are first
-// every (token group, W13 row tile), then every (token group, W2 row tile),
-// each over the whole K extent. A token group is up to 8 consecutive
-// permuted slots of one expert, so at T <= 8 there is exactly one group per
-// touched expert. Persistent CTAs (2 per SM) pull items from a global work
-// queue that resets itself. A W2 item reads the group's h rows, so its
-// producer first waits (bounded) until every W13 item of that group has
-// been written: each consumer warp counts its finished W13 items into a
-// per-group counter with release semantics. W13 items never wait on
-// anything, and every W13 item is dequeued before any W2 item, so the waits
-// always end. The W13 tail overlaps the W2 start, and there is one launch
-// instead of two. (Past the counter array's capacity the host runs the two
-// phases as two launches of the same kernel.)
+// every (token group, W13 rows), then every (token group, W2 rows), each
+// over the whole K extent. The rows of an item are a pair of 128-row tiles
+// when the batch makes at least two W13 pair items per CTA (the host
+// decides from T * topk and E), else one tile, so that small batches keep
+// more SMs busy. A token group is up to 8 consecutive permuted slots of one
+// expert, so at T <= 8 there is exactly one group per touched expert.
+// Persistent CTAs (2 per SM) pull items from a global work queue that
+// resets itself. A W2 item reads the group's h rows, so its producer first
+// waits (bounded) until every W13 item of that group has been written: each
+// consumer warp counts its finished W13 items into a per-group counter with
+// release semantics. W13 items never wait on anything, and every W13 item
+// is dequeued before any W2 item, so the waits always end. The W13 tail
+// overlaps the W2 start, and there is one launch instead of two. (Past the
+// counter array's capacity the host runs the two phases as two launches of
+// the same kernel.)
 //
 // The producer warp streams each item's packed tiles and the group's
-// activation rows into a 2-stage shared-memory ring of up to 8 k-blocks per
-// stage with 1D bulk copies (TMA engine), one warp instruction per stage: an
-// elected lane copies the weight tiles and lane j the activation row of
-// token j. Eight k-blocks per stage instead of four halve the per-stage waits
-// and bookkeeping of the consumers; measured 308 -> 284 us at M=8. It writes
-// the item number into each stage header, and a terminator stage ends the
-// consumers' loop. Eight consumer warps, one per 16-row group, dequantise in
-// registers and issue m16n8k16 MMAs (bf16 or fp16 operands, template ACT)
-// with the tokens as the N=8 side, two k-blocks' slots decoded before their
-// MMAs:
+// activation rows into a 2-stage shared-memory ring with 1D bulk copies
+// (TMA engine), one warp instruction per stage: an elected lane copies the
+// weight tiles and lane j the activation row of token j. A stage holds up
+// to 8 k-block tiles: 4 k-blocks of each tile of a pair item, or 8 of a
+// single-tile item. Eight k-blocks per stage instead of four halve the
+// per-stage waits and bookkeeping of the consumers; measured 308 -> 284 us
+// at M=8. It writes the item number into each stage header, and a
+// terminator stage ends the consumers' loop. Eight consumer warps, one per
+// 16-row group, dequantise in registers and issue m16n8k16 MMAs (bf16 or
+// fp16 operands, template ACT) with the tokens as the N=8 side. Pair items
+// decode the warp's slots of both tiles for one k-block and share one load
+// of the activation fragments between them (the activation loads were a
+// third of the kernel's shared-memory traffic); single-tile items decode
+// two k-blocks' slots before their MMAs. The decoders:
 //   NVFP4: shift-and-mask decode (bf16) or nibble-table decode (fp16), the
 //     E4M3 scales from a shared table of operand-type pairs, one x2 multiply;
 //   MXFP4: nibble-table decode, E8M0 scale multiply;
-//   NF3: half of the code pairs looked up in a bank-replicated shared
-//     table of operand pairs, the other half decoded with byte-table
-//     permutes (the table is bound by shared-memory bandwidth, the permutes
-//     by ALU issue; counters put the kernel's shared-memory wavefronts at
-//     74% of peak with the table alone), raw codebook values with the group
-//     scale applied to the fp32 partial sums; for W4A4 layers (template
-//     TILE) the tile values rne(cb * s), the weights the definition and the
+//   NF3: three of four selector words looked up in a bank-replicated shared
+//     table of operand pairs, the fourth decoded with byte-table permutes
+//     (the table is bound by shared-memory bandwidth, the permutes by ALU
+//     issue; counters put the kernel's shared-memory wavefronts at 74% of
+//     peak with the table alone), raw codebook values with the group scale
+//     applied to the fp32 partial sums; for W4A4 layers (template TILE) the
+//     tile values rne(cb * s), the weights the definition and the
 //     tensor-core kernel use.
-// Accumulation is fp32, with two accumulator sets per thread. The epilogue
+// Accumulation is fp32 with two accumulator sets per thread: the two tiles
+// of a pair item, or alternate k-blocks of a single-tile item. The epilogue
 // writes straight from registers:
 //   W13: h[p][c] = act(silu(g13 * gate) * (g13 * up)), SwiGLU fused.
 //   W2:  y[s][r] = g2 * sum, fp32, indexed by the flat slot s.
@@ -50,7 +58,9 @@
 // in slot order, so every output element is summed in a fixed order.
 // Splitting K across CTAs was measured slower at every batch size (the
 // cross-CTA reduction costs more than the idle SMs it fills), so items
-// always cover the whole K extent.
+// always cover the whole K extent. Measured per M=8 launch: single-tile
+// items 240.3 us, pair items 231.3 us; at M=1, pair items 85.4 us against
+// 57.0 (too few items for 304 CTAs), hence the choice by batch size.
 #include "common.cuh"
 #include "internal.h"
 
@@ -60,13 +70,14 @@ constexpr int SK_CONSUMER_WARPS = 8;
 constexpr int SK_WARP_PRODUCER = SK_CONSUMER_WARPS;       // warp 8
 constexpr int SK_THREADS = (SK_CONSUMER_WARPS + 1) * 32;
 constexpr int SK_STAGES = 2;
-constexpr int SK_MAX_KBS = STREAM_MAX_KBS;
+constexpr int SK_TILES = 2;                                // row tiles per work item
+constexpr int SK_MAX_KBS = STREAM_MAX_KBS;                 // k-blocks per tile and stage
 // Two CTAs per SM: three (4 k-blocks per stage, 72 registers) measured
 // slower, 252.3 against 249.5 us per M=8 launch, and 88.8 against 74.8 us at
 // M=1.
 constexpr int SK_CTAS_PER_SM = 2;
-constexpr int SK_XROW = SK_MAX_KBS * 128 + 16;            // padded token row, bytes
-constexpr int SK_W_BYTES = SK_MAX_KBS * 4608;
+constexpr int SK_XROW = 2 * SK_MAX_KBS * 128 + 16;        // padded token row, bytes
+constexpr int SK_W_BYTES = SK_TILES * SK_MAX_KBS * 4608;
 constexpr int SK_X_BYTES = 8 * SK_XROW;
 constexpr int SK_HDR_BYTES = 16;                           // {item, stage} written by the producer
 constexpr int SK_STAGE_BYTES = SK_W_BYTES + SK_X_BYTES + SK_HDR_BYTES;
@@ -77,21 +88,28 @@ static_assert(SK_CTAS_PER_SM * (SK_SMEM_BYTES + 1024) <= 233472, "CTAs per SM");
 static_assert(SK_STAGE_BYTES % 16 == 0, "stage alignment");
 
 struct SkItem {
-  int e, p0, n, rt, grp, ph;  // ph: 0 = W13, 1 = W2
+  int e, p0, n, rt, grp, ph;  // rt: row tile, or tile pair (row tiles 2 rt, 2 rt + 1); ph: 0 = W13, 1 = W2
+  bool two;                   // pair items: row tile 2 rt + 1 exists (an odd tile count ends on one tile)
 };
+
+// Work items of one phase per token group: pairs of row tiles, or row tiles.
+__device__ __forceinline__ int tile_pairs(const StreamPhase& P) { return (P.RT + 1) >> 1; }
+__device__ __forceinline__ int phase_units(const StreamPhase& P, bool pair) { return pair ? tile_pairs(P) : P.RT; }
 
 __device__ __forceinline__ int expert_fmt(const StreamParams& p, int e) {
   return (p.tab.loc[e] & LOC_NF3) ? FMT_NF3 : p.kept_fmt;
 }
 
-__device__ __forceinline__ SkItem decode_item(const StreamParams& p, const int* s_gstart, const int* s_off, int i) {
+__device__ __forceinline__ SkItem decode_item(const StreamParams& p, const int* s_gstart, const int* s_off, int i,
+                                              bool pair) {
   SkItem it;
-  const int n13 = p.ph_begin == 0 ? s_gstart[p.E] * p.ph[0].RT : 0;
+  const int n13 = p.ph_begin == 0 ? s_gstart[p.E] * phase_units(p.ph[0], pair) : 0;
   it.ph = i >= n13 ? 1 : 0;
   const int local = it.ph ? i - n13 : i;
-  const int RT = p.ph[it.ph].RT;
-  it.rt = local % RT;
-  it.grp = local / RT;
+  const int PT = phase_units(p.ph[it.ph], pair);
+  it.rt = local % PT;
+  it.grp = local / PT;
+  it.two = pair && 2 * it.rt + 1 < p.ph[it.ph].RT;
   int lo = 0, hi = p.E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -107,7 +125,7 @@ __device__ __forceinline__ SkItem decode_item(const StreamParams& p, const int* 
 
 // Output of one thread's 2 rows x 2 tokens (v[0],v[1]: row R0; v[2],v[3]: row R1).
 template <int ACT>
-__device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it, int rg, int g, int q,
+__device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it, int rt, int rg, int g, int q,
                                         const float* v) {
   const int S = p.T * p.topk;
 #pragma unroll
@@ -118,7 +136,7 @@ __device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it,
     if (it.ph == 0) {
       const float gsc =
           p.tab.g13[it.e] * (expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f) * p.act_scale13;
-      const int ch = it.rt * 64 + rg * 8 + g;
+      const int ch = rt * 64 + rg * 8 + g;
       const float gate = v[h] * gsc, up = v[2 + h] * gsc;
       p.h_out[(size_t)pp * p.I + ch] = f32_to_act<ACT>(silu_f(gate) * up);
     } else {
@@ -129,14 +147,90 @@ __device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it,
         set_status(p.status, DEV_BAD_ROUTE);
         continue;
       }
-      const int row = it.rt * 128 + rg * 16 + g;
+      const int row = rt * 128 + rg * 16 + g;
       p.y_out[(size_t)s * p.H + row] = v[h] * gsc;
       p.y_out[(size_t)s * p.H + row + 8] = v[2 + h] * gsc;
     }
   }
 }
 
-// One k-block of one thread slot: dequantise through dequant_slot (the
+// Pair items. One k-block of one thread slot in both row tiles: dequantise
+// through dequant_slot (the decoder hmoe_debug_decode_operand exports;
+// NVFP4/MXFP4 scales applied in the operand type from the shared lookup
+// table, NF3 values raw with the row scales applied to the fp32 sum of the
+// k-block), both slots before any MMA, then 4 MMAs per tile. The two tiles
+// share the activation fragments, so one load of the token rows serves 32
+// weight rows. With TILE (W4A4 layers) NF3 is decoded to the tile values
+// rne(cb * s) instead, the weights the definition and the tensor-core
+// kernel use: W4A4 quantises h, so h must come from the same weights on
+// both paths. Without TWO (the last item of a phase with an odd tile
+// count) only tile 0 is computed.
+template <int FMT, int ACT, bool TILE, bool TWO>
+__device__ __forceinline__ void sk_kblock(const uint8_t* tile0, const uint8_t* tile1, const uint8_t* xrow, int rg,
+                                          int lane, const uint32_t* s_e4m3, uint32_t nf3_lut, float* acc0,
+                                          float* acc1) {
+  uint32_t a0[8], a1[8], b0[8], b1[8];
+  float sa0, sa1, sb0 = 1.0f, sb1 = 1.0f;
+  dequant_slot<FMT, TILE, ACT, NF3_MIX_LUT>(tile0, rg, lane, a0, a1, &sa0, &sa1, s_e4m3, nf3_lut);
+  if constexpr (TWO) dequant_slot<FMT, TILE, ACT, NF3_MIX_LUT>(tile1, rg, lane, b0, b1, &sb0, &sb1, s_e4m3, nf3_lut);
+  const uint4 xa = *reinterpret_cast<const uint4*>(xrow);
+  const uint4 xb = *reinterpret_cast<const uint4*>(xrow + 16);
+  const uint32_t xr[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+  if constexpr (FMT == FMT_NVFP4 || FMT == FMT_MXFP4 || TILE) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      mma_16816<ACT>(acc0, a0[2 * s], a1[2 * s], a0[2 * s + 1], a1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
+      if constexpr (TWO)
+        mma_16816<ACT>(acc1, b0[2 * s], b1[2 * s], b0[2 * s + 1], b1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
+    }
+  } else {
+    float d[4], e[4];
+    mma_16816_zc<ACT>(d, a0[0], a1[0], a0[1], a1[1], xr[0], xr[1]);
+    if constexpr (TWO) mma_16816_zc<ACT>(e, b0[0], b1[0], b0[1], b1[1], xr[0], xr[1]);
+#pragma unroll
+    for (int s = 1; s < 4; ++s) {
+      mma_16816<ACT>(d, a0[2 * s], a1[2 * s], a0[2 * s + 1], a1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
+      if constexpr (TWO)
+        mma_16816<ACT>(e, b0[2 * s], b1[2 * s], b0[2 * s + 1], b1[2 * s + 1], xr[2 * s], xr[2 * s + 1]);
+    }
+    acc0[0] = fmaf(sa0, d[0], acc0[0]);
+    acc0[1] = fmaf(sa0, d[1], acc0[1]);
+    acc0[2] = fmaf(sa1, d[2], acc0[2]);
+    acc0[3] = fmaf(sa1, d[3], acc0[3]);
+    if constexpr (TWO) {
+      acc1[0] = fmaf(sb0, e[0], acc1[0]);
+      acc1[1] = fmaf(sb0, e[1], acc1[1]);
+      acc1[2] = fmaf(sb1, e[2], acc1[2]);
+      acc1[3] = fmaf(sb1, e[3], acc1[3]);
+    }
+  }
+}
+
+// All k-blocks of one stage: kbs tiles of row tile 0, then kbs of row tile 1.
+template <int FMT, int ACT, bool TILE, bool TWO>
+__device__ __forceinline__ void sk_stage(const uint8_t* sw, const uint8_t* sx, int kbs, int rg, int lane,
+                                         const uint32_t* s_e4m3, uint32_t nf3_lut, float* acc0, float* acc1) {
+  constexpr int TB = tile_bytes(FMT);
+  if (kbs == SK_MAX_KBS) {
+#pragma unroll
+    for (int j = 0; j < SK_MAX_KBS; ++j)
+      sk_kblock<FMT, ACT, TILE, TWO>(sw + j * TB, sw + (SK_MAX_KBS + j) * TB, sx + j * 128, rg, lane, s_e4m3, nf3_lut,
+                                     acc0, acc1);
+  } else {
+    for (int j = 0; j < kbs; ++j)
+      sk_kblock<FMT, ACT, TILE, TWO>(sw + j * TB, sw + (kbs + j) * TB, sx + j * 128, rg, lane, s_e4m3, nf3_lut, acc0,
+                                     acc1);
+  }
+}
+
+template <int FMT, int ACT, bool TILE>
+__device__ __forceinline__ void sk_stage_any(bool two, const uint8_t* sw, const uint8_t* sx, int kbs, int rg, int lane,
+                                             const uint32_t* s_e4m3, uint32_t nf3_lut, float* acc0, float* acc1) {
+  if (two) sk_stage<FMT, ACT, TILE, true>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, acc0, acc1);
+  else sk_stage<FMT, ACT, TILE, false>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, acc0, acc1);
+}
+
+// Single-tile items. One k-block of one thread slot: dequantise through dequant_slot (the
 // decoder hmoe_debug_decode_operand exports; NVFP4/MXFP4 scales applied in
 // the operand type from the shared lookup table, NF3 values raw with the row
 // scales applied to the fp32 sum of the k-block) and 4 MMAs. With TILE (W4A4
@@ -144,7 +238,7 @@ __device__ __forceinline__ void sk_emit(const StreamParams& p, const SkItem& it,
 // the definition and the tensor-core kernel use: W4A4 quantises h, so h must
 // come from the same weights on both paths.
 template <int FMT, int ACT, bool TILE>
-__device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xrow, int rg, int lane,
+__device__ __forceinline__ void sk1_kblock(const uint8_t* tile, const uint8_t* xrow, int rg, int lane,
                                           const uint32_t* s_e4m3, uint32_t nf3_lut, float* acc) {
   const uint4 xa = *reinterpret_cast<const uint4*>(xrow);
   const uint4 xb = *reinterpret_cast<const uint4*>(xrow + 16);
@@ -173,7 +267,7 @@ __device__ __forceinline__ void sk_kblock(const uint8_t* tile, const uint8_t* xr
 // either k-block's MMAs, so the warp has two independent decode chains to
 // interleave (k-block j into accA, j + 1 into accB).
 template <int FMT, int ACT, bool TILE>
-__device__ __forceinline__ void sk_kblock2(const uint8_t* tile, const uint8_t* xrow, int rg, int lane,
+__device__ __forceinline__ void sk1_kblock2(const uint8_t* tile, const uint8_t* xrow, int rg, int lane,
                                            const uint32_t* s_e4m3, uint32_t nf3_lut, float* accA, float* accB) {
   constexpr int TB = tile_bytes(FMT);
   uint32_t a0[8], a1[8], b0[8], b1[8];
@@ -214,18 +308,18 @@ __device__ __forceinline__ void sk_kblock2(const uint8_t* tile, const uint8_t* x
 
 // All k-blocks of one stage, two accumulator sets to break the MMA chain.
 template <int FMT, int ACT, bool TILE>
-__device__ __forceinline__ void sk_stage(const uint8_t* sw, const uint8_t* sx, int kbs, int rg, int lane,
+__device__ __forceinline__ void sk1_stage(const uint8_t* sw, const uint8_t* sx, int kbs, int rg, int lane,
                                          const uint32_t* s_e4m3, uint32_t nf3_lut, float* accA, float* accB) {
   constexpr int TB = tile_bytes(FMT);
-  if (kbs == 8) {
+  if (kbs == 2 * SK_MAX_KBS) {
 #pragma unroll
-    for (int j = 0; j < 8; j += 2)
-      sk_kblock2<FMT, ACT, TILE>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, nf3_lut, accA, accB);
+    for (int j = 0; j < 2 * SK_MAX_KBS; j += 2)
+      sk1_kblock2<FMT, ACT, TILE>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, nf3_lut, accA, accB);
   } else if (kbs == 4) {
-    sk_kblock2<FMT, ACT, TILE>(sw, sx, rg, lane, s_e4m3, nf3_lut, accA, accB);
-    sk_kblock2<FMT, ACT, TILE>(sw + 2 * TB, sx + 256, rg, lane, s_e4m3, nf3_lut, accA, accB);
+    sk1_kblock2<FMT, ACT, TILE>(sw, sx, rg, lane, s_e4m3, nf3_lut, accA, accB);
+    sk1_kblock2<FMT, ACT, TILE>(sw + 2 * TB, sx + 256, rg, lane, s_e4m3, nf3_lut, accA, accB);
   } else {
-    for (int j = 0; j < kbs; ++j) sk_kblock<FMT, ACT, TILE>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, nf3_lut, (j & 1) ? accB : accA);
+    for (int j = 0; j < kbs; ++j) sk1_kblock<FMT, ACT, TILE>(sw + j * TB, sx + j * 128, rg, lane, s_e4m3, nf3_lut, (j & 1) ? accB : accA);
   }
 }
 
@@ -291,9 +385,10 @@ __global__ void __launch_bounds__(SK_THREADS, SK_CTAS_PER_SM) stream_gemm_kernel
   __syncthreads();
 
   const int n_groups = s_gstart[p.E];
-  int rt_sum = 0;
-  for (int f = p.ph_begin; f < p.ph_end; ++f) rt_sum += p.ph[f].RT;
-  const int n_items = n_groups * rt_sum;
+  const bool pair = p.pair_items != 0;
+  int units = 0;
+  for (int f = p.ph_begin; f < p.ph_end; ++f) units += phase_units(p.ph[f], pair);
+  const int n_items = n_groups * units;
   const bool fused = p.ph_begin == 0 && p.ph_end == 2;
 
   if (warp == SK_WARP_PRODUCER) {
@@ -315,7 +410,7 @@ __global__ void __launch_bounds__(SK_THREADS, SK_CTAS_PER_SM) stream_gemm_kernel
         if (lane == 0) i = atomicAdd(p.queue, 1);
         i = __shfl_sync(0xffffffffu, i, 0);
         if (i >= n_items) break;
-        const SkItem it = decode_item(p, s_gstart, s_off, i);
+        const SkItem it = decode_item(p, s_gstart, s_off, i, pair);
         const StreamPhase& P = p.ph[it.ph];
         const int fmt = expert_fmt(p, it.e);
         const size_t tb = (size_t)tile_bytes(fmt);
@@ -341,7 +436,8 @@ __global__ void __launch_bounds__(SK_THREADS, SK_CTAS_PER_SM) stream_gemm_kernel
           // The group's h rows come from its W13 items (any CTA): wait until
           // all of them are written, then order the bulk copies after.
           bool ok = true;
-          if (lane == 0) ok = wait_count_at_least(p.done13 + it.grp, SK_CONSUMER_WARPS * p.ph[0].RT, s_flags, lim);
+          if (lane == 0)
+            ok = wait_count_at_least(p.done13 + it.grp, SK_CONSUMER_WARPS * phase_units(p.ph[0], pair), s_flags, lim);
           if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
             aborted = true;
             if (lane == 0) {
@@ -352,7 +448,8 @@ __global__ void __launch_bounds__(SK_THREADS, SK_CTAS_PER_SM) stream_gemm_kernel
           }
           fence_proxy_async_global();
         }
-        const int nst = P.KB / P.kbs;
+        const int kbs = pair ? P.kbs : P.kbs1;
+        const int nst = P.KB / kbs;
         for (int st = 0; st < nst; ++st) {
           if (!__all_sync(0xffffffffu, mbar_wait(&empty[slot], ph ^ 1u, s_flags, lim))) {
             aborted = true;
@@ -362,9 +459,9 @@ __global__ void __launch_bounds__(SK_THREADS, SK_CTAS_PER_SM) stream_gemm_kernel
             }
             break;
           }
-          const int kbA = st * P.kbs;
-          const uint32_t wbytes = (uint32_t)(P.kbs * tb);
-          const uint32_t xbytes = (uint32_t)(P.kbs * 128);
+          const int kbA = st * kbs;
+          const uint32_t wbytes = (uint32_t)(kbs * tb);
+          const uint32_t xbytes = (uint32_t)(kbs * 128);
           uint8_t* sw = smem + slot * SK_STAGE_BYTES;
           uint8_t* sx = sw + SK_W_BYTES;
           if (lane == 0) {
@@ -373,8 +470,11 @@ __global__ void __launch_bounds__(SK_THREADS, SK_CTAS_PER_SM) stream_gemm_kernel
             hdr[1] = st;
           }
           __syncwarp();
-          bulk_expect_and_copy_elect(sw, base + ((size_t)it.rt * P.KB + kbA) * tb, wbytes,
-                                     wbytes + (uint32_t)it.n * xbytes, &full[slot], pol);
+          // Pair items: row tile 2 rt's k-blocks, then row tile 2 rt + 1's,
+          // each one contiguous range of the tile layout. Single: row tile rt.
+          const uint8_t* src0 = base + ((size_t)(pair ? 2 * it.rt : it.rt) * P.KB + kbA) * tb;
+          bulk_expect_and_copy2_elect(sw, src0, sw + wbytes, src0 + (size_t)P.KB * tb, wbytes, it.two,
+                                      (it.two ? 2u : 1u) * wbytes + (uint32_t)it.n * xbytes, &full[slot], pol);
           bulk_g2s_if(lane < it.n, sx + lane * SK_XROW, P.act + (size_t)my_row * P.act_stride + (size_t)kbA * 64,
                       xbytes, &full[slot]);
           ++issued;
@@ -420,7 +520,7 @@ __global__ void __launch_bounds__(SK_THREADS, SK_CTAS_PER_SM) stream_gemm_kernel
     uint32_t ph = 0;
     SkItem it{};
     int fmt = FMT_NF3, kbs = 1, nst = 1;
-    float accA[4], accB[4];
+    float acc0[4], acc1[4];
     while (true) {
       if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], ph, s_flags, lim))) {
         if (lane == 0) {
@@ -434,17 +534,25 @@ __global__ void __launch_bounds__(SK_THREADS, SK_CTAS_PER_SM) stream_gemm_kernel
       const int i = hdr[0], st = hdr[1];
       if (i < 0) break;
       if (st == 0) {
-        it = decode_item(p, s_gstart, s_off, i);
+        it = decode_item(p, s_gstart, s_off, i, pair);
         fmt = expert_fmt(p, it.e);
-        kbs = p.ph[it.ph].kbs;
+        kbs = pair ? p.ph[it.ph].kbs : p.ph[it.ph].kbs1;
         nst = p.ph[it.ph].KB / kbs;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) accA[r] = accB[r] = 0.f;
+        for (int r = 0; r < 4; ++r) acc0[r] = acc1[r] = 0.f;
       }
       const uint8_t* sx = sw + SK_W_BYTES + g * SK_XROW + q * 32;
-      if (fmt == FMT_NVFP4) sk_stage<FMT_NVFP4, ACT, TILE>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, accA, accB);
-      else if (fmt == FMT_MXFP4) sk_stage<FMT_MXFP4, ACT, TILE>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, accA, accB);
-      else sk_stage<FMT_NF3, ACT, TILE>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, accA, accB);
+      if (pair) {
+        if (fmt == FMT_NVFP4)
+          sk_stage_any<FMT_NVFP4, ACT, TILE>(it.two, sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, acc0, acc1);
+        else if (fmt == FMT_MXFP4)
+          sk_stage_any<FMT_MXFP4, ACT, TILE>(it.two, sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, acc0, acc1);
+        else sk_stage_any<FMT_NF3, ACT, TILE>(it.two, sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, acc0, acc1);
+      } else {
+        if (fmt == FMT_NVFP4) sk1_stage<FMT_NVFP4, ACT, TILE>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, acc0, acc1);
+        else if (fmt == FMT_MXFP4) sk1_stage<FMT_MXFP4, ACT, TILE>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, acc0, acc1);
+        else sk1_stage<FMT_NF3, ACT, TILE>(sw, sx, kbs, rg, lane, s_e4m3, nf3_lut, acc0, acc1);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
       if (++slot == SK_STAGES) {
@@ -453,10 +561,15 @@ __global__ void __launch_bounds__(SK_THREADS, SK_CTAS_PER_SM) stream_gemm_kernel
       }
       if (st != nst - 1) continue;
       // ---------------- item epilogue
-      float acc[4];
+      if (pair) {
+        sk_emit<ACT>(p, it, 2 * it.rt, rg, g, q, acc0);
+        if (it.two) sk_emit<ACT>(p, it, 2 * it.rt + 1, rg, g, q, acc1);
+      } else {
+        // single-tile items: acc0 and acc1 hold alternate k-blocks
 #pragma unroll
-      for (int r = 0; r < 4; ++r) acc[r] = accA[r] + accB[r];
-      sk_emit<ACT>(p, it, rg, g, q, acc);
+        for (int r = 0; r < 4; ++r) acc0[r] += acc1[r];
+        sk_emit<ACT>(p, it, it.rt, rg, g, q, acc0);
+      }
       if (fused && it.ph == 0) {
         // Publish this warp's h rows to the W2 producers, whose bulk copies
         // (async proxy) may run on any SM: every lane fences its own stores
@@ -499,7 +612,9 @@ cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st)
   if (p.ph_begin < 0 || p.ph_begin >= p.ph_end || p.ph_end > 2) return cudaErrorInvalidValue;
   if (p.ph_begin == 0 && p.ph_end == 2 && !p.done13) return cudaErrorInvalidValue;
   for (const StreamPhase& P : p.ph)
-    if (P.kbs < 1 || P.kbs > SK_MAX_KBS || P.KB % P.kbs != 0) return cudaErrorInvalidValue;
+    if (P.kbs < 1 || P.kbs > SK_MAX_KBS || P.KB % P.kbs != 0 || P.kbs1 < 1 || P.kbs1 > 2 * SK_MAX_KBS ||
+        P.KB % P.kbs1 != 0)
+      return cudaErrorInvalidValue;
   if (p.group_tokens < 1 || p.group_tokens > 8) return cudaErrorInvalidValue;
   auto kern = p.act_type == ACT_F16 ? (p.nf3_tile ? stream_gemm_kernel<ACT_F16, true> : stream_gemm_kernel<ACT_F16, false>)
                                     : (p.nf3_tile ? stream_gemm_kernel<ACT_BF16, true> : stream_gemm_kernel<ACT_BF16, false>);

@@ -79,6 +79,24 @@ def test_odd_k_block_counts(kept_format):
     U.assert_rows_close(g.float().cpu().numpy(), s.float().cpu().numpy())
 
 
+@pytest.mark.parametrize("kept_format", [synth.FMT_NVFP4, synth.FMT_MXFP4])
+def test_stream_pair_items_with_odd_row_tile_counts(kept_format):
+    """H=384, I=192: W13 and W2 both have 3 row tiles, so the streaming kernel's last item of
+    each phase holds one tile when its items are pairs of row tiles. 512 experts, top-8 and
+    T=64 give min(T * topk, E) = 512 token groups, enough W13 pair items per CTA (2 pairs x 512
+    against 2 per CTA) for the host to choose pair items on any GPU of up to 256 SMs. Every
+    token is checked against the oracle, on both tier orders."""
+    L = synth.make_layer(384, 192, 512, 8, kept=128, kept_format=kept_format, device="cuda")
+    T = 64
+    moe = U.build(L, T)
+    x = synth.gen_x(T, L.H, seed=21, device="cuda")
+    logits = synth.gen_logits(T, L.E, seed=21, device="cuda")
+    s, (ids, gates, _, _) = U.run(moe, x, logits, path=hm.PATH_STREAM)
+    U.assert_rows_close(s.float().cpu().numpy(), U.oracle_out(L, x, ids, gates))
+    s2, _ = U.run(moe, x, logits, path=hm.PATH_STREAM, tier_order=hm.TIERS_KEPT_FIRST)
+    assert torch.equal(s, s2)
+
+
 def test_top1_single_expert_and_repeat_calls(tiny):
     """top-1 (gate = 1) reduces to one dense expert; repeated calls are bitwise stable."""
     Lh = synth.make_layer(256, 128, 8, 1, kept_ids=[1, 5], device="cuda")

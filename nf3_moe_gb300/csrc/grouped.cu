@@ -1331,34 +1331,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G2_THREADS, 1)
 }
 
 // ------------------------------------------------------------ gather of activation rows
-__global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int* __restrict__ perm, int S, int k,
-                                   int T, int H, uint16_t* __restrict__ xg, int* status) {
+// xg[p] = x[perm[p] / k]: one warp per permuted row (perm read once per row),
+// its lanes copying the row's 16-byte vectors with several loads in flight.
+// (A flat index over rows x vectors needed a 64-bit division per vector.)
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x, const int* __restrict__ perm,
+                                                          int S, int k, int H, uint16_t* __restrict__ xg, int* status) {
   pdl_wait();
   pdl_trigger();
   const int vec = H / 8;  // 16-byte vectors per row
-  const long long n = (long long)S * vec;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int pidx = (int)(i / vec), c = (int)(i % vec);
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  for (int pidx = blockIdx.x * wpb + (threadIdx.x >> 5); pidx < S; pidx += gridDim.x * wpb) {
     int s = perm[pidx];
     if (s < 0 || s >= S) {
-      if (c == 0) set_status(status, DEV_BAD_ROUTE);
+      if (lane == 0) set_status(status, DEV_BAD_ROUTE);
       s = 0;
     }
-    const int t = s / k;
-    reinterpret_cast<uint4*>(xg + (size_t)pidx * H)[c] =
-        __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + c);
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(s / k) * H);
+    uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)pidx * H);
+#pragma unroll 8
+    for (int c = lane; c < vec; c += 32) dst[c] = __ldg(src + c);
   }
-  (void)T;
 }
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int* perm, int S, int k, int T, int H, uint16_t* xg,
                                int* status, int num_sms, cudaStream_t st) {
+  (void)T;
   if (S == 0) return cudaSuccess;
-  const long long n = (long long)S * (H / 8);
-  const long long blocks = (n + 255) / 256;
-  const int grid = (int)(blocks < (long long)num_sms * 8 ? blocks : (long long)num_sms * 8);
-  cudaError_t e = launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, st, x, perm, S, k, T, H, xg, status);
+  const long long blocks = ((long long)S + 7) / 8;
+  const int grid = (int)(blocks < (long long)num_sms * 16 ? blocks : (long long)num_sms * 16);
+  cudaError_t e = launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, st, x, perm, S, k, H, xg, status);
   count_launches(1);
   return e;
 }

@@ -17,49 +17,55 @@ namespace hmoe {
 
 constexpr int ROUTE_CHUNK_TOKENS = 32;  // tokens per chunk in the large-batch path
 
+// Order-preserving map of fp32 to uint32 (a > b exactly when key(a) >
+// key(b)), with -0 mapped like +0 so that the two compare equal, as they do
+// as floats. NaN logits are not supported.
+__device__ __forceinline__ uint32_t route_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if ((u << 1) == 0u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float route_key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 // One warp routes one token. Lane l holds logits of experts l, l+32, ...
-// (E <= 512, so at most 16 per lane). Rounds of warp arg-max pick the k
-// winners in descending order, ties to the lower id. Lane r (r < k) returns
-// the r-th winner's id and gate.
+// (E <= 512, so at most 16 per lane), as order-preserving keys. Each of the
+// k rounds takes the lane's best remaining candidate (the lowest expert id
+// among equal keys), then the warp's largest key and, among the lanes that
+// hold it, the lowest expert id (two warp reductions), so the winners come
+// in descending order with ties to the lower id. Lane r (r < k) returns the
+// r-th winner's id and gate.
 __device__ __forceinline__ void warp_route_token(const float* __restrict__ row, int E, int k, int lane,
                                                  int* my_id, float* my_gate) {
-  float v[MAX_E / 32];
+  uint32_t key[MAX_E / 32];
 #pragma unroll
   for (int j = 0; j < MAX_E / 32; ++j) {
     const int e = lane + 32 * j;
-    v[j] = (e < E) ? row[e] : 0.0f;
+    key[j] = (e < E) ? route_key(row[e]) : 0u;  // 0: below every real key
   }
   uint32_t taken = 0;
   int rid = 0;
-  float rval = 0.0f;
+  uint32_t rkey = 0;
   for (int r = 0; r < k; ++r) {
-    float bv = -INFINITY;
-    int be = 0x7FFFFFFF;
+    uint32_t bk = 0;
+    uint32_t be = 0xFFFFFFFFu;
 #pragma unroll
     for (int j = 0; j < MAX_E / 32; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E && !((taken >> j) & 1u)) {
-        if (v[j] > bv || (v[j] == bv && e < be)) {
-          bv = v[j];
-          be = e;
-        }
+      if (!((taken >> j) & 1u) && key[j] > bk) {  // j ascending: the first of equal keys has the lowest id
+        bk = key[j];
+        be = (uint32_t)(lane + 32 * j);
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t w = __reduce_min_sync(0xffffffffu, bk == m ? be : 0xFFFFFFFFu);
+    if ((int)(w & 31u) == lane) taken |= 1u << (w >> 5);
     if (lane == r) {
-      rid = be;
-      rval = bv;
+      rid = (int)w;
+      rkey = m;
     }
   }
+  const float rval = route_key_value(rkey);
   const float lmax = __shfl_sync(0xffffffffu, rval, 0);
   const float z = (lane < k) ? expf(rval - lmax) : 0.0f;
   float sum = z;
@@ -117,11 +123,26 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const float* __restri
   }
   __syncthreads();
   for (int e = tid; e <= E; e += blockDim.x) offsets[e] = s_off[e];
-  for (int s = tid; s < S; s += blockDim.x) {
-    const int e = s_ids[s];
-    int rank = 0;
-    for (int s2 = 0; s2 < s; ++s2) rank += (s_ids[s2] == e);
-    perm[s_off[e] + rank] = s;
+  // Stable ranks (thread s holds slot s; S <= blockDim.x): inside a warp,
+  // match_any ranks the slots of equal experts; the warps take turns in slot
+  // order, each adding the running per-expert count (s_cnt, reused) of the
+  // warps before it.
+  for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  const int e_mine = tid < S ? s_ids[tid] : -1 - lane;  // distinct dummies never match real ids
+  const unsigned peers = __match_any_sync(0xffffffffu, e_mine);
+  const int rank_w = __popc(peers & ((1u << lane) - 1u));
+  const int nw = (S + 31) / 32;
+  for (int w = 0; w < nw; ++w) {
+    if (warp == w) {
+      const int base = tid < S ? s_cnt[e_mine] : 0;
+      __syncwarp();
+      if (tid < S) {
+        perm[s_off[e_mine] + base + rank_w] = tid;
+        if (rank_w == 0) s_cnt[e_mine] = base + __popc(peers);
+      }
+    }
+    __syncthreads();
   }
 }
 

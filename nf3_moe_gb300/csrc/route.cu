@@ -176,35 +176,40 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 }
 
 // K2: one CTA. Column-wise exclusive scan over chunks gives chunk_base; the
-// expert totals are scanned to offsets.
+// expert totals are scanned to offsets. The chunks are split into P ranges
+// (P = blockDim / E threads per expert), each summed by one thread, so that
+// every thread has few dependent round trips to L2: pass 1 sums the ranges,
+// pass 2 writes each range's prefix from its base.
 __global__ void __launch_bounds__(1024) route_scan_kernel(const int* __restrict__ chunk_cnt, int nchunks, int E,
                                                           int S, int* __restrict__ chunk_base,
                                                           int* __restrict__ offsets) {
   __shared__ int s_tot[MAX_E + 1];
+  __shared__ int s_part[1024];
   __shared__ int s_wsum[32];
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x;
-  if (tid < E) {
+  const int P = max(1, (int)blockDim.x / E);
+  const int e = tid % E, q = tid / E;
+  const bool act = q < P;
+  const int c0 = (int)((long long)q * nchunks / P), c1 = (int)((long long)(q + 1) * nchunks / P);
+  int part = 0;
+  if (act) {
+#pragma unroll 8
+    for (int c = c0; c < c1; ++c) part += chunk_cnt[(size_t)c * E + e];
+    s_part[q * E + e] = part;
+  }
+  __syncthreads();
+  if (act) {
     int run = 0;
-    int c = 0;
-    for (; c + 4 <= nchunks; c += 4) {
-      const int a0 = chunk_cnt[(size_t)(c + 0) * E + tid];
-      const int a1 = chunk_cnt[(size_t)(c + 1) * E + tid];
-      const int a2 = chunk_cnt[(size_t)(c + 2) * E + tid];
-      const int a3 = chunk_cnt[(size_t)(c + 3) * E + tid];
-      chunk_base[(size_t)(c + 0) * E + tid] = run;
-      chunk_base[(size_t)(c + 1) * E + tid] = run + a0;
-      chunk_base[(size_t)(c + 2) * E + tid] = run + a0 + a1;
-      chunk_base[(size_t)(c + 3) * E + tid] = run + a0 + a1 + a2;
-      run += a0 + a1 + a2 + a3;
-    }
-    for (; c < nchunks; ++c) {
-      const int a = chunk_cnt[(size_t)c * E + tid];
-      chunk_base[(size_t)c * E + tid] = run;
+    for (int qq = 0; qq < q; ++qq) run += s_part[qq * E + e];
+#pragma unroll 8
+    for (int c = c0; c < c1; ++c) {
+      const int a = chunk_cnt[(size_t)c * E + e];
+      chunk_base[(size_t)c * E + e] = run;
       run += a;
     }
-    s_tot[tid] = run;
+    if (q == P - 1) s_tot[e] = run;
   }
   __syncthreads();
   // block exclusive scan of s_tot[0..E)

@@ -346,6 +346,13 @@ __global__ void __launch_bounds__(SK_THREADS, SK_CTAS_PER_SM) stream_gemm_kernel
   }
   if (tid < 256) s_e4m3[tid] = e4m3_lut_entry<ACT>((uint32_t)tid);
   nf3_lut_fill<ACT>(s_nf3, tid, blockDim.x);
+  // Which experts this launch's tier selection covers, from the parameter
+  // table, before the wait on the routing kernel (the prefix below reads it
+  // from shared memory instead of indexing the parameter table per lane).
+  for (int e = tid; e < p.E; e += blockDim.x) {
+    const bool nf3 = (p.tab.loc[e] & LOC_NF3) != 0;
+    s_gstart[e] = (nf3 ? (p.tier_mask & 2) : (p.tier_mask & 1)) ? 1 : 0;
+  }
   pdl_wait();  // everything below reads or writes global memory
   pdl_trigger();
   for (int e = tid; e <= p.E; e += blockDim.x) s_off[e] = p.offsets[e];
@@ -361,8 +368,7 @@ __global__ void __launch_bounds__(SK_THREADS, SK_CTAS_PER_SM) stream_gemm_kernel
       if (e < p.E) {
         const int ne = s_off[e + 1] - s_off[e];
         if (ne < 0) bad = true;
-        const bool nf3 = (p.tab.loc[e] & LOC_NF3) != 0;
-        const bool sel = nf3 ? (p.tier_mask & 2) : (p.tier_mask & 1);
+        const bool sel = s_gstart[e] != 0;
         ng = (sel && ne > 0) ? (ne + p.group_tokens - 1) / p.group_tokens : 0;
       }
       int incl = ng;
@@ -624,33 +630,38 @@ cudaError_t launch_stream_gemm(const StreamParams& p, int grid, cudaStream_t st)
 }
 
 // ------------------------------------------------------------ finalize
+// out[t][c] = act(sum_j gates[t*k+j] * y[t*k+j][c]) in slot order: blocks
+// along x cover a row's column pairs, along y the tokens (grid-stride in
+// both), so no index needs a division.
 template <int ACT>
 __global__ void finalize_kernel(const float* __restrict__ y, const float* __restrict__ gates, int T, int k, int H,
                                 uint16_t* __restrict__ out) {
   pdl_wait();
   pdl_trigger();
   const int half = H / 2;
-  const long long n = (long long)T * half;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    const int t = (int)(i / half), c = (int)(i % half) * 2;
-    float a = 0.f, b = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const float gt = gates[t * k + j];
-      const float2 v = *reinterpret_cast<const float2*>(y + (size_t)(t * k + j) * H + c);
-      a = fmaf(gt, v.x, a);
-      b = fmaf(gt, v.y, b);
+  for (int t = blockIdx.y; t < T; t += gridDim.y) {
+    const float* yt = y + (size_t)t * k * H;
+    const float* gt = gates + (size_t)t * k;
+    for (int c2 = blockIdx.x * blockDim.x + threadIdx.x; c2 < half; c2 += gridDim.x * blockDim.x) {
+      float a = 0.f, b = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const float g = gt[j];
+        const float2 v = *reinterpret_cast<const float2*>(yt + (size_t)j * H + 2 * c2);
+        a = fmaf(g, v.x, a);
+        b = fmaf(g, v.y, b);
+      }
+      *reinterpret_cast<uint32_t*>(out + (size_t)t * H + 2 * c2) = f32x2_to_act<ACT>(a, b);
     }
-    *reinterpret_cast<uint32_t*>(out + (size_t)t * H + c) = f32x2_to_act<ACT>(a, b);
   }
 }
 
 cudaError_t launch_finalize(const float* y, const float* gates, int T, int k, int H, uint16_t* out, int act_type,
                             cudaStream_t st) {
-  const long long n = (long long)T * (H / 2);
-  if (n == 0) return cudaSuccess;
+  if (T <= 0) return cudaSuccess;
   const int threads = 256;
-  const long long blocks = (n + threads - 1) / threads;
-  const dim3 grid((unsigned)(blocks < 4096 ? blocks : 4096));
+  const int gx = (H / 2 + threads - 1) / threads;
+  const int gy = T < 65535 ? T : 65535;
+  const dim3 grid((unsigned)gx, (unsigned)gy);
   cudaError_t e = act_type == ACT_F16
                       ? launch_pdl(finalize_kernel<ACT_F16>, grid, dim3(threads), 0, st, y, gates, T, k, H, out)
                       : launch_pdl(finalize_kernel<ACT_BF16>, grid, dim3(threads), 0, st, y, gates, T, k, H, out);

@@ -52,6 +52,25 @@ def test_route_ties_and_skew(layers):
     assert ratio > 5.0
 
 
+@pytest.mark.parametrize("T", [16, 300])
+def test_route_signed_zero_ties_in_topk(layers, T):
+    """Equal logits of opposite sign (-0 and +0) inside the top-k tie like any equal values, so
+    the lower expert id comes first, on the one-CTA path (T=16) and the chunked path (T=300)."""
+    moe = layers[(256, 8)]
+    logits = synth.gen_logits(T, 256, seed=11, device="cuda")
+    logits[3] = -1.0
+    logits[3, 5] = -0.0
+    logits[3, 2] = 0.0
+    logits[3, 9] = 0.0
+    logits[3, 200] = -0.0                                 # top-4: 2, 5, 9, 200; then -1 ties by id
+    logits[4] = -0.0
+    logits[4, ::3] = 0.0                                  # a row of signed zeros: ids 0..7
+    _check(moe, logits, 8)
+    ids, _, _, _ = moe.plan(logits)
+    assert ids[3].tolist() == [2, 5, 9, 200, 0, 1, 3, 4]
+    assert ids[4].tolist() == list(range(8))
+
+
 def test_route_large_batch(layers):
     logits = synth.gen_logits(8192, 128, seed=3, device="cuda")
     _check(layers[(128, 8)], logits, 8)

@@ -18,6 +18,8 @@ def layers():
         (8, 2): U.build(synth.make_layer(128, 64, 8, 2, kept_ids=[0, 1, 2, 3], device=dev), 4096),
         (256, 8): U.build(synth.make_layer(128, 64, 256, 8, kept=64, device=dev), 8192),
         (128, 8): U.build(synth.make_layer(128, 64, 128, 8, uniform=True, device=dev), 8192),
+        (384, 6): U.build(synth.make_layer(128, 64, 384, 6, uniform=True, device=dev), 4096),
+        (512, 8): U.build(synth.make_layer(128, 64, 512, 8, uniform=True, device=dev), 4096),
     }
 
 
@@ -69,6 +71,15 @@ def test_route_signed_zero_ties_in_topk(layers, T):
     ids, _, _, _ = moe.plan(logits)
     assert ids[3].tolist() == [2, 5, 9, 200, 0, 1, 3, 4]
     assert ids[4].tolist() == list(range(8))
+
+
+@pytest.mark.parametrize("E,k", [(384, 6), (512, 8)])
+@pytest.mark.parametrize("T", [5, 127, 170, 4096])
+def test_route_parity_wide_expert_counts(layers, E, k, T):
+    """Expert counts that do not divide the scan CTA's 1024 threads (E=384: 768 of them take
+    part) or fill it with two chunk ranges per expert (E=512), on both routing paths."""
+    logits = synth.gen_logits(T, E, seed=T + E, device="cuda")
+    _check(layers[(E, k)], logits, k)
 
 
 def test_route_large_batch(layers):

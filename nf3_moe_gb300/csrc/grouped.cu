@@ -189,6 +189,12 @@ __device__ __forceinline__ void tmem_ld16x256x4(uint32_t taddr, uint32_t* v) {
       : "memory");
 }
 
+// 256-bit global store of 8 words; the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8u(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
 // 256-bit global store of 8 floats; the address must be 32-byte aligned.
 __device__ __forceinline__ void st_global_v8f(float* dst, const float* f) {
   asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "f"(f[0]), "f"(f[1]), "f"(f[2]),
@@ -754,20 +760,23 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
           const float gsc =
               p.tab.g13[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f) * p.act_scale;
 #pragma unroll
+          // 16-row groups r0 / 16 and r0 / 16 + 1: rows 0..7 gate, 8..15 up, of
+          // channels ch .. ch + 7 and ch + 8 .. ch + 15; the 16 channels go out
+          // in one 32-byte store (one L2 sector).
+          const int ch = rt * 64 + (r0 / 16) * 8;
+          uint32_t hv[8];
+#pragma unroll
           for (int g = 0; g < 2; ++g) {
-            // 16-row group (r0 / 16 + g): rows 0..7 gate, 8..15 up, of channels ch .. ch + 7
-            const int ch = rt * 64 + (r0 / 16 + g) * 8;
-            uint32_t hv[4];
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
               const float g0 = __uint_as_float(v[16 * g + 2 * w]) * gsc;
               const float g1 = __uint_as_float(v[16 * g + 2 * w + 1]) * gsc;
               const float u0 = __uint_as_float(v[16 * g + 8 + 2 * w]) * gsc;
               const float u1 = __uint_as_float(v[16 * g + 8 + 2 * w + 1]) * gsc;
-              hv[w] = f32x2_to_act<ACT>(silu_fast(g0) * u0, silu_fast(g1) * u1);
+              hv[4 * g + w] = f32x2_to_act<ACT>(silu_fast(g0) * u0, silu_fast(g1) * u1);
             }
-            *reinterpret_cast<uint4*>(p.h_out + (size_t)(it.p0 + tok) * p.I + ch) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
           }
+          st_global_v8u(p.h_out + (size_t)(it.p0 + tok) * p.I + ch, hv);
         } else {
           const int slot = tt ? slot1 : slot0;
           if (slot < 0) continue;

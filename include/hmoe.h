@@ -196,7 +196,7 @@ hmoe_status hmoe_pack_weights(const hmoe_layer_desc* desc, const int8_t* bit_map
  *   route geometry both tiers share).
  * logits: device fp32 [T][E] row-major. NaN logits are not supported.
  * ids:    device int32 [T][k]. The k largest logits, descending, with ties
- *         to the lower expert id.
+ *         to the lower expert id; -0 and +0 count as equal.
  * gates:  device fp32 [T][k]. exp(l_j - l_max) / sum over the k chosen.
  * perm:   device int32 [T*k]. The flat slot indices s = t*k + j sorted by
  *         expert, ascending s within an expert.

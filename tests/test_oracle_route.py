@@ -64,12 +64,15 @@ def test_permutation_and_offsets_invariants():
 
 
 def test_tiny_route_fixture():
-    l = np.array([[0.1, 0.9, 0.3, 0.9], [2.0, -1.0, 0.0, 1.0]], dtype=np.float32)
+    # row 2 lists a higher id first: its larger logit is at expert 3
+    l = np.array([[0.1, 0.9, 0.3, 0.9], [2.0, -1.0, 0.0, 1.0], [0.0, 0.5, -1.0, 3.0]], dtype=np.float32)
     ids, g, perm, off = route.plan(l, 2)
-    assert ids.tolist() == [[1, 3], [0, 3]]
+    assert ids.tolist() == [[1, 3], [0, 3], [3, 1]]
     assert np.allclose(g[0], [0.5, 0.5], atol=0, rtol=0)
     e = np.exp(-1.0)
     assert np.allclose(g[1], [1 / (1 + e), e / (1 + e)], rtol=1e-15)
-    # slots: 0->e1, 1->e3, 2->e0, 3->e3
-    assert perm.tolist() == [2, 0, 1, 3]
-    assert off.tolist() == [0, 1, 2, 2, 4]
+    e = np.exp(-2.5)
+    assert np.allclose(g[2], [1 / (1 + e), e / (1 + e)], rtol=1e-15)
+    # slots: 0->e1, 1->e3, 2->e0, 3->e3, 4->e3, 5->e1
+    assert perm.tolist() == [2, 0, 5, 1, 3, 4]
+    assert off.tolist() == [0, 1, 3, 3, 6]

@@ -71,7 +71,7 @@ typedef struct CUstream_st* hmoe_stream_t;
 typedef enum {
   HMOE_OK = 0,
   HMOE_ERR_INVALID_ARG = -1,         /* NULL pointer, T < 0, bad enum value, ... */
-  HMOE_ERR_UNSUPPORTED_SHAPE = -2,   /* H % 128, I % 64, E > 512, topk > 32, topk > E */
+  HMOE_ERR_UNSUPPORTED_SHAPE = -2,   /* H % 128, I % 64, E > 512, topk > 32, topk > E, T * topk > INT_MAX */
   HMOE_ERR_WORKSPACE_TOO_SMALL = -3, /* ws_bytes < hmoe_workspace_size(T) */
   HMOE_ERR_BAD_BITMAP = -4,          /* a bit_map entry other than 3 or 4 */
   HMOE_ERR_CUDA = -5,                /* a CUDA runtime call failed; see hmoe_last_error */
@@ -155,7 +155,8 @@ hmoe_status hmoe_packed_size(const hmoe_layer_desc* desc, const int8_t* bit_map,
  * the SwiGLU output h [T*k][I] (16-bit) and the per-slot W2 output [T*k][H]
  * fp32. Errors: the desc checks (HMOE_ERR_INVALID_ARG,
  * HMOE_ERR_UNSUPPORTED_SHAPE); max_tokens < 0 or bytes NULL is
- * HMOE_ERR_INVALID_ARG. */
+ * HMOE_ERR_INVALID_ARG; max_tokens * topk above INT_MAX is
+ * HMOE_ERR_UNSUPPORTED_SHAPE (the kernels index slots with 32-bit ints). */
 hmoe_status hmoe_workspace_size(const hmoe_layer_desc* desc, int max_tokens, size_t* bytes);
 
 /* The path hmoe_forward takes for T tokens when opts->path is HMOE_PATH_AUTO:
@@ -202,7 +203,9 @@ hmoe_status hmoe_pack_weights(const hmoe_layer_desc* desc, const int8_t* bit_map
  *         expert, ascending s within an expert.
  * offsets: device int32 [E+1]. The exclusive prefix sum of per-expert
  *         counts, with offsets[E] = T*k.
- * ws: the workspace (device). T = 0 is valid and writes offsets as zeros. */
+ * ws: the workspace (device). T = 0 is valid and writes offsets as zeros.
+ * T * k above INT_MAX returns HMOE_ERR_UNSUPPORTED_SHAPE before anything is
+ * enqueued. */
 hmoe_status hmoe_plan_routes(const hmoe_layer* layer, const float* logits, int T, int32_t* ids,
                              float* gates, int32_t* perm, int32_t* offsets, void* ws,
                              size_t ws_bytes, hmoe_stream_t stream);
@@ -255,6 +258,7 @@ typedef struct {
  * HMOE_ERR_INVALID_ARG (NULL layer or buffer, T < 0, x or out not 16-byte
  * aligned, a bad option, the grouped path forced at T <= 8,
  * HMOE_DEBUG_GROUPED_PAIR with fp16 activations),
+ * HMOE_ERR_UNSUPPORTED_SHAPE (T * topk above INT_MAX),
  * HMOE_ERR_WORKSPACE_TOO_SMALL, and HMOE_ERR_CUDA if a launch fails. Faults
  * the kernels find are read later with hmoe_check_device_status.
  * x: device [T][H] of the activation type. out: device [T][H] of the same

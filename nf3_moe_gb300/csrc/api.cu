@@ -8,6 +8,7 @@
 // Summary (hybrid_bit_map 4 = kept, 3 = NF3; kept_format; the metadata is
 // validated).
 #include <algorithm>
+#include <climits>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -168,6 +169,15 @@ hmoe_status check_ws(const hmoe_layer_desc& d, int T, void* ws, size_t ws_bytes,
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// The kernels index slots (s = t * topk + j) with 32-bit ints, so a batch
+// may hold at most INT_MAX slots.
+hmoe_status check_slots(const hmoe_layer_desc& d, int T) {
+  const long long S = (long long)T * d.topk;
+  if (S > (long long)INT_MAX)
+    return fail(HMOE_ERR_UNSUPPORTED_SHAPE, "T*topk = %lld slots exceed the 32-bit slot index", S);
+  return HMOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -197,6 +207,7 @@ hmoe_status hmoe_workspace_size(const hmoe_layer_desc* desc, int max_tokens, siz
   hmoe_status s = check_desc(desc);
   if (s != HMOE_OK) return s;
   if (!bytes || max_tokens < 0) return fail(HMOE_ERR_INVALID_ARG, "bytes NULL or max_tokens < 0");
+  if ((s = check_slots(*desc, max_tokens)) != HMOE_OK) return s;
   // Every T <= max_tokens must fit (the layout grows with T; the loop keeps
   // that true however the layout changes).
   size_t need = ws_layout(*desc, max_tokens).total;
@@ -309,9 +320,10 @@ hmoe_status hmoe_plan_routes(const hmoe_layer* L, const float* logits, int T, in
   if (T < 0) return fail(HMOE_ERR_INVALID_ARG, "T=%d < 0", T);
   if (!offsets || (T > 0 && (!logits || !ids || !gates || !perm)))
     return fail(HMOE_ERR_INVALID_ARG, "a route buffer is NULL");
-  WsLayout w{};
-  hmoe_status s = check_ws(L->d, T, ws, ws_bytes, &w);
+  hmoe_status s = check_slots(L->d, T);
   if (s != HMOE_OK) return s;
+  WsLayout w{};
+  if ((s = check_ws(L->d, T, ws, ws_bytes, &w)) != HMOE_OK) return s;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   cudaError_t e = launch_route(logits, T, L->d.E, L->d.topk, ids, gates, perm, offsets,
                                reinterpret_cast<int*>(wsb + w.chunk_cnt), reinterpret_cast<int*>(wsb + w.chunk_base),
@@ -531,6 +543,7 @@ hmoe_status check_forward(const hmoe_layer* L, const void* x, int T, const int32
                           bool* grouped) {
   if (!L) return fail(HMOE_ERR_INVALID_ARG, "layer is NULL");
   if (T < 0) return fail(HMOE_ERR_INVALID_ARG, "T=%d < 0", T);
+  if (check_slots(L->d, T) != HMOE_OK) return HMOE_ERR_UNSUPPORTED_SHAPE;
   if (o.tier_order < 0 || o.tier_order > 2) return fail(HMOE_ERR_INVALID_ARG, "bad tier_order %d", o.tier_order);
   if (o.path < 0 || o.path > 2) return fail(HMOE_ERR_INVALID_ARG, "bad path %d", o.path);
   if (o.wait_limit_us < 0) return fail(HMOE_ERR_INVALID_ARG, "wait_limit_us < 0");

@@ -62,6 +62,12 @@ def test_host_validation_without_gpu(lib):
     with pytest.raises(hm.HmoeError) as ei:
         hm.hmoe_packed_size(d, [4] * 255 + [2])
     assert ei.value.status == -4
+    # slots are 32-bit indices: T * topk may reach INT_MAX but not pass it
+    d1 = hm.LayerDesc(256, 128, 8, 1, hm.FMT_NVFP4)
+    assert hm.hmoe_workspace_size(d1, 2**31 - 1) > 0
+    with pytest.raises(hm.HmoeError) as ei:
+        hm.hmoe_workspace_size(d, 2**31 // 8)
+    assert ei.value.status == -2
 
 
 def test_auto_path_rule():

@@ -33,6 +33,48 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(declared) == set(_lib.EXPORTS)
 
 
+def _prototypes():
+    """{name: (return type text, [parameter texts])} of every function include/hmoe.h declares."""
+    src = open(os.path.join(ROOT, "include", "hmoe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for ret, name, params in re.findall(r"([A-Za-z_][\w \*]*?)\s*\b(hmoe_[a-z_0-9]+)\s*\(([^;{)]*)\)\s*;", src):
+        params = " ".join(params.split())
+        out[name] = (ret.split()[-1] if ret.split() else ret, [] if params in ("", "void") else params.split(", "))
+    return out
+
+
+def _ctype_kind(c):
+    if c is None:
+        return "void"
+    if c in (ctypes.c_void_p, ctypes.c_char_p) or issubclass(c, ctypes._Pointer):
+        return "ptr"
+    # c_size_t and c_uint64 are one class on LP64 platforms: both are "u64"
+    return {ctypes.c_int: "int", ctypes.c_size_t: "u64", ctypes.c_float: "float", ctypes.c_uint64: "u64"}[c]
+
+
+def _c_kind(text):
+    if "*" in text or text.split()[0] == "hmoe_stream_t":
+        return "ptr"
+    base = text.replace("const ", "").split()[0]
+    return {"int": "int", "size_t": "u64", "float": "float", "hmoe_status": "int", "uint64_t": "u64",
+            "void": "void"}[base]
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every ctypes prototype has the header's parameter count and, per parameter, the same kind
+    (pointer, int, 64-bit unsigned, float): a mismatch would pass garbage across the ABI silently."""
+    protos = _prototypes()
+    assert set(protos) == set(_declared())
+    for name, (ret, params) in protos.items():
+        fn = getattr(lib, name)
+        assert len(fn.argtypes) == len(params), (name, params)
+        for a, p in zip(fn.argtypes, params):
+            assert _ctype_kind(a) == _c_kind(p), (name, p, a)
+        want_ret = "ptr" if ret.endswith("*") else _c_kind(ret)
+        assert _ctype_kind(fn.restype) == want_ret, (name, ret, fn.restype)
+
+
 def test_version_and_last_error(lib):
     assert lib.hmoe_version() >= 100
     assert isinstance(lib.hmoe_last_error(), bytes)

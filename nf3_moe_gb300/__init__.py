@@ -65,6 +65,97 @@ def _bitmap_arg(bit_map):
     return arr, ctypes.cast(arr, ctypes.c_void_p)
 
 
+# ------------------------------------------------------------------ argument checks
+# The library sees raw device pointers only, so the binding checks every tensor it hands over:
+# type, dtype, shape (or, for checkpoint and packed buffers, size in bytes), layout and device.
+# A tensor of the wrong shape would otherwise have the kernels read or write past its end.
+# The checks run on the host before the library is called; each raises ValueError (TypeError
+# for a non-tensor). cuda=False skips the device checks, so that the rest can be tested
+# without a GPU.
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def _need(name, t, shape=None, dtype=None, min_bytes=None, device=None, cuda=True):
+    """shape: a tuple whose None entries match any extent."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and (t.dim() != len(shape) or
+                              any(w is not None and int(g) != int(w) for g, w in zip(t.shape, shape))):
+        want = "[" + ", ".join("*" if w is None else str(int(w)) for w in shape) + "]"
+        raise ValueError(f"{name} must have shape {want}, got {list(t.shape)}")
+    if min_bytes is not None and _nbytes(t) < min_bytes:
+        raise ValueError(f"{name} holds {_nbytes(t)} bytes; at least {min_bytes} are needed")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if cuda:
+        if t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor, got one on {t.device}")
+        if device is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, the other arguments on {device}")
+
+
+def _matrix_bytes(fmt, N, K):
+    """(codes bytes, scales bytes) of one [N, K] matrix in the logical layout of include/hmoe.h."""
+    if fmt == FMT_NVFP4:
+        return N * K // 2, N * K // 16
+    if fmt == FMT_MXFP4:
+        return N * K // 2, N * K // 32
+    return N * K * 3 // 8, N * (K // 64) * 2
+
+
+def _check_route_bufs(desc, T, ids, gates, perm, offsets, device, cuda):
+    k, E = int(desc.topk), int(desc.E)
+    _need("ids", ids, (T, k), torch.int32, device=device, cuda=cuda)
+    _need("gates", gates, (T, k), torch.float32, device=device, cuda=cuda)
+    _need("perm", perm, (T * k,), torch.int32, device=device, cuda=cuda)
+    _need("offsets", offsets, (E + 1,), torch.int32, device=device, cuda=cuda)
+
+
+def _check_plan(desc, logits, ids, gates, perm, offsets, ws, cuda=True):
+    _need("logits", logits, (None, int(desc.E)), torch.float32, cuda=cuda)
+    _check_route_bufs(desc, logits.shape[0], ids, gates, perm, offsets, logits.device, cuda)
+    _need("ws", ws, device=logits.device, cuda=cuda)
+
+
+def _check_forward(desc, x, ids, gates, perm, offsets, out, ws, cuda=True):
+    """ws None: the static entry point, which takes no workspace."""
+    dt, H = act_torch_dtype(desc.act_dtype), int(desc.H)
+    _need("x", x, (None, H), dt, cuda=cuda)
+    T = x.shape[0]
+    _check_route_bufs(desc, T, ids, gates, perm, offsets, x.device, cuda)
+    _need("out", out, (T, H), dt, device=x.device, cuda=cuda)
+    if ws is not None:
+        _need("ws", ws, device=x.device, cuda=cuda)
+
+
+def _check_pack(desc, bit_map, experts, kept_buf, nf3_buf, cuda=True):
+    kb, nb = hmoe_packed_size(desc, bit_map)          # the descriptor and bit map checks (library)
+    E, H, I = int(desc.E), int(desc.H), int(desc.I)
+    if len(experts) != E:
+        raise ValueError(f"expected {E} experts, got {len(experts)}")
+    for e, (c13, s13, _, c2, s2, _) in enumerate(experts):
+        fmt = FMT_NF3 if bit_map is not None and int(bit_map[e]) == 3 else int(desc.kept_format)
+        for nm, (N, K), c, sc in (("W13", (2 * I, H), c13, s13), ("W2", (H, I), c2, s2)):
+            cb, sb = _matrix_bytes(fmt, N, K)
+            _need(f"expert {e} {nm} codes", c, min_bytes=cb, cuda=cuda)
+            _need(f"expert {e} {nm} scales", sc, min_bytes=sb, cuda=cuda)
+    if kb:
+        _need("kept_buf", kept_buf, min_bytes=kb, cuda=cuda)
+    if nb:
+        _need("nf3_buf", nf3_buf, min_bytes=nb, cuda=cuda)
+
+
+def _check_linear_forward(desc, x, out, ws, cuda=True):
+    dt = act_torch_dtype(desc.act_dtype)
+    _need("x", x, (None, int(desc.K)), dt, cuda=cuda)
+    _need("out", out, (x.shape[0], int(desc.N)), dt, device=x.device, cuda=cuda)
+    _need("ws", ws, device=x.device, cuda=cuda)
+
+
 def hmoe_packed_size(desc, bit_map=None):
     kb, nb = ctypes.c_size_t(), ctypes.c_size_t()
     keep, bm = _bitmap_arg(bit_map)
@@ -113,8 +204,7 @@ def hmoe_pack_weights(desc, bit_map, experts, kept_buf, nf3_buf, stream=None):
     """experts: list of E tuples (w13_codes, w13_scales, w13_global, w2_codes, w2_scales, w2_global).
     Tensors must be CUDA tensors in the logical layout of include/hmoe.h."""
     E = desc.E
-    if len(experts) != E:
-        raise ValueError(f"expected {E} experts, got {len(experts)}")
+    _check_pack(desc, bit_map, experts, kept_buf, nf3_buf)
     src = (_lib.ExpertSrc * E)()
     for e, (c13, s13, g13, c2, s2, g2) in enumerate(experts):
         src[e] = _lib.ExpertSrc(c13.data_ptr(), s13.data_ptr(), float(g13), c2.data_ptr(), s2.data_ptr(), float(g2))
@@ -126,6 +216,7 @@ def hmoe_pack_weights(desc, bit_map, experts, kept_buf, nf3_buf, stream=None):
 
 
 def hmoe_plan_routes(layer, logits, ids, gates, perm, offsets, ws, stream=None):
+    _check_plan(layer.desc, logits, ids, gates, perm, offsets, ws)
     T = logits.shape[0]
     _lib.check(_lib.lib().hmoe_plan_routes(layer.handle, _ptr(logits), T, _ptr(ids), _ptr(gates), _ptr(perm),
                                            _ptr(offsets), _ptr(ws), ws.numel() * ws.element_size(),
@@ -135,6 +226,7 @@ def hmoe_plan_routes(layer, logits, ids, gates, perm, offsets, ws, stream=None):
 def hmoe_forward(layer, x, ids, gates, perm, offsets, out, ws, stream=None, tier_order=TIERS_ONE_LAUNCH,
                  path=PATH_AUTO, wait_limit_us=0, debug_flags=0, stage_events=None):
     """stage_events: optional list of recorded torch.cuda.Event (up to 4); see hmoe_forward_opts."""
+    _check_forward(layer.desc, x, ids, gates, perm, offsets, out, ws)
     T = x.shape[0]
     evs, n_ev = None, 0
     if stage_events:
@@ -154,13 +246,26 @@ def hmoe_check_device_status(ws, stream=None):
     _lib.check(_lib.lib().hmoe_check_device_status(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def _debug_shape(desc, which):
+    """[N, K] of the matrix which (13 or 2) selects; None for another value (the library rejects it)."""
+    H, I = int(desc.H), int(desc.I)
+    return {13: (2 * I, H), 2: (H, I)}.get(int(which))
+
+
 def hmoe_debug_dequant(layer, expert, which, dst, stream=None):
+    shape = _debug_shape(layer.desc, which)
+    if shape is not None:
+        _need("dst", dst, shape, act_torch_dtype(layer.desc.act_dtype))
     _lib.check(_lib.lib().hmoe_debug_dequant(layer.handle, int(expert), int(which), _ptr(dst), _stream(stream)))
 
 
 def hmoe_debug_decode_operand(layer, expert, which, dst, scales, stream=None):
     """The weight-streaming kernel's operand (dst [N, K] of the activation type) and per-64-group
     factors (scales fp32 [N, K/64])."""
+    shape = _debug_shape(layer.desc, which)
+    if shape is not None:
+        _need("dst", dst, shape, act_torch_dtype(layer.desc.act_dtype))
+        _need("scales", scales, (shape[0], shape[1] // 64), torch.float32, device=dst.device)
     _lib.check(_lib.lib().hmoe_debug_decode_operand(layer.handle, int(expert), int(which), _ptr(dst), _ptr(scales),
                                                     _stream(stream)))
 
@@ -210,6 +315,7 @@ class HybridMoELayer:
 def hmoe_forward_static(layer, x, ids, gates, perm, offsets, out, stream=None):
     """hmoe_forward without a caller workspace (see include/hmoe.h): the scratch is a fixed
     per-device array inside the library, so the call allocates no device memory."""
+    _check_forward(layer.desc, x, ids, gates, perm, offsets, out, None)
     T = x.shape[0]
     _lib.check(_lib.lib().hmoe_forward_static(layer.handle, _ptr(x), T, _ptr(ids), _ptr(gates), _ptr(perm),
                                               _ptr(offsets), _ptr(out), _stream(stream)))
@@ -245,6 +351,11 @@ class Linear:
 
 
 def hmoe_linear_pack(desc, codes, scales, global_scale, packed, stream=None):
+    nbytes = hmoe_linear_packed_size(desc)            # the descriptor checks (library)
+    cb, sb = _matrix_bytes(int(desc.fmt), int(desc.N), int(desc.K))
+    _need("codes", codes, min_bytes=cb)
+    _need("scales", scales, min_bytes=sb, device=codes.device)
+    _need("packed", packed, min_bytes=nbytes, device=codes.device)
     h = ctypes.c_void_p()
     _lib.check(_lib.lib().hmoe_linear_pack(ctypes.byref(desc), _ptr(codes), _ptr(scales), float(global_scale),
                                            _ptr(packed), _stream(stream), ctypes.byref(h)))
@@ -252,6 +363,7 @@ def hmoe_linear_pack(desc, codes, scales, global_scale, packed, stream=None):
 
 
 def hmoe_linear_forward(linear, x, out, ws, stream=None, path=PATH_AUTO, wait_limit_us=0, debug_flags=0):
+    _check_linear_forward(linear.desc, x, out, ws)
     opts = _lib.ForwardOpts(TIERS_ONE_LAUNCH, int(path), int(wait_limit_us), int(debug_flags), None, 0)
     _lib.check(_lib.lib().hmoe_linear_forward_ex(linear.handle, _ptr(x), int(x.shape[0]), _ptr(out), _ptr(ws),
                                                  ws.numel() * ws.element_size(), ctypes.byref(opts), _stream(stream)))
@@ -283,6 +395,13 @@ class LinearW4A16:
 def hmoe_quantize_act_nvfp4(x, global_scale, codes, scales, stream=None):
     """NVFP4 activation quantisation of x [rows, K] (bf16 or fp16): codes uint8 [rows, K/2],
     scales uint8 [rows, K/16] (include/hmoe.h)."""
+    _need("x", x, (None, None))
+    if x.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError(f"x must be torch.bfloat16 or torch.float16, got {x.dtype}")
+    R, K = x.shape
+    if K % 16 == 0:                                  # other K: the library rejects the call
+        _need("codes", codes, (R, K // 2), torch.uint8, device=x.device)
+        _need("scales", scales, (R, K // 16), torch.uint8, device=x.device)
     act = ACT_F16 if x.dtype == torch.float16 else ACT_BF16
     _lib.check(_lib.lib().hmoe_quantize_act_nvfp4(_ptr(x), int(x.shape[0]), int(x.shape[1]), act,
                                                   ctypes.c_float(global_scale), _ptr(codes), _ptr(scales),

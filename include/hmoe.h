@@ -165,13 +165,21 @@ hmoe_status hmoe_workspace_size(const hmoe_layer_desc* desc, int max_tokens, siz
  * only: no device work, no GPU needed. The pages give the M <= 8 path
  * ("quant: nvfp4_nf3_hybrid ...", How it works) but no rule above it; the
  * factor 8 is this library's measured crossover between its two kernels.
+ *   Cites: "quant: nvfp4_nf3_hybrid -- native serving ...", How it works
+ *   (the M<=8 decode path beside the batched one).
  * Errors: HMOE_ERR_INVALID_ARG (NULL pointer, T < 0) and the desc checks of
  * hmoe_workspace_size. */
 hmoe_status hmoe_auto_path(const hmoe_layer_desc* desc, int T, int* path);
 
 /* Zero the workspace once, before its first use, on the stream. Every
  * completed hmoe_forward leaves the workspace's counters at zero again. Zero
- * it once more after a call reports HMOE_ERR_DEVICE_TIMEOUT. */
+ * it once more after a call reports HMOE_ERR_DEVICE_TIMEOUT.
+ *   Cites: "quant: add native mixed NVFP4/MXFP4 plus NF3 MoE serving",
+ *   Summary (scratch sized once, up front); "quant: nvfp4_nf3_hybrid --
+ *   native serving ...", How it works (preplanned, CUDA-graph-safe launches:
+ *   the scratch needs no per-call reset on the host).
+ * ws_dev: device; all ws_bytes of it are zeroed. Errors:
+ * HMOE_ERR_INVALID_ARG (NULL), HMOE_ERR_CUDA. */
 hmoe_status hmoe_workspace_init(void* ws_dev, size_t ws_bytes, hmoe_stream_t stream);
 
 /* Demultiplex the experts into tier-local packed buffers per the bit map. Each
@@ -271,6 +279,12 @@ hmoe_status hmoe_forward(const hmoe_layer* layer, const void* x, int T, const in
                          const float* gates, const int32_t* perm, const int32_t* offsets,
                          void* out, void* ws, size_t ws_bytes, hmoe_stream_t stream);
 
+/* hmoe_forward with options (hmoe_forward_opts: tier order, path, wait
+ * limit, stage events). opts NULL is the defaults. Arguments, results and
+ * errors otherwise as hmoe_forward.
+ *   Cites: "quant: nvfp4_nf3_hybrid -- native serving ...", How it works (a
+ *   second launch for the other tier into the same topk_sum, or one launch
+ *   for both: tier_order chooses). */
 hmoe_status hmoe_forward_ex(const hmoe_layer* layer, const void* x, int T, const int32_t* ids,
                             const float* gates, const int32_t* perm, const int32_t* offsets,
                             void* out, void* ws, size_t ws_bytes, const hmoe_forward_opts* opts,
@@ -281,8 +295,9 @@ hmoe_status hmoe_forward_ex(const hmoe_layer* layer, const void* x, int T, const
  * give a library only its input and output buffers under a fixed
  * device-memory plan (some serving engines and plugin interfaces), and code
  * that must never reach the allocator or cudaFree's implicit device-wide
- * synchronisation. The pages have no counterpart; this is a library
- * convenience.
+ * synchronisation.
+ *   Cites: the same passages as hmoe_forward (the computation); the pages
+ *   have no counterpart for the scratch arrangement, a library convenience.
  *
  * Instead of a caller workspace, the call uses a file-scope device array of
  * HMOE_STATIC_SCRATCH_BYTES (16 MiB). Every GPU that loads the library
@@ -312,7 +327,8 @@ hmoe_status hmoe_forward_static(const hmoe_layer* layer, const void* x, int T, c
                                 hmoe_stream_t stream);
 
 /* hmoe_check_device_status for the array used by hmoe_forward_static on the
- * current device. It synchronises the stream. */
+ * current device. It synchronises the stream.
+ *   Cites: as hmoe_check_device_status. */
 hmoe_status hmoe_check_device_status_static(hmoe_stream_t stream);
 
 /* Synchronise the stream and read the device status word the kernels write
@@ -335,7 +351,13 @@ hmoe_status hmoe_check_device_status(void* ws, size_t ws_bytes, hmoe_stream_t st
  * e2m1*2^(b-127) (MXFP4), or rne(cb*s) (NF3; in fp16 with s first converted
  * to fp16), exact or rounded once to the activation type. The weight-streaming
  * kernel uses the same values for NVFP4 and MXFP4 but not for NF3: see
- * hmoe_debug_decode_operand. */
+ * hmoe_debug_decode_operand.
+ *   Cites: "quant: nvfp4_nf3_hybrid -- native serving ...", How it works
+ *   (the NVFP4 and NF3 tier weights); "quant: add native mixed NVFP4/MXFP4
+ *   plus NF3 MoE serving", Summary (MXFP4 as the kept format); "[Quantization]
+ *   [ModelOpt] W4A16 NVFP4 fused MoE", Summary item 2 (the activation type).
+ * Errors: HMOE_ERR_INVALID_ARG (NULL layer or dst, expert out of range,
+ * which not 13 or 2), HMOE_ERR_CUDA. */
 hmoe_status hmoe_debug_dequant(const hmoe_layer* layer, int expert, int which, void* dst,
                                hmoe_stream_t stream);
 
@@ -349,14 +371,24 @@ hmoe_status hmoe_debug_dequant(const hmoe_layer* layer, int expert, int which, v
  * bf16 scale as fp32 (for W4A4 layers, whose h the streaming kernel must form
  * from the same weights as the tensor-core kernel: the tile of
  * hmoe_debug_dequant and scales 1); NVFP4 and MXFP4: dst is the tile of hmoe_debug_dequant and
- * scales are 1. */
+ * scales are 1.
+ *   Cites: as hmoe_debug_dequant. Errors as hmoe_debug_dequant (scales NULL
+ *   is HMOE_ERR_INVALID_ARG). */
 hmoe_status hmoe_debug_decode_operand(const hmoe_layer* layer, int expert, int which, void* dst,
                                       float* scales, hmoe_stream_t stream);
 
-/* Global scales and tier of one expert, as the handle holds them. */
+/* Global scales and tier of one expert, as the handle holds them: *fmt is
+ * the expert's format (HMOE_FMT_*), the globals are 1 for MXFP4 and NF3.
+ *   Cites: "quant: add native mixed NVFP4/MXFP4 plus NF3 MoE serving",
+ *   Summary (hybrid_bit_map: the tier of each expert).
+ * Errors: HMOE_ERR_INVALID_ARG (NULL layer, expert out of range). */
 hmoe_status hmoe_layer_expert_info(const hmoe_layer* layer, int expert, int* fmt,
                                    float* w13_global, float* w2_global);
 
+/* Free the handle (host memory only; the caller's device buffers are left
+ * as they are). NULL is ignored.
+ *   Cites: "quant: nvfp4_nf3_hybrid -- native serving ...", How it works (the
+ *   two prepared weight objects of a layer, which the handle describes). */
 void hmoe_layer_destroy(hmoe_layer* layer);
 
 /* ------------------------------------------------------------ dense Linear W4A16
@@ -385,35 +417,43 @@ typedef struct {
 
 typedef struct hmoe_linear hmoe_linear; /* opaque host handle: no device memory */
 
-/* Bytes of the packed matrix (the packed argument of hmoe_linear_pack). */
+/* Bytes of the packed matrix (the packed argument of hmoe_linear_pack).
+ *   Cites: the dense-Linear passage of this section. Errors:
+ *   HMOE_ERR_INVALID_ARG, HMOE_ERR_UNSUPPORTED_SHAPE (N % 128, K % 64). */
 hmoe_status hmoe_linear_packed_size(const hmoe_linear_desc* desc, size_t* bytes);
 
 /* Workspace bytes for hmoe_linear_forward at up to max_tokens rows: the
  * status word, the kernels' work queues, the one-expert route geometry and
- * the fp32 product [max_tokens][N]. */
+ * the fp32 product [max_tokens][N].
+ *   Cites: the dense-Linear passage of this section. */
 hmoe_status hmoe_linear_workspace_size(const hmoe_linear_desc* desc, int max_tokens, size_t* bytes);
 
 /* Repack W into the tile layout and create the handle. codes, scales: device
  * tensors in the logical layout of desc->fmt; global_scale: the NVFP4 fp32
  * global scale (ignored otherwise). packed: device buffer of
  * hmoe_linear_packed_size bytes, 16-byte aligned, alive while the handle is
- * used. The sources may be freed once the stream has passed this point. */
+ * used. The sources may be freed once the stream has passed this point.
+ *   Cites: the dense-Linear passage of this section. */
 hmoe_status hmoe_linear_pack(const hmoe_linear_desc* desc, const void* codes, const void* scales,
                              float global_scale, void* packed, hmoe_stream_t stream, hmoe_linear** out);
 
 /* out[t][n] = act(sum_k x[t][k] W[n][k]). x: device [T][K] and out: device
  * [T][N], both of the activation type (act), out fully overwritten; both
- * 16-byte aligned. T = 0 is valid. */
+ * 16-byte aligned. T = 0 is valid.
+ *   Cites: the dense-Linear passage of this section. */
 hmoe_status hmoe_linear_forward(const hmoe_linear* linear, const void* x, int T, void* out, void* ws,
                                 size_t ws_bytes, hmoe_stream_t stream);
 
 /* With options: path (HMOE_PATH_AUTO chooses the streaming kernel for T <= 8),
  * wait_limit_us and debug_flags as for hmoe_forward_ex (HMOE_DEBUG_GROUPED_PAIR
  * with fp16 is HMOE_ERR_INVALID_ARG); tier_order and stage_events are
- * ignored. */
+ * ignored.
+ *   Cites: the dense-Linear passage of this section. */
 hmoe_status hmoe_linear_forward_ex(const hmoe_linear* linear, const void* x, int T, void* out, void* ws,
                                    size_t ws_bytes, const hmoe_forward_opts* opts, hmoe_stream_t stream);
 
+/* Free the handle (host memory only). NULL is ignored.
+ *   Cites: the dense-Linear passage of this section. */
 void hmoe_linear_destroy(hmoe_linear* linear);
 
 /* NVFP4 activation quantisation, the rule the W4A4 forward applies:
@@ -433,13 +473,16 @@ void hmoe_linear_destroy(hmoe_linear* linear);
 hmoe_status hmoe_quantize_act_nvfp4(const void* x, int rows, int K, int act_dtype, float global_scale,
                                     void* codes, void* scales, hmoe_stream_t stream);
 
-/* Message for the last failing call on this thread ("" if none). */
+/* Message for the last failing call on this thread ("" if none). Part of
+ * the error convention at the top of this file; no page defines it. */
 const char* hmoe_last_error(void);
 
-/* Number of kernels this library has launched in this process so far (all entry points). */
+/* Number of kernels this library has launched in this process so far (all
+ * entry points). A library utility for launch accounting; no page defines it. */
 uint64_t hmoe_launch_count(void);
 
-/* Library version, major*10000 + minor*100 + patch. */
+/* Library version, major*10000 + minor*100 + patch. A library utility; no
+ * page defines it. */
 int hmoe_version(void);
 
 #ifdef __cplusplus

@@ -759,7 +759,6 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
           if (tok >= it.n) continue;
           const float gsc =
               p.tab.g13[it.e] * (gt_expert_fmt(p, it.e) == FMT_NVFP4 ? nvfp4_unscale<ACT>() : 1.0f) * p.act_scale;
-#pragma unroll
           // 16-row groups r0 / 16 and r0 / 16 + 1: rows 0..7 gate, 8..15 up, of
           // channels ch .. ch + 7 and ch + 8 .. ch + 15; the 16 channels go out
           // in one 32-byte store (one L2 sector).

@@ -3,7 +3,6 @@
 Tolerance: per token row, max|out - ref| <= 2e-2 * max|ref| (fp32 accumulation).
 """
 
-import numpy as np
 import pytest
 import torch
 

@@ -75,6 +75,58 @@ def test_binding_signatures_match_the_header(lib):
         assert _ctype_kind(fn.restype) == want_ret, (name, ret, fn.restype)
 
 
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "hmoe.h"
+
+int main(void) {
+  hmoe_layer_desc d;
+  size_t kept = 0, nf3 = 0, ws = 0;
+  int path = -1, e;
+  int8_t bit_map[256];
+  memset(&d, 0, sizeof d);                      /* a zeroed descriptor: bf16, W4A16 */
+  d.H = 6144; d.I = 2048; d.E = 256; d.topk = 8; d.kept_format = HMOE_FMT_NVFP4;
+  for (e = 0; e < 256; ++e) bit_map[e] = (int8_t)(e < 64 ? 4 : 3);
+  if (hmoe_packed_size(&d, bit_map, &kept, &nf3) != HMOE_OK) return 1;
+  if (hmoe_workspace_size(&d, 4096, &ws) != HMOE_OK) return 2;
+  if (hmoe_auto_path(&d, 4096, &path) != HMOE_OK) return 3;
+  if (hmoe_plan_routes(NULL, NULL, 1, NULL, NULL, NULL, NULL, NULL, 0, NULL) != HMOE_ERR_INVALID_ARG) return 4;
+  if (strlen(hmoe_last_error()) == 0) return 5;
+  printf("%d %zu %zu %zu %d\n", hmoe_version(), kept, nf3, ws, path);
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links_from_c(lib, tmp_path):
+    """A C99 client, compiled with -Wall -Werror -pedantic against include/hmoe.h and linked
+    with libhmoe.so, calls the host-only entry points: the boundary needs no C++ and no torch."""
+    import shutil
+    import subprocess
+    import nf3_moe_gb300 as hm
+    from nf3_moe_gb300 import _lib
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-o", str(exe), f"-L{libdir}", "-l:libhmoe.so", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    version, kept, nf3, ws, path = (int(v) for v in r.stdout.split())
+    d = hm.LayerDesc(6144, 2048, 256, 8, hm.FMT_NVFP4)
+    assert version == lib.hmoe_version()
+    assert (kept, nf3) == hm.hmoe_packed_size(d, [4] * 64 + [3] * 192)
+    assert ws == hm.hmoe_workspace_size(d, 4096)
+    assert path == hm.PATH_GROUPED
+
+
 def test_version_and_last_error(lib):
     assert lib.hmoe_version() >= 100
     assert isinstance(lib.hmoe_last_error(), bytes)
